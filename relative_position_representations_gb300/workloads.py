@@ -1,0 +1,115 @@
+"""Named workloads and the seeded synthetic-input generator.
+
+This module holds shapes, distributions and random draws only: none of the attention
+arithmetic. Both the CUDA path (through bench.py and the GPU tests) and the CPU oracle are
+fed from here, so the two see bit-identical inputs.
+
+Shapes follow the translation Transformer configurations on the paper summary page
+(section 5, "Evaluation Methodology": base d_z = 64 with 8 heads and clip k = 16,
+big d_z = 64 with 16 heads), plus a long-sequence key-only case and the T5 bias case ("Relative position
+embeddings" page, section "T5": 32 buckets, max_distance 128). No dataset is read:
+every value is drawn from a torch CPU generator seeded by the caller.
+
+Draw order (fp32 draws, then a round-to-nearest-even cast to the workload dtype):
+Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. N(0, s^2) means s * randn.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    n: int
+    d: int
+    dtype: str                      # "bf16" or "f32"
+    kind: str = "shaw"              # "shaw" or "t5"
+    clip_k: int = 0
+    causal: bool = False
+    key_term: bool = True           # a^K present (Shaw)
+    value_term: bool = True         # a^V present (Shaw)
+    qkv_std: float = 1.0
+    table_std: float = 0.02
+    shared_tables: bool = False     # one table for all heads (head stride 0)
+    kv_len_range: Optional[tuple] = None   # inclusive (lo, hi) per sequence, or None
+    scale: Optional[float] = None   # default 1/sqrt(d) for Shaw, 1.0 for T5
+    num_buckets: int = 32
+    max_distance: int = 128
+    bidirectional: bool = True
+    bias_std: float = 1.0
+
+    @property
+    def softmax_scale(self) -> float:
+        if self.scale is not None:
+            return float(self.scale)
+        return 1.0 if self.kind == "t5" else 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    # tiny fp32 case the oracle finishes instantly
+    "tiny_fp32": Workload("tiny_fp32", B=1, H=2, n=16, d=8, dtype="f32", clip_k=2,
+                          table_std=0.1, scale=1.0 / math.sqrt(8)),
+    # Transformer-base encoder self-attention with per-sequence key padding
+    "base_encoder": Workload("base_encoder", B=64, H=8, n=128, d=64, dtype="bf16", clip_k=16,
+                             table_std=0.02, kv_len_range=(32, 128), scale=1.0 / 8),
+    # Transformer-big decoder self-attention (causal)
+    "big_decoder": Workload("big_decoder", B=32, H=16, n=256, d=64, dtype="bf16", clip_k=16,
+                            table_std=0.02, causal=True, scale=1.0 / 8),
+    # long sequence, key-relative term only, causal
+    "long_keyonly": Workload("long_keyonly", B=4, H=16, n=4096, d=128, dtype="bf16",
+                             clip_k=64, table_std=0.02, causal=True, value_term=False,
+                             scale=1.0 / math.sqrt(128)),
+    # T5 scalar bucketed bias, no 1/sqrt(d)
+    "t5_bias": Workload("t5_bias", B=8, H=12, n=2048, d=64, dtype="bf16", kind="t5",
+                        qkv_std=1.0 / 8, scale=1.0, num_buckets=32, max_distance=128,
+                        bidirectional=True, bias_std=1.0),
+}
+
+ORDER = ["tiny_fp32", "base_encoder", "big_decoder", "long_keyonly", "t5_bias"]
+
+
+def draw_inputs(w: Workload, seed: int = 0) -> dict:
+    """Seeded CPU tensors for workload w (see the module docstring for the recipe)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    shape = (w.B, w.H, w.n, w.d)
+    dt = w.torch_dtype
+
+    def normal(shp, std):
+        return (torch.randn(shp, generator=g, dtype=torch.float32) * std).to(dt)
+
+    out = {"q": normal(shape, w.qkv_std), "k": normal(shape, w.qkv_std),
+           "v": normal(shape, w.qkv_std)}
+    if w.kind == "t5":
+        out["bias"] = torch.randn((w.num_buckets, w.H), generator=g,
+                                  dtype=torch.float32) * w.bias_std
+        out["kv_len"] = None
+        return out
+    W = 2 * w.clip_k + 1
+    Ht = 1 if w.shared_tables else w.H
+    out["aK"] = normal((Ht, W, w.d), w.table_std) if w.key_term else None
+    out["aV"] = normal((Ht, W, w.d), w.table_std) if w.value_term else None
+    if w.kv_len_range is not None:
+        lo, hi = w.kv_len_range
+        out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
+    else:
+        out["kv_len"] = None
+    return out
+
+
+def table_head_stride(w: Workload) -> int:
+    return 0 if w.shared_tables else (2 * w.clip_k + 1) * w.d
