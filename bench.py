@@ -1,0 +1,531 @@
+"""Benchmark of the relation-aware attention forward hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one forward pass over one batch of the named workload (default: the
+Transformer-base encoder shape, B=64 H=8 n=128 d=64 k=16 bf16 with per-sequence key
+padding): a single kernel launch through the C ABI. Inputs are seeded and synthetic
+(workloads.py) and resident in HBM; to keep L2 (126 MB) from serving them, the timed
+steps rotate over enough input sets to exceed 4x L2 and are replayed from a CUDA graph
+(the kernel is a few microseconds long, so host launch overhead would otherwise dominate).
+
+Printed (rank 0, one JSON line): the whole-job TFLOP/s over the timed steps; the per-launch
+kernel time measured with CUDA events on the launching stream and its roofline fraction;
+an end-to-end number through the same C ABI with host (pinned) buffers and the
+host<->device copies inside the timed region; the fp64 CPU oracle timed on a bounded
+sample of the same workload; SM clocks sampled while the timed region runs.
+
+Under torchrun (N > 1) each rank runs the same per-GPU workload on its own GPU (the path
+shards over independent (batch, head) units, so there is no collective on the data path;
+only the timing reduction uses the process group): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("fused rel-attn fwd TFLOP/s (bf16) and % of GB300 tensor/HBM roofline vs CPU oracle")
+DEFAULT_WORKLOAD = "base_encoder"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------- accounting
+def pairs_per_sequence(w, kv_len_b: int) -> int:
+    """Unmasked (i, j) pairs of one (b, h)."""
+    n = w.n
+    kv = n if kv_len_b is None else max(0, min(int(kv_len_b), n))
+    if not w.causal:
+        return n * kv
+    # row i keeps j <= min(i, kv - 1)
+    return sum(min(i + 1, kv) for i in range(n))
+
+
+def algorithmic_flops(w, kv_len) -> float:
+    """4*d per unmasked pair (Q.K^T and P.V) + 2*d*n per reachable table row and term."""
+    kvs = [None] * w.B if kv_len is None else [int(x) for x in kv_len]
+    pairs = sum(pairs_per_sequence(w, kvs[b]) for b in range(w.B)) * w.H
+    flops = 4.0 * w.d * pairs
+    if w.kind == "shaw":
+        reach = (w.clip_k + 1) if w.causal else (2 * w.clip_k + 1)
+        terms = int(w.key_term) + int(w.value_term)
+        flops += 2.0 * w.d * w.n * reach * terms * w.B * w.H
+    return flops
+
+
+def algorithmic_bytes(w, kv_len) -> float:
+    """Q and O in full, K and V rows below kv_len, the tables once (bf16 / fp32 elements)."""
+    es = 2 if w.dtype == "bf16" else 4
+    BHnd = w.B * w.H * w.n * w.d
+    kvs = [w.n] * w.B if kv_len is None else [min(int(x), w.n) for x in kv_len]
+    kv_rows = sum(kvs) * w.H
+    byt = es * (2 * BHnd + 2 * kv_rows * w.d)
+    if w.kind == "shaw":
+        Ht = 1 if w.shared_tables else w.H
+        byt += es * Ht * (2 * w.clip_k + 1) * w.d * (int(w.key_term) + int(w.value_term))
+    else:
+        byt += 4 * w.num_buckets * w.H
+    return float(byt)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "relative_position_representations_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is busy."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu = gpu_index
+        self.interval = interval_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        mhz, max_mhz, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if ts < t0 or ts > t1:
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                max_mhz = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz, "reasons": sorted(reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max_mhz,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------- CPU oracle
+def oracle_rows_call(w, x, rows, nthreads):
+    import oracle
+
+    def np_(t):
+        return None if t is None else t.float().numpy()
+
+    kv = None if x.get("kv_len") is None else x["kv_len"].numpy()
+    if w.kind == "t5":
+        return oracle.t5bias_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), x["bias"].numpy(),
+                                 w.num_buckets, w.max_distance, w.bidirectional, w.causal,
+                                 w.softmax_scale, kv_len=kv, rows=rows, nthreads=nthreads)
+    from relative_position_representations_gb300 import workloads as wl
+    return oracle.relattn_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), np_(x["aK"]), np_(x["aV"]),
+                              w.clip_k, w.causal, w.softmax_scale, kv_len=kv,
+                              table_head_stride=wl.table_head_stride(w), rows=rows,
+                              nthreads=nthreads)
+
+
+def row_flops(w, kv_len, rows):
+    """Algorithmic FLOPs of a set of flat row ids (same accounting as algorithmic_flops)."""
+    total = 0.0
+    reach = 0
+    if w.kind == "shaw":
+        reach = ((w.clip_k + 1) if w.causal else (2 * w.clip_k + 1)) * (
+            int(w.key_term) + int(w.value_term))
+    for r in rows:
+        bh, i = divmod(int(r), w.n)
+        b = bh // w.H
+        kv = w.n if kv_len is None else min(int(kv_len[b]), w.n)
+        keys = min(i + 1, kv) if w.causal else kv
+        total += 4.0 * w.d * keys + 2.0 * w.d * reach
+    return total
+
+
+def time_oracle(w, x, budget_s: float, seed: int = 1):
+    """Run the oracle on random rows of the workload for about budget_s seconds."""
+    import numpy as np
+    import oracle
+    nthreads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.H * w.n
+    kv = None if x.get("kv_len") is None else x["kv_len"].numpy()
+    # calibrate on a small batch of rows
+    count = min(total_rows, max(nthreads * 4, 64))
+    while True:
+        rows = rng.choice(total_rows, size=count, replace=False)
+        t0 = time.perf_counter()
+        oracle_rows_call(w, x, rows, nthreads)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 or count >= total_rows:
+            break
+        count = min(total_rows, count * 4)
+    target = min(total_rows, max(count, int(count * budget_s / max(dt, 1e-6))))
+    rows = rng.choice(total_rows, size=target, replace=False)
+    t0 = time.perf_counter()
+    oracle_rows_call(w, x, rows, nthreads)
+    dt = time.perf_counter() - t0
+    fl = row_flops(w, kv, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d of %d query rows (random, seed %d), fp64 C loop, %.1f s" % (
+                target, total_rows, seed, dt)}, fl, dt
+
+
+# ----------------------------------------------------------------------- GPU arm
+def gpu_call(rp, w, g, out, stream):
+    from relative_position_representations_gb300 import workloads as wl
+    if w.kind == "t5":
+        return rp.relattn_t5bias_fwd(g["q"], g["k"], g["v"], g["bias"], w.num_buckets,
+                                     w.max_distance, w.bidirectional, w.causal, w.softmax_scale,
+                                     kv_len=g.get("kv_len"), out=out, stream=stream)
+    return rp.relattn_fwd(g["q"], g["k"], g["v"], g["aK"], g["aV"], w.clip_k, w.causal,
+                          w.softmax_scale, kv_len=g["kv_len"], out=out,
+                          table_head_stride=wl.table_head_stride(w), stream=stream)
+
+
+def make_event(external: bool):
+    import torch
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import relative_position_representations_gb300 as rp
+    from relative_position_representations_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    x = wl.draw_inputs(w, seed=args.seed + rank)
+    kv_len = None if x.get("kv_len") is None else x["kv_len"].tolist()
+    flops = algorithmic_flops(w, kv_len)
+    byts = algorithmic_bytes(w, kv_len)
+
+    # rotate over enough resident input sets that the timed reads come from HBM
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    in_bytes = sum(t.numel() * t.element_size() for t in x.values() if t is not None)
+    n_sets = max(1, min(64, math.ceil(4 * l2 / max(in_bytes, 1))))
+    sets = []
+    for s in range(n_sets):
+        g = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in x.items()}
+        if s > 0:  # distinct buffers with the same values
+            g = {kk: (vv.clone() if vv is not None else None) for kk, vv in g.items()}
+        sets.append((g, torch.empty_like(g["q"])))
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    # warm-up (also sets the kernel attributes before graph capture)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):
+            g, o = sets[i % n_sets]
+            gpu_call(rp, w, g, o, stream)
+    stream.synchronize()
+
+    # one graph = one pass over all input sets, with external timing events between launches
+    probe = make_event(True)
+    use_events = probe is not None
+    graph = torch.cuda.CUDAGraph()
+    evs = [make_event(True) for _ in range(n_sets + 1)] if use_events else []
+    with torch.cuda.graph(graph, stream=stream):
+        for s in range(n_sets):
+            if use_events:
+                evs[s].record(stream)
+            g, o = sets[s]
+            gpu_call(rp, w, g, o, stream)
+        if use_events:
+            evs[n_sets].record(stream)
+    reps = max(1, math.ceil(args.steps / n_sets))
+    steps = reps * n_sets
+    with torch.cuda.stream(stream):
+        graph.replay()  # untimed replay
+    stream.synchronize()
+
+    # clocks sampled around and during the timed region, with the same launches running
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    soak_until = time.time() + 0.6
+    with torch.cuda.stream(stream):
+        while time.time() < soak_until:
+            graph.replay()
+            stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start_wall = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kernel_ms = []
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for r in range(reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_end_wall = time.time()
+    if use_events:
+        # the in-graph events hold the timestamps of the last timed replay
+        kernel_ms = [evs[s].elapsed_time(evs[s + 1]) for s in range(n_sets)]
+    if world > 1:
+        dist.barrier()
+    soak_until = time.time() + 0.6
+    with torch.cuda.stream(stream):
+        while time.time() < soak_until:
+            graph.replay()
+            stream.synchronize()
+    sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(t_start_wall - 0.6, t_end_wall + 0.6)
+    if use_events and any(m > 0 for m in kernel_ms):
+        kern_ms = statistics.mean(kernel_ms)
+        kern_src = ("cuda events between the launches of the last timed graph replay "
+                    "(%d launches)" % len(kernel_ms))
+    else:
+        kern_ms = elapsed_ms / steps
+        kern_src = "timed-region elapsed / steps (events in graphs unavailable)"
+
+    # whole-job reduction over ranks (max time, summed work)
+    import torch as _t
+    t_max = elapsed_ms
+    total_flops = flops * steps
+    if world > 1:
+        tt = _t.tensor([elapsed_ms], device=dev, dtype=_t.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+        ff = _t.tensor([total_flops], device=dev, dtype=_t.float64)
+        dist.all_reduce(ff, op=dist.ReduceOp.SUM)
+        total_flops = float(ff.item())
+    value = total_flops / (t_max * 1e-3) / 1e12
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = measure_e2e(rp, w, x, dev, stream, flops, args)
+
+    peaks, peak_src = read_peaks()
+    t_roof_compute = flops / (peaks["bf16_tflops"] * 1e12)
+    t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
+    if t_roof_mem >= t_roof_compute:
+        achieved = byts / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": peak_src + " (STREAM-style copy)"}
+    else:
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": peak_src + " (cuBLAS bf16 burst)"}
+    roof["traffic"] = profiled_traffic(w.name)
+    roof["kernel_ms"] = round(kern_ms, 5)
+    roof["kernel_time_source"] = kern_src
+    roof["algorithmic_flops"] = flops
+    roof["algorithmic_bytes"] = byts
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, _, _ = time_oracle(w, x, args.cpu_budget)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(t_max / steps, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
+                   "kind": w.kind, "clip_k": w.clip_k if w.kind == "shaw" else None,
+                   "causal": w.causal,
+                   "terms": ("t5 bias" if w.kind == "t5" else
+                             "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
+                                      if on) or "none"),
+                   "kv_len": "U{%d..%d} per sequence" % w.kv_len_range if w.kv_len_range else None,
+                   "parallelism": "dp%d (independent shards, no collective)" % world,
+                   "l2": "inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > "
+                         "4 x %.0f MB L2), replayed from a CUDA graph" % (
+                             n_sets, in_bytes / 1e6, n_sets * in_bytes / 1e6, l2 / 1e6)},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+def measure_e2e(rp, w, x, dev, stream, flops, args):
+    """Same step through the C ABI with pinned host inputs: H2D copies, launch, D2H copy."""
+    import torch
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in x.items()}
+    g = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in x.items()}
+    out = torch.empty_like(g["q"])
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k, v in host.items():
+            if v is not None:
+                g[k].copy_(v, non_blocking=True)
+        gpu_call(rp, w, g, out, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    n = max(5, min(200, args.steps))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(flops / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 5), "steps": n}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, on bounded samples of the workload."""
+    from relative_position_representations_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    x = wl.draw_inputs(w, seed=args.seed)
+    per_step = max(1.0, args.ref_budget / max(1, args.steps + args.warmup))
+    for i in range(args.warmup):
+        time_oracle(w, x, min(per_step, 2.0), seed=100 + i)
+    tot_fl, tot_dt, last = 0.0, 0.0, None
+    for i in range(args.steps):
+        last, fl, dt = time_oracle(w, x, per_step, seed=1 + i)
+        tot_fl += fl
+        tot_dt += dt
+    value = tot_fl / tot_dt / 1e12
+    cpu = dict(last)
+    cpu["value"] = round(value, 6)
+    cpu["sample"] = "each step: " + last["sample"]
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="total seconds of oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

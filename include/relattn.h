@@ -1,0 +1,144 @@
+/*
+ * relattn — relation-aware self-attention forward for GB300 (sm_103a), C ABI.
+ *
+ * Method: Shaw, Uszkoreit & Vaswani, "Self-Attention with Relative Position
+ * Representations" (paper summary page, section 3.4: eq. 3 for the output, eq. 4 for the
+ * compatibility, clip(j - i, k) and the 2k+1 edge vectors w_{-k}..w_{k}; section
+ * "Efficient Implementation" for the eq. 5 split). T5 variant: "Relative position
+ * embeddings" page, section "T5".
+ *
+ * Conventions shared by every entry point
+ *   - Tensors q, k, v, out are [B, H, n, d], contiguous, d fastest (row-major).
+ *   - Every tensor pointer is caller-owned DEVICE memory, 16-byte aligned. The library
+ *     never allocates, frees or keeps a pointer after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Nothing is synchronised; there is no CPU fallback.
+ *   - Arguments are validated on the host before any launch: a bad argument returns
+ *     RELATTN_ERR_INVALID_ARG, a valid but unimplemented combination returns
+ *     RELATTN_ERR_UNSUPPORTED, and a failed launch returns RELATTN_ERR_CUDA. In all three
+ *     cases nothing was enqueued.
+ *   - Device-side waits are bounded (about one second); a wait that runs out records
+ *     RELATTN_ERR_TIMEOUT in a device status word, which relattn_get_device_error reads.
+ */
+#ifndef RELATTN_H
+#define RELATTN_H
+
+#if defined(__GNUC__)
+#define RELATTN_API __attribute__((visibility("default")))
+#else
+#define RELATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RELATTN_OK = 0,
+    RELATTN_ERR_INVALID_ARG = 1,
+    RELATTN_ERR_UNSUPPORTED = 2,
+    RELATTN_ERR_CUDA = 3,
+    RELATTN_ERR_TIMEOUT = 4
+} relattn_status_t;
+
+/* Element type of q, k, v, the Shaw tables and out. */
+typedef enum {
+    RELATTN_BF16 = 0, /* tcgen05 tensor-core path: d in {64, 128} */
+    RELATTN_F32 = 1   /* fp32 SIMT path: 1 <= d <= 128 */
+} relattn_dtype_t;
+
+struct CUstream_st;
+typedef struct CUstream_st *relattn_stream_t; /* same type as cudaStream_t */
+
+/*
+ * relattn_fwd — Shaw relation-aware self-attention forward (eq. 3 and eq. 4).
+ *
+ *   e_ij = scale * q_i . (k_j + aK[h][clip(j - i, clip_k) + clip_k])
+ *   z_i  = sum_j softmax_j(e)_ij * (v_j + aV[h][clip(j - i, clip_k) + clip_k])
+ *
+ * over the allowed keys j: j < kv_len[b] (all j when kv_len is NULL) and, if causal,
+ * j <= i. A row with no allowed key is written as zeros.
+ *
+ *   q, k, v           [B, H, n, d] of `dtype`.
+ *   aK, aV            edge tables [*, 2*clip_k + 1, d] of `dtype`, row r holding
+ *                     w_{r - clip_k} (row 0 = w_{-k}). NULL drops that term (aV NULL is
+ *                     the key-only mode; both NULL is plain attention).
+ *   table_head_stride elements between consecutive heads' tables; 0 = one table shared
+ *                     by all heads. Otherwise >= (2*clip_k + 1) * d and, for bf16, a
+ *                     multiple of 8.
+ *   clip_k            clipping distance k >= 0.
+ *   causal            0 or 1.
+ *   scale             multiplies the whole compatibility (content and edge terms);
+ *                     1/sqrt(d) in the paper.
+ *   kv_len            [B] int32 device array of key lengths, or NULL.
+ *   out               [B, H, n, d] of `dtype`; must not alias an input.
+ *
+ * bf16 limits (else RELATTN_ERR_UNSUPPORTED): the staged table rows (clip_k + 1 when
+ * causal, else 2*clip_k + 1) must be <= 128.
+ */
+RELATTN_API relattn_status_t relattn_fwd(const void *q, const void *k, const void *v,
+                             const void *aK, const void *aV, long long table_head_stride,
+                             int clip_k, int causal, float scale, const int *kv_len,
+                             int B, int H, int n, int d, int dtype,
+                             void *out, relattn_stream_t stream);
+
+/*
+ * relattn_t5bias_fwd — T5 scalar bucketed relative bias ("Relative position embeddings",
+ * section "T5"):
+ *
+ *   e_ij = scale * q_i . k_j + bias[bucket(j - i) * H + h]
+ *
+ * softmax and output as above (no edge vector on the values). bias is a [num_buckets, H]
+ * fp32 device array. bucket(): bidirectional splits the buckets into two halves of
+ * num_buckets/2, one per sign (j - i > 0 takes the upper half), each exact below
+ * half/2 and logarithmic up to max_distance, clamped to the half's last bucket;
+ * unidirectional uses one half of num_buckets on max(i - j, 0). The floor in the
+ * logarithmic part is exact (integer arithmetic on the host). T5 itself uses scale = 1.
+ *
+ * Requires 4 <= num_buckets <= 256 (bidirectional) or 2 <= num_buckets <= 256, and
+ * max_distance greater than the exact range, else RELATTN_ERR_INVALID_ARG.
+ */
+RELATTN_API relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
+                                    const float *bias, int num_buckets, int max_distance,
+                                    int bidirectional, int causal, float scale,
+                                    const int *kv_len, int B, int H, int n, int d, int dtype,
+                                    void *out, relattn_stream_t stream);
+
+/*
+ * relattn_labels — the integer edge label of every (i, j), computed by the same device
+ * functions the attention kernels use, written as int32 labels[i * n_k + j].
+ *   kind 0: clip row clip(j - i, clip_k) + clip_k (paper summary, section 3.4).
+ *   kind 1: T5 bucket(j - i) with (num_buckets, max_distance, bidirectional).
+ * labels is caller-owned device memory of n_q * n_k int32.
+ */
+RELATTN_API relattn_status_t relattn_labels(int kind, int clip_k, int num_buckets, int max_distance,
+                                int bidirectional, int n_q, int n_k, int *labels,
+                                relattn_stream_t stream);
+
+/*
+ * relattn_t5_thresholds — host only, no GPU needed. Writes the exact first distance a of
+ * each logarithmic T5 bucket (buckets exact+1 .. half-1 of one half) into
+ * thresholds[0 .. *count - 1]; capacity is the array length.
+ */
+RELATTN_API relattn_status_t relattn_t5_thresholds(int num_buckets, int max_distance, int bidirectional,
+                                       int *thresholds, int capacity, int *count);
+
+/*
+ * relattn_get_device_error — synchronises `stream`, then reads and clears the device
+ * status word of the current device: RELATTN_OK, or RELATTN_ERR_TIMEOUT if a bounded
+ * device wait ran out since the last call. RELATTN_ERR_CUDA if the stream reports an
+ * error.
+ */
+RELATTN_API relattn_status_t relattn_get_device_error(relattn_stream_t stream);
+
+/* Static English text for a status code. */
+RELATTN_API const char *relattn_status_string(relattn_status_t s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+RELATTN_API int relattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RELATTN_H */

@@ -1,0 +1,22 @@
+"""relation-aware self-attention forward on GB300 (sm_103a).
+
+The compute lives in librelattn.so (C ABI, include/relattn.h); this package holds its
+ctypes binding (`_lib`), the in-tree build script (`build`) and the named workloads with
+their seeded input generator (`workloads`). The binding is imported lazily so that
+`workloads` can be used without the compiled library; touching a binding function when
+the library is not built raises ImportError.
+"""
+from __future__ import annotations
+
+_BINDING = ("relattn_fwd", "relattn_t5bias_fwd", "relattn_labels", "relattn_t5_thresholds",
+            "relattn_get_device_error", "relattn_status_string", "relattn_version",
+            "RelattnError")
+
+__all__ = list(_BINDING)
+
+
+def __getattr__(name):
+    if name in _BINDING:
+        from . import _lib
+        return getattr(_lib, name)
+    raise AttributeError(name)

@@ -1,0 +1,199 @@
+"""ctypes binding of librelattn.so — argument marshalling only.
+
+Each function has the name of the C entry point it calls (include/relattn.h). Tensors are
+torch CUDA tensors (torch is used for device memory and streams only): the binding checks
+device, dtype, shape and contiguity, passes raw pointers and the current CUDA stream, and
+raises RelattnError on a non-OK status. Every step of the computation runs in the
+library's kernels; if the library is missing this module raises at import time.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librelattn.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+BF16, F32 = 0, 1
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("librelattn.so is not built (%s); run `python -c \"import __graft_entry__ "
+                      "as g; g.build()\"` first" % LIB_PATH)
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_lib.relattn_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, _I, ctypes.c_float, _P,
+                             _I, _I, _I, _I, _I, _P, _P]
+_lib.relattn_fwd.restype = _I
+_lib.relattn_t5bias_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I,
+                                    _I, _I, _I, _P, _P]
+_lib.relattn_t5bias_fwd.restype = _I
+_lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
+_lib.relattn_labels.restype = _I
+_lib.relattn_t5_thresholds.argtypes = [_I, _I, _I, ctypes.POINTER(_I), _I, ctypes.POINTER(_I)]
+_lib.relattn_t5_thresholds.restype = _I
+_lib.relattn_get_device_error.argtypes = [_P]
+_lib.relattn_get_device_error.restype = _I
+_lib.relattn_status_string.argtypes = [_I]
+_lib.relattn_status_string.restype = ctypes.c_char_p
+_lib.relattn_version.argtypes = []
+_lib.relattn_version.restype = _I
+
+EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_labels", "relattn_t5_thresholds",
+            "relattn_get_device_error", "relattn_status_string", "relattn_version"]
+
+
+class RelattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, relattn_status_string(status), status))
+
+
+def relattn_status_string(status: int) -> str:
+    return _lib.relattn_status_string(int(status)).decode()
+
+
+def relattn_version() -> int:
+    return int(_lib.relattn_version())
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise RelattnError(status, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _qkv(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name, q.dtype)
+        if t.dim() != 4 or t.shape != q.shape:
+            raise ValueError("%s must be [B, H, n, d] like q" % name)
+    return q.shape
+
+
+def relattn_fwd(q, k, v, aK=None, aV=None, clip_k=0, causal=False, scale=None, kv_len=None,
+                out=None, table_head_stride=None, stream=None):
+    """Shaw relation-aware attention forward (paper summary page, section 3.4, eqs. 3-4).
+
+    q, k, v: [B, H, n, d] bf16 or fp32 CUDA tensors. aK / aV: [H or 1, 2*clip_k+1, d]
+    (None drops the term). kv_len: [B] int32 CUDA tensor or None. Returns out.
+    """
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    W = 2 * int(clip_k) + 1
+    for name, t in (("aK", aK), ("aV", aV)):
+        if t is not None:
+            _dev(t, name, q.dtype)
+            if t.dim() != 3 or t.shape[1] != W or t.shape[2] != d or t.shape[0] not in (1, H):
+                raise ValueError("%s must be [H or 1, 2*clip_k+1, d]" % name)
+    if table_head_stride is None:
+        ref = aK if aK is not None else aV
+        table_head_stride = 0 if (ref is None or ref.shape[0] == 1) else W * d
+    _dev(kv_len, "kv_len", torch.int32)
+    if kv_len is not None and kv_len.numel() != B:
+        raise ValueError("kv_len must have B entries")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(aK), _ptr(aV), int(table_head_stride),
+                          int(clip_k), int(bool(causal)), float(scale), _ptr(kv_len), B, H, n, d,
+                          dt, _ptr(out), _stream(stream))
+    _check(st, "relattn_fwd")
+    return out
+
+
+def relattn_t5bias_fwd(q, k, v, bias, num_buckets=32, max_distance=128, bidirectional=True,
+                       causal=False, scale=1.0, kv_len=None, out=None, stream=None):
+    """T5 scalar bucketed-bias attention ("Relative position embeddings", section "T5").
+
+    bias: [num_buckets, H] fp32 CUDA tensor. Returns out.
+    """
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    _dev(bias, "bias", torch.float32)
+    if bias.shape != (num_buckets, H):
+        raise ValueError("bias must be [num_buckets, H]")
+    _dev(kv_len, "kv_len", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    st = _lib.relattn_t5bias_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), int(num_buckets),
+                                 int(max_distance), int(bool(bidirectional)), int(bool(causal)),
+                                 float(scale), _ptr(kv_len), B, H, n, d, dt, _ptr(out),
+                                 _stream(stream))
+    _check(st, "relattn_t5bias_fwd")
+    return out
+
+
+def relattn_labels(kind, n_q, n_k, clip_k=0, num_buckets=32, max_distance=128,
+                   bidirectional=True, out=None, stream=None, device=None):
+    """Edge label of every (i, j) from the device index functions: int32 [n_q, n_k].
+
+    kind "clip": clip(j - i, clip_k) + clip_k. kind "t5": T5 bucket(j - i).
+    """
+    code = {"clip": 0, "t5": 1}[kind]
+    if out is None:
+        out = torch.empty((n_q, n_k), dtype=torch.int32,
+                          device=device or torch.device("cuda", torch.cuda.current_device()))
+    _dev(out, "out", torch.int32)
+    st = _lib.relattn_labels(code, int(clip_k), int(num_buckets), int(max_distance),
+                             int(bool(bidirectional)), int(n_q), int(n_k), _ptr(out),
+                             _stream(stream))
+    _check(st, "relattn_labels")
+    return out
+
+
+def relattn_t5_thresholds(num_buckets=32, max_distance=128, bidirectional=True):
+    """First distance of each logarithmic T5 bucket of one half (host computation)."""
+    cap = 256
+    arr = (_I * cap)()
+    cnt = _I(0)
+    st = _lib.relattn_t5_thresholds(int(num_buckets), int(max_distance), int(bool(bidirectional)),
+                                    arr, cap, ctypes.byref(cnt))
+    _check(st, "relattn_t5_thresholds")
+    return [arr[i] for i in range(cnt.value)]
+
+
+def relattn_get_device_error(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return int(_lib.relattn_get_device_error(_stream(stream)))
+
+
+def raw_call(name, *args):
+    """Call an exported C function directly with ctypes arguments (tests of the ABI)."""
+    return getattr(_lib, name)(*args)

@@ -1,0 +1,236 @@
+// Public C ABI of librelattn.so (declared in include/relattn.h): argument validation,
+// dispatch to the fp32 SIMT path or the bf16 tcgen05 path, device status word.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/relattn.h"
+#include "relattn_internal.h"
+
+namespace {
+
+// device status word: bounded waits that run out record RELATTN_ERR_TIMEOUT here
+__device__ int g_status_word;
+
+int *status_word_for_current_device() {
+    static int *addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<int *>(p);
+    }
+    return addr[dev];
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// compute capability of the current device (major*10 + minor), or -1
+int current_cc() {
+    int dev = 0, ma = 0, mi = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return -1;
+    return ma * 10 + mi;
+}
+
+relattn_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return RELATTN_OK;
+    if (e == cudaErrorNotSupported) return RELATTN_ERR_UNSUPPORTED;
+    cudaGetLastError();  // do not leave a launch-configuration error sticky for the caller
+    return RELATTN_ERR_CUDA;
+}
+
+bool shapes_ok(int B, int H, int n, int d) {
+    if (B < 1 || H < 1 || n < 1 || d < 1) return false;
+    const long long total = (long long)B * H * n;
+    return total <= (1LL << 31) - 1 && (long long)B * H <= (1LL << 31) - 1;
+}
+
+// common checks of q, k, v, out
+relattn_status_t check_qkv(const void *q, const void *k, const void *v, const void *out, int B,
+                           int H, int n, int d, int dtype) {
+    if (!q || !k || !v || !out) return RELATTN_ERR_INVALID_ARG;
+    if (!shapes_ok(B, H, n, d)) return RELATTN_ERR_INVALID_ARG;
+    if (out == q || out == k || out == v) return RELATTN_ERR_INVALID_ARG;
+    if (dtype == RELATTN_BF16) {
+        if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+            return RELATTN_ERR_INVALID_ARG;
+        if (d != 64 && d != 128) return RELATTN_ERR_UNSUPPORTED;
+    } else if (dtype == RELATTN_F32) {
+        if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4))
+            return RELATTN_ERR_INVALID_ARG;
+        if (d > 128) return RELATTN_ERR_UNSUPPORTED;
+    } else {
+        return RELATTN_ERR_INVALID_ARG;
+    }
+    return RELATTN_OK;
+}
+
+relattn_status_t dispatch_bf16(const relattn::TcArgs &a, const relattn::T5Buckets *t5,
+                               cudaStream_t s) {
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    int *err = status_word_for_current_device();
+    if (!err) return RELATTN_ERR_CUDA;
+    const cudaError_t e = a.d == 64 ? relattn::launch_tc_bf16_d64(a, t5, err, s)
+                                    : relattn::launch_tc_bf16_d128(a, t5, err, s);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+relattn_status_t relattn_fwd(const void *q, const void *k, const void *v, const void *aK,
+                             const void *aV, long long table_head_stride, int clip_k, int causal,
+                             float scale, const int *kv_len, int B, int H, int n, int d, int dtype,
+                             void *out, relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, out, B, H, n, d, dtype);
+    if (st != RELATTN_OK) return st;
+    if (clip_k < 0 || (causal != 0 && causal != 1)) return RELATTN_ERR_INVALID_ARG;
+    if (clip_k > (1 << 20)) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    if (aK || aV) {
+        const long long rows_d = (2LL * clip_k + 1) * d;
+        if (table_head_stride != 0 && table_head_stride < rows_d) return RELATTN_ERR_INVALID_ARG;
+        if (out == aK || out == aV) return RELATTN_ERR_INVALID_ARG;
+        const uintptr_t al = dtype == RELATTN_BF16 ? 16 : 4;
+        if ((aK && !aligned(aK, al)) || (aV && !aligned(aV, al))) return RELATTN_ERR_INVALID_ARG;
+        if (dtype == RELATTN_BF16 && (table_head_stride % 8) != 0) return RELATTN_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == RELATTN_F32) {
+        relattn::SimtArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.aK = static_cast<const float *>(aK);
+        a.aV = static_cast<const float *>(aV);
+        a.ths = table_head_stride;
+        a.clip_k = clip_k;
+        a.causal = causal;
+        a.scale = scale;
+        a.kv_len = kv_len;
+        a.bias = nullptr;
+        a.B = B; a.H = H; a.n = n; a.d = d;
+        a.out = static_cast<float *>(out);
+        return from_cuda(relattn::launch_simt_f32(a, nullptr, s));
+    }
+    relattn::TcArgs a{};
+    a.q = q; a.k = k; a.v = v; a.aK = aK; a.aV = aV;
+    a.ths = table_head_stride;
+    a.clip_k = clip_k;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.bias = nullptr;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.out = out;
+    a.mode = relattn::kShaw;
+    return dispatch_bf16(a, nullptr, s);
+}
+
+relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
+                                    const float *bias, int num_buckets, int max_distance,
+                                    int bidirectional, int causal, float scale,
+                                    const int *kv_len, int B, int H, int n, int d, int dtype,
+                                    void *out, relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, out, B, H, n, d, dtype);
+    if (st != RELATTN_OK) return st;
+    if (!bias || !aligned(bias, 4)) return RELATTN_ERR_INVALID_ARG;
+    if ((causal != 0 && causal != 1) || (bidirectional != 0 && bidirectional != 1))
+        return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    relattn::T5Buckets t5{};
+    if (!relattn::t5_make_buckets(num_buckets, max_distance, bidirectional, &t5))
+        return RELATTN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == RELATTN_F32) {
+        relattn::SimtArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.causal = causal;
+        a.scale = scale;
+        a.kv_len = kv_len;
+        a.bias = bias;
+        a.B = B; a.H = H; a.n = n; a.d = d;
+        a.out = static_cast<float *>(out);
+        return from_cuda(relattn::launch_simt_f32(a, &t5, s));
+    }
+    relattn::TcArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.bias = bias;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.out = out;
+    a.mode = relattn::kT5;
+    return dispatch_bf16(a, &t5, s);
+}
+
+relattn_status_t relattn_labels(int kind, int clip_k, int num_buckets, int max_distance,
+                                int bidirectional, int n_q, int n_k, int *labels,
+                                relattn_stream_t stream) {
+    if (!labels || !aligned(labels, 4) || n_q < 0 || n_k < 0) return RELATTN_ERR_INVALID_ARG;
+    if ((long long)n_q * n_k > (1LL << 40)) return RELATTN_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kind == 0) {
+        if (clip_k < 0) return RELATTN_ERR_INVALID_ARG;
+        return from_cuda(relattn::launch_labels(0, clip_k, nullptr, n_q, n_k, labels, s));
+    }
+    if (kind == 1) {
+        relattn::T5Buckets t5{};
+        if (!relattn::t5_make_buckets(num_buckets, max_distance, bidirectional ? 1 : 0, &t5))
+            return RELATTN_ERR_INVALID_ARG;
+        return from_cuda(relattn::launch_labels(1, 0, &t5, n_q, n_k, labels, s));
+    }
+    return RELATTN_ERR_INVALID_ARG;
+}
+
+relattn_status_t relattn_t5_thresholds(int num_buckets, int max_distance, int bidirectional,
+                                       int *thresholds, int capacity, int *count) {
+    if (!count) return RELATTN_ERR_INVALID_ARG;
+    relattn::T5Buckets t5{};
+    if (!relattn::t5_make_buckets(num_buckets, max_distance, bidirectional ? 1 : 0, &t5))
+        return RELATTN_ERR_INVALID_ARG;
+    *count = t5.nthr;
+    if (t5.nthr > 0 && (!thresholds || capacity < t5.nthr)) return RELATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < t5.nthr; ++i) thresholds[i] = t5.thr[i];
+    return RELATTN_OK;
+}
+
+relattn_status_t relattn_get_device_error(relattn_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RELATTN_ERR_CUDA;
+    int *w = status_word_for_current_device();
+    if (!w) return RELATTN_ERR_CUDA;
+    int host = 0;
+    if (cudaMemcpyAsync(&host, w, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return RELATTN_ERR_CUDA;
+    if (cudaMemsetAsync(w, 0, sizeof(int), s) != cudaSuccess) return RELATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return RELATTN_ERR_CUDA;
+    return host == 0 ? RELATTN_OK : static_cast<relattn_status_t>(host);
+}
+
+const char *relattn_status_string(relattn_status_t s) {
+    switch (s) {
+        case RELATTN_OK: return "ok";
+        case RELATTN_ERR_INVALID_ARG: return "invalid argument";
+        case RELATTN_ERR_UNSUPPORTED: return "unsupported combination";
+        case RELATTN_ERR_CUDA: return "CUDA error";
+        case RELATTN_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int relattn_version(void) { return 100; }
+
+}  // extern "C"

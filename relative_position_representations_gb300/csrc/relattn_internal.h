@@ -1,0 +1,66 @@
+// Internal declarations shared by the translation units of librelattn.so.
+// Nothing here is part of the public C ABI (include/relattn.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace relattn {
+
+constexpr int kMaxT5Thresholds = 128;
+
+// Exact T5 bucketing parameters; thr[m] is the first distance a of bucket exact+1+m.
+struct T5Buckets {
+    int half;      // buckets per sign half (num_buckets/2 bidirectional, num_buckets otherwise)
+    int exact;     // half/2: distances below this map to themselves
+    int bidir;     // 1: j - i > 0 takes the upper half
+    int nthr;      // half - 1 - exact
+    int sat;       // first distance whose bucket is the clamp value (the table radius)
+    int thr[kMaxT5Thresholds];
+};
+
+// Host: fills b from (num_buckets, max_distance, bidirectional); returns false on
+// invalid parameters. Exact integer arithmetic.
+bool t5_make_buckets(int num_buckets, int max_distance, int bidirectional, T5Buckets *b);
+
+// Device status word (one per device), set by bounded waits that run out.
+int *device_error_word();  // device address of the word for the current device, or null
+
+// ---- fp32 SIMT path --------------------------------------------------------------------
+struct SimtArgs {
+    const float *q, *k, *v, *aK, *aV;
+    long long ths;
+    int clip_k, causal;
+    float scale;
+    const int *kv_len;
+    const float *bias;  // T5 [nb, H] or null
+    int B, H, n, d;
+    float *out;
+};
+cudaError_t launch_simt_f32(const SimtArgs &a, const T5Buckets *t5, cudaStream_t s);
+
+// ---- label kernel ----------------------------------------------------------------------
+cudaError_t launch_labels(int kind, int clip_k, const T5Buckets *t5, int n_q, int n_k,
+                          int *labels, cudaStream_t s);
+
+// ---- bf16 tcgen05 path -------------------------------------------------------------------
+enum Mode : int { kShaw = 0, kT5 = 1 };
+
+struct TcArgs {
+    const void *q, *k, *v, *aK, *aV;
+    long long ths;
+    int clip_k, causal;
+    float scale;
+    const int *kv_len;
+    const float *bias;
+    int B, H, n, d;
+    void *out;
+    int mode;
+};
+// Returns cudaErrorNotSupported for combinations the kernel does not cover (checked
+// before any launch), cudaErrorInvalidValue for bad tensor-map parameters.
+cudaError_t launch_tc_bf16_d64(const TcArgs &a, const T5Buckets *t5, int *err, cudaStream_t s);
+cudaError_t launch_tc_bf16_d128(const TcArgs &a, const T5Buckets *t5, int *err, cudaStream_t s);
+
+}  // namespace relattn

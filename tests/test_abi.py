@@ -1,0 +1,98 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/relattn.h declares,
+and its host-only logic is right. No kernel is launched here (these run without a GPU):
+invalid arguments are rejected before any CUDA call, and the exact T5 thresholds come from
+host code."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from oracle import t5 as ot5
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from relative_position_representations_gb300 import build
+    build.build()
+    from relative_position_representations_gb300 import _lib
+    return _lib
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "relattn.h")).read()
+    return sorted(set(re.findall(r"RELATTN_API\s+[\w\s\*]+?\b(relattn_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for want in ("relattn_fwd", "relattn_t5bias_fwd", "relattn_labels", "relattn_t5_thresholds",
+                 "relattn_get_device_error", "relattn_status_string", "relattn_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(so, name), name
+    assert sorted(lib.EXPORTED) == sorted(declared_symbols())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.relattn_version() >= 100
+    assert lib.relattn_status_string(0) == "ok"
+    assert "timed out" in lib.relattn_status_string(4)
+    assert lib.relattn_status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("nb,md,bidir", [(32, 128, True), (32, 128, False), (16, 40, True),
+                                         (64, 1000, True), (8, 5, False), (4, 3, True),
+                                         (256, 100000, True), (200, 7000, False)])
+def test_host_t5_thresholds_match_oracle_buckets(lib, nb, md, bidir):
+    thr = lib.relattn_t5_thresholds(nb, md, bidir)
+    half = nb // 2 if bidir else nb
+    exact = half // 2
+    assert len(thr) == half - 1 - exact
+    sign = -1  # lower half (offsets <= 0)
+    for m, a in enumerate(thr):
+        b = exact + 1 + m
+        assert ot5.t5_bucket(sign * a, nb, md, bidir) >= b
+        assert ot5.t5_bucket(sign * (a - 1), nb, md, bidir) < b
+
+
+def test_default_thresholds_are_the_closed_form_values(lib):
+    assert lib.relattn_t5_thresholds(32, 128, True) == [12, 16, 23, 32, 46, 64, 91]
+
+
+FAKE = ctypes.c_void_p(0x100000)  # aligned, never dereferenced on the host
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, aK=None, aV=None, ths=0, clip_k=2, causal=0, scale=1.0,
+         kv=None, B=1, H=1, n=16, d=64, dtype=0, out=ctypes.c_void_p(0x200000)):
+    return lib.raw_call("relattn_fwd", q, k, v, aK, aV, ctypes.c_longlong(ths), clip_k, causal,
+                        ctypes.c_float(scale), kv, B, H, n, d, dtype, out, None)
+
+
+def test_invalid_arguments_rejected_before_any_launch(lib):
+    assert _fwd(lib, q=None) == 1
+    assert _fwd(lib, out=FAKE) == 1                      # aliases q
+    assert _fwd(lib, B=0) == 1
+    assert _fwd(lib, clip_k=-1) == 1
+    assert _fwd(lib, causal=2) == 1
+    assert _fwd(lib, dtype=7) == 1
+    assert _fwd(lib, q=ctypes.c_void_p(0x100008)) == 1   # bf16 needs 16-byte alignment
+    assert _fwd(lib, d=96) == 2                          # bf16 head dims: 64 and 128
+    assert _fwd(lib, dtype=1, d=200) == 2                # fp32 path: d <= 128
+    assert _fwd(lib, aK=ctypes.c_void_p(0x300000), ths=10) == 1   # stride below the table
+    bad_t5 = lib.raw_call("relattn_t5bias_fwd", FAKE, FAKE, FAKE, ctypes.c_void_p(0x300000), 2,
+                          128, 1, 0, ctypes.c_float(1.0), None, 1, 1, 16, 64, 0,
+                          ctypes.c_void_p(0x200000), None)
+    assert bad_t5 == 1                                   # 2 buckets bidirectional: no exact range
+    bad_t5 = lib.raw_call("relattn_t5bias_fwd", FAKE, FAKE, FAKE, ctypes.c_void_p(0x300000), 32,
+                          8, 1, 0, ctypes.c_float(1.0), None, 1, 1, 16, 64, 0,
+                          ctypes.c_void_p(0x200000), None)
+    assert bad_t5 == 1                                   # max_distance inside the exact range
+    assert lib.raw_call("relattn_labels", 5, 0, 32, 128, 1, 4, 4, FAKE, None) == 1
