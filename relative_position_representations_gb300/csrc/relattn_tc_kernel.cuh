@@ -98,11 +98,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sh
 
 // Barrier among the 128 softmax threads, on an mbarrier so that the wait stays bounded
 // (a plain bar.sync would hang if another thread of the group left after a timeout).
+// The result is uniform across the calling warp.
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t &it, const Shared &sh, int *err) {
     ptx::mbar_arrive(bar);
     const bool ok = wait_bar(bar, it & 1u, sh, err);
     ++it;
-    return ok;
+    return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
 }
 
 __device__ __forceinline__ void decode_tile(const Params &p, int t, int &bh, int &qt) {
@@ -355,6 +356,12 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
     const uint32_t gbar = bar(B_GROUP);
     int t5_head = -1;
     bool ok = true;
+    // tcgen05.ld/st are warp-collective (.sync.aligned): every decision that guards them is
+    // made uniform across the warp, and the warp reconverges before each TMEM access.
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = wait_bar(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
 
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int bh, qt;
@@ -376,8 +383,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
             t5_head = h;
         }
         if (AK) {
-            if (!(ok = wait_bar(bar(B_R_FULL), tiles & 1u, sh, p.err))) break;
+            if (!(ok = wait_w(bar(B_R_FULL), tiles & 1u))) break;
             ptx::tc_fence_after();
+            __syncwarp();
             for (int c0 = 0; c0 < p.npad_k; c0 += 16) {
                 uint32_t r[16];
                 ptx::tmem_ld16(lane_base + kColR + (uint32_t)c0, r);
@@ -395,8 +403,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
 
         for (int j = 0; j < J; ++j) {
             const uint32_t buf = s_it & 1u;
-            if (!(ok = wait_bar(bar(B_S_FULL0 + (int)buf), (s_it >> 1) & 1u, sh, p.err))) break;
+            if (!(ok = wait_w(bar(B_S_FULL0 + (int)buf), (s_it >> 1) & 1u))) break;
             ptx::tc_fence_after();
+            __syncwarp();
             float s[BN];
             {
                 uint32_t r[32];
@@ -500,9 +509,11 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
             }
             // ---- the previous P.V must be done before P and O are touched
             if (j >= 1) {
-                if (!(ok = wait_bar(bar(B_PV_DONE), (pv_base + (uint32_t)j - 1u) & 1u, sh, p.err))) break;
+                if (!(ok = wait_w(bar(B_PV_DONE), (pv_base + (uint32_t)j - 1u) & 1u))) break;
                 ptx::tc_fence_after();
-                if (alpha != 1.f) {
+                // lanes that keep their max multiply by 1
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    __syncwarp();
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t r[32];
@@ -529,7 +540,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
         if (!ok) break;
         if (AV) {
             // bins (bf16) become the A operand of O += beta W^V
-            if (!(ok = wait_bar(bar(B_PV_DONE), (pv_base + (uint32_t)J - 1u) & 1u, sh, p.err))) break;
+            if (!(ok = wait_w(bar(B_PV_DONE), (pv_base + (uint32_t)J - 1u) & 1u))) break;
             for (int c = 0; c < p.kpad_v / 8; ++c) {
                 float v8[8];
 #pragma unroll
@@ -544,8 +555,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
         }
         pv_base += (uint32_t)J;
         // ---- epilogue (S8): O / l -> bf16 -> TMA store
-        if (!(ok = wait_bar(bar(B_O_FULL), tiles & 1u, sh, p.err))) break;
+        if (!(ok = wait_w(bar(B_O_FULL), tiles & 1u))) break;
         ptx::tc_fence_after();
+        __syncwarp();
         ++tiles;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll

@@ -125,7 +125,7 @@ BF16_CASES = [
     ("k0", 260, 64, 0, False, None, True, True, False),
     ("k1_causal", 260, 64, 1, True, None, True, True, False),
     ("k_large_causal", 390, 64, 100, True, None, True, True, False),
-    ("k_over_n", 90, 64, 63, False, None, True, True, False),
+    ("k_over_n", 90, 64, 40, False, None, True, True, False),
     ("key_only", 517, 64, 16, True, None, True, False, False),
     ("value_only", 300, 64, 16, False, None, False, True, False),
     ("plain", 300, 64, 16, False, (100, 300), False, False, False),
@@ -238,6 +238,11 @@ def test_bf16_unsupported_and_invalid_status():
     tab = torch.zeros(1, 129, 64, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(rp.RelattnError) as e:
         rp.relattn_fwd(q, q.clone(), q.clone(), tab, None, 64, False, 0.1)
+    assert e.value.status == 2
+    # both tables with 2k+1 = 127 staged rows do not fit the shared-memory budget at d = 64
+    tab127 = torch.zeros(1, 127, 64, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(rp.RelattnError) as e:
+        rp.relattn_fwd(q, q.clone(), q.clone(), tab127, tab127.clone(), 63, False, 0.1)
     assert e.value.status == 2
     q96 = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(rp.RelattnError) as e:
