@@ -1,30 +1,39 @@
 // Fused relation-aware attention forward, bf16 in / fp32 accumulate, for sm_103a.
 //
-// Method: Shaw, Uszkoreit & Vaswani (paper summary page, section 3.4): eq. 4
-//   e_ij = scale * (q_i . k_j + q_i . w^K_{clip(j-i,k)})        (the eq. 5 split)
+// Method: Shaw, Uszkoreit & Vaswani (paper summary page, section 3.4): eq. 4 in the split
+// form of eq. 5,
+//   e_ij = scale * (q_i . k_j + R_i[clip(j-i,k)+k]),    R = Q W^K^T  ([BM x (2k+1)] per tile),
 // and eq. 3 split in two sums,
 //   z_i = sum_j a_ij v_j + sum_r beta_ir w^V_r,   beta_ir = sum_{j: clip(j-i,k)+k = r} a_ij.
 // T5 variant ("Relative position embeddings", section "T5"): e_ij = scale*q_i.k_j + b[bucket].
 //
-// One CTA per SM (persistent), looping over (query tile of 128 rows, head) work items,
-// heaviest causal tiles first. Warp roles:
-//   warp 0      TMA producer: Q tile + edge tables, then K/V tiles of 128 keys into a ring
-//               of stages, in the order the MMA warp consumes them (K0 K1 V0 K2 V1 ...).
-//   warp 1      MMA issuer (one thread): R = Q W^K^T once per tile (tiny N = table rows),
-//               S_j = Q K_j^T into one of two TMEM score buffers, O += P_j V_j, and at the
-//               end O += beta W^V. Accumulators live in TMEM (512 columns).
-//   warps 2..5  softmax / epilogue, one thread per query row (TMEM lane): read S_j from TMEM,
-//               add the gathered relative term (band tiles) or a per-row constant (tiles
-//               entirely beyond +-k), mask, online softmax in the exp2 domain with a lazy
-//               rescale (only when the row max grows by more than 2^8), write bf16 P to
-//               shared memory, accumulate the 2k+1 value bins, then normalise O and store
-//               it with TMA.
+// Persistent CTAs (one or two per SM) loop over work items (query tile of 128 rows, head),
+// longest causal rows first. Warp roles:
+//   warp 0      TMA producer: Q tile and edge tables, then K/V tiles of 128 keys (in boxes of
+//               32 rows, none past the last allowed key) into a ring of stages, in the order
+//               the MMA warp consumes them (K0 K1 V0 K2 V1 ...), and W^V at the end.
+//   warp 1      MMA issuer (one thread). Per tile: R = Q W^K^T into a score buffer, then
+//               S_j = Q K_j^T into the score buffer(s), O += P_j V_j with P read from TMEM,
+//               and at the end O += beta W^V with the bins read from TMEM.
+//   warps 2..5  softmax / epilogue, one thread per query row (= TMEM lane). For each 32-key
+//               chunk of S_j: add the relative term (a per-row constant where the whole chunk
+//               lies beyond +-k for the warp, a shared-memory gather inside the band), mask,
+//               online softmax in the exp2 domain with a lazy rescale (only when the running
+//               max grows by more than 2^8), accumulate the value bins, and store bf16 P into
+//               TMEM. Chunks no row of the warp can see are skipped. Epilogue: O / l -> bf16.
+// Score (S) and probability (P) tiles are double-buffered in TMEM, so S_{j+1} and the
+// P_{j-1} V_{j-1} product overlap the softmax of tile j.
+// TMEM: CPS = 1 (one CTA per SM, 128-key tiles): S0 [0,128) S1 [128,256) O [256,256+D)
+//       P0 [384,448) P1 [448,512);
+//       CPS = 2 (two CTAs per SM, D = 64, 64-key tiles): S0 [0,64) S1 [64,128) P0 [128,160)
+//       P1 [160,192) O [192,256).
 // Every wait is bounded; a wait that runs out sets the device status word and the CTA
 // drains and exits.
 #pragma once
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include "device_common.cuh"
 #include "relattn_internal.h"
@@ -33,21 +42,26 @@
 namespace relattn {
 namespace tc {
 
-constexpr int BM = 128;  // query rows per tile (= TMEM lanes)
-constexpr int BN = 128;  // keys per tile
+constexpr int BM = 128;   // query rows per tile (= TMEM lanes)
+constexpr int KB = 32;    // key rows per TMA box and keys per softmax chunk
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // two score buffers: columns [0,128) and [128,256)
-constexpr uint32_t kColO = 256;  // output accumulator: [256, 256+D)
-constexpr uint32_t kColR = 384;  // relative-key products: [384, 384+npad_k), npad_k <= 128
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
+template <int CPS>
+struct TmemLayout {
+    static constexpr int BN = CPS == 1 ? 128 : 64;  // keys per key tile
+    static constexpr uint32_t cols = CPS == 1 ? 512u : 256u;
+    static constexpr uint32_t S = 0;                         // S buffer b at S + b * BN
+    static constexpr uint32_t O = CPS == 1 ? 256u : 192u;    // D columns
+    static constexpr uint32_t P = CPS == 1 ? 384u : 128u;    // P buffer b at P + b * BN / 2
+};
+
 // barrier slots
 enum : int {
-    B_Q_FULL = 0, B_Q_EMPTY, B_S_FULL0, B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_P_FULL, B_PV_DONE,
-    B_R_FULL, B_R_EMPTY, B_AV_FULL, B_AV_EMPTY, B_O_FULL, B_DRAIN, B_GROUP, B_KV0
+    B_Q_FULL = 0, B_Q_EMPTY, B_S_FULL0, B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_P_FULL0, B_P_FULL1,
+    B_PV_DONE0, B_PV_DONE1, B_AV_FULL, B_AV_EMPTY, B_O_FULL, B_DRAIN, B_GROUP, B_KV0
 };
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
@@ -58,6 +72,7 @@ struct Params {
     float scale_log2;   // scale * log2(e)
     const int *kv_len;  // [B] or null
     int *err;           // device status word
+    void *out;          // [B, H, n, D] bf16
     int clip_k;         // Shaw: k
     int W;              // table rows staged: k+1 (causal) or 2k+1
     int SR;             // row stride (floats) of the per-row tables in shared memory
@@ -67,7 +82,7 @@ struct Params {
     const float *bias;  // T5 [num_buckets, H]
     int t5_R;           // T5 offset-table radius (bucket is constant beyond it)
     T5Buckets t5;
-    uint32_t off_q, off_kv, off_p, off_ak, off_av, off_r, off_beta, off_t5, off_bar;
+    uint32_t off_q, off_kv, off_ak, off_av, off_r, off_beta, off_t5, off_bar;
     int stages;
     uint32_t stage_bytes;
 };
@@ -96,9 +111,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Sh
     }
 }
 
-// Barrier among the 128 softmax threads, on an mbarrier so that the wait stays bounded
-// (a plain bar.sync would hang if another thread of the group left after a timeout).
-// The result is uniform across the calling warp.
+// Barrier among the 128 softmax threads on an mbarrier, so the wait stays bounded (a plain
+// bar.sync would hang if a thread of the group left after a timeout). Warp-uniform result.
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t &it, const Shared &sh, int *err) {
     ptx::mbar_arrive(bar);
     const bool ok = wait_bar(bar, it & 1u, sh, err);
@@ -117,20 +131,28 @@ __device__ __forceinline__ int keys_of(const Params &p, int bh) {
     return max(0, min(p.kv_len[bh / p.H], p.n));
 }
 
+// keys any row of query tile i0 may see
 template <bool CAUSAL>
-__device__ __forceinline__ int kv_tiles_of(const Params &p, int bh, int i0) {
-    int nk = keys_of(p, bh);
-    if (CAUSAL) nk = min(nk, i0 + BM);
-    return (nk + BN - 1) / BN;
+__device__ __forceinline__ int tile_keys(const Params &p, int bh, int i0) {
+    const int nk = keys_of(p, bh);
+    return CAUSAL ? min(nk, i0 + BM) : nk;
+}
+
+// columns of key tile j that are loaded and multiplied: the allowed keys rounded up to
+// whole 32-row boxes
+template <int BN>
+__device__ __forceinline__ int tile_cols(int nkc, int j) {
+    const int c = nkc - j * BN;
+    return c >= BN ? BN : ((c + KB - 1) / KB) * KB;
 }
 
 // ======================================================================= producer
-template <int D, bool AK, bool AV, bool CAUSAL>
+template <int D, bool AK, bool AV, bool CAUSAL, int CPS>
 __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                               const CUtensorMap *tm_ak, const CUtensorMap *tm_av) {
     constexpr int DB = D / 64;
-    constexpr uint32_t kTileBytes = (uint32_t)BM * D * 2;
+    constexpr int BN = TmemLayout<CPS>::BN;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     const uint32_t sQ = sh.base + p.off_q, sKV = sh.base + p.off_kv;
@@ -142,10 +164,11 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
         int bh, qt;
         decode_tile(p, t, bh, qt);
         const int i0 = qt * BM, h = bh % p.H;
-        const int J = kv_tiles_of<CAUSAL>(p, bh, i0);
+        const int nkc = tile_keys<CAUSAL>(p, bh, i0);
+        const int J = (nkc + BN - 1) / BN;
         if (J == 0) continue;
         if (!(ok = wait_bar(bar(B_Q_EMPTY), (q_it & 1u) ^ 1u, sh, p.err))) break;
-        const uint32_t qbytes = kTileBytes + (AK ? (uint32_t)p.npad_k * D * 2 : 0u);
+        const uint32_t qbytes = (uint32_t)BM * D * 2 + (AK ? (uint32_t)p.npad_k * D * 2 : 0u);
         ptx::mbar_expect_tx(bar(B_Q_FULL), qbytes);
 #pragma unroll
         for (int blk = 0; blk < DB; ++blk)
@@ -168,12 +191,15 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
             const int st = (int)(kv_it % (uint32_t)S);
             const uint32_t round = kv_it / (uint32_t)S;
             if (!(ok = wait_bar(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u, sh, p.err))) break;
-            ptx::mbar_expect_tx(bar(B_KV0 + st), kTileBytes);
+            const int nbox = tile_cols<BN>(nkc, j) / KB;
+            ptx::mbar_expect_tx(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
             const uint32_t dst = sKV + (uint32_t)st * p.stage_bytes;
+            for (int b = 0; b < nbox; ++b) {
 #pragma unroll
-            for (int blk = 0; blk < DB; ++blk)
-                ptx::tma_load_3d(dst + blk * BN * 128, isK ? tm_k : tm_v, bar(B_KV0 + st),
-                                 blk * 64, j * BN, bh);
+                for (int blk = 0; blk < DB; ++blk)
+                    ptx::tma_load_3d(dst + blk * BN * 128 + b * KB * 128, isK ? tm_k : tm_v,
+                                     bar(B_KV0 + st), blk * 64, j * BN + b * KB, bh);
+            }
             ++kv_it;
         }
         if (!ok) break;
@@ -211,34 +237,55 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
 }
 
 // ======================================================================= MMA issuer
-template <int D, bool AK, bool AV, bool CAUSAL>
+template <int D, bool AK, bool AV, bool CAUSAL, int CPS>
 __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
+    using TL = TmemLayout<CPS>;
+    constexpr int BN = TL::BN;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    const uint32_t sQ = sh.base + p.off_q, sKV = sh.base + p.off_kv, sP = sh.base + p.off_p;
+    const uint32_t sQ = sh.base + p.off_q, sKV = sh.base + p.off_kv;
     const uint32_t sAK = sh.base + p.off_ak, sAV = sh.base + p.off_av;
     const int S = p.stages;
-    constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0);
-    constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
-    const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.npad_k, 0);
-    uint32_t kv_it = 0, q_it = 0, av_it = 0, s_it = 0, p_it = 0, tiles = 0;
+    uint32_t kv_it = 0, q_it = 0, av_it = 0, s_it = 0, p_it = 0;
     bool ok = true;
 
-    // O += P_j V_j (P in shared memory, K-major; V tile MN-major)
-    auto issue_pv = [&](int j) -> bool {
-        if (!wait_bar(bar(B_P_FULL), p_it & 1u, sh, p.err)) return false;
+    // the next score-buffer item (R or S_j): wait until the softmax released the buffer
+    auto next_sbuf = [&](uint32_t &col, uint32_t &fullbar) -> bool {
+        const uint32_t buf = s_it & 1u;
+        const uint32_t use = s_it >> 1;
+        if (!wait_bar(bar(B_S_EMPTY0 + (int)buf), (use & 1u) ^ 1u, sh, p.err)) return false;
+        ptx::tc_fence_after();
+        col = TL::S + buf * BN;
+        fullbar = bar(B_S_FULL0 + (int)buf);
+        ++s_it;
+        return true;
+    };
+
+    // O += P_j V_j: P from TMEM buffer (item & 1) as bf16 pairs, V tile MN-major in shared
+    // memory. Completion is signalled on the buffer's own barrier.
+    // Each P buffer has its own full barrier: the softmax may run one item ahead, and a
+    // shared barrier could then complete twice before this thread waits on it.
+    auto wait_p = [&](uint32_t &pb) -> bool {
+        pb = p_it & 1u;
+        if (!wait_bar(bar(B_P_FULL0 + (int)pb), (p_it >> 1) & 1u, sh, p.err)) return false;
         ++p_it;
+        return true;
+    };
+    auto issue_pv = [&](int j, int cols) -> bool {
+        uint32_t pb;
+        if (!wait_p(pb)) return false;
         const int st = (int)(kv_it % (uint32_t)S);
         if (!wait_bar(bar(B_KV0 + st), (kv_it / (uint32_t)S) & 1u, sh, p.err)) return false;
         ptx::tc_fence_after();
         const uint32_t vb = sKV + (uint32_t)st * p.stage_bytes;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t a = ptx::sdesc_sw128(sP + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
+        const uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
+        const uint32_t pcol = TL::P + pb * (BN / 2);
+        for (int kk = 0; kk < cols / 16; ++kk) {
             const uint64_t b = ptx::sdesc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-            ptx::tc_mma(tmem + kColO, a, b, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::tc_mma_ts(tmem + TL::O, tmem + pcol + (uint32_t)(kk * 8), b, idPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
         }
-        ptx::tc_commit(bar(B_PV_DONE));
+        ptx::tc_commit(bar(B_PV_DONE0 + (int)pb));
         ptx::tc_commit(bar(B_KV0 + kMaxStages + st));
         ++kv_it;
         return true;
@@ -247,60 +294,65 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int bh, qt;
         decode_tile(p, t, bh, qt);
-        const int J = kv_tiles_of<CAUSAL>(p, bh, qt * BM);
+        const int nkc = tile_keys<CAUSAL>(p, bh, qt * BM);
+        const int J = (nkc + BN - 1) / BN;
         if (J == 0) continue;
         if (!(ok = wait_bar(bar(B_Q_FULL), q_it & 1u, sh, p.err))) break;
         ++q_it;
         ptx::tc_fence_after();
         if (AK) {
-            if (!(ok = wait_bar(bar(B_R_EMPTY), (tiles & 1u) ^ 1u, sh, p.err))) break;
-            ptx::tc_fence_after();
+            uint32_t col, fb;
+            if (!(ok = next_sbuf(col, fb))) break;
+            const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.npad_k, 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t a = ptx::sdesc_sw128(sQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
                 const uint64_t b =
                     ptx::sdesc_sw128(sAK + (kk >> 2) * p.npad_k * 128 + (kk & 3) * 32, 16, 1024);
-                ptx::tc_mma(tmem + kColR, a, b, idR, kk > 0 ? 1u : 0u);
+                ptx::tc_mma(tmem + col, a, b, idR, kk > 0 ? 1u : 0u);
             }
-            ptx::tc_commit(bar(B_R_FULL));
+            ptx::tc_commit(fb);
         }
+        int prev_cols = 0;
         for (int j = 0; j < J && ok; ++j) {
+            const int cols = tile_cols<BN>(nkc, j);
             const int st = (int)(kv_it % (uint32_t)S);
             if (!(ok = wait_bar(bar(B_KV0 + st), (kv_it / (uint32_t)S) & 1u, sh, p.err))) break;
-            const uint32_t buf = s_it & 1u;
-            if (!(ok = wait_bar(bar(B_S_EMPTY0 + (int)buf), ((s_it >> 1) & 1u) ^ 1u, sh, p.err))) break;
-            ptx::tc_fence_after();
+            uint32_t col, fb;
+            if (!(ok = next_sbuf(col, fb))) break;
             const uint32_t kb = sKV + (uint32_t)st * p.stage_bytes;
+            const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint64_t a = ptx::sdesc_sw128(sQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
                 const uint64_t b = ptx::sdesc_sw128(kb + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
-                ptx::tc_mma(tmem + kColS + buf * BN, a, b, idS, kk > 0 ? 1u : 0u);
+                ptx::tc_mma(tmem + col, a, b, idS, kk > 0 ? 1u : 0u);
             }
-            ptx::tc_commit(bar(B_S_FULL0 + (int)buf));
+            ptx::tc_commit(fb);
             ptx::tc_commit(bar(B_KV0 + kMaxStages + st));
             ++kv_it;
-            ++s_it;
             if (j == J - 1) ptx::tc_commit(bar(B_Q_EMPTY));
-            if (j >= 1) ok = issue_pv(j - 1);
+            if (j >= 1) ok = issue_pv(j - 1, prev_cols);
+            prev_cols = cols;
         }
         if (!ok) break;
-        if (!(ok = issue_pv(J - 1))) break;
+        if (!(ok = issue_pv(J - 1, prev_cols))) break;
         if (AV) {
-            if (!(ok = wait_bar(bar(B_P_FULL), p_it & 1u, sh, p.err))) break;
-            ++p_it;
+            uint32_t pb;
+            if (!(ok = wait_p(pb))) break;
             if (!(ok = wait_bar(bar(B_AV_FULL), av_it & 1u, sh, p.err))) break;
             ++av_it;
             ptx::tc_fence_after();
+            const uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
+            const uint32_t pcol = TL::P + pb * (BN / 2);
             for (int kk = 0; kk < p.kpad_v / 16; ++kk) {
-                const uint64_t a = ptx::sdesc_sw128(sP + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
                 const uint64_t b = ptx::sdesc_sw128(sAV + kk * 16 * 128, (uint32_t)p.kpad_v * 128, 1024);
-                ptx::tc_mma(tmem + kColO, a, b, idPV, 1u);
+                ptx::tc_mma_ts(tmem + TL::O, tmem + pcol + (uint32_t)(kk * 8), b, idPV, 1u);
             }
+            ptx::tc_commit(bar(B_PV_DONE0 + (int)pb));
             ptx::tc_commit(bar(B_AV_EMPTY));
         }
         ptx::tc_commit(bar(B_O_FULL));
-        ++tiles;
     }
     // every MMA issued by this thread completes before TMEM is released
     ptx::tc_commit(bar(B_DRAIN));
@@ -310,33 +362,24 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
 }
 
 // ======================================================================= softmax / epilogue
-template <int D>
-__device__ __forceinline__ bool store_tile(const Params &p, const Shared &sh, const CUtensorMap *tm_o,
-                                           int i0, int bh, int stid, uint32_t &grp) {
-    constexpr int DB = D / 64;
-    const uint32_t gbar = sh.base + p.off_bar + 8u * B_GROUP;
-    ptx::fence_proxy_async_smem();
-    if (!group_sync(gbar, grp, sh, p.err)) return false;
-    if (stid == 0) {
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
+
+// Multiply 16 packed-bf16 TMEM columns (32 values) of this warp's lanes by a per-lane factor.
+__device__ __forceinline__ void scale_packed16(uint32_t taddr, float a) {
+    uint32_t r[16];
+    ptx::tmem_ld16(taddr, r);
+    ptx::tmem_ld_wait();
 #pragma unroll
-        for (int blk = 0; blk < DB; ++blk)
-            ptx::tma_store_3d(tm_o, sh.base + p.off_p + blk * BM * 128, blk * 64, i0, bh);
-        ptx::bulk_commit();
-        ptx::bulk_wait_read0();
-    }
-    return group_sync(gbar, grp, sh, p.err);
+    for (int e = 0; e < 16; ++e)
+        r[e] = pack2(ptx::bf16lo_to_f32(r[e]) * a, ptx::bf16hi_to_f32(r[e]) * a);
+    ptx::tmem_st16(taddr, r);
 }
 
-// address of 16-byte chunk c (8 bf16 columns) of row `row` in a 128-byte-swizzled,
-// K-major tile made of 64-column blocks of BM rows
-__device__ __forceinline__ uint32_t sw128_chunk(uint32_t tile, int row, int c) {
-    return tile + (uint32_t)(c >> 3) * (BM * 128) + (uint32_t)row * 128 +
-           (uint32_t)(((c & 7) ^ (row & 7)) << 4);
-}
-
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
-__device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
-                             const CUtensorMap *tm_o) {
+template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
+__device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
+    using TL = TmemLayout<CPS>;
+    constexpr int BN = TL::BN;
+    constexpr int NCH = BN / KB;  // chunks per key tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
@@ -344,7 +387,6 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    const uint32_t sP = sh.base + p.off_p;
     float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r) + row * p.SR;
     float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta) + row * p.SR;
     float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5);
@@ -352,27 +394,54 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
     const int k = p.clip_k;
     const int hi_off = CAUSAL ? 0 : k;  // largest offset held in the staged table rows
     const int W = p.W;
-    uint32_t s_it = 0, pv_base = 0, tiles = 0, grp = 0;
+    uint32_t s_it = 0, p_item = 0, tiles = 0, grp = 0;
     const uint32_t gbar = bar(B_GROUP);
     int t5_head = -1;
     bool ok = true;
-    // tcgen05.ld/st are warp-collective (.sync.aligned): every decision that guards them is
-    // made uniform across the warp, and the warp reconverges before each TMEM access.
+    // tcgen05.ld/st are warp-collective (.sync.aligned): every decision guarding them is
+    // uniform across the warp, and the warp reconverges before each TMEM access.
     auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar(b, parity, sh, p.err);
         return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+    // completion of the MMA that read P item `item` (each P buffer has its own barrier, and
+    // that barrier cannot run two completions ahead: its next one needs our next item)
+    auto wait_pv_item = [&](uint32_t item) -> bool {
+        if (!wait_w(bar(B_PV_DONE0 + (int)(item & 1u)), (item >> 1) & 1u)) return false;
+        ptx::tc_fence_after();
+        __syncwarp();
+        return true;
+    };
+    auto wait_sfull = [&](uint32_t &col, int &buf) -> bool {
+        buf = (int)(s_it & 1u);
+        if (!wait_w(bar(B_S_FULL0 + buf), (s_it >> 1) & 1u)) return false;
+        ptx::tc_fence_after();
+        __syncwarp();
+        col = TL::S + (uint32_t)buf * BN;
+        ++s_it;
+        return true;
+    };
+    auto release_s = [&](int buf) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(B_S_EMPTY0 + buf));
     };
 
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int bh, qt;
         decode_tile(p, t, bh, qt);
         const int i0 = qt * BM, gi = i0 + row, h = bh % p.H;
+        const int gmin = i0 + quad * 32, gmax = gmin + 31;  // rows of this warp
         const int nk = keys_of(p, bh);
-        const int J = kv_tiles_of<CAUSAL>(p, bh, i0);
+        const int nkc = tile_keys<CAUSAL>(p, bh, i0);
+        const int J = (nkc + BN - 1) / BN;
+        __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                              ((long long)bh * p.n + gi) * D;
         if (J == 0) {
+            if (gi < p.n) {
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) ptx::st_shared_v4(sw128_chunk(sP, row, c), 0, 0, 0, 0);
-            ok = store_tile<D>(p, sh, tm_o, i0, bh, stid, grp);
+                for (int c = 0; c < D / 8; ++c)
+                    reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
+            }
             continue;
         }
         if (T5 && h != t5_head) {
@@ -383,178 +452,214 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
             t5_head = h;
         }
         if (AK) {
-            if (!(ok = wait_w(bar(B_R_FULL), tiles & 1u))) break;
-            ptx::tc_fence_after();
-            __syncwarp();
+            uint32_t col;
+            int buf;
+            if (!(ok = wait_sfull(col, buf))) break;
             for (int c0 = 0; c0 < p.npad_k; c0 += 16) {
                 uint32_t r[16];
-                ptx::tmem_ld16(lane_base + kColR + (uint32_t)c0, r);
+                ptx::tmem_ld16(lane_base + col + (uint32_t)c0, r);
                 ptx::tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     if (c0 + e < W) Rrow[c0 + e] = __uint_as_float(r[e]) * sl2;
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_R_EMPTY));
+            release_s(buf);
         }
         if (AV)
             for (int r = 0; r < W; ++r) brow[r] = 0.f;
-        float m_ref = -INFINITY, l = 0.f;
+        float m_ref = -INFINITY, l = 0.f, lo_sum = 0.f, hi_sum = 0.f;
 
         for (int j = 0; j < J; ++j) {
-            const uint32_t buf = s_it & 1u;
-            if (!(ok = wait_w(bar(B_S_FULL0 + (int)buf), (s_it >> 1) & 1u))) break;
-            ptx::tc_fence_after();
-            __syncwarp();
-            float s[BN];
-            {
-                uint32_t r[32];
+            const int j0 = j * BN;
+            const int cols = tile_cols<BN>(nkc, j);  // multiple of 32, > 0
+            // chunks this warp must look at: the ones inside `cols` that a row of the warp
+            // can see (causal: up to key gmax)
+            int live = cols / KB;
+            if (CAUSAL) live = min(live, max(0, (gmax - j0) / KB + 1));
+            const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
+            bool p_free = p_item < 2;  // the buffer's previous P . V is known to be done
+            uint32_t scol;
+            int buf;
+            if (!(ok = wait_sfull(scol, buf))) break;
+            if (live == 0) release_s(buf);
 #pragma unroll
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    ptx::tmem_ld32(lane_base + kColS + buf * BN + (uint32_t)c0, r);
+            for (int c = 0; c < NCH; ++c) {
+                if (c >= cols / KB) break;
+                const uint32_t pcol = pbase + (uint32_t)(c * (KB / 2));
+                if (c >= live) {  // no row of this warp sees these keys: zero P
+                    if (!p_free) {
+                        if (!(ok = wait_pv_item(p_item - 2))) break;
+                        p_free = true;
+                    }
+                    uint32_t z[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) z[e] = 0u;
+                    __syncwarp();
+                    ptx::tmem_st16(pcol, z);
+                    continue;
+                }
+                float x[KB];
+                {
+                    uint32_t r[KB];
+                    __syncwarp();
+                    ptx::tmem_ld32(lane_base + scol + (uint32_t)(c * KB), r);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c0 + e] = __uint_as_float(r[e]);
+                    for (int e = 0; e < KB; ++e) x[e] = __uint_as_float(r[e]);
                 }
-            }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_S_EMPTY0 + (int)buf));
-            ++s_it;
-
-            const int j0 = j * BN;
-            const int omin = j0 - (i0 + BM - 1), omax = j0 + BN - 1 - i0;  // offset range of the tile
-            // ---- logits in the log2 domain, relative term added (S2-S4)
-            if (AK) {
-                if (omax <= -k) {
-                    const float c = Rrow[0];
+                if (c == live - 1) release_s(buf);
+                const int e0 = j0 + c * KB;  // first key of the chunk
+                // offsets j - i over the warp's rows lie in [e0 - gmax, e0 + 31 - gmin]
+                const int lo_lim = T5 ? -p.t5_R : -k;      // at or below: first table row
+                const int hi_lim = T5 ? p.t5_R : hi_off;   // at or above: last table row
+                const bool w_left = (e0 + KB - 1 - gmin) <= lo_lim;
+                const bool w_right = (e0 - gmax) >= hi_lim;
+                const int base = e0 - gi;  // offset of element 0 for this row
+                // ---- logits in the log2 domain, relative term added (S2-S4)
+                if (AK) {
+                    if (w_left) {
+                        const float cst = Rrow[0];
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) s[e] = fmaf(s[e], sl2, c);
-                } else if (omin >= hi_off) {
-                    const float c = Rrow[W - 1];
+                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
+                    } else if (w_right) {
+                        const float cst = Rrow[W - 1];
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) s[e] = fmaf(s[e], sl2, c);
+                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < KB; ++e) {
+                            const int o = min(hi_off, max(-k, base + e));
+                            x[e] = fmaf(x[e], sl2, Rrow[o + k]);
+                        }
+                    }
+                } else if (T5) {
+                    const int R = p.t5_R;
+                    if (w_left) {
+                        const float cst = t5tab[0];
+#pragma unroll
+                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
+                    } else if (w_right) {
+                        const float cst = t5tab[2 * R];
+#pragma unroll
+                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < KB; ++e) {
+                            const int o = min(R, max(-R, base + e));
+                            x[e] = fmaf(x[e], sl2, t5tab[o + R]);
+                        }
+                    }
                 } else {
-                    const int base = j0 - gi;
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) {
-                        const int o = min(hi_off, max(-k, base + e));
-                        s[e] = fmaf(s[e], sl2, Rrow[o + k]);
+                    for (int e = 0; e < KB; ++e) x[e] *= sl2;
+                }
+                // ---- masks: key padding and causal (only chunks that cross a boundary)
+                const bool full = (e0 + KB <= nk) && (!CAUSAL || e0 + KB - 1 <= gmin);
+                if (!full) {
+#pragma unroll
+                    for (int e = 0; e < KB; ++e) {
+                        const int jj = e0 + e;
+                        if (jj >= nk || (CAUSAL && jj > gi)) x[e] = -INFINITY;
                     }
                 }
-            } else if (T5) {
-                const int R = p.t5_R;
-                if (omax <= -R) {
-                    const float c = t5tab[0];
+                // ---- online softmax (S5) with a lazy rescale
+                float cmax = x[0];
 #pragma unroll
-                    for (int e = 0; e < BN; ++e) s[e] = fmaf(s[e], sl2, c);
-                } else if (omin >= R) {
-                    const float c = t5tab[2 * R];
-#pragma unroll
-                    for (int e = 0; e < BN; ++e) s[e] = fmaf(s[e], sl2, c);
-                } else {
-                    const int base = j0 - gi;
-#pragma unroll
-                    for (int e = 0; e < BN; ++e) {
-                        const int o = min(R, max(-R, base + e));
-                        s[e] = fmaf(s[e], sl2, t5tab[o + R]);
-                    }
+                for (int e = 1; e < KB; ++e) cmax = fmaxf(cmax, x[e]);
+                float alpha = 1.f;
+                if (cmax > m_ref + kRescaleLog2) {
+                    alpha = ptx::ex2(m_ref - cmax);  // 0 while nothing was seen yet
+                    m_ref = cmax;
                 }
-            } else {
+                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                float rs = 0.f;
 #pragma unroll
-                for (int e = 0; e < BN; ++e) s[e] *= sl2;
-            }
-            // ---- masks: key padding and causal
-            const bool full = (j0 + BN <= nk) && (!CAUSAL || j0 + BN - 1 <= i0);
-            if (!full) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e) {
-                    const int jj = j0 + e;
-                    if (jj >= nk || (CAUSAL && jj > gi)) s[e] = -INFINITY;
+                for (int e = 0; e < KB; ++e) {
+                    x[e] = ptx::ex2(x[e] - m_use);
+                    rs += x[e];
                 }
-            }
-            // ---- online softmax (S5) with a lazy rescale
-            float mx = s[0];
-#pragma unroll
-            for (int e = 1; e < BN; ++e) mx = fmaxf(mx, s[e]);
-            const float m_new = fmaxf(m_ref, mx);
-            float alpha = 1.f;
-            if (m_new > m_ref + kRescaleLog2) {
-                alpha = ptx::ex2(m_ref - m_new);
-                m_ref = m_new;
-            }
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            float rs = 0.f;
-#pragma unroll
-            for (int e = 0; e < BN; ++e) {
-                s[e] = ptx::ex2(s[e] - m_use);
-                rs += s[e];
-            }
-            l = l * alpha + rs;
-            // ---- value bins (S7)
-            if (AV) {
-                if (alpha != 1.f)
-                    for (int r = 0; r < W; ++r) brow[r] *= alpha;
-                if (omax <= -k) {
-                    brow[0] += rs;
-                } else if (omin >= hi_off) {
-                    brow[W - 1] += rs;
-                } else {
-                    const int base = j0 - gi;
-#pragma unroll
-                    for (int e = 0; e < BN; ++e) {
-                        const int o = min(hi_off, max(-k, base + e));
-                        brow[o + k] += s[e];
-                    }
+                if (!p_free) {  // before the first P store of this tile
+                    if (!(ok = wait_pv_item(p_item - 2))) break;
+                    p_free = true;
                 }
-            }
-            // ---- the previous P.V must be done before P and O are touched
-            if (j >= 1) {
-                if (!(ok = wait_w(bar(B_PV_DONE), (pv_base + (uint32_t)j - 1u) & 1u))) break;
-                ptx::tc_fence_after();
-                // lanes that keep their max multiply by 1
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    l *= alpha;
+                    lo_sum *= alpha;
+                    hi_sum *= alpha;
+                    if (AV && alpha != 1.f)
+                        for (int r = 0; r < W; ++r) brow[r] *= alpha;
                     __syncwarp();
+                    if (j >= 1) {  // O holds P V of the earlier key tiles: wait for the last
+                        if (!(ok = wait_pv_item(p_item - 1))) break;
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t r[32];
-                        ptx::tmem_ld32(lane_base + kColO + (uint32_t)c0, r);
-                        ptx::tmem_ld_wait();
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t r[32];
+                            ptx::tmem_ld32(lane_base + TL::O + (uint32_t)c0, r);
+                            ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        ptx::tmem_st32(lane_base + kColO + (uint32_t)c0, r);
+                            for (int e = 0; e < 32; ++e)
+                                r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                            ptx::tmem_st32(lane_base + TL::O + (uint32_t)c0, r);
+                        }
                     }
+                    for (int c2 = 0; c2 < c; ++c2)  // P chunks already written for this tile
+                        scale_packed16(pbase + (uint32_t)(c2 * (KB / 2)), alpha);
                     ptx::tmem_st_wait();
                 }
-            }
-            // ---- P (bf16) to shared memory, 128-byte swizzled K-major
+                l += rs;
+                // ---- value bins (S7)
+                if (AV) {
+                    if (w_left) {
+                        lo_sum += rs;
+                    } else if (w_right) {
+                        hi_sum += rs;
+                    } else {
 #pragma unroll
-            for (int c = 0; c < BN / 8; ++c)
-                ptx::st_shared_v4(sw128_chunk(sP, row, c), ptx::pack_bf16x2(s[8 * c], s[8 * c + 1]),
-                                  ptx::pack_bf16x2(s[8 * c + 2], s[8 * c + 3]),
-                                  ptx::pack_bf16x2(s[8 * c + 4], s[8 * c + 5]),
-                                  ptx::pack_bf16x2(s[8 * c + 6], s[8 * c + 7]));
-            ptx::fence_proxy_async_smem();
+                        for (int e = 0; e < KB; ++e) {
+                            const int o = min(hi_off, max(-k, base + e));
+                            brow[o + k] += x[e];
+                        }
+                    }
+                }
+                // ---- P (bf16 pairs) into TMEM
+                {
+                    uint32_t pk[KB / 2];
+#pragma unroll
+                    for (int e = 0; e < KB / 2; ++e) pk[e] = pack2(x[2 * e], x[2 * e + 1]);
+                    __syncwarp();
+                    ptx::tmem_st16(pcol, pk);
+                }
+            }
+            if (!ok) break;
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_P_FULL));
+            ptx::mbar_arrive(bar(B_P_FULL0 + (int)(p_item & 1u)));
+            ++p_item;
         }
         if (!ok) break;
         if (AV) {
-            // bins (bf16) become the A operand of O += beta W^V
-            if (!(ok = wait_w(bar(B_PV_DONE), (pv_base + (uint32_t)J - 1u) & 1u))) break;
-            for (int c = 0; c < p.kpad_v / 8; ++c) {
-                float v8[8];
+            // bins (bf16 pairs) become the A operand of O += beta W^V
+            brow[0] += lo_sum;
+            brow[W - 1] += hi_sum;
+            if (p_item >= 2 && !(ok = wait_pv_item(p_item - 2))) break;
+            const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
+            __syncwarp();
+            for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v8[e] = (8 * c + e < W) ? brow[8 * c + e] : 0.f;
-                ptx::st_shared_v4(sw128_chunk(sP, row, c), ptx::pack_bf16x2(v8[0], v8[1]),
-                                  ptx::pack_bf16x2(v8[2], v8[3]), ptx::pack_bf16x2(v8[4], v8[5]),
-                                  ptx::pack_bf16x2(v8[6], v8[7]));
+                for (int e = 0; e < 16; ++e) {
+                    const int r0 = c0 + 2 * e;
+                    pk[e] = pack2(r0 < W ? brow[r0] : 0.f, r0 + 1 < W ? brow[r0 + 1] : 0.f);
+                }
+                __syncwarp();
+                ptx::tmem_st16(pbase + (uint32_t)(c0 / 2), pk);
             }
-            ptx::fence_proxy_async_smem();
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_P_FULL));
+            ptx::mbar_arrive(bar(B_P_FULL0 + (int)(p_item & 1u)));
+            ++p_item;
         }
-        pv_base += (uint32_t)J;
-        // ---- epilogue (S8): O / l -> bf16 -> TMA store
+        // ---- epilogue (S8): O / l -> bf16 -> global
         if (!(ok = wait_w(bar(B_O_FULL), tiles & 1u))) break;
         ptx::tc_fence_after();
         __syncwarp();
@@ -563,32 +668,33 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem,
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t r[32];
-            ptx::tmem_ld32(lane_base + kColO + (uint32_t)c0, r);
+            ptx::tmem_ld32(lane_base + TL::O + (uint32_t)c0, r);
             ptx::tmem_ld_wait();
+            if (gi < p.n) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[8 * q + e]) * inv;
-                ptx::st_shared_v4(sw128_chunk(sP, row, c0 / 8 + q), ptx::pack_bf16x2(f[0], f[1]),
-                                  ptx::pack_bf16x2(f[2], f[3]), ptx::pack_bf16x2(f[4], f[5]),
-                                  ptx::pack_bf16x2(f[6], f[7]));
+                for (int q = 0; q < 4; ++q) {
+                    uint4 v;
+                    v.x = pack2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+                    v.y = pack2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+                    v.z = pack2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+                    v.w = pack2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+                    reinterpret_cast<uint4 *>(orow)[c0 / 8 + q] = v;
+                }
             }
+            __syncwarp();
         }
         ptx::tc_fence_before();
-        ok = store_tile<D>(p, sh, tm_o, i0, bh, stid, grp);
     }
-    if (stid == 0) ptx::bulk_wait0();
 }
 
 // ======================================================================= kernel
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
     relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                      const __grid_constant__ CUtensorMap tm_ak, const __grid_constant__ CUtensorMap tm_av,
-                      const __grid_constant__ Params p) {
-    extern __shared__ uint8_t smem_raw[];
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ak,
+                      const __grid_constant__ CUtensorMap tm_av, const __grid_constant__ Params p) {
+    using TL = TmemLayout<CPS>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     Shared sh;
     sh.base = (raw + 1023u) & ~1023u;
@@ -602,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
-            if (i == B_S_EMPTY0 || i == B_S_EMPTY1 || i == B_P_FULL || i == B_R_EMPTY ||
+            if (i == B_S_EMPTY0 || i == B_S_EMPTY1 || i == B_P_FULL0 || i == B_P_FULL1 ||
                 i == B_GROUP)
                 cnt = 128;
             ptx::mbar_init(bars + 8u * (uint32_t)i, cnt);
@@ -612,29 +718,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_prefetch_desc(&tm_q);
         ptx::tma_prefetch_desc(&tm_k);
         ptx::tma_prefetch_desc(&tm_v);
-        ptx::tma_prefetch_desc(&tm_o);
     }
-    if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TL::cols);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if ((threadIdx.x & 31) == 0) producer_role<D, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_ak, &tm_av);
+        if ((threadIdx.x & 31) == 0) producer_role<D, AK, AV, CAUSAL, CPS>(p, sh, &tm_q, &tm_k, &tm_v, &tm_ak, &tm_av);
         __syncwarp();
     } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) mma_role<D, AK, AV, CAUSAL>(p, sh, tmem);
+        if ((threadIdx.x & 31) == 0) mma_role<D, AK, AV, CAUSAL, CPS>(p, sh, tmem);
         __syncwarp();
     } else {
-        softmax_role<D, AK, AV, T5, CAUSAL>(p, sh, tmem, &tm_o);
+        softmax_role<D, AK, AV, T5, CAUSAL, CPS>(p, sh, tmem);
     }
 
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        ptx::tmem_dealloc(tmem, TL::cols);
     }
 }
 

@@ -48,7 +48,9 @@ inline bool make_map(CUtensorMap *m, const void *ptr, uint64_t dim0, uint64_t di
 
 struct DeviceInfo {
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;      // max dynamic shared memory of one block
+    int smem_per_sm = 0;     // shared memory of one SM
+    int smem_reserved = 0;   // shared memory the system keeps per block
 };
 
 inline DeviceInfo device_info() {
@@ -61,48 +63,80 @@ inline DeviceInfo device_info() {
     if (cache[dev].sms == 0) {
         cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&cache[dev].smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&cache[dev].smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     }
     return cache[dev];
 }
 
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
-cudaError_t launch_variant(const CUtensorMap (&tm)[6], const Params &p, uint32_t smem_bytes, int grid,
+template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
+cudaError_t launch_variant(const CUtensorMap (&tm)[5], const Params &p, uint32_t smem_bytes,
                            cudaStream_t s) {
-    auto kern = relattn_tc_kernel<D, AK, AV, T5, CAUSAL>;
+    auto kern = relattn_tc_kernel<D, AK, AV, T5, CAUSAL, CPS>;
     // Opt in to the device's whole shared-memory budget once per device and variant, so
     // that later calls (including ones captured into a CUDA graph) only launch.
     static bool opted[64] = {};
+    static int resident[64] = {};
     static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const DeviceInfo di = device_info();
+    int per_sm = 1;
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!opted[dev]) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     device_info().smem_optin);
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin);
             if (e != cudaSuccess) return e;
             opted[dev] = true;
         }
+        if (CPS > 1) {
+            int nb = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem_bytes);
+            if (e != cudaSuccess) return e;
+            resident[dev] = nb;
+            per_sm = nb < 1 ? 1 : (nb > CPS ? CPS : nb);
+        }
     }
-    kern<<<grid, kThreads, smem_bytes, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], p);
+    const int want = di.sms * per_sm;
+    const int grid = p.num_tiles < want ? p.num_tiles : want;
+    kern<<<grid, kThreads, smem_bytes, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], p);
     return cudaGetLastError();
 }
 
-template <int D, bool T5, bool CAUSAL>
-cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[6], const Params &p,
-                         uint32_t smem, int grid, cudaStream_t s) {
+template <int D, bool T5, bool CAUSAL, int CPS>
+cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[5], const Params &p,
+                         uint32_t smem, cudaStream_t s) {
     if constexpr (T5) {
-        return launch_variant<D, false, false, true, CAUSAL>(tm, p, smem, grid, s);
+        return launch_variant<D, false, false, true, CAUSAL, CPS>(tm, p, smem, s);
     } else {
-        if (ak && av) return launch_variant<D, true, true, false, CAUSAL>(tm, p, smem, grid, s);
-        if (ak) return launch_variant<D, true, false, false, CAUSAL>(tm, p, smem, grid, s);
-        if (av) return launch_variant<D, false, true, false, CAUSAL>(tm, p, smem, grid, s);
-        return launch_variant<D, false, false, false, CAUSAL>(tm, p, smem, grid, s);
+        if (ak && av) return launch_variant<D, true, true, false, CAUSAL, CPS>(tm, p, smem, s);
+        if (ak) return launch_variant<D, true, false, false, CAUSAL, CPS>(tm, p, smem, s);
+        if (av) return launch_variant<D, false, true, false, CAUSAL, CPS>(tm, p, smem, s);
+        return launch_variant<D, false, false, false, CAUSAL, CPS>(tm, p, smem, s);
     }
+}
+
+// Shared-memory layout for `stages` K/V stages of `bn` keys; returns the bytes to request.
+template <int D>
+inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int bn, int stages) {
+    const uint32_t q_bytes = (uint32_t)BM * D * 2;
+    const uint32_t stage_bytes = (uint32_t)bn * D * 2;
+    uint32_t off = 0;
+    p.off_q = off;    off += q_bytes;                                     // 1024-aligned TMA targets
+    p.off_kv = off;   off += (uint32_t)stages * stage_bytes;
+    p.off_ak = off;   if (ak) off += (uint32_t)p.npad_k * D * 2;
+    p.off_av = off;   if (av) off += (uint32_t)p.kpad_v * D * 2;
+    p.off_r = off;    if (ak) off += round_up((uint32_t)BM * p.SR * 4, 16);  // per-row tables
+    p.off_beta = off; if (av) off += round_up((uint32_t)BM * p.SR * 4, 16);
+    p.off_t5 = off;   if (t5mode) off += round_up((uint32_t)(2 * p.t5_R + 1) * 4, 16);
+    p.off_bar = off;  off += (uint32_t)kNumBars * 8 + 16;
+    p.stages = stages;
+    p.stage_bytes = stage_bytes;
+    return off + 1024;  // slack to align the base to 1024 bytes
 }
 
 template <int D>
@@ -120,6 +154,7 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     p.scale_log2 = a.scale * kLog2e;
     p.kv_len = a.kv_len;
     p.err = err_word;
+    p.out = a.out;
     p.clip_k = a.clip_k;
     p.W = 1;
     if (ak || av) {
@@ -139,60 +174,61 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
 
     const DeviceInfo di = device_info();
     if (di.sms <= 0 || di.smem_optin <= 0) return cudaErrorInvalidDevice;
-    // ---- shared-memory layout (offsets from a 1024-aligned base)
-    const uint32_t tile_bytes = (uint32_t)BM * D * 2;
-    uint32_t fixed = tile_bytes;                        // Q
-    fixed += (uint32_t)BM * BN * 2;                     // P / bins / output staging
-    if (ak) fixed += (uint32_t)p.npad_k * D * 2;        // W^K rows
-    if (av) fixed += (uint32_t)p.kpad_v * D * 2;        // W^V rows
-    if (ak) fixed += round_up((uint32_t)BM * p.SR * 4, 1024);
-    if (av) fixed += round_up((uint32_t)BM * p.SR * 4, 1024);
-    if (t5mode) fixed += round_up((uint32_t)(2 * p.t5_R + 1) * 4, 1024);
-    fixed += round_up((uint32_t)kNumBars * 8 + 16, 1024);
-    const uint32_t slack = 1024;
-    const int64_t room = (int64_t)di.smem_optin - (int64_t)fixed - slack;
-    int stages = (int)(room / (int64_t)tile_bytes);
-    if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2) return cudaErrorNotSupported;
-    p.stages = stages;
-    p.stage_bytes = tile_bytes;
-    uint32_t off = 0;
-    p.off_q = off;    off += tile_bytes;
-    p.off_kv = off;   off += (uint32_t)stages * tile_bytes;
-    p.off_p = off;    off += (uint32_t)BM * BN * 2;
-    p.off_ak = off;   if (ak) off += (uint32_t)p.npad_k * D * 2;
-    p.off_av = off;   if (av) off += (uint32_t)p.kpad_v * D * 2;
-    p.off_r = off;    if (ak) off += round_up((uint32_t)BM * p.SR * 4, 1024);
-    p.off_beta = off; if (av) off += round_up((uint32_t)BM * p.SR * 4, 1024);
-    p.off_t5 = off;   if (t5mode) off += round_up((uint32_t)(2 * p.t5_R + 1) * 4, 1024);
-    p.off_bar = off;  off += round_up((uint32_t)kNumBars * 8 + 16, 1024);
-    const uint32_t smem_bytes = off + slack;
-    if (smem_bytes > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
+    // two CTAs per SM (64-key tiles, TMEM 256 columns each) when D = 64, the staged table
+    // rows fit a 64-key score buffer and the shared memory of both fits; else one CTA per
+    // SM with 128-key tiles
+    int cps = 1;
+    uint32_t smem = 0;
+    if (D == 64 && p.npad_k <= 64) {
+        const int64_t budget2 = ((int64_t)di.smem_per_sm - 2 * (int64_t)di.smem_reserved) / 2;
+        Params q = p;
+        const uint32_t fixed = layout<D>(q, ak, av, t5mode, 64, 0);
+        const int64_t st = (budget2 - (int64_t)fixed) / ((int64_t)64 * D * 2);
+        if (st >= 4) {
+            cps = 2;
+            smem = layout<D>(p, ak, av, t5mode, 64, (int)(st > kMaxStages ? kMaxStages : st));
+        }
+    }
+    if (cps == 1) {
+        Params q = p;
+        const uint32_t fixed = layout<D>(q, ak, av, t5mode, 128, 0);
+        const int64_t st = ((int64_t)di.smem_optin - (int64_t)fixed) / ((int64_t)128 * D * 2);
+        if (st < 2) return cudaErrorNotSupported;
+        smem = layout<D>(p, ak, av, t5mode, 128, (int)(st > kMaxStages ? kMaxStages : st));
+    }
+    if (smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
 
-    // ---- TMA descriptors
-    CUtensorMap tm[6];
+    // ---- TMA descriptors (the output is written with plain stores)
+    CUtensorMap tm[5];
     const uint64_t d = (uint64_t)D, n = (uint64_t)a.n, BH = (uint64_t)p.BH;
     const uint64_t rs = d * 2, hs = n * d * 2;
-    if (!make_map(&tm[0], a.q, d, n, BH, rs, hs, BM) || !make_map(&tm[1], a.k, d, n, BH, rs, hs, BN) ||
-        !make_map(&tm[2], a.v, d, n, BH, rs, hs, BN) || !make_map(&tm[3], a.out, d, n, BH, rs, hs, BM))
+    if (!make_map(&tm[0], a.q, d, n, BH, rs, hs, BM) || !make_map(&tm[1], a.k, d, n, BH, rs, hs, KB) ||
+        !make_map(&tm[2], a.v, d, n, BH, rs, hs, KB))
         return cudaErrorInvalidValue;
+    tm[3] = tm[0];
     tm[4] = tm[0];
-    tm[5] = tm[0];
     const uint64_t rows = (uint64_t)(2 * a.clip_k + 1);
     const uint64_t Ht = p.table_heads ? (uint64_t)a.H : 1;
     const uint64_t ths_bytes = p.table_heads ? (uint64_t)a.ths * 2 : rows * d * 2;
-    if (ak && !make_map(&tm[4], a.aK, d, rows, Ht, rs, ths_bytes, (uint32_t)p.npad_k))
+    if (ak && !make_map(&tm[3], a.aK, d, rows, Ht, rs, ths_bytes, (uint32_t)p.npad_k))
         return cudaErrorInvalidValue;
-    if (av && !make_map(&tm[5], a.aV, d, rows, Ht, rs, ths_bytes, (uint32_t)p.kpad_v))
+    if (av && !make_map(&tm[4], a.aV, d, rows, Ht, rs, ths_bytes, (uint32_t)p.kpad_v))
         return cudaErrorInvalidValue;
 
-    const int grid = p.num_tiles < di.sms ? p.num_tiles : di.sms;
-    if (a.causal) {
-        return t5mode ? launch_terms<D, true, true>(ak, av, tm, p, smem_bytes, grid, s)
-                      : launch_terms<D, false, true>(ak, av, tm, p, smem_bytes, grid, s);
+    if constexpr (D == 64) {
+        if (cps == 2) {
+            if (a.causal)
+                return t5mode ? launch_terms<D, true, true, 2>(ak, av, tm, p, smem, s)
+                              : launch_terms<D, false, true, 2>(ak, av, tm, p, smem, s);
+            return t5mode ? launch_terms<D, true, false, 2>(ak, av, tm, p, smem, s)
+                          : launch_terms<D, false, false, 2>(ak, av, tm, p, smem, s);
+        }
     }
-    return t5mode ? launch_terms<D, true, false>(ak, av, tm, p, smem_bytes, grid, s)
-                  : launch_terms<D, false, false>(ak, av, tm, p, smem_bytes, grid, s);
+    if (a.causal)
+        return t5mode ? launch_terms<D, true, true, 1>(ak, av, tm, p, smem, s)
+                      : launch_terms<D, false, true, 1>(ak, av, tm, p, smem, s);
+    return t5mode ? launch_terms<D, true, false, 1>(ak, av, tm, p, smem, s)
+                  : launch_terms<D, false, false, 1>(ak, av, tm, p, smem, s);
 }
 
 }  // namespace tc

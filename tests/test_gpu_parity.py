@@ -125,7 +125,7 @@ BF16_CASES = [
     ("k0", 260, 64, 0, False, None, True, True, False),
     ("k1_causal", 260, 64, 1, True, None, True, True, False),
     ("k_large_causal", 390, 64, 100, True, None, True, True, False),
-    ("k_over_n", 90, 64, 40, False, None, True, True, False),
+    ("k_over_n", 90, 64, 63, False, None, True, True, False),
     ("key_only", 517, 64, 16, True, None, True, False, False),
     ("value_only", 300, 64, 16, False, None, False, True, False),
     ("plain", 300, 64, 16, False, (100, 300), False, False, False),
@@ -177,6 +177,36 @@ def test_bf16_t5_variants(n, bidir, causal, kv):
     got = run_gpu(w, x).float().cpu().numpy()
     ref = run_oracle(w, x)
     assert np.abs(got - ref).max() <= tol_for(w, ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_rising_logits_force_rescales(d):
+    """Logits that keep rising along the row make the running max jump by more than 2^8
+    inside a key tile and across tiles, exercising the rescale of O, of the bins and of the
+    P values already written for the tile."""
+    w = wl.Workload("ramp_t5", B=1, H=2, n=700, d=d, dtype="bf16", kind="t5", qkv_std=0.3,
+                    scale=1.0, num_buckets=32, max_distance=600)
+    x = wl.draw_inputs(w, 21)
+    x["bias"] = torch.zeros(32, 2)
+    x["bias"][16:, :] = 2.5 * torch.arange(16, dtype=torch.float32)[:, None]
+    got = run_gpu(w, x).float().cpu().numpy()
+    ref = run_oracle(w, x)
+    assert np.abs(got - ref).max() <= tol_for(w, ref)
+    # Shaw: w^K_r = (r - k) * u with q . u > 0 on average -> rising relative logits
+    kk = 60 if d == 64 else 24  # both tables at d = 128 must fit shared memory
+    ws = wl.Workload("ramp_shaw", B=1, H=2, n=600, d=d, dtype="bf16", clip_k=kk,
+                     table_std=0.0, kv_len_range=None)
+    xs = wl.draw_inputs(ws, 22)
+    u = torch.zeros(d)
+    u[0] = 1.0
+    xs["q"][..., 0] = 4.0
+    ramp = (torch.arange(2 * kk + 1, dtype=torch.float32) - kk)[:, None] * u[None, :] * 0.8
+    xs["aK"] = ramp[None].repeat(2, 1, 1).to(torch.bfloat16)
+    xs["aV"] = (torch.randn(2, 2 * kk + 1, d, generator=torch.Generator().manual_seed(3)) *
+                0.5).to(torch.bfloat16)
+    got = run_gpu(ws, xs).float().cpu().numpy()
+    ref = run_oracle(ws, xs)
+    assert np.abs(got - ref).max() <= tol_for(ws, ref)
 
 
 def test_bf16_t5_d128():
@@ -239,10 +269,11 @@ def test_bf16_unsupported_and_invalid_status():
     with pytest.raises(rp.RelattnError) as e:
         rp.relattn_fwd(q, q.clone(), q.clone(), tab, None, 64, False, 0.1)
     assert e.value.status == 2
-    # both tables with 2k+1 = 127 staged rows do not fit the shared-memory budget at d = 64
-    tab127 = torch.zeros(1, 127, 64, dtype=torch.bfloat16, device=DEV)
+    # both tables with 2k+1 = 127 staged rows do not fit the shared-memory budget at d = 128
+    q128 = torch.zeros(1, 1, 64, 128, dtype=torch.bfloat16, device=DEV)
+    tab127 = torch.zeros(1, 127, 128, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(rp.RelattnError) as e:
-        rp.relattn_fwd(q, q.clone(), q.clone(), tab127, tab127.clone(), 63, False, 0.1)
+        rp.relattn_fwd(q128, q128.clone(), q128.clone(), tab127, tab127.clone(), 63, False, 0.1)
     assert e.value.status == 2
     q96 = torch.zeros(1, 1, 64, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(rp.RelattnError) as e:
