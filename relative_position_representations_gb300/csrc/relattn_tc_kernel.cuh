@@ -15,12 +15,14 @@
 //   warp 1      MMA issuer (one thread). Per tile: R = Q W^K^T into a score buffer, then
 //               S_j = Q K_j^T into the score buffer(s), O += P_j V_j with P read from TMEM,
 //               and at the end O += beta W^V with the bins read from TMEM.
-//   warps 2..5  softmax / epilogue, one thread per query row (= TMEM lane). For each 32-key
-//               chunk of S_j: add the relative term (a per-row constant where the whole chunk
-//               lies beyond +-k for the warp, a shared-memory gather inside the band), mask,
-//               online softmax in the exp2 domain with a lazy rescale (only when the running
-//               max grows by more than 2^8), accumulate the value bins, and store bf16 P into
-//               TMEM. Chunks no row of the warp can see are skipped. Epilogue: O / l -> bf16.
+//   warps 2..   softmax / epilogue: each query row (= TMEM lane) is handled by NSPLIT
+//               threads (one per 64 keys of a key tile; the two halves of a 128-key tile
+//               exchange their row maxima through shared memory). Per key tile: add the
+//               relative term (a per-row constant for 32-key chunks that lie beyond +-k for
+//               the whole warp, a shared-memory gather inside the band), mask, online softmax
+//               in the exp2 domain with a lazy rescale (only when the running max grows by
+//               more than 2^8), value bins, bf16 P into TMEM. Chunks no row of the warp can
+//               see are skipped. Epilogue: O / l -> bf16.
 // Score (S) and probability (P) tiles are double-buffered in TMEM, so S_{j+1} and the
 // P_{j-1} V_{j-1} product overlap the softmax of tile j.
 // TMEM: CPS = 1 (one CTA per SM, 128-key tiles): S0 [0,128) S1 [128,256) O [256,256+D)
@@ -44,14 +46,21 @@ namespace tc {
 
 constexpr int BM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int KB = 32;    // key rows per TMA box and keys per softmax chunk
-constexpr int kThreads = 192;
+constexpr int HC = 64;    // keys of a key tile handled by one softmax thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// bound of every device wait, in SM clock cycles (about one second at 2 GHz); clock64 is
+// read only after a wait did not succeed at once and then every 256 polls
+constexpr long long kWaitLimitCycles = 2000000000ll;
 
 template <int CPS>
 struct TmemLayout {
     static constexpr int BN = CPS == 1 ? 128 : 64;  // keys per key tile
+    static constexpr int NSPLIT = BN / HC;          // softmax threads per query row
+    // registers are allocated per 4-warp group: two CTAs per SM need whole warpgroups
+    // (warps 2-3 idle) to stay within 128 registers a thread
+    static constexpr int SW0 = CPS == 2 ? 4 : 2;     // first softmax warp
+    static constexpr int THREADS = 32 * SW0 + 128 * NSPLIT;
     static constexpr uint32_t cols = CPS == 1 ? 512u : 256u;
     static constexpr uint32_t S = 0;                         // S buffer b at S + b * BN
     static constexpr uint32_t O = CPS == 1 ? 256u : 192u;    // D columns
@@ -61,7 +70,8 @@ struct TmemLayout {
 // barrier slots
 enum : int {
     B_Q_FULL = 0, B_Q_EMPTY, B_S_FULL0, B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_P_FULL0, B_P_FULL1,
-    B_PV_DONE0, B_PV_DONE1, B_AV_FULL, B_AV_EMPTY, B_O_FULL, B_DRAIN, B_GROUP, B_KV0
+    B_PV_DONE0, B_PV_DONE1, B_AV_FULL, B_AV_EMPTY, B_O_FULL, B_DRAIN, B_GROUP, B_PAIR0,
+    B_KV0 = B_PAIR0 + 4
 };
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
@@ -82,9 +92,10 @@ struct Params {
     const float *bias;  // T5 [num_buckets, H]
     int t5_R;           // T5 offset-table radius (bucket is constant beyond it)
     T5Buckets t5;
-    uint32_t off_q, off_kv, off_ak, off_av, off_r, off_beta, off_t5, off_bar;
+    uint32_t off_q, off_kv, off_ak, off_av, off_r, off_beta, off_t5, off_x, off_bar;
     int stages;
     uint32_t stage_bytes;
+    int head_group;     // heads whose tiles are scheduled together (K/V reuse in L2)
 };
 
 struct Shared {
@@ -96,18 +107,25 @@ struct Shared {
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared &sh,
                                          int *err) {
     if (ptx::mbar_try(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer();
+    const long long t0 = clock64();
     uint32_t spins = 0;
     while (true) {
         if (ptx::mbar_try(bar, parity)) return true;
-        if ((++spins & 127u) == 0) {
+        if ((++spins & 255u) == 0) {
             if (*sh.abort_flag) return false;
-            if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+            if (clock64() - t0 > kWaitLimitCycles) {
                 *sh.abort_flag = 1;
                 atomicCAS(err, 0, 4 /* RELATTN_ERR_TIMEOUT */);
                 return false;
             }
         }
+    }
+}
+
+// bounded poll of a barrier during teardown (no abort check)
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!ptx::mbar_try(bar, parity) && clock64() - t0 < kWaitLimitCycles) {
     }
 }
 
@@ -120,9 +138,15 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t &it, const Sha
     return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
 }
 
+// Work order: heads in groups of head_group (their K/V stay in L2 while the group runs);
+// inside a group, the query tiles with the most keys (causal) come first.
 __device__ __forceinline__ void decode_tile(const Params &p, int t, int &bh, int &qt) {
-    qt = p.n_qtiles - 1 - t / p.BH;  // longest causal rows first
-    bh = t % p.BH;
+    const int per_group = p.head_group * p.n_qtiles;
+    const int g = t / per_group, r = t - g * per_group;
+    const int g0 = g * p.head_group;
+    const int gsize = min(p.head_group, p.BH - g0);
+    qt = p.n_qtiles - 1 - r / gsize;
+    bh = g0 + r % gsize;
 }
 
 // number of allowed keys (before the causal clip) of the sequence of head bh
@@ -150,6 +174,7 @@ __device__ __forceinline__ int tile_cols(int nkc, int j) {
 template <int D, bool AK, bool AV, bool CAUSAL, int CPS>
 __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                              const CUtensorMap *tm_kf, const CUtensorMap *tm_vf,
                               const CUtensorMap *tm_ak, const CUtensorMap *tm_av) {
     constexpr int DB = D / 64;
     constexpr int BN = TmemLayout<CPS>::BN;
@@ -194,11 +219,18 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
             const int nbox = tile_cols<BN>(nkc, j) / KB;
             ptx::mbar_expect_tx(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
             const uint32_t dst = sKV + (uint32_t)st * p.stage_bytes;
-            for (int b = 0; b < nbox; ++b) {
+            if (nbox == BN / KB) {  // whole tile: one box of BN rows per 64-column block
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d(dst + blk * BN * 128 + b * KB * 128, isK ? tm_k : tm_v,
-                                     bar(B_KV0 + st), blk * 64, j * BN + b * KB, bh);
+                    ptx::tma_load_3d(dst + blk * BN * 128, isK ? tm_kf : tm_vf, bar(B_KV0 + st),
+                                     blk * 64, j * BN, bh);
+            } else {  // last tile: only the 32-row boxes holding allowed keys
+                for (int b = 0; b < nbox; ++b) {
+#pragma unroll
+                    for (int blk = 0; blk < DB; ++blk)
+                        ptx::tma_load_3d(dst + blk * BN * 128 + b * KB * 128, isK ? tm_k : tm_v,
+                                         bar(B_KV0 + st), blk * 64, j * BN + b * KB, bh);
+                }
             }
             ++kv_it;
         }
@@ -215,24 +247,10 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
     }
     if (!ok) {
         // drain: wait (bounded) for copies already issued into shared memory
-        for (uint32_t it = kv_it > (uint32_t)S ? kv_it - S : 0; it < kv_it; ++it) {
-            const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try(bar(B_KV0 + (int)(it % (uint32_t)S)), (it / (uint32_t)S) & 1u) &&
-                   ptx::globaltimer() - t0 < kWaitLimitNs) {
-            }
-        }
-        if (q_it) {
-            const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try(bar(B_Q_FULL), (q_it - 1) & 1u) &&
-                   ptx::globaltimer() - t0 < kWaitLimitNs) {
-            }
-        }
-        if (AV && av_it) {
-            const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try(bar(B_AV_FULL), (av_it - 1) & 1u) &&
-                   ptx::globaltimer() - t0 < kWaitLimitNs) {
-            }
-        }
+        for (uint32_t it = kv_it > (uint32_t)S ? kv_it - S : 0; it < kv_it; ++it)
+            drain_bar(bar(B_KV0 + (int)(it % (uint32_t)S)), (it / (uint32_t)S) & 1u);
+        if (q_it) drain_bar(bar(B_Q_FULL), (q_it - 1) & 1u);
+        if (AV && av_it) drain_bar(bar(B_AV_FULL), (av_it - 1) & 1u);
     }
 }
 
@@ -356,46 +374,40 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
     }
     // every MMA issued by this thread completes before TMEM is released
     ptx::tc_commit(bar(B_DRAIN));
-    const uint64_t t0 = ptx::globaltimer();
-    while (!ptx::mbar_try(bar(B_DRAIN), 0) && ptx::globaltimer() - t0 < kWaitLimitNs) {
-    }
+    drain_bar(bar(B_DRAIN), 0);
 }
 
 // ======================================================================= softmax / epilogue
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
 
-// Multiply 16 packed-bf16 TMEM columns (32 values) of this warp's lanes by a per-lane factor.
-__device__ __forceinline__ void scale_packed16(uint32_t taddr, float a) {
-    uint32_t r[16];
-    ptx::tmem_ld16(taddr, r);
-    ptx::tmem_ld_wait();
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-        r[e] = pack2(ptx::bf16lo_to_f32(r[e]) * a, ptx::bf16hi_to_f32(r[e]) * a);
-    ptx::tmem_st16(taddr, r);
-}
-
 template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
 __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
     using TL = TmemLayout<CPS>;
     constexpr int BN = TL::BN;
-    constexpr int NCH = BN / KB;  // chunks per key tile
+    constexpr int NSPLIT = TL::NSPLIT;
+    constexpr int NC = HC / KB;  // chunks per thread per key tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - TL::SW0) >> 2;    // which 64 keys of a key tile
     const int row = quad * 32 + lane;
-    const int stid = threadIdx.x - 64;
+    const int stid = threadIdx.x - 32 * TL::SW0;  // 0 .. 128*NSPLIT-1
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r) + row * p.SR;
     float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta) + row * p.SR;
     float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5);
+    // exchange slots between the halves of a row: [parity][half][row] maxima, then
+    // [half][row] x {l, low-bin sum, high-bin sum}
+    float *xmax = reinterpret_cast<float *>(sh.ptr + p.off_x);
+    float *xsum = xmax + 2 * 2 * BM;
     const float sl2 = p.scale_log2;
     const int k = p.clip_k;
     const int hi_off = CAUSAL ? 0 : k;  // largest offset held in the staged table rows
     const int W = p.W;
-    uint32_t s_it = 0, p_item = 0, tiles = 0, grp = 0;
+    uint32_t s_it = 0, p_item = 0, tiles = 0, grp = 0, pair_it = 0;
     const uint32_t gbar = bar(B_GROUP);
+    const uint32_t pbar = bar(B_PAIR0 + quad);
     int t5_head = -1;
     bool ok = true;
     // tcgen05.ld/st are warp-collective (.sync.aligned): every decision guarding them is
@@ -403,6 +415,14 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
     auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar(b, parity, sh, p.err);
         return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+    // the NSPLIT threads of the same rows (warps quad and quad + 4)
+    auto pair_sync = [&]() -> bool {
+        if (NSPLIT == 1) {
+            __syncwarp();
+            return true;
+        }
+        return group_sync(pbar, pair_it, sh, p.err);
     };
     // completion of the MMA that read P item `item` (each P buffer has its own barrier, and
     // that barrier cannot run two completions ahead: its next one needs our next item)
@@ -439,23 +459,23 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
         if (J == 0) {
             if (gi < p.n) {
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c)
-                    reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < D / 8 / NSPLIT; ++c)
+                    reinterpret_cast<uint4 *>(orow)[half * (D / 8 / NSPLIT) + c] = make_uint4(0, 0, 0, 0);
             }
             continue;
         }
         if (T5 && h != t5_head) {
             if (!(ok = group_sync(gbar, grp, sh, p.err))) break;
-            for (int idx = stid; idx <= 2 * p.t5_R; idx += 128)
+            for (int idx = stid; idx <= 2 * p.t5_R; idx += 128 * NSPLIT)
                 t5tab[idx] = p.bias[t5_bucket(idx - p.t5_R, p.t5) * p.H + h] * kLog2e;
             if (!(ok = group_sync(gbar, grp, sh, p.err))) break;
             t5_head = h;
         }
-        if (AK) {
+        if (AK) {  // R row -> shared memory, split between the halves
             uint32_t col;
             int buf;
             if (!(ok = wait_sfull(col, buf))) break;
-            for (int c0 = 0; c0 < p.npad_k; c0 += 16) {
+            for (int c0 = 16 * half; c0 < p.npad_k; c0 += 16 * NSPLIT) {
                 uint32_t r[16];
                 ptx::tmem_ld16(lane_base + col + (uint32_t)c0, r);
                 ptx::tmem_ld_wait();
@@ -465,49 +485,40 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
             }
             release_s(buf);
         }
-        if (AV)
+        if (AV && half == 0)
             for (int r = 0; r < W; ++r) brow[r] = 0.f;
+        if (AK || AV) {
+            if (!(ok = pair_sync())) break;  // R copied and bins cleared by both halves
+        }
         float m_ref = -INFINITY, l = 0.f, lo_sum = 0.f, hi_sum = 0.f;
 
         for (int j = 0; j < J; ++j) {
             const int j0 = j * BN;
             const int cols = tile_cols<BN>(nkc, j);  // multiple of 32, > 0
-            // chunks this warp must look at: the ones inside `cols` that a row of the warp
-            // can see (causal: up to key gmax)
-            int live = cols / KB;
+            const int cbeg = half * NC;              // first chunk of this thread
+            int live = cols / KB;                    // chunks any row of the warp can see
             if (CAUSAL) live = min(live, max(0, (gmax - j0) / KB + 1));
-            const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
-            bool p_free = p_item < 2;  // the buffer's previous P . V is known to be done
             uint32_t scol;
             int buf;
             if (!(ok = wait_sfull(scol, buf))) break;
-            if (live == 0) release_s(buf);
+            // ---- S chunks of this thread into registers
+            float x[HC];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                if (c >= cols / KB) break;
-                const uint32_t pcol = pbase + (uint32_t)(c * (KB / 2));
-                if (c >= live) {  // no row of this warp sees these keys: zero P
-                    if (!p_free) {
-                        if (!(ok = wait_pv_item(p_item - 2))) break;
-                        p_free = true;
-                    }
-                    uint32_t z[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) z[e] = 0u;
+            for (int cc = 0; cc < NC; ++cc) {
+                if (cbeg + cc < live) {
                     __syncwarp();
-                    ptx::tmem_st16(pcol, z);
-                    continue;
+                    ptx::tmem_ld32f(lane_base + scol + (uint32_t)((cbeg + cc) * KB), x + cc * KB);
                 }
-                float x[KB];
-                {
-                    uint32_t r[KB];
-                    __syncwarp();
-                    ptx::tmem_ld32(lane_base + scol + (uint32_t)(c * KB), r);
-                    ptx::tmem_ld_wait();
+            }
+            ptx::tmem_ld_wait();
+            release_s(buf);
+            // ---- logits in the log2 domain, relative term added, masks (S2-S4)
+            float hmax = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < KB; ++e) x[e] = __uint_as_float(r[e]);
-                }
-                if (c == live - 1) release_s(buf);
+            for (int cc = 0; cc < NC; ++cc) {
+                const int c = cbeg + cc;
+                if (c >= live) continue;
+                float *xc = x + cc * KB;
                 const int e0 = j0 + c * KB;  // first key of the chunk
                 // offsets j - i over the warp's rows lie in [e0 - gmax, e0 + 31 - gmin]
                 const int lo_lim = T5 ? -p.t5_R : -k;      // at or below: first table row
@@ -515,81 +526,62 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
                 const bool w_left = (e0 + KB - 1 - gmin) <= lo_lim;
                 const bool w_right = (e0 - gmax) >= hi_lim;
                 const int base = e0 - gi;  // offset of element 0 for this row
-                // ---- logits in the log2 domain, relative term added (S2-S4)
-                if (AK) {
+                if (AK || T5) {
+                    const float *tab = AK ? Rrow : t5tab;
+                    const int lim = AK ? k : p.t5_R;
+                    const int top = AK ? hi_off : p.t5_R;
                     if (w_left) {
-                        const float cst = Rrow[0];
+                        const float cst = tab[0];
 #pragma unroll
-                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
+                        for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
                     } else if (w_right) {
-                        const float cst = Rrow[W - 1];
+                        const float cst = tab[lim + top];
 #pragma unroll
-                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
+                        for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
                     } else {
 #pragma unroll
                         for (int e = 0; e < KB; ++e) {
-                            const int o = min(hi_off, max(-k, base + e));
-                            x[e] = fmaf(x[e], sl2, Rrow[o + k]);
-                        }
-                    }
-                } else if (T5) {
-                    const int R = p.t5_R;
-                    if (w_left) {
-                        const float cst = t5tab[0];
-#pragma unroll
-                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
-                    } else if (w_right) {
-                        const float cst = t5tab[2 * R];
-#pragma unroll
-                        for (int e = 0; e < KB; ++e) x[e] = fmaf(x[e], sl2, cst);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < KB; ++e) {
-                            const int o = min(R, max(-R, base + e));
-                            x[e] = fmaf(x[e], sl2, t5tab[o + R]);
+                            const int o = min(top, max(-lim, base + e));
+                            xc[e] = fmaf(xc[e], sl2, tab[o + lim]);
                         }
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < KB; ++e) x[e] *= sl2;
+                    for (int e = 0; e < KB; ++e) xc[e] *= sl2;
                 }
-                // ---- masks: key padding and causal (only chunks that cross a boundary)
                 const bool full = (e0 + KB <= nk) && (!CAUSAL || e0 + KB - 1 <= gmin);
                 if (!full) {
 #pragma unroll
                     for (int e = 0; e < KB; ++e) {
                         const int jj = e0 + e;
-                        if (jj >= nk || (CAUSAL && jj > gi)) x[e] = -INFINITY;
+                        if (jj >= nk || (CAUSAL && jj > gi)) xc[e] = -INFINITY;
                     }
                 }
-                // ---- online softmax (S5) with a lazy rescale
-                float cmax = x[0];
 #pragma unroll
-                for (int e = 1; e < KB; ++e) cmax = fmaxf(cmax, x[e]);
-                float alpha = 1.f;
-                if (cmax > m_ref + kRescaleLog2) {
-                    alpha = ptx::ex2(m_ref - cmax);  // 0 while nothing was seen yet
-                    m_ref = cmax;
-                }
-                const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                float rs = 0.f;
-#pragma unroll
-                for (int e = 0; e < KB; ++e) {
-                    x[e] = ptx::ex2(x[e] - m_use);
-                    rs += x[e];
-                }
-                if (!p_free) {  // before the first P store of this tile
-                    if (!(ok = wait_pv_item(p_item - 2))) break;
-                    p_free = true;
-                }
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    l *= alpha;
-                    lo_sum *= alpha;
-                    hi_sum *= alpha;
+                for (int e = 0; e < KB; ++e) hmax = fmaxf(hmax, xc[e]);
+            }
+            // ---- row maximum over both halves, lazy rescale (S5)
+            float rmax = hmax;
+            if (NSPLIT > 1) {
+                float *slot = xmax + (j & 1) * 2 * BM;
+                slot[half * BM + row] = hmax;
+                if (!(ok = pair_sync())) break;
+                rmax = fmaxf(hmax, slot[(1 - half) * BM + row]);
+            }
+            float alpha = 1.f;
+            if (rmax > m_ref + kRescaleLog2) {
+                alpha = ptx::ex2(m_ref - rmax);  // 0 while nothing was seen yet
+                m_ref = rmax;
+            }
+            // on the first key tile l, the bins and O hold nothing yet: no rescale needed
+            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {  // same in every half
+                l *= alpha;
+                lo_sum *= alpha;
+                hi_sum *= alpha;
+                if (half == 0) {
                     if (AV && alpha != 1.f)
                         for (int r = 0; r < W; ++r) brow[r] *= alpha;
-                    __syncwarp();
-                    if (j >= 1) {  // O holds P V of the earlier key tiles: wait for the last
+                    if (j >= 1) {  // O holds P V of the earlier key tiles
                         if (!(ok = wait_pv_item(p_item - 1))) break;
 #pragma unroll
                         for (int c0 = 0; c0 < D; c0 += 32) {
@@ -601,72 +593,114 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
                                 r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
                             ptx::tmem_st32(lane_base + TL::O + (uint32_t)c0, r);
                         }
-                    }
-                    for (int c2 = 0; c2 < c; ++c2)  // P chunks already written for this tile
-                        scale_packed16(pbase + (uint32_t)(c2 * (KB / 2)), alpha);
-                    ptx::tmem_st_wait();
-                }
-                l += rs;
-                // ---- value bins (S7)
-                if (AV) {
-                    if (w_left) {
-                        lo_sum += rs;
-                    } else if (w_right) {
-                        hi_sum += rs;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < KB; ++e) {
-                            const int o = min(hi_off, max(-k, base + e));
-                            brow[o + k] += x[e];
-                        }
+                        ptx::tmem_st_wait();
                     }
                 }
-                // ---- P (bf16 pairs) into TMEM
-                {
-                    uint32_t pk[KB / 2];
-#pragma unroll
-                    for (int e = 0; e < KB / 2; ++e) pk[e] = pack2(x[2 * e], x[2 * e + 1]);
-                    __syncwarp();
-                    ptx::tmem_st16(pcol, pk);
+                if (AV && NSPLIT > 1) {  // bins are rescaled before the other half adds new ones
+                    if (!(ok = pair_sync())) break;
                 }
             }
-            if (!ok) break;
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            // ---- exponentials, row sum, value bins (S7), P (bf16 pairs) into TMEM
+            if (p_item >= 2) {  // the P buffer's previous P . V is done
+                if (!(ok = wait_pv_item(p_item - 2))) break;
+            }
+            const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc) {
+                const int c = cbeg + cc;
+                if (c * KB >= cols) continue;  // never read by P V
+                const uint32_t pcol = pbase + (uint32_t)(c * (KB / 2));
+                uint32_t pk[KB / 2];
+                if (c >= live) {  // no row of this warp sees these keys
+#pragma unroll
+                    for (int e = 0; e < KB / 2; ++e) pk[e] = 0u;
+                } else {
+                    float *xc = x + cc * KB;
+                    float rs = 0.f;
+#pragma unroll
+                    for (int e = 0; e < KB; ++e) {
+                        xc[e] = ptx::ex2(xc[e] - m_use);
+                        rs += xc[e];
+                    }
+                    l += rs;
+                    if (AV) {
+                        const int e0 = j0 + c * KB;
+                        const bool w_left = (e0 + KB - 1 - gmin) <= -k;
+                        const bool w_right = (e0 - gmax) >= hi_off;
+                        if (w_left) {
+                            lo_sum += rs;
+                        } else if (w_right) {
+                            hi_sum += rs;
+                        } else {
+                            // interior bins get exactly one key each over the whole row, so
+                            // they are stored (not accumulated); the two end bins are sums
+                            // branch-free: end-bin terms go to the sums, interior ones
+                            // to their bin; the others write a spare slot (index W)
+                            const int base = e0 - gi;
+#pragma unroll
+                            for (int e = 0; e < KB; ++e) {
+                                const int o = base + e;
+                                const bool lo = o <= -k, hi = !lo && o >= hi_off;
+                                lo_sum += lo ? xc[e] : 0.f;
+                                hi_sum += hi ? xc[e] : 0.f;
+                                brow[(lo || hi) ? W : o + k] = xc[e];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < KB / 2; ++e) pk[e] = pack2(xc[2 * e], xc[2 * e + 1]);
+                }
+                __syncwarp();
+                ptx::tmem_st16(pcol, pk);
+            }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(B_P_FULL0 + (int)(p_item & 1u)));
             ++p_item;
         }
         if (!ok) break;
+        // ---- combine the halves: l and the end-bin sums
+        if (NSPLIT > 1) {
+            xsum[(half * 3 + 0) * BM + row] = l;
+            xsum[(half * 3 + 1) * BM + row] = lo_sum;
+            xsum[(half * 3 + 2) * BM + row] = hi_sum;
+            if (!(ok = pair_sync())) break;
+            l += xsum[((1 - half) * 3 + 0) * BM + row];
+            lo_sum += xsum[((1 - half) * 3 + 1) * BM + row];
+            hi_sum += xsum[((1 - half) * 3 + 2) * BM + row];
+        }
         if (AV) {
-            // bins (bf16 pairs) become the A operand of O += beta W^V
-            brow[0] += lo_sum;
-            brow[W - 1] += hi_sum;
+            // bins (bf16 pairs) become the A operand of O += beta W^V (written by half 0)
             if (p_item >= 2 && !(ok = wait_pv_item(p_item - 2))) break;
-            const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
-            __syncwarp();
-            for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
-                uint32_t pk[16];
+            if (half == 0) {
+                brow[0] += lo_sum;
+                brow[W - 1] += hi_sum;
+                const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
+                for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r0 = c0 + 2 * e;
-                    pk[e] = pack2(r0 < W ? brow[r0] : 0.f, r0 + 1 < W ? brow[r0 + 1] : 0.f);
+                    for (int e = 0; e < 16; ++e) {
+                        const int r0 = c0 + 2 * e;
+                        pk[e] = pack2(r0 < W ? brow[r0] : 0.f, r0 + 1 < W ? brow[r0 + 1] : 0.f);
+                    }
+                    __syncwarp();
+                    ptx::tmem_st16(pbase + (uint32_t)(c0 / 2), pk);
                 }
-                __syncwarp();
-                ptx::tmem_st16(pbase + (uint32_t)(c0 / 2), pk);
+                ptx::tmem_st_wait();
             }
-            ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(B_P_FULL0 + (int)(p_item & 1u)));
             ++p_item;
         }
-        // ---- epilogue (S8): O / l -> bf16 -> global
+        // ---- epilogue (S8): O / l -> bf16 -> global, D / NSPLIT columns per thread
         if (!(ok = wait_w(bar(B_O_FULL), tiles & 1u))) break;
         ptx::tc_fence_after();
         __syncwarp();
         ++tiles;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = half * (D / NSPLIT); c0 < (half + 1) * (D / NSPLIT); c0 += 32) {
             uint32_t r[32];
             ptx::tmem_ld32(lane_base + TL::O + (uint32_t)c0, r);
             ptx::tmem_ld_wait();
@@ -689,9 +723,10 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
 
 // ======================================================================= kernel
 template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
-__global__ void __launch_bounds__(kThreads, CPS)
+__global__ void __launch_bounds__(TmemLayout<CPS>::THREADS, CPS)
     relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ak,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kf,
+                      const __grid_constant__ CUtensorMap tm_vf, const __grid_constant__ CUtensorMap tm_ak,
                       const __grid_constant__ CUtensorMap tm_av, const __grid_constant__ Params p) {
     using TL = TmemLayout<CPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -710,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
             uint32_t cnt = 1;
             if (i == B_S_EMPTY0 || i == B_S_EMPTY1 || i == B_P_FULL0 || i == B_P_FULL1 ||
                 i == B_GROUP)
-                cnt = 128;
+                cnt = 128 * TL::NSPLIT;
+            if (i >= B_PAIR0 && i < B_PAIR0 + 4) cnt = 32 * TL::NSPLIT;
             ptx::mbar_init(bars + 8u * (uint32_t)i, cnt);
         }
         *sh.abort_flag = 0;
@@ -718,6 +754,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
         ptx::tma_prefetch_desc(&tm_q);
         ptx::tma_prefetch_desc(&tm_k);
         ptx::tma_prefetch_desc(&tm_v);
+        ptx::tma_prefetch_desc(&tm_kf);
+        ptx::tma_prefetch_desc(&tm_vf);
     }
     if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TL::cols);
     ptx::tc_fence_before();
@@ -726,12 +764,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if ((threadIdx.x & 31) == 0) producer_role<D, AK, AV, CAUSAL, CPS>(p, sh, &tm_q, &tm_k, &tm_v, &tm_ak, &tm_av);
+        if ((threadIdx.x & 31) == 0) producer_role<D, AK, AV, CAUSAL, CPS>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
+                                                      &tm_av);
         __syncwarp();
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0) mma_role<D, AK, AV, CAUSAL, CPS>(p, sh, tmem);
         __syncwarp();
-    } else {
+    } else if (warp >= TL::SW0) {
         softmax_role<D, AK, AV, T5, CAUSAL, CPS>(p, sh, tmem);
     }
 

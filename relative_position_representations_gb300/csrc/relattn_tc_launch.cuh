@@ -51,6 +51,7 @@ struct DeviceInfo {
     int smem_optin = 0;      // max dynamic shared memory of one block
     int smem_per_sm = 0;     // shared memory of one SM
     int smem_reserved = 0;   // shared memory the system keeps per block
+    int l2_bytes = 0;
 };
 
 inline DeviceInfo device_info() {
@@ -65,6 +66,7 @@ inline DeviceInfo device_info() {
         cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         cudaDeviceGetAttribute(&cache[dev].smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         cudaDeviceGetAttribute(&cache[dev].smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        cudaDeviceGetAttribute(&cache[dev].l2_bytes, cudaDevAttrL2CacheSize, dev);
     }
     return cache[dev];
 }
@@ -72,7 +74,7 @@ inline DeviceInfo device_info() {
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
-cudaError_t launch_variant(const CUtensorMap (&tm)[5], const Params &p, uint32_t smem_bytes,
+cudaError_t launch_variant(const CUtensorMap (&tm)[7], const Params &p, uint32_t smem_bytes,
                            cudaStream_t s) {
     auto kern = relattn_tc_kernel<D, AK, AV, T5, CAUSAL, CPS>;
     // Opt in to the device's whole shared-memory budget once per device and variant, so
@@ -91,11 +93,16 @@ cudaError_t launch_variant(const CUtensorMap (&tm)[5], const Params &p, uint32_t
         if (!opted[dev]) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin);
             if (e != cudaSuccess) return e;
+            // all of the unified L1/shared storage as shared memory, so that two CTAs fit
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
             opted[dev] = true;
         }
         if (CPS > 1) {
             int nb = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kThreads, smem_bytes);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, TmemLayout<CPS>::THREADS,
+                                                              smem_bytes);
             if (e != cudaSuccess) return e;
             resident[dev] = nb;
             per_sm = nb < 1 ? 1 : (nb > CPS ? CPS : nb);
@@ -103,12 +110,13 @@ cudaError_t launch_variant(const CUtensorMap (&tm)[5], const Params &p, uint32_t
     }
     const int want = di.sms * per_sm;
     const int grid = p.num_tiles < want ? p.num_tiles : want;
-    kern<<<grid, kThreads, smem_bytes, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], p);
+    kern<<<grid, TmemLayout<CPS>::THREADS, smem_bytes, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5],
+                                                          tm[6], p);
     return cudaGetLastError();
 }
 
 template <int D, bool T5, bool CAUSAL, int CPS>
-cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[5], const Params &p,
+cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[7], const Params &p,
                          uint32_t smem, cudaStream_t s) {
     if constexpr (T5) {
         return launch_variant<D, false, false, true, CAUSAL, CPS>(tm, p, smem, s);
@@ -133,6 +141,7 @@ inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int bn, int sta
     p.off_r = off;    if (ak) off += round_up((uint32_t)BM * p.SR * 4, 16);  // per-row tables
     p.off_beta = off; if (av) off += round_up((uint32_t)BM * p.SR * 4, 16);
     p.off_t5 = off;   if (t5mode) off += round_up((uint32_t)(2 * p.t5_R + 1) * 4, 16);
+    p.off_x = off;    if (bn == 128) off += (2 * 2 + 2 * 3) * BM * 4;  // row-half exchange
     p.off_bar = off;  off += (uint32_t)kNumBars * 8 + 16;
     p.stages = stages;
     p.stage_bytes = stage_bytes;
@@ -161,7 +170,7 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         p.W = a.causal ? a.clip_k + 1 : 2 * a.clip_k + 1;
         if (p.W > 128) return cudaErrorNotSupported;
     }
-    p.SR = p.W + (p.W & 1);
+    p.SR = (p.W + 2) & ~1;  // even (conflict-free gathers), with a spare slot at index W
     p.npad_k = (int)round_up((uint32_t)p.W, 16);
     p.kpad_v = p.npad_k;
     p.table_heads = a.ths != 0 ? 1 : 0;
@@ -174,13 +183,20 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
 
     const DeviceInfo di = device_info();
     if (di.sms <= 0 || di.smem_optin <= 0) return cudaErrorInvalidDevice;
+    // schedule heads in groups whose K and V fit in half of L2
+    {
+        const int64_t per_head = 2LL * a.n * D * 2;
+        const int64_t fit = di.l2_bytes > 0 ? (int64_t)di.l2_bytes / 2 / (per_head > 0 ? per_head : 1) : p.BH;
+        p.head_group = (int)(fit < 1 ? 1 : (fit > p.BH ? p.BH : fit));
+    }
     // two CTAs per SM (64-key tiles, TMEM 256 columns each) when D = 64, the staged table
     // rows fit a 64-key score buffer and the shared memory of both fits; else one CTA per
     // SM with 128-key tiles
     int cps = 1;
     uint32_t smem = 0;
     if (D == 64 && p.npad_k <= 64) {
-        const int64_t budget2 = ((int64_t)di.smem_per_sm - 2 * (int64_t)di.smem_reserved) / 2;
+        const int64_t budget2 =
+            ((int64_t)di.smem_per_sm - 2 * (int64_t)di.smem_reserved) / 2 - 2048;  // margin
         Params q = p;
         const uint32_t fixed = layout<D>(q, ak, av, t5mode, 64, 0);
         const int64_t st = (budget2 - (int64_t)fixed) / ((int64_t)64 * D * 2);
@@ -199,20 +215,23 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     if (smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
 
     // ---- TMA descriptors (the output is written with plain stores)
-    CUtensorMap tm[5];
+    // q; k and v in 32-row boxes; k and v in whole-tile boxes; the two edge tables
+    CUtensorMap tm[7];
     const uint64_t d = (uint64_t)D, n = (uint64_t)a.n, BH = (uint64_t)p.BH;
     const uint64_t rs = d * 2, hs = n * d * 2;
+    const uint32_t bn = cps == 2 ? 64u : 128u;
     if (!make_map(&tm[0], a.q, d, n, BH, rs, hs, BM) || !make_map(&tm[1], a.k, d, n, BH, rs, hs, KB) ||
-        !make_map(&tm[2], a.v, d, n, BH, rs, hs, KB))
+        !make_map(&tm[2], a.v, d, n, BH, rs, hs, KB) || !make_map(&tm[3], a.k, d, n, BH, rs, hs, bn) ||
+        !make_map(&tm[4], a.v, d, n, BH, rs, hs, bn))
         return cudaErrorInvalidValue;
-    tm[3] = tm[0];
-    tm[4] = tm[0];
+    tm[5] = tm[0];
+    tm[6] = tm[0];
     const uint64_t rows = (uint64_t)(2 * a.clip_k + 1);
     const uint64_t Ht = p.table_heads ? (uint64_t)a.H : 1;
     const uint64_t ths_bytes = p.table_heads ? (uint64_t)a.ths * 2 : rows * d * 2;
-    if (ak && !make_map(&tm[3], a.aK, d, rows, Ht, rs, ths_bytes, (uint32_t)p.npad_k))
+    if (ak && !make_map(&tm[5], a.aK, d, rows, Ht, rs, ths_bytes, (uint32_t)p.npad_k))
         return cudaErrorInvalidValue;
-    if (av && !make_map(&tm[4], a.aV, d, rows, Ht, rs, ths_bytes, (uint32_t)p.kpad_v))
+    if (av && !make_map(&tm[6], a.aV, d, rows, Ht, rs, ths_bytes, (uint32_t)p.kpad_v))
         return cudaErrorInvalidValue;
 
     if constexpr (D == 64) {

@@ -134,6 +134,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : RELATTN_R8(0), RELATTN_R8(8), RELATTN_R8(16), RELATTN_R8(24)
         : "r"(taddr));
 }
+// same as tmem_ld32, straight into fp32 registers
+#define RELATTN_F8(i) "=f"(r[i]), "=f"(r[i + 1]), "=f"(r[i + 2]), "=f"(r[i + 3]), \
+    "=f"(r[i + 4]), "=f"(r[i + 5]), "=f"(r[i + 6]), "=f"(r[i + 7])
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : RELATTN_F8(0), RELATTN_F8(8), RELATTN_F8(16), RELATTN_F8(24)
+        : "r"(taddr));
+}
+#undef RELATTN_F8
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
