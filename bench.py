@@ -269,6 +269,22 @@ def make_event(external: bool):
     return torch.cuda.Event(enable_timing=True)
 
 
+def whole_job(elapsed_ms: float, work: float, world: int, device) -> tuple:
+    """Whole-job timing over ranks: the slowest rank's time and the work of all ranks.
+
+    Each rank processes its own independent shard (weak scaling), so the job ends when the
+    slowest rank ends. No data moves between ranks; only these two scalars are reduced."""
+    if world <= 1:
+        return float(elapsed_ms), float(work)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    ww = torch.tensor([work], device=device, dtype=torch.float64)
+    dist.all_reduce(ww, op=dist.ReduceOp.SUM)
+    return float(tt.item()), float(ww.item())
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -368,16 +384,7 @@ def run_ours(args, rank, world, local_rank):
         kern_src = "timed-region elapsed / steps (events in graphs unavailable)"
 
     # whole-job reduction over ranks (max time, summed work)
-    import torch as _t
-    t_max = elapsed_ms
-    total_flops = flops * steps
-    if world > 1:
-        tt = _t.tensor([elapsed_ms], device=dev, dtype=_t.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-        ff = _t.tensor([total_flops], device=dev, dtype=_t.float64)
-        dist.all_reduce(ff, op=dist.ReduceOp.SUM)
-        total_flops = float(ff.item())
+    t_max, total_flops = whole_job(elapsed_ms, flops * steps, world, dev)
     value = total_flops / (t_max * 1e-3) / 1e12
 
     # end to end through the C ABI with pinned host buffers

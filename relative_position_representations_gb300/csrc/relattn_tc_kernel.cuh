@@ -7,30 +7,34 @@
 //   z_i = sum_j a_ij v_j + sum_r beta_ir w^V_r,   beta_ir = sum_{j: clip(j-i,k)+k = r} a_ij.
 // T5 variant ("Relative position embeddings", section "T5"): e_ij = scale*q_i.k_j + b[bucket].
 //
-// Persistent CTAs (one or two per SM) loop over work items (query tile of 128 rows, head),
-// longest causal rows first. Warp roles:
-//   warp 0      TMA producer: Q tile and edge tables, then K/V tiles of 128 keys (in boxes of
-//               32 rows, none past the last allowed key) into a ring of stages, in the order
-//               the MMA warp consumes them (K0 K1 V0 K2 V1 ...), and W^V at the end.
-//   warp 1      MMA issuer (one thread). Per tile: R = Q W^K^T into a score buffer, then
-//               S_j = Q K_j^T into the score buffer(s), O += P_j V_j with P read from TMEM,
-//               and at the end O += beta W^V with the bins read from TMEM.
-//   warps 2..   softmax / epilogue: each query row (= TMEM lane) is handled by NSPLIT
-//               threads (one per 64 keys of a key tile; the two halves of a 128-key tile
-//               exchange their row maxima through shared memory). Per key tile: add the
-//               relative term (a per-row constant for 32-key chunks that lie beyond +-k for
-//               the whole warp, a shared-memory gather inside the band), mask, online softmax
-//               in the exp2 domain with a lazy rescale (only when the running max grows by
-//               more than 2^8), value bins, bf16 P into TMEM. Chunks no row of the warp can
-//               see are skipped. Epilogue: O / l -> bf16.
-// Score (S) and probability (P) tiles are double-buffered in TMEM, so S_{j+1} and the
-// P_{j-1} V_{j-1} product overlap the softmax of tile j.
-// TMEM: CPS = 1 (one CTA per SM, 128-key tiles): S0 [0,128) S1 [128,256) O [256,256+D)
-//       P0 [384,448) P1 [448,512);
-//       CPS = 2 (two CTAs per SM, D = 64, 64-key tiles): S0 [0,64) S1 [64,128) P0 [128,160)
-//       P1 [160,192) O [192,256).
-// Every wait is bounded; a wait that runs out sets the device status word and the CTA
-// drains and exits.
+// One persistent CTA per SM. A work item is two query tiles of 128 rows ("slots" 0 and 1):
+// normally two neighbouring tiles of the same head, which then share every K/V tile, or,
+// for heads with an odd number of query tiles, the leftover tiles of two heads. Items are
+// scheduled in groups of heads whose K/V fit in half of L2, longest causal rows first. When
+// the per-row tables of two slots do not fit shared memory, an item is one tile.
+// Warp roles (384 threads):
+//   warp 0      TMA producer: both Q tiles and the edge tables, then K/V tiles of 128 keys
+//               (whole-tile boxes, 32-row boxes for the last, partly valid tile) into a ring,
+//               in the order the MMA warp consumes them.
+//   warp 1      MMA issuer (the whole warp runs it; one elected lane issues each tcgen05
+//               instruction, so operands stay warp-uniform): per slot R = Q W^K^T,
+//               S_j = Q K_j^T, O += P_j V_j (P read from TMEM), O += beta W^V, walking the
+//               K/V ring in the order it was filled; one wait per K/V tile serves both slots.
+//   warps 2-3   idle (registers are allocated per 4-warp group).
+//   warps 4-7   softmax / epilogue of slot 0, warps 8-11 of slot 1: one thread per query row
+//               (= TMEM lane) holding the whole 128-key score row. The relative term is a
+//               per-row constant on 32-key chunks that lie beyond +-k for the whole warp (the
+//               scale and that constant then fold into the exponent's FMA, and the row
+//               maximum is taken on the raw scores) and a shared-memory gather inside the
+//               band; online softmax in the exp2 domain with a lazy rescale (only when the
+//               running max grows by more than 2^8); value bins; bf16 P into TMEM; epilogue
+//               O / l -> bf16 -> global.
+// TMEM (512 columns): S of slot s at 128 s, O at 256 + D s; P (bf16 pairs, 64 columns) at
+// 384 + 64 s when D = 64, over the first half of the slot's S when D = 128. With its own P
+// columns a slot's S_{j+1} is computed while its softmax still works on S_j; over S, S_{j+1}
+// waits for the P_j . V_j that reads those columns.
+// Every wait is bounded; a wait that runs out sets the device status word and the CTA drains
+// and exits.
 #pragma once
 
 #include <cstdint>
@@ -44,58 +48,67 @@
 namespace relattn {
 namespace tc {
 
-constexpr int BM = 128;   // query rows per tile (= TMEM lanes)
-constexpr int KB = 32;    // key rows per TMA box and keys per softmax chunk
-constexpr int HC = 64;    // keys of a key tile handled by one softmax thread
+constexpr int BM = 128;        // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;        // keys per key tile
+constexpr int KB = 32;         // key rows per partial TMA box and keys per softmax chunk
+constexpr int NCH = BN / KB;   // chunks per key tile
+constexpr int kThreads = 384;
+constexpr int kSoftWarp0 = 4;  // first softmax warp; slot s uses warps 4 + 4 s .. 7 + 4 s
+// registers per thread: launched with kLaunchRegs; the producer/MMA warpgroup hands
+// registers to the two softmax warpgroups (sum stays kThreads * kLaunchRegs)
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 72;
+constexpr int kSoftRegs = 216;
+static_assert(128 * kCtrlRegs + 256 * kSoftRegs == kThreads * kLaunchRegs, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 // bound of every device wait, in SM clock cycles (about one second at 2 GHz); clock64 is
 // read only after a wait did not succeed at once and then every 256 polls
 constexpr long long kWaitLimitCycles = 2000000000ll;
 
-template <int CPS>
-struct TmemLayout {
-    static constexpr int BN = CPS == 1 ? 128 : 64;  // keys per key tile
-    static constexpr int NSPLIT = BN / HC;          // softmax threads per query row
-    // registers are allocated per 4-warp group: two CTAs per SM need whole warpgroups
-    // (warps 2-3 idle) to stay within 128 registers a thread
-    static constexpr int SW0 = CPS == 2 ? 4 : 2;     // first softmax warp
-    static constexpr int THREADS = 32 * SW0 + 128 * NSPLIT;
-    static constexpr uint32_t cols = CPS == 1 ? 512u : 256u;
-    static constexpr uint32_t S = 0;                         // S buffer b at S + b * BN
-    static constexpr uint32_t O = CPS == 1 ? 256u : 192u;    // D columns
-    static constexpr uint32_t P = CPS == 1 ? 384u : 128u;    // P buffer b at P + b * BN / 2
+template <int D>
+struct Tm {
+    static constexpr bool P_ALIAS = D == 128;
+    static __device__ __forceinline__ uint32_t S(int s) { return 128u * (uint32_t)s; }
+    static __device__ __forceinline__ uint32_t O(int s) { return 256u + (uint32_t)(D * s); }
+    static __device__ __forceinline__ uint32_t P(int s) {
+        return P_ALIAS ? 128u * (uint32_t)s : 384u + 64u * (uint32_t)s;
+    }
 };
 
 // barrier slots
 enum : int {
-    B_Q_FULL = 0, B_Q_EMPTY, B_S_FULL0, B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_P_FULL0, B_P_FULL1,
-    B_PV_DONE0, B_PV_DONE1, B_AV_FULL, B_AV_EMPTY, B_O_FULL, B_DRAIN, B_GROUP, B_PAIR0,
-    B_KV0 = B_PAIR0 + 4
+    B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_DRAIN,
+    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, GROUP
+    B_KV0 = B_SLOT0 + 2 * 6
 };
+enum : int { SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_GROUP };
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
 
 struct Params {
     int BH, H, n;
-    int n_qtiles, num_tiles;
+    int n_qtiles, num_items, head_group;
     float scale_log2;   // scale * log2(e)
     const int *kv_len;  // [B] or null
     int *err;           // device status word
     void *out;          // [B, H, n, D] bf16
     int clip_k;         // Shaw: k
     int W;              // table rows staged: k+1 (causal) or 2k+1
-    int SR;             // row stride (floats) of the per-row tables in shared memory
+    int SR;             // row stride (elements) of the R rows in shared memory
+    int SB;             // row stride (floats) of the value bins, with a spare slot at index W
+    int pair;           // 1: two query tiles per item, 0: one
     int npad_k;         // W rounded up to 16: N of the R = Q W^K^T MMA
     int kpad_v;         // W rounded up to 16: K of the beta W^V MMA
     int table_heads;    // 1: tables indexed by head, 0: one shared table
+    int r_bf16;         // the R rows are kept as bf16 (when fp32 does not fit)
+    int two_tables;     // the two slots may belong to different heads: own table buffers
     const float *bias;  // T5 [num_buckets, H]
     int t5_R;           // T5 offset-table radius (bucket is constant beyond it)
     T5Buckets t5;
-    uint32_t off_q, off_kv, off_ak, off_av, off_r, off_beta, off_t5, off_x, off_bar;
+    uint32_t off_q[2], off_kv, off_ak[2], off_av[2], off_r[2], off_beta[2], off_t5[2], off_bar;
     int stages;
     uint32_t stage_bytes;
-    int head_group;     // heads whose tiles are scheduled together (K/V reuse in L2)
 };
 
 struct Shared {
@@ -129,8 +142,8 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Barrier among the 128 softmax threads on an mbarrier, so the wait stays bounded (a plain
-// bar.sync would hang if a thread of the group left after a timeout). Warp-uniform result.
+// Barrier among the 128 softmax threads of a slot on an mbarrier, so the wait stays bounded
+// (a plain bar.sync would hang if a thread of the group left after a timeout).
 __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t &it, const Shared &sh, int *err) {
     ptx::mbar_arrive(bar);
     const bool ok = wait_bar(bar, it & 1u, sh, err);
@@ -138,15 +151,56 @@ __device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t &it, const Sha
     return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
 }
 
-// Work order: heads in groups of head_group (their K/V stay in L2 while the group runs);
-// inside a group, the query tiles with the most keys (causal) come first.
-__device__ __forceinline__ void decode_tile(const Params &p, int t, int &bh, int &qt) {
-    const int per_group = p.head_group * p.n_qtiles;
-    const int g = t / per_group, r = t - g * per_group;
-    const int g0 = g * p.head_group;
-    const int gsize = min(p.head_group, p.BH - g0);
-    qt = p.n_qtiles - 1 - r / gsize;
-    bh = g0 + r % gsize;
+// ----------------------------------------------------------------------- work items
+struct Item {
+    int bh[2], qt[2];
+    bool valid[2];
+    bool shared;  // both slots are tiles of one head: they share K/V
+};
+
+__host__ __device__ inline int items_per_group(int gsize, int Q, int pair) {
+    if (!pair) return Q * gsize;
+    return ((Q & 1) ? (gsize + 1) / 2 : 0) + (Q >> 1) * gsize;
+}
+
+// Items of a group of heads: first the leftover (last, longest) query tile of heads with an
+// odd tile count, two heads per item; then pairs (2i+1, 2i) of the same head, i descending.
+// Without pairing an item is one tile, again longest first.
+__device__ __forceinline__ Item decode_item(const Params &p, int t) {
+    const int Q = p.n_qtiles, G = p.head_group;
+    const int full = items_per_group(G, Q, p.pair);
+    const int g = t / full;
+    int r = t - g * full;
+    const int g0 = g * G;
+    const int gsize = min(G, p.BH - g0);
+    Item it;
+    if (!p.pair) {
+        it.qt[0] = it.qt[1] = Q - 1 - r / gsize;
+        it.bh[0] = it.bh[1] = g0 + r % gsize;
+        it.valid[0] = true;
+        it.valid[1] = false;
+        it.shared = false;
+        return it;
+    }
+    const int singles = (Q & 1) ? (gsize + 1) / 2 : 0;
+    if (r < singles) {
+        it.qt[0] = it.qt[1] = Q - 1;
+        it.bh[0] = g0 + 2 * r;
+        it.bh[1] = g0 + 2 * r + 1;
+        it.valid[0] = true;
+        it.valid[1] = 2 * r + 1 < gsize;
+        it.shared = false;
+    } else {
+        r -= singles;
+        const int i = (Q >> 1) - 1 - r / gsize;
+        const int h = g0 + r % gsize;
+        it.bh[0] = it.bh[1] = h;
+        it.qt[0] = 2 * i + 1;
+        it.qt[1] = 2 * i;
+        it.valid[0] = it.valid[1] = true;
+        it.shared = true;
+    }
+    return it;
 }
 
 // number of allowed keys (before the causal clip) of the sequence of head bh
@@ -155,71 +209,149 @@ __device__ __forceinline__ int keys_of(const Params &p, int bh) {
     return max(0, min(p.kv_len[bh / p.H], p.n));
 }
 
-// keys any row of query tile i0 may see
+// keys any row of query tile qt may see
 template <bool CAUSAL>
-__device__ __forceinline__ int tile_keys(const Params &p, int bh, int i0) {
+__device__ __forceinline__ int tile_keys(const Params &p, int bh, int qt) {
     const int nk = keys_of(p, bh);
-    return CAUSAL ? min(nk, i0 + BM) : nk;
+    return CAUSAL ? min(nk, qt * BM + BM) : nk;
 }
 
 // columns of key tile j that are loaded and multiplied: the allowed keys rounded up to
 // whole 32-row boxes
-template <int BN>
 __device__ __forceinline__ int tile_cols(int nkc, int j) {
     const int c = nkc - j * BN;
     return c >= BN ? BN : ((c + KB - 1) / KB) * KB;
 }
 
+// K/V ring order of an item, which is also the order the MMA warp consumes the entries in.
+// Every slot starts with K_0. With its own P columns (EARLY_S) a slot then takes K_{j+1}
+// before V_j, so S_{j+1} is computed while its softmax works on S_j; with P over S it takes
+// V_j before K_{j+1}. Shared items hold one entry per tile for both slots (an entry serves
+// every slot whose tiles reach it); otherwise each slot has its own entries, interleaved.
+template <bool CAUSAL, bool EARLY_S>
+struct Plan {
+    int nkc[2], J[2];
+    int Jmax;
+    bool shared;
+    __device__ __forceinline__ void make(const Params &p, const Item &it) {
+        shared = it.shared;
+        Jmax = 0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            nkc[s] = it.valid[s] ? tile_keys<CAUSAL>(p, it.bh[s], it.qt[s]) : 0;
+            J[s] = (nkc[s] + BN - 1) / BN;
+            Jmax = max(Jmax, J[s]);
+        }
+    }
+    __device__ __forceinline__ bool active(int s) const { return J[s] > 0; }
+    // slots (bit mask) that use K or V tile j
+    __device__ __forceinline__ int users(int j) const {
+        return (j < J[0] ? 1 : 0) | (j < J[1] ? 2 : 0);
+    }
+    // calls fn(isK, j, mask, src) for each ring entry in order; stops when fn returns false
+    template <class F>
+    __device__ __forceinline__ bool visit(F &&fn) const {
+        if (shared) {
+            if (!fn(true, 0, users(0), 0)) return false;
+            for (int j = 0; j < Jmax; ++j) {
+                const bool k_next = j + 1 < Jmax;
+                if (EARLY_S && k_next && !fn(true, j + 1, users(j + 1), 0)) return false;
+                if (!fn(false, j, users(j), 0)) return false;
+                if (!EARLY_S && k_next && !fn(true, j + 1, users(j + 1), 0)) return false;
+            }
+            return true;
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            if (J[s] > 0 && !fn(true, 0, 1 << s, s)) return false;
+        for (int j = 0; j < Jmax; ++j) {
+            if (EARLY_S) {
+#pragma unroll
+                for (int s = 0; s < 2; ++s)
+                    if (j + 1 < J[s] && !fn(true, j + 1, 1 << s, s)) return false;
+            }
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+                if (j < J[s] && !fn(false, j, 1 << s, s)) return false;
+            if (!EARLY_S) {
+#pragma unroll
+                for (int s = 0; s < 2; ++s)
+                    if (j + 1 < J[s] && !fn(true, j + 1, 1 << s, s)) return false;
+            }
+        }
+        return true;
+    }
+    // keys of tile j loaded for an entry (the largest of the slots using it)
+    __device__ __forceinline__ int load_cols(int j, int mask) const {
+        int c = 0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            if (mask & (1 << s)) c = max(c, tile_cols(nkc[s], j));
+        return c;
+    }
+};
+
 // ======================================================================= producer
-template <int D, bool AK, bool AV, bool CAUSAL, int CPS>
+template <int D, bool AK, bool AV, bool CAUSAL>
 __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                               const CUtensorMap *tm_kf, const CUtensorMap *tm_vf,
                               const CUtensorMap *tm_ak, const CUtensorMap *tm_av) {
     constexpr int DB = D / 64;
-    constexpr int BN = TmemLayout<CPS>::BN;
+    constexpr bool EARLY_S = !Tm<D>::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    const uint32_t sQ = sh.base + p.off_q, sKV = sh.base + p.off_kv;
-    const uint32_t sAK = sh.base + p.off_ak, sAV = sh.base + p.off_av;
+    const uint32_t sKV = sh.base + p.off_kv;
     const int S = p.stages;
     uint32_t kv_it = 0, q_it = 0, av_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        int bh, qt;
-        decode_tile(p, t, bh, qt);
-        const int i0 = qt * BM, h = bh % p.H;
-        const int nkc = tile_keys<CAUSAL>(p, bh, i0);
-        const int J = (nkc + BN - 1) / BN;
-        if (J == 0) continue;
+    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+        const Item it = decode_item(p, t);
+        Plan<CAUSAL, EARLY_S> pl;
+        pl.make(p, it);
+        if (pl.Jmax == 0) continue;
         if (!(ok = wait_bar(bar(B_Q_EMPTY), (q_it & 1u) ^ 1u, sh, p.err))) break;
-        const uint32_t qbytes = (uint32_t)BM * D * 2 + (AK ? (uint32_t)p.npad_k * D * 2 : 0u);
-        ptx::mbar_expect_tx(bar(B_Q_FULL), qbytes);
-#pragma unroll
-        for (int blk = 0; blk < DB; ++blk)
-            ptx::tma_load_3d(sQ + blk * BM * 128, tm_q, bar(B_Q_FULL), blk * 64, i0, bh);
-        if (AK) {
-#pragma unroll
-            for (int blk = 0; blk < DB; ++blk)
-                ptx::tma_load_3d(sAK + blk * p.npad_k * 128, tm_ak, bar(B_Q_FULL), blk * 64, 0,
-                                 p.table_heads ? h : 0);
-        }
         ++q_it;
-        // K/V tiles in consumption order: K0, K1, V0, K2, V1, ..., K_{J-1}, V_{J-2}, V_{J-1}
-        for (int s = 0; s < 2 * J; ++s) {
-            int j;
-            bool isK;
-            if (s == 0) { j = 0; isK = true; }
-            else if (s == 2 * J - 1) { j = J - 1; isK = false; }
-            else if (s & 1) { j = (s + 1) >> 1; isK = true; }
-            else { j = (s >> 1) - 1; isK = false; }
+        // edge-table buffer b serves slot b (two_tables) or both slots; tab_head[b] < 0: unused
+        int tab_head[2] = {-1, -1};
+        if (p.two_tables) {
+            for (int s = 0; s < 2; ++s)
+                if (pl.active(s)) tab_head[s] = p.table_heads ? it.bh[s] % p.H : 0;
+        } else {
+            const int s = pl.active(0) ? 0 : 1;
+            tab_head[0] = p.table_heads ? it.bh[s] % p.H : 0;
+        }
+        uint32_t qbytes = 0;
+        for (int s = 0; s < 2; ++s) {
+            if (pl.active(s)) qbytes += (uint32_t)BM * D * 2;
+            if (AK && tab_head[s] >= 0) qbytes += (uint32_t)p.npad_k * D * 2;
+        }
+        ptx::mbar_expect_tx(bar(B_Q_FULL), qbytes);
+        for (int s = 0; s < 2; ++s) {
+            if (pl.active(s)) {
+                const uint32_t sQ = sh.base + p.off_q[s];
+#pragma unroll
+                for (int blk = 0; blk < DB; ++blk)
+                    ptx::tma_load_3d(sQ + blk * BM * 128, tm_q, bar(B_Q_FULL), blk * 64,
+                                     it.qt[s] * BM, it.bh[s]);
+            }
+            if (AK && tab_head[s] >= 0) {
+                const uint32_t sAK = sh.base + p.off_ak[s];
+#pragma unroll
+                for (int blk = 0; blk < DB; ++blk)
+                    ptx::tma_load_3d(sAK + blk * p.npad_k * 128, tm_ak, bar(B_Q_FULL), blk * 64, 0,
+                                     tab_head[s]);
+            }
+        }
+        ok = pl.visit([&](bool isK, int j, int mask, int src) -> bool {
             const int st = (int)(kv_it % (uint32_t)S);
             const uint32_t round = kv_it / (uint32_t)S;
-            if (!(ok = wait_bar(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u, sh, p.err))) break;
-            const int nbox = tile_cols<BN>(nkc, j) / KB;
+            if (!wait_bar(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u, sh, p.err)) return false;
+            const int nbox = pl.load_cols(j, mask) / KB;
             ptx::mbar_expect_tx(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
             const uint32_t dst = sKV + (uint32_t)st * p.stage_bytes;
-            if (nbox == BN / KB) {  // whole tile: one box of BN rows per 64-column block
+            const int bh = it.bh[src];
+            if (nbox == BN / KB) {  // whole tile: one box of 128 rows per 64-column block
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
                     ptx::tma_load_3d(dst + blk * BN * 128, isK ? tm_kf : tm_vf, bar(B_KV0 + st),
@@ -233,181 +365,240 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
                 }
             }
             ++kv_it;
-        }
+            return true;
+        });
         if (!ok) break;
         if (AV) {
             if (!(ok = wait_bar(bar(B_AV_EMPTY), (av_it & 1u) ^ 1u, sh, p.err))) break;
-            ptx::mbar_expect_tx(bar(B_AV_FULL), (uint32_t)p.kpad_v * D * 2);
-#pragma unroll
-            for (int blk = 0; blk < DB; ++blk)
-                ptx::tma_load_3d(sAV + blk * p.kpad_v * 128, tm_av, bar(B_AV_FULL), blk * 64, 0,
-                                 p.table_heads ? h : 0);
             ++av_it;
+            uint32_t vbytes = 0;
+            for (int s = 0; s < 2; ++s)
+                if (tab_head[s] >= 0) vbytes += (uint32_t)p.kpad_v * D * 2;
+            ptx::mbar_expect_tx(bar(B_AV_FULL), vbytes);
+            for (int s = 0; s < 2; ++s) {
+                if (tab_head[s] < 0) continue;
+                const uint32_t sAV = sh.base + p.off_av[s];
+#pragma unroll
+                for (int blk = 0; blk < DB; ++blk)
+                    ptx::tma_load_3d(sAV + blk * p.kpad_v * 128, tm_av, bar(B_AV_FULL), blk * 64, 0,
+                                     tab_head[s]);
+            }
         }
     }
     if (!ok) {
         // drain: wait (bounded) for copies already issued into shared memory
-        for (uint32_t it = kv_it > (uint32_t)S ? kv_it - S : 0; it < kv_it; ++it)
-            drain_bar(bar(B_KV0 + (int)(it % (uint32_t)S)), (it / (uint32_t)S) & 1u);
+        for (uint32_t i = kv_it > (uint32_t)S ? kv_it - S : 0; i < kv_it; ++i)
+            drain_bar(bar(B_KV0 + (int)(i % (uint32_t)S)), (i / (uint32_t)S) & 1u);
         if (q_it) drain_bar(bar(B_Q_FULL), (q_it - 1) & 1u);
         if (AV && av_it) drain_bar(bar(B_AV_FULL), (av_it - 1) & 1u);
     }
 }
 
 // ======================================================================= MMA issuer
-template <int D, bool AK, bool AV, bool CAUSAL, int CPS>
+// The whole warp runs this role with warp-uniform control flow; one elected lane issues
+// each tcgen05 instruction. Descriptors are built once per buffer and stepped by
+// compile-time offsets, so an MMA costs a 64-bit add or two and the issue itself.
+template <int D, bool AK, bool AV, bool CAUSAL>
 __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
-    using TL = TmemLayout<CPS>;
-    constexpr int BN = TL::BN;
+    using T = Tm<D>;
+    constexpr bool EARLY_S = !T::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    const uint32_t sQ = sh.base + p.off_q, sKV = sh.base + p.off_kv;
-    const uint32_t sAK = sh.base + p.off_ak, sAV = sh.base + p.off_av;
-    const int S = p.stages;
-    uint32_t kv_it = 0, q_it = 0, av_it = 0, s_it = 0, p_it = 0;
+    auto sbar = [&](int s, int which) { return bar(B_SLOT0 + 6 * s + which); };
+    const uint32_t S = (uint32_t)p.stages;
+    constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
+    auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = wait_bar(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+    // descriptors: Q (K-major, per slot), K/V stage 0 (K-major for S, MN-major for P V).
+    // launder() keeps the compiler from hoisting every stepped descriptor out of the loops
+    // (that would hold dozens of 64-bit values in registers for the whole kernel).
+    auto launder = [](uint64_t v) {
+        asm volatile("" : "+l"(v));
+        return v;
+    };
+    const uint64_t dq0 = ptx::sdesc_sw128(sh.base + p.off_q[0], 16, 1024);
+    const uint64_t dq1 = ptx::sdesc_sw128(sh.base + p.off_q[1], 16, 1024);
+    const uint64_t dk0 = ptx::sdesc_sw128(sh.base + p.off_kv, 16, 1024);
+    const uint64_t dv0 = ptx::sdesc_sw128(sh.base + p.off_kv, BN * 128, 1024);
+    const uint64_t stage16 = p.stage_bytes >> 4;
+    // K-major operand, k-step kk of 16: 64-column block kk / 4 (rows x 128 bytes apart),
+    // 32 bytes per step inside the 128-byte swizzle atom
+    auto kstep = [](int kk, int rows) -> uint64_t {
+        return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+    };
+    uint32_t kv_it = 0, q_it = 0, av_it = 0;
+    uint32_t s_it[2] = {0, 0}, p_it[2] = {0, 0}, pv_it[2] = {0, 0};
+    bool pv_pending[2] = {false, false};
     bool ok = true;
 
-    // the next score-buffer item (R or S_j): wait until the softmax released the buffer
-    auto next_sbuf = [&](uint32_t &col, uint32_t &fullbar) -> bool {
-        const uint32_t buf = s_it & 1u;
-        const uint32_t use = s_it >> 1;
-        if (!wait_bar(bar(B_S_EMPTY0 + (int)buf), (use & 1u) ^ 1u, sh, p.err)) return false;
-        ptx::tc_fence_after();
-        col = TL::S + buf * BN;
-        fullbar = bar(B_S_FULL0 + (int)buf);
-        ++s_it;
-        return true;
-    };
-
-    // O += P_j V_j: P from TMEM buffer (item & 1) as bf16 pairs, V tile MN-major in shared
-    // memory. Completion is signalled on the buffer's own barrier.
-    // Each P buffer has its own full barrier: the softmax may run one item ahead, and a
-    // shared barrier could then complete twice before this thread waits on it.
-    auto wait_p = [&](uint32_t &pb) -> bool {
-        pb = p_it & 1u;
-        if (!wait_bar(bar(B_P_FULL0 + (int)pb), (p_it >> 1) & 1u, sh, p.err)) return false;
-        ++p_it;
-        return true;
-    };
-    auto issue_pv = [&](int j, int cols) -> bool {
-        uint32_t pb;
-        if (!wait_p(pb)) return false;
-        const int st = (int)(kv_it % (uint32_t)S);
-        if (!wait_bar(bar(B_KV0 + st), (kv_it / (uint32_t)S) & 1u, sh, p.err)) return false;
-        ptx::tc_fence_after();
-        const uint32_t vb = sKV + (uint32_t)st * p.stage_bytes;
-        const uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
-        const uint32_t pcol = TL::P + pb * (BN / 2);
-        for (int kk = 0; kk < cols / 16; ++kk) {
-            const uint64_t b = ptx::sdesc_sw128(vb + kk * 16 * 128, BN * 128, 1024);
-            ptx::tc_mma_ts(tmem + TL::O, tmem + pcol + (uint32_t)(kk * 8), b, idPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+    // before an MMA writes the slot's S columns: the softmax has read the previous S item,
+    // and (P over S) the MMAs reading P from those columns are done
+    auto claim_s = [&](int s) -> bool {
+        if (T::P_ALIAS && pv_pending[s]) {
+            if (!wait(sbar(s, SB_PV_DONE), (pv_it[s] - 1u) & 1u)) return false;
+            pv_pending[s] = false;
         }
-        ptx::tc_commit(bar(B_PV_DONE0 + (int)pb));
-        ptx::tc_commit(bar(B_KV0 + kMaxStages + st));
-        ++kv_it;
+        if (!wait(sbar(s, SB_S_EMPTY), (s_it[s] & 1u) ^ 1u)) return false;
+        ++s_it[s];
+        ptx::tc_fence_after();
         return true;
     };
 
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        int bh, qt;
-        decode_tile(p, t, bh, qt);
-        const int nkc = tile_keys<CAUSAL>(p, bh, qt * BM);
-        const int J = (nkc + BN - 1) / BN;
-        if (J == 0) continue;
-        if (!(ok = wait_bar(bar(B_Q_FULL), q_it & 1u, sh, p.err))) break;
+    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+        const Item it = decode_item(p, t);
+        Plan<CAUSAL, EARLY_S> pl;
+        pl.make(p, it);
+        if (pl.Jmax == 0) continue;
+        if (!(ok = wait(bar(B_Q_FULL), q_it & 1u))) break;
         ++q_it;
         ptx::tc_fence_after();
-        if (AK) {
-            uint32_t col, fb;
-            if (!(ok = next_sbuf(col, fb))) break;
+        if (AK) {  // R = Q W^K^T into each active slot's S columns
             const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.npad_k, 0);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t a = ptx::sdesc_sw128(sQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
-                const uint64_t b =
-                    ptx::sdesc_sw128(sAK + (kk >> 2) * p.npad_k * 128 + (kk & 3) * 32, 16, 1024);
-                ptx::tc_mma(tmem + col, a, b, idR, kk > 0 ? 1u : 0u);
-            }
-            ptx::tc_commit(fb);
-        }
-        int prev_cols = 0;
-        for (int j = 0; j < J && ok; ++j) {
-            const int cols = tile_cols<BN>(nkc, j);
-            const int st = (int)(kv_it % (uint32_t)S);
-            if (!(ok = wait_bar(bar(B_KV0 + st), (kv_it / (uint32_t)S) & 1u, sh, p.err))) break;
-            uint32_t col, fb;
-            if (!(ok = next_sbuf(col, fb))) break;
-            const uint32_t kb = sKV + (uint32_t)st * p.stage_bytes;
-            const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
+            for (int s = 0; s < 2; ++s) {
+                if (!ok || !pl.active(s)) continue;
+                if (!(ok = claim_s(s))) break;
+                const uint64_t dak = ptx::sdesc_sw128(sh.base + p.off_ak[p.two_tables ? s : 0], 16, 1024);
+                const uint64_t dq = s ? dq1 : dq0;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t a = ptx::sdesc_sw128(sQ + (kk >> 2) * BM * 128 + (kk & 3) * 32, 16, 1024);
-                const uint64_t b = ptx::sdesc_sw128(kb + (kk >> 2) * BN * 128 + (kk & 3) * 32, 16, 1024);
-                ptx::tc_mma(tmem + col, a, b, idS, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::tc_mma_w(tmem + T::S(s), launder(dq) + kstep(kk, BM),
+                                  launder(dak) + kstep(kk, p.npad_k), idR, kk > 0 ? 1u : 0u);
+                ptx::tc_commit_w(sbar(s, SB_S_FULL));
             }
-            ptx::tc_commit(fb);
-            ptx::tc_commit(bar(B_KV0 + kMaxStages + st));
-            ++kv_it;
-            if (j == J - 1) ptx::tc_commit(bar(B_Q_EMPTY));
-            if (j >= 1) ok = issue_pv(j - 1, prev_cols);
-            prev_cols = cols;
+            if (!ok) break;
         }
-        if (!ok) break;
-        if (!(ok = issue_pv(J - 1, prev_cols))) break;
-        if (AV) {
-            uint32_t pb;
-            if (!(ok = wait_p(pb))) break;
-            if (!(ok = wait_bar(bar(B_AV_FULL), av_it & 1u, sh, p.err))) break;
-            ++av_it;
+        int k_left = pl.shared ? pl.Jmax : pl.J[0] + pl.J[1];  // K entries still to consume
+        ok = pl.visit([&](bool isK, int j, int mask, int src) -> bool {
+            const uint32_t stg = kv_it % S;
+            if (!wait(bar(B_KV0 + (int)stg), (kv_it / S) & 1u)) return false;
             ptx::tc_fence_after();
-            const uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
-            const uint32_t pcol = TL::P + pb * (BN / 2);
-            for (int kk = 0; kk < p.kpad_v / 16; ++kk) {
-                const uint64_t b = ptx::sdesc_sw128(sAV + kk * 16 * 128, (uint32_t)p.kpad_v * 128, 1024);
-                ptx::tc_mma_ts(tmem + TL::O, tmem + pcol + (uint32_t)(kk * 8), b, idPV, 1u);
+            const uint64_t off = (uint64_t)stg * stage16;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                if (!(mask & (1 << s))) continue;
+                const int cols = tile_cols(pl.nkc[s], j);
+                if (isK) {  // S_j = Q K_j^T
+                    if (!claim_s(s)) return false;
+                    const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
+                    const uint64_t dk = dk0 + off;
+                    const uint64_t dq = s ? dq1 : dq0;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        ptx::tc_mma_w(tmem + T::S(s), launder(dq) + kstep(kk, BM),
+                                      launder(dk) + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+                    ptx::tc_commit_w(sbar(s, SB_S_FULL));
+                } else {  // O += P_j V_j
+                    if (!wait(sbar(s, SB_P_FULL), p_it[s] & 1u)) return false;
+                    ++p_it[s];
+                    ptx::tc_fence_after();
+                    const uint64_t dv = dv0 + off;
+                    const int nk16 = cols / 16;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        if (kk < nk16)
+                            ptx::tc_mma_ts_w(tmem + T::O(s), tmem + T::P(s) + (uint32_t)(kk * 8),
+                                             launder(dv) + (uint64_t)(kk * 16 * 128 >> 4), idPV,
+                                             (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::tc_commit_w(sbar(s, SB_PV_DONE));
+                    ++pv_it[s];
+                    pv_pending[s] = true;
+                }
             }
-            ptx::tc_commit(bar(B_PV_DONE0 + (int)pb));
-            ptx::tc_commit(bar(B_AV_EMPTY));
+            ptx::tc_commit_w(bar(B_KV0 + kMaxStages + (int)stg));  // entry consumed
+            ++kv_it;
+            if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
+            return true;
+        });
+        if (!ok) break;
+        if (AV) {  // O += beta W^V, beta (bf16 pairs) in the slot's P columns
+            if (!(ok = wait(bar(B_AV_FULL), av_it & 1u))) break;
+            ++av_it;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                if (!ok || !pl.active(s)) continue;
+                if (!(ok = wait(sbar(s, SB_P_FULL), p_it[s] & 1u))) break;
+                ++p_it[s];
+                ptx::tc_fence_after();
+                const uint64_t dav = ptx::sdesc_sw128(sh.base + p.off_av[p.two_tables ? s : 0],
+                                                      (uint32_t)p.kpad_v * 128, 1024);
+                for (int kk = 0; kk < p.kpad_v / 16; ++kk)
+                    ptx::tc_mma_ts_w(tmem + T::O(s), tmem + T::P(s) + (uint32_t)(kk * 8),
+                                     dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
+                ptx::tc_commit_w(sbar(s, SB_PV_DONE));
+                ++pv_it[s];
+                pv_pending[s] = true;
+            }
+            if (!ok) break;
+            ptx::tc_commit_w(bar(B_AV_EMPTY));
         }
-        ptx::tc_commit(bar(B_O_FULL));
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            if (pl.active(s)) ptx::tc_commit_w(sbar(s, SB_O_FULL));
     }
-    // every MMA issued by this thread completes before TMEM is released
-    ptx::tc_commit(bar(B_DRAIN));
+    // every MMA issued by this warp completes before TMEM is released
+    ptx::tc_commit_w(bar(B_DRAIN));
     drain_bar(bar(B_DRAIN), 0);
 }
 
 // ======================================================================= softmax / epilogue
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
 
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
-__device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
-    using TL = TmemLayout<CPS>;
-    constexpr int BN = TL::BN;
-    constexpr int NSPLIT = TL::NSPLIT;
-    constexpr int NC = HC / KB;  // chunks per thread per key tile
+// maximum / minimum of 32 values, 16 three-input instructions, depth 5
+__device__ __forceinline__ float max32(const float *x) {
+    float a0 = ptx::max3(x[0], x[1], x[2]), a1 = ptx::max3(x[3], x[4], x[5]);
+    float a2 = ptx::max3(x[6], x[7], x[8]), a3 = ptx::max3(x[9], x[10], x[11]);
+    a0 = ptx::max3(a0, x[12], x[13]);
+    a1 = ptx::max3(a1, x[14], x[15]);
+    a2 = ptx::max3(a2, x[16], x[17]);
+    a3 = ptx::max3(a3, x[18], x[19]);
+    a0 = ptx::max3(a0, x[20], x[21]);
+    a1 = ptx::max3(a1, x[22], x[23]);
+    a2 = ptx::max3(a2, x[24], x[25]);
+    a3 = ptx::max3(a3, x[26], x[27]);
+    a0 = ptx::max3(a0, x[28], x[29]);
+    a1 = ptx::max3(a1, x[30], x[31]);
+    return ptx::max3(a0, a1, fmaxf(a2, a3));
+}
+__device__ __forceinline__ float min32(const float *x) {
+    float a0 = ptx::min3(x[0], x[1], x[2]), a1 = ptx::min3(x[3], x[4], x[5]);
+    float a2 = ptx::min3(x[6], x[7], x[8]), a3 = ptx::min3(x[9], x[10], x[11]);
+    a0 = ptx::min3(a0, x[12], x[13]);
+    a1 = ptx::min3(a1, x[14], x[15]);
+    a2 = ptx::min3(a2, x[16], x[17]);
+    a3 = ptx::min3(a3, x[18], x[19]);
+    a0 = ptx::min3(a0, x[20], x[21]);
+    a1 = ptx::min3(a1, x[22], x[23]);
+    a2 = ptx::min3(a2, x[24], x[25]);
+    a3 = ptx::min3(a3, x[26], x[27]);
+    a0 = ptx::min3(a0, x[28], x[29]);
+    a1 = ptx::min3(a1, x[30], x[31]);
+    return ptx::min3(a0, a1, fminf(a2, a3));
+}
+
+template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
+__device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
+    using T = Tm<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = (warp - TL::SW0) >> 2;    // which 64 keys of a key tile
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
-    const int stid = threadIdx.x - 32 * TL::SW0;  // 0 .. 128*NSPLIT-1
+    const int stid = threadIdx.x - 32 * (kSoftWarp0 + 4 * slot);  // 0 .. 127
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r) + row * p.SR;
-    float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta) + row * p.SR;
-    float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5);
-    // exchange slots between the halves of a row: [parity][half][row] maxima, then
-    // [half][row] x {l, low-bin sum, high-bin sum}
-    float *xmax = reinterpret_cast<float *>(sh.ptr + p.off_x);
-    float *xsum = xmax + 2 * 2 * BM;
+    auto sbar = [&](int which) { return bar(B_SLOT0 + 6 * slot + which); };
+    float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r[slot]) + row * p.SR;
+    __nv_bfloat16 *Rrow16 = reinterpret_cast<__nv_bfloat16 *>(sh.ptr + p.off_r[slot]) + row * p.SR;
+    float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta[slot]) + row * p.SB;
+    float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5[slot]);
     const float sl2 = p.scale_log2;
+    const bool neg_scale = sl2 < 0.f;
     const int k = p.clip_k;
     const int hi_off = CAUSAL ? 0 : k;  // largest offset held in the staged table rows
     const int W = p.W;
-    uint32_t s_it = 0, p_item = 0, tiles = 0, grp = 0, pair_it = 0;
-    const uint32_t gbar = bar(B_GROUP);
-    const uint32_t pbar = bar(B_PAIR0 + quad);
+    uint32_t s_it = 0, pv_it = 0, o_it = 0, grp = 0;
     int t5_head = -1;
     bool ok = true;
     // tcgen05.ld/st are warp-collective (.sync.aligned): every decision guarding them is
@@ -416,140 +607,159 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
         const bool r = wait_bar(b, parity, sh, p.err);
         return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
     };
-    // the NSPLIT threads of the same rows (warps quad and quad + 4)
-    auto pair_sync = [&]() -> bool {
-        if (NSPLIT == 1) {
-            __syncwarp();
-            return true;
-        }
-        return group_sync(pbar, pair_it, sh, p.err);
-    };
-    // completion of the MMA that read P item `item` (each P buffer has its own barrier, and
-    // that barrier cannot run two completions ahead: its next one needs our next item)
-    auto wait_pv_item = [&](uint32_t item) -> bool {
-        if (!wait_w(bar(B_PV_DONE0 + (int)(item & 1u)), (item >> 1) & 1u)) return false;
-        ptx::tc_fence_after();
-        __syncwarp();
-        return true;
-    };
-    auto wait_sfull = [&](uint32_t &col, int &buf) -> bool {
-        buf = (int)(s_it & 1u);
-        if (!wait_w(bar(B_S_FULL0 + buf), (s_it >> 1) & 1u)) return false;
-        ptx::tc_fence_after();
-        __syncwarp();
-        col = TL::S + (uint32_t)buf * BN;
+    auto wait_s = [&]() -> bool {
+        if (!wait_w(sbar(SB_S_FULL), s_it & 1u)) return false;
         ++s_it;
+        ptx::tc_fence_after();
+        __syncwarp();
         return true;
     };
-    auto release_s = [&](int buf) {
+    auto release_s = [&]() {
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(B_S_EMPTY0 + buf));
+        ptx::mbar_arrive(sbar(SB_S_EMPTY));
+    };
+    // completion number c of the slot's P-reading MMAs (waited in increasing order; the
+    // next completion needs a P item this thread has not written yet)
+    auto wait_pv = [&](uint32_t c) -> bool {
+        if (!wait_w(sbar(SB_PV_DONE), c & 1u)) return false;
+        ptx::tc_fence_after();
+        __syncwarp();
+        return true;
+    };
+    auto rel = [&](int idx) -> float {  // scaled R value of table row idx
+        if (AK && p.r_bf16) return __bfloat162float(Rrow16[idx]);
+        return Rrow[idx];
     };
 
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        int bh, qt;
-        decode_tile(p, t, bh, qt);
+    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+        const Item it = decode_item(p, t);
+        if (!it.valid[slot]) continue;
+        const int bh = it.bh[slot], qt = it.qt[slot];
         const int i0 = qt * BM, gi = i0 + row, h = bh % p.H;
         const int gmin = i0 + quad * 32, gmax = gmin + 31;  // rows of this warp
         const int nk = keys_of(p, bh);
-        const int nkc = tile_keys<CAUSAL>(p, bh, i0);
+        const int nkc = tile_keys<CAUSAL>(p, bh, qt);
         const int J = (nkc + BN - 1) / BN;
         __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                               ((long long)bh * p.n + gi) * D;
         if (J == 0) {
             if (gi < p.n) {
 #pragma unroll
-                for (int c = 0; c < D / 8 / NSPLIT; ++c)
-                    reinterpret_cast<uint4 *>(orow)[half * (D / 8 / NSPLIT) + c] = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < D / 8; ++c)
+                    reinterpret_cast<uint4 *>(orow)[c] = make_uint4(0, 0, 0, 0);
             }
             continue;
         }
         if (T5 && h != t5_head) {
-            if (!(ok = group_sync(gbar, grp, sh, p.err))) break;
-            for (int idx = stid; idx <= 2 * p.t5_R; idx += 128 * NSPLIT)
+            if (!(ok = group_sync(sbar(SB_GROUP), grp, sh, p.err))) break;
+            for (int idx = stid; idx <= 2 * p.t5_R; idx += 128)
                 t5tab[idx] = p.bias[t5_bucket(idx - p.t5_R, p.t5) * p.H + h] * kLog2e;
-            if (!(ok = group_sync(gbar, grp, sh, p.err))) break;
+            if (!(ok = group_sync(sbar(SB_GROUP), grp, sh, p.err))) break;
             t5_head = h;
         }
-        if (AK) {  // R row -> shared memory, split between the halves
-            uint32_t col;
-            int buf;
-            if (!(ok = wait_sfull(col, buf))) break;
-            for (int c0 = 16 * half; c0 < p.npad_k; c0 += 16 * NSPLIT) {
+        if (AK) {  // R row -> shared memory (scaled to the log2 domain)
+            if (!(ok = wait_s())) break;
+            for (int c0 = 0; c0 < p.npad_k; c0 += 16) {
                 uint32_t r[16];
-                ptx::tmem_ld16(lane_base + col + (uint32_t)c0, r);
+                ptx::tmem_ld16(lane_base + T::S(slot) + (uint32_t)c0, r);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (c0 + e < W) Rrow[c0 + e] = __uint_as_float(r[e]) * sl2;
+                for (int e = 0; e < 16; ++e) {
+                    if (c0 + e < W) {
+                        const float v = __uint_as_float(r[e]) * sl2;
+                        if (p.r_bf16) Rrow16[c0 + e] = __float2bfloat16(v);
+                        else Rrow[c0 + e] = v;
+                    }
+                }
             }
-            release_s(buf);
+            release_s();
         }
-        if (AV && half == 0)
+        // relative term of keys beyond the window on either side (constant per row)
+        float c_left = 0.f, c_right = 0.f;
+        if (AK) {
+            c_left = rel(0);
+            c_right = rel(W - 1);
+        } else if (T5) {
+            c_left = t5tab[0];
+            c_right = t5tab[2 * p.t5_R];
+        }
+        // offsets at or beyond these take the first / last table row
+        const int lo_lim = T5 ? -p.t5_R : -k;
+        const int hi_lim = T5 ? p.t5_R : hi_off;
+        if (AV)
             for (int r = 0; r < W; ++r) brow[r] = 0.f;
-        if (AK || AV) {
-            if (!(ok = pair_sync())) break;  // R copied and bins cleared by both halves
-        }
         float m_ref = -INFINITY, l = 0.f, lo_sum = 0.f, hi_sum = 0.f;
 
         for (int j = 0; j < J; ++j) {
             const int j0 = j * BN;
-            const int cols = tile_cols<BN>(nkc, j);  // multiple of 32, > 0
-            const int cbeg = half * NC;              // first chunk of this thread
-            int live = cols / KB;                    // chunks any row of the warp can see
+            const int cols = tile_cols(nkc, j);  // multiple of 32, > 0
+            int live = cols / KB;                 // chunks any row of the warp can see
             if (CAUSAL) live = min(live, max(0, (gmax - j0) / KB + 1));
-            uint32_t scol;
-            int buf;
-            if (!(ok = wait_sfull(scol, buf))) break;
-            // ---- S chunks of this thread into registers
-            float x[HC];
+            if (!(ok = wait_s())) break;
+            // ---- the score row into registers, then the buffer goes back to the MMA warp
+            float x[BN];
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                if (cbeg + cc < live) {
-                    __syncwarp();
-                    ptx::tmem_ld32f(lane_base + scol + (uint32_t)((cbeg + cc) * KB), x + cc * KB);
-                }
-            }
+            for (int c = 0; c < NCH; ++c)
+                if (c < live) ptx::tmem_ld32f(lane_base + T::S(slot) + (uint32_t)(c * KB), x + c * KB);
             ptx::tmem_ld_wait();
-            release_s(buf);
-            // ---- logits in the log2 domain, relative term added, masks (S2-S4)
-            float hmax = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                const int c = cbeg + cc;
-                if (c >= live) continue;
-                float *xc = x + cc * KB;
+            release_s();
+            // ---- logits in the log2 domain (S2-S4). A chunk whose relative term is one
+            // constant for every row of the warp and that needs no mask stays raw: its
+            // exponent is x * sl2 + (c - m), and its maximum comes from the raw maximum (or
+            // minimum, for a negative scale). Other chunks get the full logit (gathered
+            // relative term, masks) written in place and exponent x - m.
+            // chunk c of the tile: is it kept raw, and with which constant
+            auto raw_chunk = [&](int c, float &cst) -> bool {
                 const int e0 = j0 + c * KB;  // first key of the chunk
                 // offsets j - i over the warp's rows lie in [e0 - gmax, e0 + 31 - gmin]
-                const int lo_lim = T5 ? -p.t5_R : -k;      // at or below: first table row
-                const int hi_lim = T5 ? p.t5_R : hi_off;   // at or above: last table row
                 const bool w_left = (e0 + KB - 1 - gmin) <= lo_lim;
                 const bool w_right = (e0 - gmax) >= hi_lim;
-                const int base = e0 - gi;  // offset of element 0 for this row
-                if (AK || T5) {
-                    const float *tab = AK ? Rrow : t5tab;
-                    const int lim = AK ? k : p.t5_R;
-                    const int top = AK ? hi_off : p.t5_R;
-                    if (w_left) {
-                        const float cst = tab[0];
+                const bool uniform = (!AK && !T5) || w_left || w_right;
+                const bool full = (e0 + KB <= nk) && (!CAUSAL || e0 + KB - 1 <= gmin);
+                cst = (!AK && !T5) ? 0.f : (w_left ? c_left : c_right);
+                return uniform && full;
+            };
+            float rmax = -INFINITY;
 #pragma unroll
-                        for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
-                    } else if (w_right) {
-                        const float cst = tab[lim + top];
+            for (int c = 0; c < NCH; ++c) {
+                if (c >= live) continue;
+                float *xc = x + c * KB;
+                float cst;
+                if (raw_chunk(c, cst)) {
+                    const float ext = neg_scale ? min32(xc) : max32(xc);
+                    rmax = fmaxf(rmax, fmaf(ext, sl2, cst));
+                    continue;
+                }
+                const int e0 = j0 + c * KB;
+                const bool w_left = (e0 + KB - 1 - gmin) <= lo_lim;
+                const bool w_right = (e0 - gmax) >= hi_lim;
+                const bool full = (e0 + KB <= nk) && (!CAUSAL || e0 + KB - 1 <= gmin);
+                const int base = e0 - gi;  // offset of element 0 for this row
+                if (AK) {
+                    if (w_left || w_right) {
+                        const float cst = w_left ? c_left : c_right;
 #pragma unroll
                         for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < KB; ++e) {
-                            const int o = min(top, max(-lim, base + e));
-                            xc[e] = fmaf(xc[e], sl2, tab[o + lim]);
-                        }
+                        for (int e = 0; e < KB; ++e)
+                            xc[e] = fmaf(xc[e], sl2, rel(min(hi_off, max(-k, base + e)) + k));
+                    }
+                } else if (T5) {
+                    const int R = p.t5_R;
+                    if (w_left || w_right) {
+                        const float cst = w_left ? c_left : c_right;
+#pragma unroll
+                        for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < KB; ++e)
+                            xc[e] = fmaf(xc[e], sl2, t5tab[min(R, max(-R, base + e)) + R]);
                     }
                 } else {
 #pragma unroll
                     for (int e = 0; e < KB; ++e) xc[e] *= sl2;
                 }
-                const bool full = (e0 + KB <= nk) && (!CAUSAL || e0 + KB - 1 <= gmin);
                 if (!full) {
 #pragma unroll
                     for (int e = 0; e < KB; ++e) {
@@ -557,72 +767,62 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
                         if (jj >= nk || (CAUSAL && jj > gi)) xc[e] = -INFINITY;
                     }
                 }
-#pragma unroll
-                for (int e = 0; e < KB; ++e) hmax = fmaxf(hmax, xc[e]);
+                rmax = fmaxf(rmax, max32(xc));
             }
-            // ---- row maximum over both halves, lazy rescale (S5)
-            float rmax = hmax;
-            if (NSPLIT > 1) {
-                float *slot = xmax + (j & 1) * 2 * BM;
-                slot[half * BM + row] = hmax;
-                if (!(ok = pair_sync())) break;
-                rmax = fmaxf(hmax, slot[(1 - half) * BM + row]);
-            }
+            // ---- online softmax (S5) with a lazy rescale
             float alpha = 1.f;
             if (rmax > m_ref + kRescaleLog2) {
                 alpha = ptx::ex2(m_ref - rmax);  // 0 while nothing was seen yet
                 m_ref = rmax;
             }
+            // P and O of the slot are free once the previous P . V is done
+            if (j >= 1 && !(ok = wait_pv(pv_it + (uint32_t)j - 1u))) break;
             // on the first key tile l, the bins and O hold nothing yet: no rescale needed
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {  // same in every half
+            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 l *= alpha;
                 lo_sum *= alpha;
                 hi_sum *= alpha;
-                if (half == 0) {
-                    if (AV && alpha != 1.f)
-                        for (int r = 0; r < W; ++r) brow[r] *= alpha;
-                    if (j >= 1) {  // O holds P V of the earlier key tiles
-                        if (!(ok = wait_pv_item(p_item - 1))) break;
+                if (AV && alpha != 1.f)
+                    for (int r = 0; r < W; ++r) brow[r] *= alpha;
+                __syncwarp();
 #pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t r[32];
-                            ptx::tmem_ld32(lane_base + TL::O + (uint32_t)c0, r);
-                            ptx::tmem_ld_wait();
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(lane_base + T::O(slot) + (uint32_t)c0, r);
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                            ptx::tmem_st32(lane_base + TL::O + (uint32_t)c0, r);
-                        }
-                        ptx::tmem_st_wait();
-                    }
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    ptx::tmem_st32(lane_base + T::O(slot) + (uint32_t)c0, r);
                 }
-                if (AV && NSPLIT > 1) {  // bins are rescaled before the other half adds new ones
-                    if (!(ok = pair_sync())) break;
-                }
+                ptx::tmem_st_wait();
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
             // ---- exponentials, row sum, value bins (S7), P (bf16 pairs) into TMEM
-            if (p_item >= 2) {  // the P buffer's previous P . V is done
-                if (!(ok = wait_pv_item(p_item - 2))) break;
-            }
-            const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc) {
-                const int c = cbeg + cc;
+            for (int c = 0; c < NCH; ++c) {
                 if (c * KB >= cols) continue;  // never read by P V
-                const uint32_t pcol = pbase + (uint32_t)(c * (KB / 2));
                 uint32_t pk[KB / 2];
                 if (c >= live) {  // no row of this warp sees these keys
 #pragma unroll
                     for (int e = 0; e < KB / 2; ++e) pk[e] = 0u;
                 } else {
-                    float *xc = x + cc * KB;
-                    float rs = 0.f;
+                    float *xc = x + c * KB;
+                    float cst;
+                    const bool rawc = raw_chunk(c, cst);
+                    const float a = rawc ? sl2 : 1.f, b = (rawc ? cst : 0.f) - m_use;
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-                    for (int e = 0; e < KB; ++e) {
-                        xc[e] = ptx::ex2(xc[e] - m_use);
-                        rs += xc[e];
+                    for (int e = 0; e < KB; e += 4) {
+                        xc[e] = ptx::ex2(fmaf(xc[e], a, b));
+                        xc[e + 1] = ptx::ex2(fmaf(xc[e + 1], a, b));
+                        xc[e + 2] = ptx::ex2(fmaf(xc[e + 2], a, b));
+                        xc[e + 3] = ptx::ex2(fmaf(xc[e + 3], a, b));
+                        s0 += xc[e];
+                        s1 += xc[e + 1];
+                        s2 += xc[e + 2];
+                        s3 += xc[e + 3];
                     }
+                    const float rs = (s0 + s1) + (s2 + s3);
                     l += rs;
                     if (AV) {
                         const int e0 = j0 + c * KB;
@@ -633,10 +833,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
                         } else if (w_right) {
                             hi_sum += rs;
                         } else {
-                            // interior bins get exactly one key each over the whole row, so
-                            // they are stored (not accumulated); the two end bins are sums
-                            // branch-free: end-bin terms go to the sums, interior ones
-                            // to their bin; the others write a spare slot (index W)
+                            // branch-free: end-bin terms go to the sums; interior bins get
+                            // exactly one key each over the whole row and are stored; the
+                            // others write a spare slot (index W)
                             const int base = e0 - gi;
 #pragma unroll
                             for (int e = 0; e < KB; ++e) {
@@ -652,57 +851,45 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
                     for (int e = 0; e < KB / 2; ++e) pk[e] = pack2(xc[2 * e], xc[2 * e + 1]);
                 }
                 __syncwarp();
-                ptx::tmem_st16(pcol, pk);
+                ptx::tmem_st16(lane_base + T::P(slot) + (uint32_t)(c * (KB / 2)), pk);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_P_FULL0 + (int)(p_item & 1u)));
-            ++p_item;
+            ptx::mbar_arrive(sbar(SB_P_FULL));
         }
         if (!ok) break;
-        // ---- combine the halves: l and the end-bin sums
-        if (NSPLIT > 1) {
-            xsum[(half * 3 + 0) * BM + row] = l;
-            xsum[(half * 3 + 1) * BM + row] = lo_sum;
-            xsum[(half * 3 + 2) * BM + row] = hi_sum;
-            if (!(ok = pair_sync())) break;
-            l += xsum[((1 - half) * 3 + 0) * BM + row];
-            lo_sum += xsum[((1 - half) * 3 + 1) * BM + row];
-            hi_sum += xsum[((1 - half) * 3 + 2) * BM + row];
-        }
+        uint32_t pv_next = pv_it + (uint32_t)J;  // completions after this tile's P . V
         if (AV) {
-            // bins (bf16 pairs) become the A operand of O += beta W^V (written by half 0)
-            if (p_item >= 2 && !(ok = wait_pv_item(p_item - 2))) break;
-            if (half == 0) {
-                brow[0] += lo_sum;
-                brow[W - 1] += hi_sum;
-                const uint32_t pbase = lane_base + TL::P + (p_item & 1u) * (BN / 2);
-                for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
-                    uint32_t pk[16];
+            // bins (bf16 pairs) become the A operand of O += beta W^V
+            if (!(ok = wait_pv(pv_next - 1u))) break;
+            brow[0] += lo_sum;
+            brow[W - 1] += hi_sum;
+            for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
+                uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int r0 = c0 + 2 * e;
-                        pk[e] = pack2(r0 < W ? brow[r0] : 0.f, r0 + 1 < W ? brow[r0 + 1] : 0.f);
-                    }
-                    __syncwarp();
-                    ptx::tmem_st16(pbase + (uint32_t)(c0 / 2), pk);
+                for (int e = 0; e < 16; ++e) {
+                    const int r0 = c0 + 2 * e;
+                    pk[e] = pack2(r0 < W ? brow[r0] : 0.f, r0 + 1 < W ? brow[r0 + 1] : 0.f);
                 }
-                ptx::tmem_st_wait();
+                __syncwarp();
+                ptx::tmem_st16(lane_base + T::P(slot) + (uint32_t)(c0 / 2), pk);
             }
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(B_P_FULL0 + (int)(p_item & 1u)));
-            ++p_item;
+            ptx::mbar_arrive(sbar(SB_P_FULL));
+            ++pv_next;
         }
-        // ---- epilogue (S8): O / l -> bf16 -> global, D / NSPLIT columns per thread
-        if (!(ok = wait_w(bar(B_O_FULL), tiles & 1u))) break;
+        pv_it = pv_next;
+        // ---- epilogue (S8): O / l -> bf16 -> global
+        if (!(ok = wait_w(sbar(SB_O_FULL), o_it & 1u))) break;
+        ++o_it;
         ptx::tc_fence_after();
         __syncwarp();
-        ++tiles;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c0 = half * (D / NSPLIT); c0 < (half + 1) * (D / NSPLIT); c0 += 32) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t r[32];
-            ptx::tmem_ld32(lane_base + TL::O + (uint32_t)c0, r);
+            ptx::tmem_ld32(lane_base + T::O(slot) + (uint32_t)c0, r);
             ptx::tmem_ld_wait();
             if (gi < p.n) {
 #pragma unroll
@@ -722,13 +909,12 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem) {
 }
 
 // ======================================================================= kernel
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
-__global__ void __launch_bounds__(TmemLayout<CPS>::THREADS, CPS)
+template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
     relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kf,
                       const __grid_constant__ CUtensorMap tm_vf, const __grid_constant__ CUtensorMap tm_ak,
                       const __grid_constant__ CUtensorMap tm_av, const __grid_constant__ Params p) {
-    using TL = TmemLayout<CPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     Shared sh;
@@ -743,10 +929,10 @@ __global__ void __launch_bounds__(TmemLayout<CPS>::THREADS, CPS)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
-            if (i == B_S_EMPTY0 || i == B_S_EMPTY1 || i == B_P_FULL0 || i == B_P_FULL1 ||
-                i == B_GROUP)
-                cnt = 128 * TL::NSPLIT;
-            if (i >= B_PAIR0 && i < B_PAIR0 + 4) cnt = 32 * TL::NSPLIT;
+            if (i >= B_SLOT0 && i < B_KV0) {
+                const int which = (i - B_SLOT0) % 6;
+                if (which == SB_S_EMPTY || which == SB_P_FULL || which == SB_GROUP) cnt = 128;
+            }
             ptx::mbar_init(bars + 8u * (uint32_t)i, cnt);
         }
         *sh.abort_flag = 0;
@@ -757,28 +943,32 @@ __global__ void __launch_bounds__(TmemLayout<CPS>::THREADS, CPS)
         ptx::tma_prefetch_desc(&tm_kf);
         ptx::tma_prefetch_desc(&tm_vf);
     }
-    if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TL::cols);
+    if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if ((threadIdx.x & 31) == 0) producer_role<D, AK, AV, CAUSAL, CPS>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
-                                                      &tm_av);
+    if (warp < kSoftWarp0) {
+        ptx::reg_dealloc<kCtrlRegs>();
+        if (warp == 0) {
+            if ((threadIdx.x & 31) == 0)
+                producer_role<D, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
+                                                 &tm_av);
+        } else if (warp == 1) {
+            mma_role<D, AK, AV, CAUSAL>(p, sh, tmem);  // the whole warp; one lane issues
+        }
         __syncwarp();
-    } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) mma_role<D, AK, AV, CAUSAL, CPS>(p, sh, tmem);
-        __syncwarp();
-    } else if (warp >= TL::SW0) {
-        softmax_role<D, AK, AV, T5, CAUSAL, CPS>(p, sh, tmem);
+    } else {
+        ptx::reg_alloc<kSoftRegs>();
+        softmax_role<D, AK, AV, T5, CAUSAL>(p, sh, tmem, (warp - kSoftWarp0) >> 2);
     }
 
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, TL::cols);
+        ptx::tmem_dealloc(tmem, 512);
     }
 }
 

@@ -73,76 +73,96 @@ inline DeviceInfo device_info() {
 
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL, int CPS>
+template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
 cudaError_t launch_variant(const CUtensorMap (&tm)[7], const Params &p, uint32_t smem_bytes,
                            cudaStream_t s) {
-    auto kern = relattn_tc_kernel<D, AK, AV, T5, CAUSAL, CPS>;
+    auto kern = relattn_tc_kernel<D, AK, AV, T5, CAUSAL>;
     // Opt in to the device's whole shared-memory budget once per device and variant, so
     // that later calls (including ones captured into a CUDA graph) only launch.
     static bool opted[64] = {};
-    static int resident[64] = {};
     static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const DeviceInfo di = device_info();
-    int per_sm = 1;
     {
         std::lock_guard<std::mutex> lk(mu);
         if (!opted[dev]) {
+            // the warpgroups' register shares add up to kThreads * kLaunchRegs: launching
+            // with fewer registers per thread would leave the softmax warps waiting for
+            // registers that never come
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, kern);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != kLaunchRegs) return cudaErrorNotSupported;
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin);
             if (e != cudaSuccess) return e;
-            // all of the unified L1/shared storage as shared memory, so that two CTAs fit
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      (int)cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess) return e;
             opted[dev] = true;
         }
-        if (CPS > 1) {
-            int nb = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, TmemLayout<CPS>::THREADS,
-                                                              smem_bytes);
-            if (e != cudaSuccess) return e;
-            resident[dev] = nb;
-            per_sm = nb < 1 ? 1 : (nb > CPS ? CPS : nb);
-        }
     }
-    const int want = di.sms * per_sm;
-    const int grid = p.num_tiles < want ? p.num_tiles : want;
-    kern<<<grid, TmemLayout<CPS>::THREADS, smem_bytes, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5],
-                                                          tm[6], p);
+    const int grid = p.num_items < di.sms ? p.num_items : di.sms;  // persistent: one CTA per SM
+    kern<<<grid, kThreads, smem_bytes, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], tm[6], p);
     return cudaGetLastError();
 }
 
-template <int D, bool T5, bool CAUSAL, int CPS>
+template <int D, bool T5, bool CAUSAL>
 cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[7], const Params &p,
                          uint32_t smem, cudaStream_t s) {
     if constexpr (T5) {
-        return launch_variant<D, false, false, true, CAUSAL, CPS>(tm, p, smem, s);
+        return launch_variant<D, false, false, true, CAUSAL>(tm, p, smem, s);
     } else {
-        if (ak && av) return launch_variant<D, true, true, false, CAUSAL, CPS>(tm, p, smem, s);
-        if (ak) return launch_variant<D, true, false, false, CAUSAL, CPS>(tm, p, smem, s);
-        if (av) return launch_variant<D, false, true, false, CAUSAL, CPS>(tm, p, smem, s);
-        return launch_variant<D, false, false, false, CAUSAL, CPS>(tm, p, smem, s);
+        if (ak && av) return launch_variant<D, true, true, false, CAUSAL>(tm, p, smem, s);
+        if (ak) return launch_variant<D, true, false, false, CAUSAL>(tm, p, smem, s);
+        if (av) return launch_variant<D, false, true, false, CAUSAL>(tm, p, smem, s);
+        return launch_variant<D, false, false, false, CAUSAL>(tm, p, smem, s);
     }
 }
 
-// Shared-memory layout for `stages` K/V stages of `bn` keys; returns the bytes to request.
+// Shared-memory layout for `stages` K/V stages (p.pair, p.two_tables and p.r_bf16 set);
+// returns the bytes to request.
 template <int D>
-inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int bn, int stages) {
+inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
+    const int nslots = p.pair ? 2 : 1;
+    const int ntab = p.two_tables ? 2 : 1;
     const uint32_t q_bytes = (uint32_t)BM * D * 2;
-    const uint32_t stage_bytes = (uint32_t)bn * D * 2;
+    const uint32_t stage_bytes = (uint32_t)BN * D * 2;
+    const uint32_t r_bytes = round_up((uint32_t)BM * p.SR * (p.r_bf16 ? 2 : 4), 16);
+    const uint32_t b_bytes = round_up((uint32_t)BM * p.SB * 4, 16);
+    const uint32_t t_bytes = round_up((uint32_t)(2 * p.t5_R + 1) * 4, 16);
     uint32_t off = 0;
-    p.off_q = off;    off += q_bytes;                                     // 1024-aligned TMA targets
-    p.off_kv = off;   off += (uint32_t)stages * stage_bytes;
-    p.off_ak = off;   if (ak) off += (uint32_t)p.npad_k * D * 2;
-    p.off_av = off;   if (av) off += (uint32_t)p.kpad_v * D * 2;
-    p.off_r = off;    if (ak) off += round_up((uint32_t)BM * p.SR * 4, 16);  // per-row tables
-    p.off_beta = off; if (av) off += round_up((uint32_t)BM * p.SR * 4, 16);
-    p.off_t5 = off;   if (t5mode) off += round_up((uint32_t)(2 * p.t5_R + 1) * 4, 16);
-    p.off_x = off;    if (bn == 128) off += (2 * 2 + 2 * 3) * BM * 4;  // row-half exchange
-    p.off_bar = off;  off += (uint32_t)kNumBars * 8 + 16;
+    // TMA targets first: every size below is a multiple of 1024 bytes
+    for (int s = 0; s < 2; ++s) {
+        p.off_q[s] = off;
+        if (s < nslots) off += q_bytes;
+    }
+    p.off_kv = off;
+    off += (uint32_t)stages * stage_bytes;
+    for (int s = 0; s < 2; ++s) {
+        p.off_ak[s] = s < ntab ? off : p.off_ak[0];
+        if (ak && s < ntab) off += (uint32_t)p.npad_k * D * 2;
+    }
+    for (int s = 0; s < 2; ++s) {
+        p.off_av[s] = s < ntab ? off : p.off_av[0];
+        if (av && s < ntab) off += (uint32_t)p.kpad_v * D * 2;
+    }
+    for (int s = 0; s < 2; ++s) {
+        p.off_r[s] = off;
+        if (ak && s < nslots) off += r_bytes;
+    }
+    for (int s = 0; s < 2; ++s) {
+        p.off_beta[s] = off;
+        if (av && s < nslots) off += b_bytes;
+    }
+    for (int s = 0; s < 2; ++s) {
+        p.off_t5[s] = off;
+        if (t5mode && s < nslots) off += t_bytes;
+    }
+    p.off_bar = off;
+    off += (uint32_t)kNumBars * 8 + 16;
     p.stages = stages;
     p.stage_bytes = stage_bytes;
     return off + 1024;  // slack to align the base to 1024 bytes
@@ -159,7 +179,6 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     p.H = a.H;
     p.n = a.n;
     p.n_qtiles = (a.n + BM - 1) / BM;
-    p.num_tiles = p.BH * p.n_qtiles;
     p.scale_log2 = a.scale * kLog2e;
     p.kv_len = a.kv_len;
     p.err = err_word;
@@ -170,7 +189,7 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         p.W = a.causal ? a.clip_k + 1 : 2 * a.clip_k + 1;
         if (p.W > 128) return cudaErrorNotSupported;
     }
-    p.SR = (p.W + 2) & ~1;  // even (conflict-free gathers), with a spare slot at index W
+    p.SB = (p.W + 2) & ~1;  // even, > W: conflict-free bin gathers and a spare slot
     p.npad_k = (int)round_up((uint32_t)p.W, 16);
     p.kpad_v = p.npad_k;
     p.table_heads = a.ths != 0 ? 1 : 0;
@@ -179,7 +198,7 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         p.t5 = *t5;
         p.t5_R = t5->sat;
     }
-    if (p.num_tiles == 0) return cudaSuccess;
+    if (p.BH == 0 || p.n_qtiles == 0) return cudaSuccess;
 
     const DeviceInfo di = device_info();
     if (di.sms <= 0 || di.smem_optin <= 0) return cudaErrorInvalidDevice;
@@ -189,40 +208,49 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         const int64_t fit = di.l2_bytes > 0 ? (int64_t)di.l2_bytes / 2 / (per_head > 0 ? per_head : 1) : p.BH;
         p.head_group = (int)(fit < 1 ? 1 : (fit > p.BH ? p.BH : fit));
     }
-    // two CTAs per SM (64-key tiles, TMEM 256 columns each) when D = 64, the staged table
-    // rows fit a 64-key score buffer and the shared memory of both fits; else one CTA per
-    // SM with 128-key tiles
-    int cps = 1;
+    // Choose the first configuration that fits shared memory: two query tiles per item
+    // before one, fp32 R rows before bf16 ones, three K/V stages before two.
+    struct Choice { int pair, r_bf16, min_stages; };
+    const Choice choices[] = {{1, 0, 3}, {1, 1, 3}, {1, 0, 2}, {1, 1, 2},
+                              {0, 0, 3}, {0, 1, 3}, {0, 0, 2}, {0, 1, 2}};
     uint32_t smem = 0;
-    if (D == 64 && p.npad_k <= 64) {
-        const int64_t budget2 =
-            ((int64_t)di.smem_per_sm - 2 * (int64_t)di.smem_reserved) / 2 - 2048;  // margin
+    bool found = false;
+    for (const Choice &c : choices) {
+        if (c.r_bf16 && !ak) continue;
         Params q = p;
-        const uint32_t fixed = layout<D>(q, ak, av, t5mode, 64, 0);
-        const int64_t st = (budget2 - (int64_t)fixed) / ((int64_t)64 * D * 2);
-        if (st >= 4) {
-            cps = 2;
-            smem = layout<D>(p, ak, av, t5mode, 64, (int)(st > kMaxStages ? kMaxStages : st));
-        }
+        q.pair = c.pair;
+        // the two tiles of an item belong to different heads only for odd tile counts
+        q.two_tables = (c.pair && (p.n_qtiles & 1) && p.table_heads && (ak || av)) ? 1 : 0;
+        q.r_bf16 = c.r_bf16;
+        // R row stride: W - 1 + stride coprime with the bank count, so the banded gathers
+        // of the 32 rows of a warp hit 32 distinct banks (fp32: odd SR - 1; bf16: SR = 3 mod 4)
+        q.SR = c.r_bf16 ? p.W + ((3 - p.W % 4) + 4) % 4 : p.W + (p.W & 1);
+        const uint32_t fixed = layout<D>(q, ak, av, t5mode, 0);
+        const int64_t st = ((int64_t)di.smem_optin - (int64_t)fixed) / ((int64_t)BN * D * 2);
+        if (st < c.min_stages) continue;
+        p = q;
+        smem = layout<D>(p, ak, av, t5mode, (int)(st > kMaxStages ? kMaxStages : st));
+        found = true;
+        break;
     }
-    if (cps == 1) {
-        Params q = p;
-        const uint32_t fixed = layout<D>(q, ak, av, t5mode, 128, 0);
-        const int64_t st = ((int64_t)di.smem_optin - (int64_t)fixed) / ((int64_t)128 * D * 2);
-        if (st < 2) return cudaErrorNotSupported;
-        smem = layout<D>(p, ak, av, t5mode, 128, (int)(st > kMaxStages ? kMaxStages : st));
+    if (!found || smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
+    {
+        const int G = p.head_group;
+        const int full = p.BH / G, rest = p.BH - full * G;
+        const int64_t items = (int64_t)full * items_per_group(G, p.n_qtiles, p.pair) +
+                              (rest ? items_per_group(rest, p.n_qtiles, p.pair) : 0);
+        if (items > INT32_MAX) return cudaErrorNotSupported;
+        p.num_items = (int)items;
     }
-    if (smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
 
     // ---- TMA descriptors (the output is written with plain stores)
     // q; k and v in 32-row boxes; k and v in whole-tile boxes; the two edge tables
     CUtensorMap tm[7];
     const uint64_t d = (uint64_t)D, n = (uint64_t)a.n, BH = (uint64_t)p.BH;
     const uint64_t rs = d * 2, hs = n * d * 2;
-    const uint32_t bn = cps == 2 ? 64u : 128u;
     if (!make_map(&tm[0], a.q, d, n, BH, rs, hs, BM) || !make_map(&tm[1], a.k, d, n, BH, rs, hs, KB) ||
-        !make_map(&tm[2], a.v, d, n, BH, rs, hs, KB) || !make_map(&tm[3], a.k, d, n, BH, rs, hs, bn) ||
-        !make_map(&tm[4], a.v, d, n, BH, rs, hs, bn))
+        !make_map(&tm[2], a.v, d, n, BH, rs, hs, KB) || !make_map(&tm[3], a.k, d, n, BH, rs, hs, BN) ||
+        !make_map(&tm[4], a.v, d, n, BH, rs, hs, BN))
         return cudaErrorInvalidValue;
     tm[5] = tm[0];
     tm[6] = tm[0];
@@ -234,20 +262,11 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     if (av && !make_map(&tm[6], a.aV, d, rows, Ht, rs, ths_bytes, (uint32_t)p.kpad_v))
         return cudaErrorInvalidValue;
 
-    if constexpr (D == 64) {
-        if (cps == 2) {
-            if (a.causal)
-                return t5mode ? launch_terms<D, true, true, 2>(ak, av, tm, p, smem, s)
-                              : launch_terms<D, false, true, 2>(ak, av, tm, p, smem, s);
-            return t5mode ? launch_terms<D, true, false, 2>(ak, av, tm, p, smem, s)
-                          : launch_terms<D, false, false, 2>(ak, av, tm, p, smem, s);
-        }
-    }
     if (a.causal)
-        return t5mode ? launch_terms<D, true, true, 1>(ak, av, tm, p, smem, s)
-                      : launch_terms<D, false, true, 1>(ak, av, tm, p, smem, s);
-    return t5mode ? launch_terms<D, true, false, 1>(ak, av, tm, p, smem, s)
-                  : launch_terms<D, false, false, 1>(ak, av, tm, p, smem, s);
+        return t5mode ? launch_terms<D, true, true>(ak, av, tm, p, smem, s)
+                      : launch_terms<D, false, true>(ak, av, tm, p, smem, s);
+    return t5mode ? launch_terms<D, true, false>(ak, av, tm, p, smem, s)
+                  : launch_terms<D, false, false>(ak, av, tm, p, smem, s);
 }
 
 }  // namespace tc
