@@ -13,7 +13,8 @@
 // scheduled in groups of heads whose K/V fit in half of L2, longest causal rows first. When
 // the per-row tables of two slots do not fit shared memory, an item is one tile.
 // Warp roles (384 threads):
-//   warp 0      TMA producer: both Q tiles and the edge tables, then K/V tiles of 128 keys
+//   warp 0      TMA producer (the whole warp runs it, one elected lane issues): both Q tiles
+//               and the edge tables, then K/V tiles of 128 keys
 //               (whole-tile boxes, 32-row boxes for the last, partly valid tile) into a ring,
 //               in the order the MMA warp consumes them.
 //   warp 1      MMA issuer (the whole warp runs it; one elected lane issues each tcgen05
@@ -95,13 +96,12 @@ struct Params {
     void *out;          // [B, H, n, D] bf16
     int clip_k;         // Shaw: k
     int W;              // table rows staged: k+1 (causal) or 2k+1
-    int SR;             // row stride (elements) of the R rows in shared memory
+    int SR;             // row stride (floats) of the R rows in shared memory
     int SB;             // row stride (floats) of the value bins, with a spare slot at index W
     int pair;           // 1: two query tiles per item, 0: one
     int npad_k;         // W rounded up to 16: N of the R = Q W^K^T MMA
     int kpad_v;         // W rounded up to 16: K of the beta W^V MMA
     int table_heads;    // 1: tables indexed by head, 0: one shared table
-    int r_bf16;         // the R rows are kept as bf16 (when fp32 does not fit)
     int two_tables;     // the two slots may belong to different heads: own table buffers
     const float *bias;  // T5 [num_buckets, H]
     int t5_R;           // T5 offset-table radius (bucket is constant beyond it)
@@ -117,22 +117,40 @@ struct Shared {
     volatile int *abort_flag;
 };
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared &sh,
-                                         int *err) {
-    if (ptx::mbar_try(bar, parity)) return true;
+// slow path of a bounded wait (spins with an abort check and a cycle limit)
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           int *err) {
     const long long t0 = clock64();
     uint32_t spins = 0;
     while (true) {
         if (ptx::mbar_try(bar, parity)) return true;
         if ((++spins & 255u) == 0) {
-            if (*sh.abort_flag) return false;
+            if (*abort_flag) return false;
             if (clock64() - t0 > kWaitLimitCycles) {
-                *sh.abort_flag = 1;
+                *abort_flag = 1;
                 atomicCAS(err, 0, 4 /* RELATTN_ERR_TIMEOUT */);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared &sh,
+                                         int *err) {
+    if (ptx::mbar_try(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, sh.abort_flag, err);
+}
+
+// the same for the producer and MMA warps, with the slow path out of line (those warps have
+// registers to spare for a call, and their many waits would otherwise each carry a copy)
+static __device__ __noinline__ bool wait_bar_slow_call(uint32_t bar, uint32_t parity,
+                                                volatile int *abort_flag, int *err) {
+    return wait_bar_slow(bar, parity, abort_flag, err);
+}
+__device__ __forceinline__ bool wait_bar_ctrl(uint32_t bar, uint32_t parity, const Shared &sh,
+                                              int *err) {
+    if (ptx::mbar_try(bar, parity)) return true;
+    return wait_bar_slow_call(bar, parity, sh.abort_flag, err);
 }
 
 // bounded poll of a barrier during teardown (no abort check)
@@ -248,38 +266,30 @@ struct Plan {
     __device__ __forceinline__ int users(int j) const {
         return (j < J[0] ? 1 : 0) | (j < J[1] ? 2 : 0);
     }
-    // calls fn(isK, j, mask, src) for each ring entry in order; stops when fn returns false
-    template <class F>
-    __device__ __forceinline__ bool visit(F &&fn) const {
+    // The entries come in groups: group 0 is K_0; then, per tile j, the groups K_{j+1} and
+    // V_j (in the order above). A group is one entry in shared items and one entry per slot
+    // that has that tile otherwise. Callers walk g = 0 .. groups()-1 and e = 0 .. 1 with
+    // entry(g, e, ...), so the per-entry code exists once.
+    __device__ __forceinline__ int groups() const { return 1 + 2 * Jmax; }
+    // entry e of group g: false if there is none; else isK, tile j, slot mask and source slot
+    __device__ __forceinline__ bool entry(int g, int e, bool &isK, int &j, int &mask, int &src) const {
+        if (g == 0) {
+            isK = true;
+            j = 0;
+        } else {
+            const int jj = (g - 1) >> 1;
+            const bool first = ((g - 1) & 1) == 0;
+            isK = EARLY_S ? first : !first;
+            j = isK ? jj + 1 : jj;
+        }
         if (shared) {
-            if (!fn(true, 0, users(0), 0)) return false;
-            for (int j = 0; j < Jmax; ++j) {
-                const bool k_next = j + 1 < Jmax;
-                if (EARLY_S && k_next && !fn(true, j + 1, users(j + 1), 0)) return false;
-                if (!fn(false, j, users(j), 0)) return false;
-                if (!EARLY_S && k_next && !fn(true, j + 1, users(j + 1), 0)) return false;
-            }
-            return true;
+            src = 0;
+            mask = e == 0 ? users(j) : 0;
+        } else {
+            src = e;
+            mask = j < J[e] ? (1 << e) : 0;
         }
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-            if (J[s] > 0 && !fn(true, 0, 1 << s, s)) return false;
-        for (int j = 0; j < Jmax; ++j) {
-            if (EARLY_S) {
-#pragma unroll
-                for (int s = 0; s < 2; ++s)
-                    if (j + 1 < J[s] && !fn(true, j + 1, 1 << s, s)) return false;
-            }
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-                if (j < J[s] && !fn(false, j, 1 << s, s)) return false;
-            if (!EARLY_S) {
-#pragma unroll
-                for (int s = 0; s < 2; ++s)
-                    if (j + 1 < J[s] && !fn(true, j + 1, 1 << s, s)) return false;
-            }
-        }
-        return true;
+        return mask != 0;
     }
     // keys of tile j loaded for an entry (the largest of the slots using it)
     __device__ __forceinline__ int load_cols(int j, int mask) const {
@@ -303,6 +313,11 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     const uint32_t sKV = sh.base + p.off_kv;
     const int S = p.stages;
+    // the whole warp runs this role; waits are made warp-uniform and one lane issues
+    auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = wait_bar_ctrl(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
     uint32_t kv_it = 0, q_it = 0, av_it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
@@ -310,7 +325,7 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
         Plan<CAUSAL, EARLY_S> pl;
         pl.make(p, it);
         if (pl.Jmax == 0) continue;
-        if (!(ok = wait_bar(bar(B_Q_EMPTY), (q_it & 1u) ^ 1u, sh, p.err))) break;
+        if (!(ok = wait(bar(B_Q_EMPTY), (q_it & 1u) ^ 1u))) break;
         ++q_it;
         // edge-table buffer b serves slot b (two_tables) or both slots; tab_head[b] < 0: unused
         int tab_head[2] = {-1, -1};
@@ -326,61 +341,65 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
             if (pl.active(s)) qbytes += (uint32_t)BM * D * 2;
             if (AK && tab_head[s] >= 0) qbytes += (uint32_t)p.npad_k * D * 2;
         }
-        ptx::mbar_expect_tx(bar(B_Q_FULL), qbytes);
+        ptx::mbar_expect_tx_w(bar(B_Q_FULL), qbytes);
         for (int s = 0; s < 2; ++s) {
             if (pl.active(s)) {
                 const uint32_t sQ = sh.base + p.off_q[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d(sQ + blk * BM * 128, tm_q, bar(B_Q_FULL), blk * 64,
+                    ptx::tma_load_3d_w(sQ + blk * BM * 128, tm_q, bar(B_Q_FULL), blk * 64,
                                      it.qt[s] * BM, it.bh[s]);
             }
             if (AK && tab_head[s] >= 0) {
                 const uint32_t sAK = sh.base + p.off_ak[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d(sAK + blk * p.npad_k * 128, tm_ak, bar(B_Q_FULL), blk * 64, 0,
+                    ptx::tma_load_3d_w(sAK + blk * p.npad_k * 128, tm_ak, bar(B_Q_FULL), blk * 64, 0,
                                      tab_head[s]);
             }
         }
-        ok = pl.visit([&](bool isK, int j, int mask, int src) -> bool {
-            const int st = (int)(kv_it % (uint32_t)S);
-            const uint32_t round = kv_it / (uint32_t)S;
-            if (!wait_bar(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u, sh, p.err)) return false;
-            const int nbox = pl.load_cols(j, mask) / KB;
-            ptx::mbar_expect_tx(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
-            const uint32_t dst = sKV + (uint32_t)st * p.stage_bytes;
-            const int bh = it.bh[src];
-            if (nbox == BN / KB) {  // whole tile: one box of 128 rows per 64-column block
-#pragma unroll
-                for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d(dst + blk * BN * 128, isK ? tm_kf : tm_vf, bar(B_KV0 + st),
-                                     blk * 64, j * BN, bh);
-            } else {  // last tile: only the 32-row boxes holding allowed keys
-                for (int b = 0; b < nbox; ++b) {
+        for (int g = 0; g < pl.groups() && ok; ++g) {
+            for (int e = 0; e < 2; ++e) {
+                bool isK;
+                int j, mask, src;
+                if (!pl.entry(g, e, isK, j, mask, src)) continue;
+                const int st = (int)(kv_it % (uint32_t)S);
+                const uint32_t round = kv_it / (uint32_t)S;
+                if (!(ok = wait(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u))) break;
+                const int nbox = pl.load_cols(j, mask) / KB;
+                ptx::mbar_expect_tx_w(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
+                const uint32_t dst = sKV + (uint32_t)st * p.stage_bytes;
+                const int bh = it.bh[src];
+                if (nbox == BN / KB) {  // whole tile: one box of 128 rows per 64-column block
 #pragma unroll
                     for (int blk = 0; blk < DB; ++blk)
-                        ptx::tma_load_3d(dst + blk * BN * 128 + b * KB * 128, isK ? tm_k : tm_v,
-                                         bar(B_KV0 + st), blk * 64, j * BN + b * KB, bh);
+                        ptx::tma_load_3d_w(dst + blk * BN * 128, isK ? tm_kf : tm_vf, bar(B_KV0 + st),
+                                         blk * 64, j * BN, bh);
+                } else {  // last tile: only the 32-row boxes holding allowed keys
+                    for (int b = 0; b < nbox; ++b) {
+#pragma unroll
+                        for (int blk = 0; blk < DB; ++blk)
+                            ptx::tma_load_3d_w(dst + blk * BN * 128 + b * KB * 128, isK ? tm_k : tm_v,
+                                             bar(B_KV0 + st), blk * 64, j * BN + b * KB, bh);
+                    }
                 }
+                ++kv_it;
             }
-            ++kv_it;
-            return true;
-        });
+        }
         if (!ok) break;
         if (AV) {
-            if (!(ok = wait_bar(bar(B_AV_EMPTY), (av_it & 1u) ^ 1u, sh, p.err))) break;
+            if (!(ok = wait(bar(B_AV_EMPTY), (av_it & 1u) ^ 1u))) break;
             ++av_it;
             uint32_t vbytes = 0;
             for (int s = 0; s < 2; ++s)
                 if (tab_head[s] >= 0) vbytes += (uint32_t)p.kpad_v * D * 2;
-            ptx::mbar_expect_tx(bar(B_AV_FULL), vbytes);
+            ptx::mbar_expect_tx_w(bar(B_AV_FULL), vbytes);
             for (int s = 0; s < 2; ++s) {
                 if (tab_head[s] < 0) continue;
                 const uint32_t sAV = sh.base + p.off_av[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d(sAV + blk * p.kpad_v * 128, tm_av, bar(B_AV_FULL), blk * 64, 0,
+                    ptx::tma_load_3d_w(sAV + blk * p.kpad_v * 128, tm_av, bar(B_AV_FULL), blk * 64, 0,
                                      tab_head[s]);
             }
         }
@@ -408,16 +427,11 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
     const uint32_t S = (uint32_t)p.stages;
     constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
-        const bool r = wait_bar(b, parity, sh, p.err);
+        const bool r = wait_bar_ctrl(b, parity, sh, p.err);
         return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
     };
-    // descriptors: Q (K-major, per slot), K/V stage 0 (K-major for S, MN-major for P V).
-    // launder() keeps the compiler from hoisting every stepped descriptor out of the loops
-    // (that would hold dozens of 64-bit values in registers for the whole kernel).
-    auto launder = [](uint64_t v) {
-        asm volatile("" : "+l"(v));
-        return v;
-    };
+    // descriptors: Q (K-major, per slot), K/V stage 0 (K-major for S, MN-major for P V);
+    // the MMA loops step them by the k-offset of each instruction
     const uint64_t dq0 = ptx::sdesc_sw128(sh.base + p.off_q[0], 16, 1024);
     const uint64_t dq1 = ptx::sdesc_sw128(sh.base + p.off_q[1], 16, 1024);
     const uint64_t dk0 = ptx::sdesc_sw128(sh.base + p.off_kv, 16, 1024);
@@ -462,56 +476,60 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
                 if (!(ok = claim_s(s))) break;
                 const uint64_t dak = ptx::sdesc_sw128(sh.base + p.off_ak[p.two_tables ? s : 0], 16, 1024);
                 const uint64_t dq = s ? dq1 : dq0;
-#pragma unroll
+#pragma unroll 1
                 for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::tc_mma_w(tmem + T::S(s), launder(dq) + kstep(kk, BM),
-                                  launder(dak) + kstep(kk, p.npad_k), idR, kk > 0 ? 1u : 0u);
+                    ptx::tc_mma_w(tmem + T::S(s), dq + kstep(kk, BM), dak + kstep(kk, p.npad_k), idR,
+                                  kk > 0 ? 1u : 0u);
                 ptx::tc_commit_w(sbar(s, SB_S_FULL));
             }
             if (!ok) break;
         }
         int k_left = pl.shared ? pl.Jmax : pl.J[0] + pl.J[1];  // K entries still to consume
-        ok = pl.visit([&](bool isK, int j, int mask, int src) -> bool {
-            const uint32_t stg = kv_it % S;
-            if (!wait(bar(B_KV0 + (int)stg), (kv_it / S) & 1u)) return false;
-            ptx::tc_fence_after();
-            const uint64_t off = (uint64_t)stg * stage16;
+        for (int g = 0; g < pl.groups() && ok; ++g) {
+            for (int e = 0; e < 2 && ok; ++e) {
+                bool isK;
+                int j, mask, src;
+                if (!pl.entry(g, e, isK, j, mask, src)) continue;
+                const uint32_t stg = kv_it % S;
+                if (!(ok = wait(bar(B_KV0 + (int)stg), (kv_it / S) & 1u))) break;
+                ptx::tc_fence_after();
+                const uint64_t off = (uint64_t)stg * stage16;
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                if (!(mask & (1 << s))) continue;
-                const int cols = tile_cols(pl.nkc[s], j);
-                if (isK) {  // S_j = Q K_j^T
-                    if (!claim_s(s)) return false;
-                    const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
-                    const uint64_t dk = dk0 + off;
-                    const uint64_t dq = s ? dq1 : dq0;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        ptx::tc_mma_w(tmem + T::S(s), launder(dq) + kstep(kk, BM),
-                                      launder(dk) + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
-                    ptx::tc_commit_w(sbar(s, SB_S_FULL));
-                } else {  // O += P_j V_j
-                    if (!wait(sbar(s, SB_P_FULL), p_it[s] & 1u)) return false;
-                    ++p_it[s];
-                    ptx::tc_fence_after();
-                    const uint64_t dv = dv0 + off;
-                    const int nk16 = cols / 16;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        if (kk < nk16)
+                for (int s = 0; s < 2; ++s) {
+                    if (!(mask & (1 << s))) continue;
+                    const int cols = tile_cols(pl.nkc[s], j);
+                    if (isK) {  // S_j = Q K_j^T
+                        if (!(ok = claim_s(s))) break;
+                        const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
+                        const uint64_t dk = dk0 + off;
+                        const uint64_t dq = s ? dq1 : dq0;
+#pragma unroll 1
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            ptx::tc_mma_w(tmem + T::S(s), dq + kstep(kk, BM), dk + kstep(kk, BN), idS,
+                                          kk > 0 ? 1u : 0u);
+                        ptx::tc_commit_w(sbar(s, SB_S_FULL));
+                    } else {  // O += P_j V_j
+                        if (!(ok = wait(sbar(s, SB_P_FULL), p_it[s] & 1u))) break;
+                        ++p_it[s];
+                        ptx::tc_fence_after();
+                        const uint64_t dv = dv0 + off;
+                        const int nk16 = cols / 16;
+#pragma unroll 1
+                        for (int kk = 0; kk < nk16; ++kk)
                             ptx::tc_mma_ts_w(tmem + T::O(s), tmem + T::P(s) + (uint32_t)(kk * 8),
-                                             launder(dv) + (uint64_t)(kk * 16 * 128 >> 4), idPV,
+                                             dv + (uint64_t)(kk * 16 * 128 >> 4), idPV,
                                              (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::tc_commit_w(sbar(s, SB_PV_DONE));
-                    ++pv_it[s];
-                    pv_pending[s] = true;
+                        ptx::tc_commit_w(sbar(s, SB_PV_DONE));
+                        ++pv_it[s];
+                        pv_pending[s] = true;
+                    }
                 }
+                if (!ok) break;
+                ptx::tc_commit_w(bar(B_KV0 + kMaxStages + (int)stg));  // entry consumed
+                ++kv_it;
+                if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
             }
-            ptx::tc_commit_w(bar(B_KV0 + kMaxStages + (int)stg));  // entry consumed
-            ++kv_it;
-            if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
-            return true;
-        });
+        }
         if (!ok) break;
         if (AV) {  // O += beta W^V, beta (bf16 pairs) in the slot's P columns
             if (!(ok = wait(bar(B_AV_FULL), av_it & 1u))) break;
@@ -524,6 +542,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
                 ptx::tc_fence_after();
                 const uint64_t dav = ptx::sdesc_sw128(sh.base + p.off_av[p.two_tables ? s : 0],
                                                       (uint32_t)p.kpad_v * 128, 1024);
+#pragma unroll 1
                 for (int kk = 0; kk < p.kpad_v / 16; ++kk)
                     ptx::tc_mma_ts_w(tmem + T::O(s), tmem + T::P(s) + (uint32_t)(kk * 8),
                                      dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
@@ -546,7 +565,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
 // ======================================================================= softmax / epilogue
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
 
-// maximum / minimum of 32 values, 16 three-input instructions, depth 5
+// maximum of 32 values, 16 three-input instructions, depth 5
 __device__ __forceinline__ float max32(const float *x) {
     float a0 = ptx::max3(x[0], x[1], x[2]), a1 = ptx::max3(x[3], x[4], x[5]);
     float a2 = ptx::max3(x[6], x[7], x[8]), a3 = ptx::max3(x[9], x[10], x[11]);
@@ -562,22 +581,6 @@ __device__ __forceinline__ float max32(const float *x) {
     a1 = ptx::max3(a1, x[30], x[31]);
     return ptx::max3(a0, a1, fmaxf(a2, a3));
 }
-__device__ __forceinline__ float min32(const float *x) {
-    float a0 = ptx::min3(x[0], x[1], x[2]), a1 = ptx::min3(x[3], x[4], x[5]);
-    float a2 = ptx::min3(x[6], x[7], x[8]), a3 = ptx::min3(x[9], x[10], x[11]);
-    a0 = ptx::min3(a0, x[12], x[13]);
-    a1 = ptx::min3(a1, x[14], x[15]);
-    a2 = ptx::min3(a2, x[16], x[17]);
-    a3 = ptx::min3(a3, x[18], x[19]);
-    a0 = ptx::min3(a0, x[20], x[21]);
-    a1 = ptx::min3(a1, x[22], x[23]);
-    a2 = ptx::min3(a2, x[24], x[25]);
-    a3 = ptx::min3(a3, x[26], x[27]);
-    a0 = ptx::min3(a0, x[28], x[29]);
-    a1 = ptx::min3(a1, x[30], x[31]);
-    return ptx::min3(a0, a1, fminf(a2, a3));
-}
-
 template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
 __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
     using T = Tm<D>;
@@ -590,11 +593,10 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     auto sbar = [&](int which) { return bar(B_SLOT0 + 6 * slot + which); };
     float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r[slot]) + row * p.SR;
-    __nv_bfloat16 *Rrow16 = reinterpret_cast<__nv_bfloat16 *>(sh.ptr + p.off_r[slot]) + row * p.SR;
     float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta[slot]) + row * p.SB;
     float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5[slot]);
     const float sl2 = p.scale_log2;
-    const bool neg_scale = sl2 < 0.f;
+    const bool pos_scale = sl2 >= 0.f;  // raw chunks need max(x * sl2) = sl2 * max(x)
     const int k = p.clip_k;
     const int hi_off = CAUSAL ? 0 : k;  // largest offset held in the staged table rows
     const int W = p.W;
@@ -626,10 +628,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         __syncwarp();
         return true;
     };
-    auto rel = [&](int idx) -> float {  // scaled R value of table row idx
-        if (AK && p.r_bf16) return __bfloat162float(Rrow16[idx]);
-        return Rrow[idx];
-    };
+    auto rel = [&](int idx) -> float { return Rrow[idx]; };  // scaled R value of table row idx
 
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
         const Item it = decode_item(p, t);
@@ -664,13 +663,8 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                 ptx::tmem_ld16(lane_base + T::S(slot) + (uint32_t)c0, r);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    if (c0 + e < W) {
-                        const float v = __uint_as_float(r[e]) * sl2;
-                        if (p.r_bf16) Rrow16[c0 + e] = __float2bfloat16(v);
-                        else Rrow[c0 + e] = v;
-                    }
-                }
+                for (int e = 0; e < 16; ++e)
+                    if (c0 + e < W) Rrow[c0 + e] = __uint_as_float(r[e]) * sl2;
             }
             release_s();
         }
@@ -704,10 +698,10 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             ptx::tmem_ld_wait();
             release_s();
             // ---- logits in the log2 domain (S2-S4). A chunk whose relative term is one
-            // constant for every row of the warp and that needs no mask stays raw: its
-            // exponent is x * sl2 + (c - m), and its maximum comes from the raw maximum (or
-            // minimum, for a negative scale). Other chunks get the full logit (gathered
-            // relative term, masks) written in place and exponent x - m.
+            // constant for every row of the warp and that needs no mask stays raw (for a
+            // non-negative scale): its exponent is x * sl2 + (c - m), and its maximum comes
+            // from the raw maximum. Other chunks get the full logit (gathered relative term,
+            // masks) written in place and exponent x - m.
             // chunk c of the tile: is it kept raw, and with which constant
             auto raw_chunk = [&](int c, float &cst) -> bool {
                 const int e0 = j0 + c * KB;  // first key of the chunk
@@ -717,7 +711,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                 const bool uniform = (!AK && !T5) || w_left || w_right;
                 const bool full = (e0 + KB <= nk) && (!CAUSAL || e0 + KB - 1 <= gmin);
                 cst = (!AK && !T5) ? 0.f : (w_left ? c_left : c_right);
-                return uniform && full;
+                return uniform && full && pos_scale;
             };
             float rmax = -INFINITY;
 #pragma unroll
@@ -726,8 +720,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                 float *xc = x + c * KB;
                 float cst;
                 if (raw_chunk(c, cst)) {
-                    const float ext = neg_scale ? min32(xc) : max32(xc);
-                    rmax = fmaxf(rmax, fmaf(ext, sl2, cst));
+                    rmax = fmaxf(rmax, fmaf(max32(xc), sl2, cst));
                     continue;
                 }
                 const int e0 = j0 + c * KB;
@@ -947,20 +940,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_raw = *tmem_slot;
 
+    // Each role starts with a full-warp broadcast of the TMEM base: it tells the compiler the
+    // warp is converged and the value warp-uniform, so tcgen05 and TMA operands stay in uniform
+    // registers and each such instruction is a single issue.
     if (warp < kSoftWarp0) {
         ptx::reg_dealloc<kCtrlRegs>();
         if (warp == 0) {
-            if ((threadIdx.x & 31) == 0)
-                producer_role<D, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
-                                                 &tm_av);
+            (void)__shfl_sync(0xffffffffu, tmem_raw, 0);
+            producer_role<D, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
+                                             &tm_av);  // the whole warp; one lane issues
         } else if (warp == 1) {
+            const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_raw, 0);
             mma_role<D, AK, AV, CAUSAL>(p, sh, tmem);  // the whole warp; one lane issues
         }
         __syncwarp();
     } else {
         ptx::reg_alloc<kSoftRegs>();
+        const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_raw, 0);
         softmax_role<D, AK, AV, T5, CAUSAL>(p, sh, tmem, (warp - kSoftWarp0) >> 2);
     }
 
@@ -968,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, 512);
+        ptx::tmem_dealloc(tmem_raw, 512);
     }
 }
 

@@ -122,7 +122,7 @@ cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[7], const Par
     }
 }
 
-// Shared-memory layout for `stages` K/V stages (p.pair, p.two_tables and p.r_bf16 set);
+// Shared-memory layout for `stages` K/V stages (p.pair, p.two_tables and p.SR set);
 // returns the bytes to request.
 template <int D>
 inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
@@ -130,7 +130,7 @@ inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
     const int ntab = p.two_tables ? 2 : 1;
     const uint32_t q_bytes = (uint32_t)BM * D * 2;
     const uint32_t stage_bytes = (uint32_t)BN * D * 2;
-    const uint32_t r_bytes = round_up((uint32_t)BM * p.SR * (p.r_bf16 ? 2 : 4), 16);
+    const uint32_t r_bytes = round_up((uint32_t)BM * p.SR * 4, 16);
     const uint32_t b_bytes = round_up((uint32_t)BM * p.SB * 4, 16);
     const uint32_t t_bytes = round_up((uint32_t)(2 * p.t5_R + 1) * 4, 16);
     uint32_t off = 0;
@@ -209,22 +209,19 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         p.head_group = (int)(fit < 1 ? 1 : (fit > p.BH ? p.BH : fit));
     }
     // Choose the first configuration that fits shared memory: two query tiles per item
-    // before one, fp32 R rows before bf16 ones, three K/V stages before two.
-    struct Choice { int pair, r_bf16, min_stages; };
-    const Choice choices[] = {{1, 0, 3}, {1, 1, 3}, {1, 0, 2}, {1, 1, 2},
-                              {0, 0, 3}, {0, 1, 3}, {0, 0, 2}, {0, 1, 2}};
+    // before one, three K/V stages before two.
+    struct Choice { int pair, min_stages; };
+    const Choice choices[] = {{1, 3}, {1, 2}, {0, 3}, {0, 2}};
+    // R rows (fp32): an even stride, so that W - 1 + stride is odd and the banded gathers of
+    // the 32 rows of a warp fall in 32 distinct banks
+    p.SR = p.W + (p.W & 1);
     uint32_t smem = 0;
     bool found = false;
     for (const Choice &c : choices) {
-        if (c.r_bf16 && !ak) continue;
         Params q = p;
         q.pair = c.pair;
         // the two tiles of an item belong to different heads only for odd tile counts
         q.two_tables = (c.pair && (p.n_qtiles & 1) && p.table_heads && (ak || av)) ? 1 : 0;
-        q.r_bf16 = c.r_bf16;
-        // R row stride: W - 1 + stride coprime with the bank count, so the banded gathers
-        // of the 32 rows of a warp hit 32 distinct banks (fp32: odd SR - 1; bf16: SR = 3 mod 4)
-        q.SR = c.r_bf16 ? p.W + ((3 - p.W % 4) + 4) % 4 : p.W + (p.W & 1);
         const uint32_t fixed = layout<D>(q, ak, av, t5mode, 0);
         const int64_t st = ((int64_t)di.smem_optin - (int64_t)fixed) / ((int64_t)BN * D * 2);
         if (st < c.min_stages) continue;
