@@ -101,13 +101,14 @@ def kernel_source_hash() -> str:
 
 def profiled_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d.get(workload)
-        if e and e.get("source_hash") == kernel_source_hash():
-            return float(e["dram_bytes_per_launch"])
+            for line in f:
+                parts = line.split()
+                if len(parts) == 3 and not line.startswith("#") and parts[0] == workload:
+                    if parts[1] == kernel_source_hash():
+                        return float(parts[2])
     except Exception:
         pass
     return None
@@ -269,6 +270,19 @@ def make_event(external: bool):
     return torch.cuda.Event(enable_timing=True)
 
 
+def workload_config(w, world: int, l2_note: str) -> dict:
+    """The JSON `config` of both arms: the workload by name and shape."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
+            "kind": w.kind, "clip_k": w.clip_k if w.kind == "shaw" else None,
+            "causal": w.causal,
+            "terms": ("t5 bias" if w.kind == "t5" else
+                      "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
+                               if on) or "none"),
+            "kv_len": "U{%d..%d} per sequence" % w.kv_len_range if w.kv_len_range else None,
+            "parallelism": "dp%d (independent shards, no collective)" % world,
+            "l2": l2_note}
+
+
 def whole_job(elapsed_ms: float, work: float, world: int, device) -> tuple:
     """Whole-job timing over ranks: the slowest rank's time and the work of all ranks.
 
@@ -418,17 +432,10 @@ def run_ours(args, rank, world, local_rank):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(t_max / steps, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
-                   "kind": w.kind, "clip_k": w.clip_k if w.kind == "shaw" else None,
-                   "causal": w.causal,
-                   "terms": ("t5 bias" if w.kind == "t5" else
-                             "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
-                                      if on) or "none"),
-                   "kv_len": "U{%d..%d} per sequence" % w.kv_len_range if w.kv_len_range else None,
-                   "parallelism": "dp%d (independent shards, no collective)" % world,
-                   "l2": "inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > "
-                         "4 x %.0f MB L2), replayed from a CUDA graph" % (
-                             n_sets, in_bytes / 1e6, n_sets * in_bytes / 1e6, l2 / 1e6)},
+        "config": workload_config(
+            w, world, "inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > "
+                      "4 x %.0f MB L2), replayed from a CUDA graph" % (
+                          n_sets, in_bytes / 1e6, n_sets * in_bytes / 1e6, l2 / 1e6)),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
         "clocks": clocks,
     }
@@ -475,7 +482,8 @@ def run_reference(args, rank, world):
     from relative_position_representations_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload]
     x = wl.draw_inputs(w, seed=args.seed)
-    per_step = max(1.0, args.ref_budget / max(1, args.steps + args.warmup))
+    # the whole run stays within about ref_budget seconds whatever --steps is
+    per_step = max(0.05, args.ref_budget / max(1, args.steps + args.warmup))
     for i in range(args.warmup):
         time_oracle(w, x, min(per_step, 2.0), seed=100 + i)
     tot_fl, tot_dt, last = 0.0, 0.0, None
@@ -492,7 +500,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d},
+        "config": workload_config(w, world, "host memory (the oracle runs on the CPU cores)"),
         "cpu_baseline": cpu,
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
