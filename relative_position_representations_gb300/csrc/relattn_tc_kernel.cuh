@@ -109,7 +109,15 @@ struct Params {
     uint32_t off_q[2], off_kv, off_ak[2], off_av[2], off_r[2], off_beta[2], off_t5[2], off_bar;
     int stages;
     uint32_t stage_bytes;
+    uint32_t stage_mul;  // ceil(2^32 / stages): e / stages = umulhi(e, stage_mul) for the
+                         // ring positions used (e < 2^29)
 };
+
+// ring position e -> (stage, round) without a division
+__device__ __forceinline__ void ring_pos(const Params &p, uint32_t e, uint32_t &stage, uint32_t &round) {
+    round = __umulhi(e, p.stage_mul);
+    stage = e - round * (uint32_t)p.stages;
+}
 
 struct Shared {
     uint32_t base;  // 1024-aligned shared address
@@ -117,7 +125,7 @@ struct Shared {
     volatile int *abort_flag;
 };
 
-// slow path of a bounded wait (spins with an abort check and a cycle limit)
+// slow path of a bounded wait (polls, with an abort check and a cycle limit every 256 polls)
 __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            int *err) {
     const long long t0 = clock64();
@@ -160,13 +168,12 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Barrier among the 128 softmax threads of a slot on an mbarrier, so the wait stays bounded
-// (a plain bar.sync would hang if a thread of the group left after a timeout).
-__device__ __forceinline__ bool group_sync(uint32_t bar, uint32_t &it, const Shared &sh, int *err) {
-    ptx::mbar_arrive(bar);
-    const bool ok = wait_bar(bar, it & 1u, sh, err);
-    ++it;
-    return __all_sync(0xffffffffu, ok ? 1 : 0) != 0;
+// Barrier among the 128 softmax threads of a slot (hardware named barrier 1 + slot): warps
+// blocked in it take no issue slots. `ok` is AND-reduced over the 128 threads, so every
+// thread sees the same result; all 128 threads always reach it together (they follow the
+// same item / tile sequence and leave it at the same point), so it cannot hang.
+__device__ __forceinline__ bool slot_sync(int slot, bool ok) {
+    return ptx::bar_red_and(1 + slot, 128, ok);
 }
 
 // ----------------------------------------------------------------------- work items
@@ -363,8 +370,9 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
                 bool isK;
                 int j, mask, src;
                 if (!pl.entry(g, e, isK, j, mask, src)) continue;
-                const int st = (int)(kv_it % (uint32_t)S);
-                const uint32_t round = kv_it / (uint32_t)S;
+                uint32_t st_u, round;
+                ring_pos(p, kv_it, st_u, round);
+                const int st = (int)st_u;
                 if (!(ok = wait(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u))) break;
                 const int nbox = pl.load_cols(j, mask) / KB;
                 ptx::mbar_expect_tx_w(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
@@ -406,8 +414,11 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
     }
     if (!ok) {
         // drain: wait (bounded) for copies already issued into shared memory
-        for (uint32_t i = kv_it > (uint32_t)S ? kv_it - S : 0; i < kv_it; ++i)
-            drain_bar(bar(B_KV0 + (int)(i % (uint32_t)S)), (i / (uint32_t)S) & 1u);
+        for (uint32_t i = kv_it > (uint32_t)S ? kv_it - S : 0; i < kv_it; ++i) {
+            uint32_t st_u, round;
+            ring_pos(p, i, st_u, round);
+            drain_bar(bar(B_KV0 + (int)st_u), round & 1u);
+        }
         if (q_it) drain_bar(bar(B_Q_FULL), (q_it - 1) & 1u);
         if (AV && av_it) drain_bar(bar(B_AV_FULL), (av_it - 1) & 1u);
     }
@@ -424,7 +435,6 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     auto sbar = [&](int s, int which) { return bar(B_SLOT0 + 6 * s + which); };
-    const uint32_t S = (uint32_t)p.stages;
     constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar_ctrl(b, parity, sh, p.err);
@@ -490,8 +500,9 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
                 bool isK;
                 int j, mask, src;
                 if (!pl.entry(g, e, isK, j, mask, src)) continue;
-                const uint32_t stg = kv_it % S;
-                if (!(ok = wait(bar(B_KV0 + (int)stg), (kv_it / S) & 1u))) break;
+                uint32_t stg, round;
+                ring_pos(p, kv_it, stg, round);
+                if (!(ok = wait(bar(B_KV0 + (int)stg), round & 1u))) break;
                 ptx::tc_fence_after();
                 const uint64_t off = (uint64_t)stg * stage16;
 #pragma unroll
@@ -600,14 +611,20 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
     const int k = p.clip_k;
     const int hi_off = CAUSAL ? 0 : k;  // largest offset held in the staged table rows
     const int W = p.W;
-    uint32_t s_it = 0, pv_it = 0, o_it = 0, grp = 0;
+    uint32_t s_it = 0, pv_it = 0, o_it = 0;
     int t5_head = -1;
     bool ok = true;
     // tcgen05.ld/st are warp-collective (.sync.aligned): every decision guarding them is
     // uniform across the warp, and the warp reconverges before each TMEM access.
+    // Only the slot's first warp polls the mbarrier; the other three wait for it at the
+    // slot's named barrier, which carries the outcome to all 128 threads.
     auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
-        const bool r = wait_bar(b, parity, sh, p.err);
-        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+        bool r = true;
+        if (quad == 0) {
+            r = wait_bar(b, parity, sh, p.err);
+            r = __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+        }
+        return slot_sync(slot, r);
     };
     auto wait_s = [&]() -> bool {
         if (!wait_w(sbar(SB_S_FULL), s_it & 1u)) return false;
@@ -650,10 +667,10 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             continue;
         }
         if (T5 && h != t5_head) {
-            if (!(ok = group_sync(sbar(SB_GROUP), grp, sh, p.err))) break;
+            if (!(ok = slot_sync(slot, true))) break;  // every row is done with the old table
             for (int idx = stid; idx <= 2 * p.t5_R; idx += 128)
                 t5tab[idx] = p.bias[t5_bucket(idx - p.t5_R, p.t5) * p.H + h] * kLog2e;
-            if (!(ok = group_sync(sbar(SB_GROUP), grp, sh, p.err))) break;
+            if (!(ok = slot_sync(slot, true))) break;
             t5_head = h;
         }
         if (AK) {  // R row -> shared memory (scaled to the log2 domain)
@@ -794,12 +811,14 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
                 if (c * KB >= cols) continue;  // never read by P V
-                uint32_t pk[KB / 2];
+                // P (bf16 pairs) is packed into the chunk's own score registers, which are dead
+                // by then, so the asynchronous TMEM store of one chunk never holds registers
+                // that the next chunk writes
+                float *xc = x + c * KB;
                 if (c >= live) {  // no row of this warp sees these keys
 #pragma unroll
-                    for (int e = 0; e < KB / 2; ++e) pk[e] = 0u;
+                    for (int e = 0; e < KB / 2; ++e) xc[e] = 0.f;
                 } else {
-                    float *xc = x + c * KB;
                     float cst;
                     const bool rawc = raw_chunk(c, cst);
                     const float a = rawc ? sl2 : 1.f, b = (rawc ? cst : 0.f) - m_use;
@@ -841,10 +860,11 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                         }
                     }
 #pragma unroll
-                    for (int e = 0; e < KB / 2; ++e) pk[e] = pack2(xc[2 * e], xc[2 * e + 1]);
+                    for (int e = 0; e < KB / 2; ++e)
+                        xc[e] = __uint_as_float(pack2(xc[2 * e], xc[2 * e + 1]));
                 }
                 __syncwarp();
-                ptx::tmem_st16(lane_base + T::P(slot) + (uint32_t)(c * (KB / 2)), pk);
+                ptx::tmem_st16f(lane_base + T::P(slot) + (uint32_t)(c * (KB / 2)), xc);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();

@@ -165,6 +165,7 @@ inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
     off += (uint32_t)kNumBars * 8 + 16;
     p.stages = stages;
     p.stage_bytes = stage_bytes;
+    p.stage_mul = stages > 0 ? (uint32_t)((0x100000000ull + (uint64_t)stages - 1) / (uint64_t)stages) : 0u;
     return off + 1024;  // slack to align the base to 1024 bytes
 }
 

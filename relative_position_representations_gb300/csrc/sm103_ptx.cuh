@@ -88,6 +88,19 @@ __device__ __forceinline__ void bulk_wait0() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// named barrier with an AND reduction of one predicate over the participating threads
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -240,6 +253,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         RELATTN_W8(0), RELATTN_W8(8)
         : "memory");
 }
+// same as tmem_st16, from fp32 registers holding the 32-bit patterns to store
+#define RELATTN_WF8(i) "f"(r[i]), "f"(r[i + 1]), "f"(r[i + 2]), "f"(r[i + 3]), \
+    "f"(r[i + 4]), "f"(r[i + 5]), "f"(r[i + 6]), "f"(r[i + 7])
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        RELATTN_WF8(0), RELATTN_WF8(8)
+        : "memory");
+}
+#undef RELATTN_WF8
 #undef RELATTN_R8
 #undef RELATTN_W8
 
