@@ -17,11 +17,11 @@
 //               and the edge tables, then K/V tiles of 128 keys
 //               (whole-tile boxes, 32-row boxes for the last, partly valid tile) into a ring,
 //               in the order the MMA warp consumes them.
-//   warp 1      MMA issuer (the whole warp runs it; one elected lane issues each tcgen05
-//               instruction, so operands stay warp-uniform): per slot R = Q W^K^T,
+//   warps 1-2   MMA issuers, one per slot (the whole warp runs it; one elected lane issues
+//               each tcgen05 instruction, so operands stay warp-uniform): R = Q W^K^T,
 //               S_j = Q K_j^T, O += P_j V_j (P read from TMEM), O += beta W^V, walking the
-//               K/V ring in the order it was filled; one wait per K/V tile serves both slots.
-//   warps 2-3   idle (registers are allocated per 4-warp group).
+//               K/V ring in the order it was filled; the two slots' chains run side by side.
+//   warp 3      idle (registers are allocated per 4-warp group).
 //   warps 4-7   softmax / epilogue of slot 0, warps 8-11 of slot 1: one thread per query row
 //               (= TMEM lane) holding the whole 128-key score row. The relative term is a
 //               per-row constant on 32-key chunks that lie beyond +-k for the whole warp (the
@@ -79,11 +79,11 @@ struct Tm {
 
 // barrier slots
 enum : int {
-    B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_DRAIN,
-    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, GROUP
+    B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_UNUSED,
+    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, DRAIN
     B_KV0 = B_SLOT0 + 2 * 6
 };
-enum : int { SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_GROUP };
+enum : int { SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN };
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
 
@@ -424,48 +424,51 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
     }
 }
 
-// ======================================================================= MMA issuer
-// The whole warp runs this role with warp-uniform control flow; one elected lane issues
-// each tcgen05 instruction. Descriptors are built once per buffer and stepped by
-// compile-time offsets, so an MMA costs a 64-bit add or two and the issue itself.
+// ======================================================================= MMA issuers
+// One MMA warp per slot (warps 1 and 2), so the two slots' wait-issue-commit chains run side
+// by side. Both warps walk every item's K/V ring entries in ring order and each releases
+// every entry (a tcgen05 commit after its MMAs on it, or a plain arrive when its slot does
+// not use it): the release barriers count two arrivals. A warp releases an entry, Q or the
+// W^V rows only after waiting for them to be filled, so neither warp can arrive for a later
+// fill than the producer has made. The whole warp runs the role with warp-uniform control
+// flow; one elected lane issues each tcgen05 instruction.
 template <int D, bool AK, bool AV, bool CAUSAL>
-__device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
+__device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
     using T = Tm<D>;
     constexpr bool EARLY_S = !T::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    auto sbar = [&](int s, int which) { return bar(B_SLOT0 + 6 * s + which); };
+    auto sbar = [&](int which) { return bar(B_SLOT0 + 6 * slot + which); };
     constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar_ctrl(b, parity, sh, p.err);
         return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
     };
-    // descriptors: Q (K-major, per slot), K/V stage 0 (K-major for S, MN-major for P V);
-    // the MMA loops step them by the k-offset of each instruction
-    const uint64_t dq0 = ptx::sdesc_sw128(sh.base + p.off_q[0], 16, 1024);
-    const uint64_t dq1 = ptx::sdesc_sw128(sh.base + p.off_q[1], 16, 1024);
+    // descriptors: Q of this slot (K-major), K/V stage 0 (K-major for S, MN-major for P V)
+    const uint64_t dq = ptx::sdesc_sw128(sh.base + p.off_q[slot], 16, 1024);
     const uint64_t dk0 = ptx::sdesc_sw128(sh.base + p.off_kv, 16, 1024);
     const uint64_t dv0 = ptx::sdesc_sw128(sh.base + p.off_kv, BN * 128, 1024);
     const uint64_t stage16 = p.stage_bytes >> 4;
+    const uint32_t tS = tmem + T::S(slot), tO = tmem + T::O(slot), tP = tmem + T::P(slot);
     // K-major operand, k-step kk of 16: 64-column block kk / 4 (rows x 128 bytes apart),
     // 32 bytes per step inside the 128-byte swizzle atom
     auto kstep = [](int kk, int rows) -> uint64_t {
         return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
     };
     uint32_t kv_it = 0, q_it = 0, av_it = 0;
-    uint32_t s_it[2] = {0, 0}, p_it[2] = {0, 0}, pv_it[2] = {0, 0};
-    bool pv_pending[2] = {false, false};
+    uint32_t s_it = 0, p_it = 0, pv_it = 0;
+    bool pv_pending = false;
     bool ok = true;
 
     // before an MMA writes the slot's S columns: the softmax has read the previous S item,
     // and (P over S) the MMAs reading P from those columns are done
-    auto claim_s = [&](int s) -> bool {
-        if (T::P_ALIAS && pv_pending[s]) {
-            if (!wait(sbar(s, SB_PV_DONE), (pv_it[s] - 1u) & 1u)) return false;
-            pv_pending[s] = false;
+    auto claim_s = [&]() -> bool {
+        if (T::P_ALIAS && pv_pending) {
+            if (!wait(sbar(SB_PV_DONE), (pv_it - 1u) & 1u)) return false;
+            pv_pending = false;
         }
-        if (!wait(sbar(s, SB_S_EMPTY), (s_it[s] & 1u) ^ 1u)) return false;
-        ++s_it[s];
+        if (!wait(sbar(SB_S_EMPTY), (s_it & 1u) ^ 1u)) return false;
+        ++s_it;
         ptx::tc_fence_after();
         return true;
     };
@@ -475,26 +478,21 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
         Plan<CAUSAL, EARLY_S> pl;
         pl.make(p, it);
         if (pl.Jmax == 0) continue;
+        const bool act = pl.active(slot);
         if (!(ok = wait(bar(B_Q_FULL), q_it & 1u))) break;
         ++q_it;
         ptx::tc_fence_after();
-        if (AK) {  // R = Q W^K^T into each active slot's S columns
+        int k_left = act ? pl.J[slot] : 0;  // S steps still to issue (Q is read until the last)
+        if (!act) ptx::mbar_arrive_w(bar(B_Q_EMPTY));
+        if (AK && act) {  // R = Q W^K^T into the slot's S columns
+            if (!(ok = claim_s())) break;
             const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.npad_k, 0);
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                if (!ok || !pl.active(s)) continue;
-                if (!(ok = claim_s(s))) break;
-                const uint64_t dak = ptx::sdesc_sw128(sh.base + p.off_ak[p.two_tables ? s : 0], 16, 1024);
-                const uint64_t dq = s ? dq1 : dq0;
+            const uint64_t dak = ptx::sdesc_sw128(sh.base + p.off_ak[p.two_tables ? slot : 0], 16, 1024);
 #pragma unroll 1
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::tc_mma_w(tmem + T::S(s), dq + kstep(kk, BM), dak + kstep(kk, p.npad_k), idR,
-                                  kk > 0 ? 1u : 0u);
-                ptx::tc_commit_w(sbar(s, SB_S_FULL));
-            }
-            if (!ok) break;
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::tc_mma_w(tS, dq + kstep(kk, BM), dak + kstep(kk, p.npad_k), idR, kk > 0 ? 1u : 0u);
+            ptx::tc_commit_w(sbar(SB_S_FULL));
         }
-        int k_left = pl.shared ? pl.Jmax : pl.J[0] + pl.J[1];  // K entries still to consume
         for (int g = 0; g < pl.groups() && ok; ++g) {
             for (int e = 0; e < 2 && ok; ++e) {
                 bool isK;
@@ -502,42 +500,39 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
                 if (!pl.entry(g, e, isK, j, mask, src)) continue;
                 uint32_t stg, round;
                 ring_pos(p, kv_it, stg, round);
+                ++kv_it;
                 if (!(ok = wait(bar(B_KV0 + (int)stg), round & 1u))) break;
+                const uint32_t empty = bar(B_KV0 + kMaxStages + (int)stg);
+                if (!(mask & (1 << slot))) {  // the other slot's entry: release at once
+                    ptx::mbar_arrive_w(empty);
+                    continue;
+                }
                 ptx::tc_fence_after();
                 const uint64_t off = (uint64_t)stg * stage16;
-#pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    if (!(mask & (1 << s))) continue;
-                    const int cols = tile_cols(pl.nkc[s], j);
-                    if (isK) {  // S_j = Q K_j^T
-                        if (!(ok = claim_s(s))) break;
-                        const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
-                        const uint64_t dk = dk0 + off;
-                        const uint64_t dq = s ? dq1 : dq0;
+                const int cols = tile_cols(pl.nkc[slot], j);
+                if (isK) {  // S_j = Q K_j^T
+                    if (!(ok = claim_s())) break;
+                    const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
+                    const uint64_t dk = dk0 + off;
 #pragma unroll 1
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            ptx::tc_mma_w(tmem + T::S(s), dq + kstep(kk, BM), dk + kstep(kk, BN), idS,
-                                          kk > 0 ? 1u : 0u);
-                        ptx::tc_commit_w(sbar(s, SB_S_FULL));
-                    } else {  // O += P_j V_j
-                        if (!(ok = wait(sbar(s, SB_P_FULL), p_it[s] & 1u))) break;
-                        ++p_it[s];
-                        ptx::tc_fence_after();
-                        const uint64_t dv = dv0 + off;
-                        const int nk16 = cols / 16;
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        ptx::tc_mma_w(tS, dq + kstep(kk, BM), dk + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+                    ptx::tc_commit_w(sbar(SB_S_FULL));
+                } else {  // O += P_j V_j
+                    if (!(ok = wait(sbar(SB_P_FULL), p_it & 1u))) break;
+                    ++p_it;
+                    ptx::tc_fence_after();
+                    const uint64_t dv = dv0 + off;
+                    const int nk16 = cols / 16;
 #pragma unroll 1
-                        for (int kk = 0; kk < nk16; ++kk)
-                            ptx::tc_mma_ts_w(tmem + T::O(s), tmem + T::P(s) + (uint32_t)(kk * 8),
-                                             dv + (uint64_t)(kk * 16 * 128 >> 4), idPV,
-                                             (j > 0 || kk > 0) ? 1u : 0u);
-                        ptx::tc_commit_w(sbar(s, SB_PV_DONE));
-                        ++pv_it[s];
-                        pv_pending[s] = true;
-                    }
+                    for (int kk = 0; kk < nk16; ++kk)
+                        ptx::tc_mma_ts_w(tO, tP + (uint32_t)(kk * 8), dv + (uint64_t)(kk * 16 * 128 >> 4), idPV,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::tc_commit_w(sbar(SB_PV_DONE));
+                    ++pv_it;
+                    pv_pending = true;
                 }
-                if (!ok) break;
-                ptx::tc_commit_w(bar(B_KV0 + kMaxStages + (int)stg));  // entry consumed
-                ++kv_it;
+                ptx::tc_commit_w(empty);  // the entry is free once these MMAs are done
                 if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
             }
         }
@@ -545,32 +540,28 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem) {
         if (AV) {  // O += beta W^V, beta (bf16 pairs) in the slot's P columns
             if (!(ok = wait(bar(B_AV_FULL), av_it & 1u))) break;
             ++av_it;
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                if (!ok || !pl.active(s)) continue;
-                if (!(ok = wait(sbar(s, SB_P_FULL), p_it[s] & 1u))) break;
-                ++p_it[s];
+            if (act) {
+                if (!(ok = wait(sbar(SB_P_FULL), p_it & 1u))) break;
+                ++p_it;
                 ptx::tc_fence_after();
-                const uint64_t dav = ptx::sdesc_sw128(sh.base + p.off_av[p.two_tables ? s : 0],
+                const uint64_t dav = ptx::sdesc_sw128(sh.base + p.off_av[p.two_tables ? slot : 0],
                                                       (uint32_t)p.kpad_v * 128, 1024);
 #pragma unroll 1
                 for (int kk = 0; kk < p.kpad_v / 16; ++kk)
-                    ptx::tc_mma_ts_w(tmem + T::O(s), tmem + T::P(s) + (uint32_t)(kk * 8),
-                                     dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
-                ptx::tc_commit_w(sbar(s, SB_PV_DONE));
-                ++pv_it[s];
-                pv_pending[s] = true;
+                    ptx::tc_mma_ts_w(tO, tP + (uint32_t)(kk * 8), dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
+                ptx::tc_commit_w(sbar(SB_PV_DONE));
+                ++pv_it;
+                pv_pending = true;
+                ptx::tc_commit_w(bar(B_AV_EMPTY));
+            } else {
+                ptx::mbar_arrive_w(bar(B_AV_EMPTY));
             }
-            if (!ok) break;
-            ptx::tc_commit_w(bar(B_AV_EMPTY));
         }
-#pragma unroll
-        for (int s = 0; s < 2; ++s)
-            if (pl.active(s)) ptx::tc_commit_w(sbar(s, SB_O_FULL));
+        if (act) ptx::tc_commit_w(sbar(SB_O_FULL));
     }
     // every MMA issued by this warp completes before TMEM is released
-    ptx::tc_commit_w(bar(B_DRAIN));
-    drain_bar(bar(B_DRAIN), 0);
+    ptx::tc_commit_w(sbar(SB_DRAIN));
+    drain_bar(sbar(SB_DRAIN), 0);
 }
 
 // ======================================================================= softmax / epilogue
@@ -944,8 +935,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t cnt = 1;
             if (i >= B_SLOT0 && i < B_KV0) {
                 const int which = (i - B_SLOT0) % 6;
-                if (which == SB_S_EMPTY || which == SB_P_FULL || which == SB_GROUP) cnt = 128;
+                if (which == SB_S_EMPTY || which == SB_P_FULL) cnt = 128;  // the slot's threads
             }
+            // released by both MMA warps
+            if (i == B_Q_EMPTY || i == B_AV_EMPTY || i >= B_KV0 + kMaxStages) cnt = 2;
             ptx::mbar_init(bars + 8u * (uint32_t)i, cnt);
         }
         *sh.abort_flag = 0;
@@ -971,9 +964,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             (void)__shfl_sync(0xffffffffu, tmem_raw, 0);
             producer_role<D, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
                                              &tm_av);  // the whole warp; one lane issues
-        } else if (warp == 1) {
+        } else if (warp == 1 || warp == 2) {
             const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_raw, 0);
-            mma_role<D, AK, AV, CAUSAL>(p, sh, tmem);  // the whole warp; one lane issues
+            mma_role<D, AK, AV, CAUSAL>(p, sh, tmem, warp - 1);  // slot warp - 1; one lane issues
         }
         __syncwarp();
     } else {

@@ -174,6 +174,14 @@ __device__ __forceinline__ void tc_commit_w(uint32_t bar) {
         : "memory");
 }
 
+// plain arrive by one elected lane (the whole warp calls it)
+__device__ __forceinline__ void mbar_arrive_w(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(bar)
+        : "memory");
+}
+
 // elected-lane forms of the TMA and transaction-count operations (whole warp calls them)
 __device__ __forceinline__ void mbar_expect_tx_w(uint32_t bar, uint32_t bytes) {
     asm volatile(
