@@ -67,12 +67,18 @@ constexpr float kRescaleLog2 = 8.0f;
 // read only after a wait did not succeed at once and then every 256 polls
 constexpr long long kWaitLimitCycles = 2000000000ll;
 
-template <int D>
+// TMEM columns of slot s. D = 64: S at 128 s, O at 256 + 64 s, P at 384 + 64 s. D = 128 with
+// two tiles per item: S at 128 s, O at 256 + 128 s, P over the first half of the slot's S.
+// D = 128 with one tile per item (SG): S at 0, O at 128, P at 256.
+template <int D, bool SG>
 struct Tm {
-    static constexpr bool P_ALIAS = D == 128;
-    static __device__ __forceinline__ uint32_t S(int s) { return 128u * (uint32_t)s; }
-    static __device__ __forceinline__ uint32_t O(int s) { return 256u + (uint32_t)(D * s); }
+    static constexpr bool P_ALIAS = D == 128 && !SG;
+    static __device__ __forceinline__ uint32_t S(int s) { return (SG && D == 128) ? 0u : 128u * (uint32_t)s; }
+    static __device__ __forceinline__ uint32_t O(int s) {
+        return (SG && D == 128) ? 128u : 256u + (uint32_t)(D * s);
+    }
     static __device__ __forceinline__ uint32_t P(int s) {
+        if (SG && D == 128) return 256u;
         return P_ALIAS ? 128u * (uint32_t)s : 384u + 64u * (uint32_t)s;
     }
 };
@@ -309,13 +315,13 @@ struct Plan {
 };
 
 // ======================================================================= producer
-template <int D, bool AK, bool AV, bool CAUSAL>
+template <int D, bool SG, bool AK, bool AV, bool CAUSAL>
 __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                               const CUtensorMap *tm_kf, const CUtensorMap *tm_vf,
                               const CUtensorMap *tm_ak, const CUtensorMap *tm_av) {
     constexpr int DB = D / 64;
-    constexpr bool EARLY_S = !Tm<D>::P_ALIAS;
+    constexpr bool EARLY_S = !Tm<D, SG>::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     const uint32_t sKV = sh.base + p.off_kv;
@@ -432,9 +438,9 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
 // W^V rows only after waiting for them to be filled, so neither warp can arrive for a later
 // fill than the producer has made. The whole warp runs the role with warp-uniform control
 // flow; one elected lane issues each tcgen05 instruction.
-template <int D, bool AK, bool AV, bool CAUSAL>
+template <int D, bool SG, bool AK, bool AV, bool CAUSAL>
 __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
-    using T = Tm<D>;
+    using T = Tm<D, SG>;
     constexpr bool EARLY_S = !T::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -583,9 +589,9 @@ __device__ __forceinline__ float max32(const float *x) {
     a1 = ptx::max3(a1, x[30], x[31]);
     return ptx::max3(a0, a1, fmaxf(a2, a3));
 }
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
+template <int D, bool SG, bool AK, bool AV, bool T5, bool CAUSAL>
 __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
-    using T = Tm<D>;
+    using T = Tm<D, SG>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
@@ -913,7 +919,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
 }
 
 // ======================================================================= kernel
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
+template <int D, bool SG, bool AK, bool AV, bool T5, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kf,
@@ -962,17 +968,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::reg_dealloc<kCtrlRegs>();
         if (warp == 0) {
             (void)__shfl_sync(0xffffffffu, tmem_raw, 0);
-            producer_role<D, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
+            producer_role<D, SG, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
                                              &tm_av);  // the whole warp; one lane issues
         } else if (warp == 1 || warp == 2) {
             const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_raw, 0);
-            mma_role<D, AK, AV, CAUSAL>(p, sh, tmem, warp - 1);  // slot warp - 1; one lane issues
+            mma_role<D, SG, AK, AV, CAUSAL>(p, sh, tmem, warp - 1);  // slot warp - 1; one lane issues
         }
         __syncwarp();
     } else {
         ptx::reg_alloc<kSoftRegs>();
         const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_raw, 0);
-        softmax_role<D, AK, AV, T5, CAUSAL>(p, sh, tmem, (warp - kSoftWarp0) >> 2);
+        softmax_role<D, SG, AK, AV, T5, CAUSAL>(p, sh, tmem, (warp - kSoftWarp0) >> 2);
     }
 
     ptx::tc_fence_before();

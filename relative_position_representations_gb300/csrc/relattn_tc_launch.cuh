@@ -73,10 +73,10 @@ inline DeviceInfo device_info() {
 
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int D, bool AK, bool AV, bool T5, bool CAUSAL>
+template <int D, bool SG, bool AK, bool AV, bool T5, bool CAUSAL>
 cudaError_t launch_variant(const CUtensorMap (&tm)[7], const Params &p, uint32_t smem_bytes,
                            cudaStream_t s) {
-    auto kern = relattn_tc_kernel<D, AK, AV, T5, CAUSAL>;
+    auto kern = relattn_tc_kernel<D, SG, AK, AV, T5, CAUSAL>;
     // Opt in to the device's whole shared-memory budget once per device and variant, so
     // that later calls (including ones captured into a CUDA graph) only launch.
     static bool opted[64] = {};
@@ -109,16 +109,16 @@ cudaError_t launch_variant(const CUtensorMap (&tm)[7], const Params &p, uint32_t
     return cudaGetLastError();
 }
 
-template <int D, bool T5, bool CAUSAL>
+template <int D, bool SG, bool T5, bool CAUSAL>
 cudaError_t launch_terms(bool ak, bool av, const CUtensorMap (&tm)[7], const Params &p,
                          uint32_t smem, cudaStream_t s) {
     if constexpr (T5) {
-        return launch_variant<D, false, false, true, CAUSAL>(tm, p, smem, s);
+        return launch_variant<D, SG, false, false, true, CAUSAL>(tm, p, smem, s);
     } else {
-        if (ak && av) return launch_variant<D, true, true, false, CAUSAL>(tm, p, smem, s);
-        if (ak) return launch_variant<D, true, false, false, CAUSAL>(tm, p, smem, s);
-        if (av) return launch_variant<D, false, true, false, CAUSAL>(tm, p, smem, s);
-        return launch_variant<D, false, false, false, CAUSAL>(tm, p, smem, s);
+        if (ak && av) return launch_variant<D, SG, true, true, false, CAUSAL>(tm, p, smem, s);
+        if (ak) return launch_variant<D, SG, true, false, false, CAUSAL>(tm, p, smem, s);
+        if (av) return launch_variant<D, SG, false, true, false, CAUSAL>(tm, p, smem, s);
+        return launch_variant<D, SG, false, false, false, CAUSAL>(tm, p, smem, s);
     }
 }
 
@@ -212,13 +212,19 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     // Choose the first configuration that fits shared memory: two query tiles per item
     // before one, three K/V stages before two.
     struct Choice { int pair, min_stages; };
-    const Choice choices[] = {{1, 3}, {1, 2}, {0, 3}, {0, 2}};
+#ifndef RELATTN_D128_PAIR_FIRST
+#define RELATTN_D128_PAIR_FIRST 1
+#endif
+    const Choice pair_first[] = {{1, 3}, {1, 2}, {0, 3}, {0, 2}};
+    const Choice single_first[] = {{0, 3}, {0, 2}, {1, 3}, {1, 2}};
+    const Choice *choices = (D == 128 && !RELATTN_D128_PAIR_FIRST) ? single_first : pair_first;
     // R rows (fp32): an even stride, so that W - 1 + stride is odd and the banded gathers of
     // the 32 rows of a warp fall in 32 distinct banks
     p.SR = p.W + (p.W & 1);
     uint32_t smem = 0;
     bool found = false;
-    for (const Choice &c : choices) {
+    for (int ci = 0; ci < 4; ++ci) {
+        const Choice &c = choices[ci];
         Params q = p;
         q.pair = c.pair;
         // the two tiles of an item belong to different heads only for odd tile counts
@@ -260,11 +266,19 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     if (av && !make_map(&tm[6], a.aV, d, rows, Ht, rs, ths_bytes, (uint32_t)p.kpad_v))
         return cudaErrorInvalidValue;
 
+    // d = 128 with one tile per item keeps P in its own TMEM columns (layout SG)
+    if (D == 128 && !p.pair) {
+        if (a.causal)
+            return t5mode ? launch_terms<D, true, true, true>(ak, av, tm, p, smem, s)
+                          : launch_terms<D, true, false, true>(ak, av, tm, p, smem, s);
+        return t5mode ? launch_terms<D, true, true, false>(ak, av, tm, p, smem, s)
+                      : launch_terms<D, true, false, false>(ak, av, tm, p, smem, s);
+    }
     if (a.causal)
-        return t5mode ? launch_terms<D, true, true>(ak, av, tm, p, smem, s)
-                      : launch_terms<D, false, true>(ak, av, tm, p, smem, s);
-    return t5mode ? launch_terms<D, true, false>(ak, av, tm, p, smem, s)
-                  : launch_terms<D, false, false>(ak, av, tm, p, smem, s);
+        return t5mode ? launch_terms<D, false, true, true>(ak, av, tm, p, smem, s)
+                      : launch_terms<D, false, false, true>(ak, av, tm, p, smem, s);
+    return t5mode ? launch_terms<D, false, true, false>(ak, av, tm, p, smem, s)
+                  : launch_terms<D, false, false, false>(ak, av, tm, p, smem, s);
 }
 
 }  // namespace tc
