@@ -748,9 +748,10 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
 #pragma unroll
                         for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
                     } else {
+                        const int rb = base + k;  // table row of element 0, before clamping
 #pragma unroll
                         for (int e = 0; e < KB; ++e)
-                            xc[e] = fmaf(xc[e], sl2, rel(min(hi_off, max(-k, base + e)) + k));
+                            xc[e] = fmaf(xc[e], sl2, rel(min(W - 1, max(0, rb + e))));
                     }
                 } else if (T5) {
                     const int R = p.t5_R;
@@ -759,20 +760,19 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
 #pragma unroll
                         for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
                     } else {
+                        const int tb = base + R;
 #pragma unroll
                         for (int e = 0; e < KB; ++e)
-                            xc[e] = fmaf(xc[e], sl2, t5tab[min(R, max(-R, base + e)) + R]);
+                            xc[e] = fmaf(xc[e], sl2, t5tab[min(2 * R, max(0, tb + e))]);
                     }
                 } else {
 #pragma unroll
                     for (int e = 0; e < KB; ++e) xc[e] *= sl2;
                 }
-                if (!full) {
+                if (!full) {  // keys j < nk (and j <= i when causal): e < lim
+                    const int lim = (CAUSAL ? min(nk, gi + 1) : nk) - e0;
 #pragma unroll
-                    for (int e = 0; e < KB; ++e) {
-                        const int jj = e0 + e;
-                        if (jj >= nk || (CAUSAL && jj > gi)) xc[e] = -INFINITY;
-                    }
+                    for (int e = 0; e < KB; ++e) xc[e] = e < lim ? xc[e] : -INFINITY;
                 }
                 rmax = fmaxf(rmax, max32(xc));
             }
