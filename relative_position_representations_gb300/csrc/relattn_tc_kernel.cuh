@@ -590,10 +590,15 @@ __device__ __forceinline__ float max32(const float *x) {
     return ptx::max3(a0, a1, fmaxf(a2, a3));
 }
 template <int D, bool SG, bool AK, bool AV, bool T5, bool CAUSAL>
-__device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
+__device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, int slot_in) {
     using T = Tm<D, SG>;
+    const int slot = __shfl_sync(0xffffffffu, slot_in, 0);  // known warp-uniform from here on
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    // warp-level values go through a full-warp broadcast: the compiler then knows them (and
+    // every branch on them) to be warp-uniform, which keeps the per-chunk control flow free of
+    // divergence handling
+    auto uni = [](int v) { return __shfl_sync(0xffffffffu, v, 0); };
+    const int quad = uni(warp & 3);  // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     const int stid = threadIdx.x - 32 * (kSoftWarp0 + 4 * slot);  // 0 .. 127
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -649,9 +654,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         if (!it.valid[slot]) continue;
         const int bh = it.bh[slot], qt = it.qt[slot];
         const int i0 = qt * BM, gi = i0 + row, h = bh % p.H;
-        const int gmin = i0 + quad * 32, gmax = gmin + 31;  // rows of this warp
-        const int nk = keys_of(p, bh);
-        const int nkc = tile_keys<CAUSAL>(p, bh, qt);
+        const int gmin = uni(i0 + quad * 32), gmax = gmin + 31;  // rows of this warp
+        const int nk = uni(keys_of(p, bh));
+        const int nkc = uni(tile_keys<CAUSAL>(p, bh, qt));
         const int J = (nkc + BN - 1) / BN;
         __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                               ((long long)bh * p.n + gi) * D;
