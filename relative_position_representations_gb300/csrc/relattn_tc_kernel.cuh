@@ -439,8 +439,9 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
 // fill than the producer has made. The whole warp runs the role with warp-uniform control
 // flow; one elected lane issues each tcgen05 instruction.
 template <int D, bool SG, bool AK, bool AV, bool CAUSAL>
-__device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int slot) {
+__device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int slot_in) {
     using T = Tm<D, SG>;
+    const int slot = __shfl_sync(0xffffffffu, slot_in, 0);  // known warp-uniform from here on
     constexpr bool EARLY_S = !T::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
