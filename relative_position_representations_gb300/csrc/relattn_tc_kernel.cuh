@@ -702,7 +702,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         const int hi_lim = T5 ? p.t5_R : hi_off;
         if (AV)
             for (int r = 0; r < W; ++r) brow[r] = 0.f;
-        float m_ref = -INFINITY, l = 0.f, lo_sum = 0.f, hi_sum = 0.f;
+        float m_ref = -INFINITY, l = 0.f, hi_sum = 0.f;
 
         for (int j = 0; j < J; ++j) {
             const int j0 = j * BN;
@@ -793,7 +793,6 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             // on the first key tile l, the bins and O hold nothing yet: no rescale needed
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 l *= alpha;
-                lo_sum *= alpha;
                 hi_sum *= alpha;
                 if (AV && alpha != 1.f)
                     for (int r = 0; r < W; ++r) brow[r] *= alpha;
@@ -840,25 +839,22 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                     const float rs = (s0 + s1) + (s2 + s3);
                     l += rs;
                     if (AV) {
+                        // bins 1 .. W-1 each get exactly one key over the whole row (offsets
+                        // -k+1 .. hi_off) and are stored as they come; keys beyond +k (not
+                        // causal) add to hi_sum; bin 0 (offsets <= -k) is what the row sum
+                        // leaves once all other bins are known, so keys left of the window
+                        // need no work here
                         const int e0 = j0 + c * KB;
                         const bool w_left = (e0 + KB - 1 - gmin) <= -k;
                         const bool w_right = (e0 - gmax) >= hi_off;
-                        if (w_left) {
-                            lo_sum += rs;
-                        } else if (w_right) {
+                        if (w_right) {
                             hi_sum += rs;
-                        } else {
-                            // branch-free: end-bin terms go to the sums; interior bins get
-                            // exactly one key each over the whole row and are stored; the
-                            // others write a spare slot (index W)
-                            const int base = e0 - gi;
+                        } else if (!w_left) {
+                            const int bk = e0 - gi + k;  // bin of element 0, before range checks
 #pragma unroll
                             for (int e = 0; e < KB; ++e) {
-                                const int o = base + e;
-                                const bool lo = o <= -k, hi = !lo && o >= hi_off;
-                                lo_sum += lo ? xc[e] : 0.f;
-                                hi_sum += hi ? xc[e] : 0.f;
-                                brow[(lo || hi) ? W : o + k] = xc[e];
+                                if ((unsigned)(bk + e) < (unsigned)W) brow[bk + e] = xc[e];
+                                if (!CAUSAL) hi_sum += bk + e >= W ? xc[e] : 0.f;
                             }
                         }
                     }
@@ -878,8 +874,15 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         if (AV) {
             // bins (bf16 pairs) become the A operand of O += beta W^V
             if (!(ok = wait_pv(pv_next - 1u))) break;
-            brow[0] += lo_sum;
-            brow[W - 1] += hi_sum;
+            if (!CAUSAL) brow[W - 1] += hi_sum;
+            float b0 = 0.f, b1 = 0.f;
+            int r = 1;
+            for (; r + 1 < W; r += 2) {
+                b0 += brow[r];
+                b1 += brow[r + 1];
+            }
+            if (r < W) b0 += brow[r];
+            brow[0] = fmaxf(0.f, l - (b0 + b1));  // every key with offset <= -k
             for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
                 uint32_t pk[16];
 #pragma unroll
