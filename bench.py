@@ -387,6 +387,11 @@ def run_ours(args, rank, world, local_rank):
             graph.replay()
             stream.synchronize()
     sampler.stop()
+    # a bounded device wait that ran out voids the timing (and the outputs)
+    status = rp.relattn_get_device_error(stream)
+    if status != 0:
+        raise RuntimeError("device status word set during the timed region: %s"
+                           % rp.relattn_status_string(status))
     elapsed_ms = e0.elapsed_time(e1)
     clocks = sampler.summary(t_start_wall - soak, t_end_wall + soak) if soak else None
     if use_events and any(m > 0 for m in kernel_ms):
@@ -471,6 +476,10 @@ def measure_e2e(rp, w, x, dev, stream, flops, args):
             step()
         e1.record(stream)
     stream.synchronize()
+    status = rp.relattn_get_device_error(stream)
+    if status != 0:
+        raise RuntimeError("device status word set during the end-to-end run: %s"
+                           % rp.relattn_status_string(status))
     ms = e0.elapsed_time(e1) / n
     return {"value": round(flops / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

@@ -81,15 +81,19 @@ struct Tm {
         if (SG && D == 128) return 256u;
         return P_ALIAS ? 128u * (uint32_t)s : 384u + 64u * (uint32_t)s;
     }
+    // value bins (bf16 pairs, up to 64 columns): the upper half of the slot's S columns, which
+    // hold nothing live once the item's last score tile is in registers (P over S takes only
+    // the lower half), so the bins never wait for the last P . V
+    static __device__ __forceinline__ uint32_t Bn(int s) { return S(s) + 64u; }
 };
 
 // barrier slots
 enum : int {
     B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_UNUSED,
-    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, DRAIN
-    B_KV0 = B_SLOT0 + 2 * 6
+    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, DRAIN, BN_FULL
+    B_KV0 = B_SLOT0 + 2 * 7
 };
-enum : int { SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN };
+enum : int { SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN, SB_BN_FULL, kSlotBars };
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
 
@@ -238,6 +242,24 @@ __device__ __forceinline__ Item decode_item(const Params &p, int t) {
 __device__ __forceinline__ int keys_of(const Params &p, int bh) {
     if (!p.kv_len) return p.n;
     return max(0, min(p.kv_len[bh / p.H], p.n));
+}
+
+// one slot's share of item t: head, query tile and the allowed keys of that head; not valid
+// past the last item or when the slot has no tile in it
+struct SlotItem {
+    int bh, qt, nk;
+    bool valid;
+};
+__device__ __forceinline__ SlotItem slot_item(const Params &p, int t, int slot) {
+    SlotItem r{0, 0, 0, false};
+    if (t < p.num_items) {
+        const Item it = decode_item(p, t);
+        r.valid = it.valid[slot];
+        r.bh = it.bh[slot];
+        r.qt = it.qt[slot];
+        if (r.valid) r.nk = keys_of(p, r.bh);
+    }
+    return r;
 }
 
 // keys any row of query tile qt may see
@@ -445,7 +467,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
     constexpr bool EARLY_S = !T::P_ALIAS;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    auto sbar = [&](int which) { return bar(B_SLOT0 + 6 * slot + which); };
+    auto sbar = [&](int which) { return bar(B_SLOT0 + kSlotBars * slot + which); };
     constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar_ctrl(b, parity, sh, p.err);
@@ -457,22 +479,23 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
     const uint64_t dv0 = ptx::sdesc_sw128(sh.base + p.off_kv, BN * 128, 1024);
     const uint64_t stage16 = p.stage_bytes >> 4;
     const uint32_t tS = tmem + T::S(slot), tO = tmem + T::O(slot), tP = tmem + T::P(slot);
+    const uint32_t tB = tmem + T::Bn(slot);
     // K-major operand, k-step kk of 16: 64-column block kk / 4 (rows x 128 bytes apart),
     // 32 bytes per step inside the 128-byte swizzle atom
     auto kstep = [](int kk, int rows) -> uint64_t {
         return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
     };
     uint32_t kv_it = 0, q_it = 0, av_it = 0;
-    uint32_t s_it = 0, p_it = 0, pv_it = 0;
-    bool pv_pending = false;
+    uint32_t s_it = 0, p_it = 0, pv_it = 0, bn_it = 0;
+    bool s_read_pending = false;  // an MMA reading the S columns (P over S, value bins) may run
     bool ok = true;
 
     // before an MMA writes the slot's S columns: the softmax has read the previous S item,
-    // and (P over S) the MMAs reading P from those columns are done
+    // and the MMAs reading P (P over S) or the value bins from those columns are done
     auto claim_s = [&]() -> bool {
-        if (T::P_ALIAS && pv_pending) {
+        if (s_read_pending) {
             if (!wait(sbar(SB_PV_DONE), (pv_it - 1u) & 1u)) return false;
-            pv_pending = false;
+            s_read_pending = false;
         }
         if (!wait(sbar(SB_S_EMPTY), (s_it & 1u) ^ 1u)) return false;
         ++s_it;
@@ -537,7 +560,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                                          (j > 0 || kk > 0) ? 1u : 0u);
                     ptx::tc_commit_w(sbar(SB_PV_DONE));
                     ++pv_it;
-                    pv_pending = true;
+                    s_read_pending = T::P_ALIAS;
                 }
                 ptx::tc_commit_w(empty);  // the entry is free once these MMAs are done
                 if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
@@ -548,17 +571,17 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
             if (!(ok = wait(bar(B_AV_FULL), av_it & 1u))) break;
             ++av_it;
             if (act) {
-                if (!(ok = wait(sbar(SB_P_FULL), p_it & 1u))) break;
-                ++p_it;
+                if (!(ok = wait(sbar(SB_BN_FULL), bn_it & 1u))) break;
+                ++bn_it;
                 ptx::tc_fence_after();
                 const uint64_t dav = ptx::sdesc_sw128(sh.base + p.off_av[p.two_tables ? slot : 0],
                                                       (uint32_t)p.kpad_v * 128, 1024);
 #pragma unroll 1
                 for (int kk = 0; kk < p.kpad_v / 16; ++kk)
-                    ptx::tc_mma_ts_w(tO, tP + (uint32_t)(kk * 8), dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
+                    ptx::tc_mma_ts_w(tO, tB + (uint32_t)(kk * 8), dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
                 ptx::tc_commit_w(sbar(SB_PV_DONE));
                 ++pv_it;
-                pv_pending = true;
+                s_read_pending = true;
                 ptx::tc_commit_w(bar(B_AV_EMPTY));
             } else {
                 ptx::mbar_arrive_w(bar(B_AV_EMPTY));
@@ -605,7 +628,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    auto sbar = [&](int which) { return bar(B_SLOT0 + 6 * slot + which); };
+    auto sbar = [&](int which) { return bar(B_SLOT0 + kSlotBars * slot + which); };
     float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r[slot]) + row * p.SR;
     float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta[slot]) + row * p.SB;
     float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5[slot]);
@@ -650,14 +673,17 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
     };
     auto rel = [&](int idx) -> float { return Rrow[idx]; };  // scaled R value of table row idx
 
+    // the next item is decoded and its key count loaded while the current one runs
+    SlotItem nxt = slot_item(p, blockIdx.x, slot);
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
-        const Item it = decode_item(p, t);
-        if (!it.valid[slot]) continue;
-        const int bh = it.bh[slot], qt = it.qt[slot];
+        const SlotItem cur = nxt;
+        nxt = slot_item(p, t + gridDim.x, slot);
+        if (!cur.valid) continue;
+        const int bh = uni(cur.bh), qt = uni(cur.qt);
         const int i0 = qt * BM, gi = i0 + row, h = bh % p.H;
         const int gmin = uni(i0 + quad * 32), gmax = gmin + 31;  // rows of this warp
-        const int nk = uni(keys_of(p, bh));
-        const int nkc = uni(tile_keys<CAUSAL>(p, bh, qt));
+        const int nk = uni(cur.nk);
+        const int nkc = CAUSAL ? min(nk, i0 + BM) : nk;  // keys any row of the tile may see
         const int J = (nkc + BN - 1) / BN;
         __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                               ((long long)bh * p.n + gi) * D;
@@ -702,7 +728,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         const int hi_lim = T5 ? p.t5_R : hi_off;
         if (AV)
             for (int r = 0; r < W; ++r) brow[r] = 0.f;
-        float m_ref = -INFINITY, l = 0.f, hi_sum = 0.f;
+        float m_ref = -INFINITY, l = 0.f, lsum = 0.f;
 
         for (int j = 0; j < J; ++j) {
             const int j0 = j * BN;
@@ -716,7 +742,8 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             for (int c = 0; c < NCH; ++c)
                 if (c < live) ptx::tmem_ld32f(lane_base + T::S(slot) + (uint32_t)(c * KB), x + c * KB);
             ptx::tmem_ld_wait();
-            release_s();
+            // with value bins, the last tile's S columns are kept for them (released below)
+            if (!AV || j + 1 < J) release_s();
             // ---- logits in the log2 domain (S2-S4). A chunk whose relative term is one
             // constant for every row of the warp and that needs no mask stays raw (for a
             // non-negative scale): its exponent is x * sl2 + (c - m), and its maximum comes
@@ -793,7 +820,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             // on the first key tile l, the bins and O hold nothing yet: no rescale needed
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 l *= alpha;
-                hi_sum *= alpha;
+                lsum *= alpha;
                 if (AV && alpha != 1.f)
                     for (int r = 0; r < W; ++r) brow[r] *= alpha;
                 __syncwarp();
@@ -839,23 +866,28 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                     const float rs = (s0 + s1) + (s2 + s3);
                     l += rs;
                     if (AV) {
-                        // bins 1 .. W-1 each get exactly one key over the whole row (offsets
-                        // -k+1 .. hi_off) and are stored as they come; keys beyond +k (not
-                        // causal) add to hi_sum; bin 0 (offsets <= -k) is what the row sum
-                        // leaves once all other bins are known, so keys left of the window
-                        // need no work here
+                        // bins 1 .. W-1 get exactly one key each over the whole row (offsets
+                        // -k+1 .. hi_off) and are stored as they come. The end bins come from
+                        // sums at the end of the row: bin 0 from l (causal) or from lsum, the
+                        // keys at or left of the diagonal (not causal), which also gives bin W-1
                         const int e0 = j0 + c * KB;
-                        const bool w_left = (e0 + KB - 1 - gmin) <= -k;
-                        const bool w_right = (e0 - gmax) >= hi_off;
-                        if (w_right) {
-                            hi_sum += rs;
-                        } else if (!w_left) {
-                            const int bk = e0 - gi + k;  // bin of element 0, before range checks
+                        if (!CAUSAL) {
+                            if (e0 + KB <= gmin) {  // left of every row's diagonal
+                                lsum += rs;
+                            } else if (e0 == gmin) {  // the warp's diagonal chunk: keys j <= i
 #pragma unroll
-                            for (int e = 0; e < KB; ++e) {
-                                if ((unsigned)(bk + e) < (unsigned)W) brow[bk + e] = xc[e];
-                                if (!CAUSAL) hi_sum += bk + e >= W ? xc[e] : 0.f;
+                                for (int e = 0; e < KB; ++e) lsum += e <= lane ? xc[e] : 0.f;
                             }
+                        }
+                        // chunks whose keys all fall in an end bin for every row need nothing
+                        const bool w_left = (e0 + KB - 1 - gmin) <= -k;
+                        const bool w_right = CAUSAL ? e0 > gmax : (e0 - gmax) >= k;
+                        if (!w_left && !w_right) {
+                            float *bp = brow + (e0 - gi + k);  // bin of element 0
+                            const int elo = gi - k - e0;  // elements elo .. elo + W - 1: bins 0 .. W-1
+#pragma unroll
+                            for (int e = 0; e < KB; ++e)
+                                if ((unsigned)(e - elo) < (unsigned)W) bp[e] = xc[e];
                         }
                     }
 #pragma unroll
@@ -872,17 +904,25 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         if (!ok) break;
         uint32_t pv_next = pv_it + (uint32_t)J;  // completions after this tile's P . V
         if (AV) {
-            // bins (bf16 pairs) become the A operand of O += beta W^V
-            if (!(ok = wait_pv(pv_next - 1u))) break;
-            if (!CAUSAL) brow[W - 1] += hi_sum;
-            float b0 = 0.f, b1 = 0.f;
-            int r = 1;
-            for (; r + 1 < W; r += 2) {
-                b0 += brow[r];
-                b1 += brow[r + 1];
+            // bins (bf16 pairs) become the A operand of O += beta W^V; that MMA is issued after
+            // the last P . V by the same thread and runs after it
+            if (!CAUSAL && W > 1) {
+                // lsum = bin 0 + bins 1 .. k; l - lsum = bins k+1 .. W-2 + bin W-1
+                float a = 0.f, b = 0.f;
+                for (int r = 1; r <= k; ++r) a += brow[r];
+                for (int r = k + 1; r < W - 1; ++r) b += brow[r];
+                brow[0] = fmaxf(0.f, lsum - a);
+                brow[W - 1] = fmaxf(0.f, (l - lsum) - b);
+            } else {  // l = bin 0 + bins 1 .. W-1
+                float a = 0.f, b = 0.f;
+                int r = 1;
+                for (; r + 1 < W; r += 2) {
+                    a += brow[r];
+                    b += brow[r + 1];
+                }
+                if (r < W) a += brow[r];
+                brow[0] = fmaxf(0.f, l - (a + b));
             }
-            if (r < W) b0 += brow[r];
-            brow[0] = fmaxf(0.f, l - (b0 + b1));  // every key with offset <= -k
             for (int c0 = 0; c0 < p.kpad_v; c0 += 32) {
                 uint32_t pk[16];
 #pragma unroll
@@ -891,11 +931,14 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                     pk[e] = pack2(r0 < W ? brow[r0] : 0.f, r0 + 1 < W ? brow[r0 + 1] : 0.f);
                 }
                 __syncwarp();
-                ptx::tmem_st16(lane_base + T::P(slot) + (uint32_t)(c0 / 2), pk);
+                ptx::tmem_st16(lane_base + T::Bn(slot) + (uint32_t)(c0 / 2), pk);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(sbar(SB_P_FULL));
+            // a barrier of their own: nothing orders this arrival after the MMA warp has seen
+            // the last P tile, so on P_FULL it could complete the next phase before that
+            ptx::mbar_arrive(sbar(SB_BN_FULL));
+            ptx::mbar_arrive(sbar(SB_S_EMPTY));  // the S columns go back once the bins are read
             ++pv_next;
         }
         pv_it = pv_next;
@@ -949,8 +992,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t cnt = 1;
             if (i >= B_SLOT0 && i < B_KV0) {
-                const int which = (i - B_SLOT0) % 6;
-                if (which == SB_S_EMPTY || which == SB_P_FULL) cnt = 128;  // the slot's threads
+                const int which = (i - B_SLOT0) % kSlotBars;
+                if (which == SB_S_EMPTY || which == SB_P_FULL || which == SB_BN_FULL)
+                    cnt = 128;  // the slot's threads
             }
             // released by both MMA warps
             if (i == B_Q_EMPTY || i == B_AV_EMPTY || i >= B_KV0 + kMaxStages) cnt = 2;

@@ -138,12 +138,16 @@ BF16_CASES = [
 
 @pytest.mark.parametrize("case", BF16_CASES, ids=[c[0] for c in BF16_CASES])
 def test_bf16_variants(case):
+    w = _bf16_workload(case)
+    check(w, seed=w.n + w.clip_k)
+
+
+def _bf16_workload(case):
     name, n, d, k, causal, kv, key, val, shared = case
     # large tables so that the relative terms move the output well beyond the tolerance
-    w = wl.Workload(name, B=2, H=3, n=n, d=d, dtype="bf16", clip_k=k, causal=causal,
-                    kv_len_range=kv, key_term=key, value_term=val, shared_tables=shared,
-                    table_std=0.5)
-    check(w, seed=n + k)
+    return wl.Workload(name, B=2, H=3, n=n, d=d, dtype="bf16", clip_k=k, causal=causal,
+                       kv_len_range=kv, key_term=key, value_term=val, shared_tables=shared,
+                       table_std=0.5)
 
 
 def test_bf16_relative_terms_matter_and_sign_is_checked():
@@ -305,6 +309,43 @@ def test_full_workload_all_rows(name):
 def test_full_workload_sampled_rows(name, count):
     w = wl.WORKLOADS[name]
     check(w, rows=_sample_rows(w, count, 7))
+
+
+@pytest.mark.parametrize("name,reps", [("base_encoder", 400), ("big_decoder", 400),
+                                       ("long_keyonly", 40), ("t5_bias", 80),
+                                       ("ragged_200_causal", 400)])
+def test_repeated_launches(name, reps):
+    """Back-to-back launches on one stream: every launch gives the bitwise-same output (the
+    kernel has no atomics or order-dependent sums in its data path) and no bounded device
+    wait runs out. Races between the warp roles show up here as timeouts or changed outputs
+    long before a single launch trips over them."""
+    rp = _rp()
+    if name in wl.WORKLOADS:
+        w = wl.WORKLOADS[name]
+    else:
+        case = next(c for c in BF16_CASES if c[0] == name)
+        w = _bf16_workload(case)
+    x = wl.draw_inputs(w, 0)
+    assert rp.relattn_get_device_error() == 0
+    first = run_gpu(w, x)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    outs = []
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            if w.kind == "t5":
+                o = rp.relattn_t5bias_fwd(g["q"], g["k"], g["v"], g["bias"], w.num_buckets,
+                                          w.max_distance, w.bidirectional, w.causal,
+                                          w.softmax_scale, kv_len=g.get("kv_len"), stream=stream)
+            else:
+                o = rp.relattn_fwd(g["q"], g["k"], g["v"], g["aK"], g["aV"], w.clip_k, w.causal,
+                                   w.softmax_scale, kv_len=g["kv_len"],
+                                   table_head_stride=wl.table_head_stride(w), stream=stream)
+            outs.append((o != first).any())
+    stream.synchronize()
+    assert rp.relattn_get_device_error(stream) == 0, "a device wait ran out"
+    differ = int(torch.stack(outs).sum())
+    assert differ == 0, "%d of %d launches differ from the first" % (differ, reps)
 
 
 def test_no_device_timeouts_recorded():
