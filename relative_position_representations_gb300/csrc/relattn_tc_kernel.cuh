@@ -597,6 +597,15 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
 // ======================================================================= softmax / epilogue
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return ptx::pack_bf16x2(lo, hi); }
 
+// Element pairs (e, e + 1) of a register array go through the two-lane fp32 instructions
+// (one issue for two fused multiply-adds, adds or multiplies, each rounded as its scalar form)
+__device__ __forceinline__ float2 pair(const float *x, int e) { return make_float2(x[e], x[e + 1]); }
+__device__ __forceinline__ void put(float *x, int e, float2 v) {
+    x[e] = v.x;
+    x[e + 1] = v.y;
+}
+__device__ __forceinline__ float2 dup(float v) { return make_float2(v, v); }
+
 // maximum of 32 values, 16 three-input instructions, depth 5
 __device__ __forceinline__ float max32(const float *x) {
     float a0 = ptx::max3(x[0], x[1], x[2]), a1 = ptx::max3(x[3], x[4], x[5]);
@@ -777,30 +786,36 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                 const int base = e0 - gi;  // offset of element 0 for this row
                 if (AK) {
                     if (w_left || w_right) {
-                        const float cst = w_left ? c_left : c_right;
+                        const float2 cst = dup(w_left ? c_left : c_right);
 #pragma unroll
-                        for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
+                        for (int e = 0; e < KB; e += 2) put(xc, e, __ffma2_rn(pair(xc, e), dup(sl2), cst));
                     } else {
                         const int rb = base + k;  // table row of element 0, before clamping
 #pragma unroll
-                        for (int e = 0; e < KB; ++e)
-                            xc[e] = fmaf(xc[e], sl2, rel(min(W - 1, max(0, rb + e))));
+                        for (int e = 0; e < KB; e += 2) {
+                            const float2 r = make_float2(rel(min(W - 1, max(0, rb + e))),
+                                                         rel(min(W - 1, max(0, rb + e + 1))));
+                            put(xc, e, __ffma2_rn(pair(xc, e), dup(sl2), r));
+                        }
                     }
                 } else if (T5) {
                     const int R = p.t5_R;
                     if (w_left || w_right) {
-                        const float cst = w_left ? c_left : c_right;
+                        const float2 cst = dup(w_left ? c_left : c_right);
 #pragma unroll
-                        for (int e = 0; e < KB; ++e) xc[e] = fmaf(xc[e], sl2, cst);
+                        for (int e = 0; e < KB; e += 2) put(xc, e, __ffma2_rn(pair(xc, e), dup(sl2), cst));
                     } else {
                         const int tb = base + R;
 #pragma unroll
-                        for (int e = 0; e < KB; ++e)
-                            xc[e] = fmaf(xc[e], sl2, t5tab[min(2 * R, max(0, tb + e))]);
+                        for (int e = 0; e < KB; e += 2) {
+                            const float2 r = make_float2(t5tab[min(2 * R, max(0, tb + e))],
+                                                         t5tab[min(2 * R, max(0, tb + e + 1))]);
+                            put(xc, e, __ffma2_rn(pair(xc, e), dup(sl2), r));
+                        }
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < KB; ++e) xc[e] *= sl2;
+                    for (int e = 0; e < KB; e += 2) put(xc, e, __fmul2_rn(pair(xc, e), dup(sl2)));
                 }
                 if (!full) {  // keys j < nk (and j <= i when causal): e < lim
                     const int lim = (CAUSAL ? min(nk, gi + 1) : nk) - e0;
@@ -830,7 +845,12 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                     ptx::tmem_ld32(lane_base + T::O(slot) + (uint32_t)c0, r);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 v = __fmul2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                                    dup(alpha));
+                        r[e] = __float_as_uint(v.x);
+                        r[e + 1] = __float_as_uint(v.y);
+                    }
                     ptx::tmem_st32(lane_base + T::O(slot) + (uint32_t)c0, r);
                 }
                 ptx::tmem_st_wait();
@@ -851,19 +871,20 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                     float cst;
                     const bool rawc = raw_chunk(c, cst);
                     const float a = rawc ? sl2 : 1.f, b = (rawc ? cst : 0.f) - m_use;
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                    const float2 a2 = dup(a), b2 = dup(b);
+                    float2 s01 = dup(0.f), s23 = dup(0.f);
 #pragma unroll
                     for (int e = 0; e < KB; e += 4) {
-                        xc[e] = ptx::ex2(fmaf(xc[e], a, b));
-                        xc[e + 1] = ptx::ex2(fmaf(xc[e + 1], a, b));
-                        xc[e + 2] = ptx::ex2(fmaf(xc[e + 2], a, b));
-                        xc[e + 3] = ptx::ex2(fmaf(xc[e + 3], a, b));
-                        s0 += xc[e];
-                        s1 += xc[e + 1];
-                        s2 += xc[e + 2];
-                        s3 += xc[e + 3];
+                        const float2 t0 = __ffma2_rn(pair(xc, e), a2, b2);
+                        const float2 t1 = __ffma2_rn(pair(xc, e + 2), a2, b2);
+                        xc[e] = ptx::ex2(t0.x);
+                        xc[e + 1] = ptx::ex2(t0.y);
+                        xc[e + 2] = ptx::ex2(t1.x);
+                        xc[e + 3] = ptx::ex2(t1.y);
+                        s01 = __fadd2_rn(s01, pair(xc, e));
+                        s23 = __fadd2_rn(s23, pair(xc, e + 2));
                     }
-                    const float rs = (s0 + s1) + (s2 + s3);
+                    const float rs = (s01.x + s01.y) + (s23.x + s23.y);
                     l += rs;
                     if (AV) {
                         // bins 1 .. W-1 get exactly one key each over the whole row (offsets
@@ -956,11 +977,15 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             if (gi < p.n) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint4 v;
-                    v.x = pack2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
-                    v.y = pack2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
-                    v.z = pack2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
-                    v.w = pack2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 o = __fmul2_rn(make_float2(__uint_as_float(r[8 * q + 2 * h]),
+                                                                __uint_as_float(r[8 * q + 2 * h + 1])),
+                                                    dup(inv));
+                        w[h] = pack2(o.x, o.y);
+                    }
+                    const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
                     reinterpret_cast<uint4 *>(orow)[c0 / 8 + q] = v;
                 }
             }
