@@ -90,10 +90,13 @@ struct Tm {
 // barrier slots
 enum : int {
     B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_UNUSED,
-    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, DRAIN, BN_FULL
-    B_KV0 = B_SLOT0 + 2 * 7
+    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, DRAIN, BN_FULL, BN_DONE
+    B_KV0 = B_SLOT0 + 2 * 8
 };
-enum : int { SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN, SB_BN_FULL, kSlotBars };
+enum : int {
+    SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN, SB_BN_FULL, SB_BN_DONE,
+    kSlotBars
+};
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
 
@@ -486,16 +489,23 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
         return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
     };
     uint32_t kv_it = 0, q_it = 0, av_it = 0;
-    uint32_t s_it = 0, p_it = 0, pv_it = 0, bn_it = 0;
-    bool s_read_pending = false;  // an MMA reading the S columns (P over S, value bins) may run
+    uint32_t s_it = 0, p_it = 0, pv_it = 0, bn_it = 0, bd_it = 0;
+    bool pv_pending = false;  // a P . V MMA (reading P over S) may still run
+    bool bn_pending = false;  // a beta W^V MMA (reading the bins in the S columns) may still run
     bool ok = true;
 
     // before an MMA writes the slot's S columns: the softmax has read the previous S item,
-    // and the MMAs reading P (P over S) or the value bins from those columns are done
+    // and the MMAs reading P (P over S) or the value bins from those columns are done (MMAs
+    // into different accumulators are not ordered among themselves). Each of the two waits
+    // is for the latest commit on its barrier, so its parity is never two phases behind.
     auto claim_s = [&]() -> bool {
-        if (s_read_pending) {
+        if (bn_pending) {
+            if (!wait(sbar(SB_BN_DONE), (bd_it - 1u) & 1u)) return false;
+            bn_pending = false;
+        }
+        if (T::P_ALIAS && pv_pending) {
             if (!wait(sbar(SB_PV_DONE), (pv_it - 1u) & 1u)) return false;
-            s_read_pending = false;
+            pv_pending = false;
         }
         if (!wait(sbar(SB_S_EMPTY), (s_it & 1u) ^ 1u)) return false;
         ++s_it;
@@ -560,14 +570,14 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                                          (j > 0 || kk > 0) ? 1u : 0u);
                     ptx::tc_commit_w(sbar(SB_PV_DONE));
                     ++pv_it;
-                    s_read_pending = T::P_ALIAS;
+                    pv_pending = true;
                 }
                 ptx::tc_commit_w(empty);  // the entry is free once these MMAs are done
                 if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
             }
         }
         if (!ok) break;
-        if (AV) {  // O += beta W^V, beta (bf16 pairs) in the slot's P columns
+        if (AV) {  // O += beta W^V, beta (bf16 pairs) in the upper S columns of the slot
             if (!(ok = wait(bar(B_AV_FULL), av_it & 1u))) break;
             ++av_it;
             if (act) {
@@ -579,9 +589,9 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
 #pragma unroll 1
                 for (int kk = 0; kk < p.kpad_v / 16; ++kk)
                     ptx::tc_mma_ts_w(tO, tB + (uint32_t)(kk * 8), dav + (uint64_t)(kk * 16 * 128 >> 4), idPV, 1u);
-                ptx::tc_commit_w(sbar(SB_PV_DONE));
-                ++pv_it;
-                s_read_pending = true;
+                ptx::tc_commit_w(sbar(SB_BN_DONE));
+                ++bd_it;
+                bn_pending = true;
                 ptx::tc_commit_w(bar(B_AV_EMPTY));
             } else {
                 ptx::mbar_arrive_w(bar(B_AV_EMPTY));
@@ -923,7 +933,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             ptx::mbar_arrive(sbar(SB_P_FULL));
         }
         if (!ok) break;
-        uint32_t pv_next = pv_it + (uint32_t)J;  // completions after this tile's P . V
+        pv_it += (uint32_t)J;  // P . V completions of this item
         if (AV) {
             // bins (bf16 pairs) become the A operand of O += beta W^V; that MMA is issued after
             // the last P . V by the same thread and runs after it
@@ -960,9 +970,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
             // the last P tile, so on P_FULL it could complete the next phase before that
             ptx::mbar_arrive(sbar(SB_BN_FULL));
             ptx::mbar_arrive(sbar(SB_S_EMPTY));  // the S columns go back once the bins are read
-            ++pv_next;
         }
-        pv_it = pv_next;
         // ---- epilogue (S8): O / l -> bf16 -> global
         if (!(ok = wait_w(sbar(SB_O_FULL), o_it & 1u))) break;
         ++o_it;
