@@ -89,13 +89,14 @@ struct Tm {
 
 // barrier slots
 enum : int {
-    B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_UNUSED,
-    B_SLOT0 = 5,  // per slot: S_FULL, S_EMPTY, P_FULL, PV_DONE, O_FULL, DRAIN, BN_FULL, BN_DONE
-    B_KV0 = B_SLOT0 + 2 * 8
+    SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN, SB_BN_FULL, SB_BN_DONE,
+    SB_Q_FULL, SB_Q_EMPTY, SB_AV_FULL, SB_AV_EMPTY,  // split feed only
+    kSlotBars
 };
 enum : int {
-    SB_S_FULL = 0, SB_S_EMPTY, SB_P_FULL, SB_PV_DONE, SB_O_FULL, SB_DRAIN, SB_BN_FULL, SB_BN_DONE,
-    kSlotBars
+    B_Q_FULL = 0, B_Q_EMPTY, B_AV_FULL, B_AV_EMPTY, B_UNUSED,  // shared feed only
+    B_SLOT0 = 5,  // per slot: the SB_* barriers
+    B_KV0 = B_SLOT0 + 2 * kSlotBars
 };
 constexpr int kMaxStages = 8;
 constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
@@ -120,16 +121,23 @@ struct Params {
     int t5_R;           // T5 offset-table radius (bucket is constant beyond it)
     T5Buckets t5;
     uint32_t off_q[2], off_kv, off_ak[2], off_av[2], off_r[2], off_beta[2], off_t5[2], off_bar;
+    // Two ways to feed the slots. Shared: one producer warp, one K/V ring whose entries may
+    // serve both slots (two query tiles of one head share K/V), and one Q and one W^V barrier
+    // pair for both. Split (items of two one-tile heads, nothing to share): each slot has its
+    // own producer warp, its own half of the ring and its own Q and W^V barriers, so the two
+    // slots run their items independently.
+    int split;
     int stages;
+    int ring_stages;     // stages of one ring: all of them (shared feed) or half (split feed)
     uint32_t stage_bytes;
-    uint32_t stage_mul;  // ceil(2^32 / stages): e / stages = umulhi(e, stage_mul) for the
-                         // ring positions used (e < 2^29)
+    uint32_t stage_mul;  // ceil(2^32 / ring_stages): e / ring_stages = umulhi(e, stage_mul)
+                         // for the ring positions used (e < 2^29)
 };
 
-// ring position e -> (stage, round) without a division
+// ring position e -> (stage within the ring, round) without a division
 __device__ __forceinline__ void ring_pos(const Params &p, uint32_t e, uint32_t &stage, uint32_t &round) {
     round = __umulhi(e, p.stage_mul);
-    stage = e - round * (uint32_t)p.stages;
+    stage = e - round * (uint32_t)p.ring_stages;
 }
 
 struct Shared {
@@ -300,6 +308,13 @@ struct Plan {
         }
     }
     __device__ __forceinline__ bool active(int s) const { return J[s] > 0; }
+    // split feed: the plan of slot s alone (the other slot's tiles come from its own ring)
+    __device__ __forceinline__ void keep_only(int s) {
+        J[1 - s] = 0;
+        nkc[1 - s] = 0;
+        shared = false;
+        Jmax = J[s];
+    }
     // slots (bit mask) that use K or V tile j
     __device__ __forceinline__ int users(int j) const {
         return (j < J[0] ? 1 : 0) | (j < J[1] ? 2 : 0);
@@ -340,17 +355,27 @@ struct Plan {
 };
 
 // ======================================================================= producer
+// Shared feed: one warp loads for both slots. Split feed: warp `me` loads for slot `me` only,
+// into its own ring (stages ring0 .. ring0 + ring_stages - 1) and on the slot's own barriers.
 template <int D, bool SG, bool AK, bool AV, bool CAUSAL>
 __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                               const CUtensorMap *tm_kf, const CUtensorMap *tm_vf,
-                              const CUtensorMap *tm_ak, const CUtensorMap *tm_av) {
+                              const CUtensorMap *tm_ak, const CUtensorMap *tm_av, int me_in) {
     constexpr int DB = D / 64;
     constexpr bool EARLY_S = !Tm<D, SG>::P_ALIAS;
+    const bool SPLIT = p.split != 0;
+    const int me = __shfl_sync(0xffffffffu, me_in, 0);
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    auto sbar = [&](int s, int which) { return bar(B_SLOT0 + kSlotBars * s + which); };
+    const uint32_t q_full = SPLIT ? sbar(me, SB_Q_FULL) : bar(B_Q_FULL);
+    const uint32_t q_empty = SPLIT ? sbar(me, SB_Q_EMPTY) : bar(B_Q_EMPTY);
+    const uint32_t av_full = SPLIT ? sbar(me, SB_AV_FULL) : bar(B_AV_FULL);
+    const uint32_t av_empty = SPLIT ? sbar(me, SB_AV_EMPTY) : bar(B_AV_EMPTY);
+    const int ring0 = SPLIT ? me * p.ring_stages : 0;
     const uint32_t sKV = sh.base + p.off_kv;
-    const int S = p.stages;
+    const int S = p.ring_stages;
     // the whole warp runs this role; waits are made warp-uniform and one lane issues
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar_ctrl(b, parity, sh, p.err);
@@ -362,12 +387,15 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
         const Item it = decode_item(p, t);
         Plan<CAUSAL, EARLY_S> pl;
         pl.make(p, it);
+        if (SPLIT) pl.keep_only(me);
         if (pl.Jmax == 0) continue;
-        if (!(ok = wait(bar(B_Q_EMPTY), (q_it & 1u) ^ 1u))) break;
+        if (!(ok = wait(q_empty, (q_it & 1u) ^ 1u))) break;
         ++q_it;
         // edge-table buffer b serves slot b (two_tables) or both slots; tab_head[b] < 0: unused
         int tab_head[2] = {-1, -1};
-        if (p.two_tables) {
+        if (SPLIT) {  // own buffers (two_tables is set with the split feed)
+            tab_head[me] = p.table_heads ? it.bh[me] % p.H : 0;
+        } else if (p.two_tables) {
             for (int s = 0; s < 2; ++s)
                 if (pl.active(s)) tab_head[s] = p.table_heads ? it.bh[s] % p.H : 0;
         } else {
@@ -379,20 +407,20 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
             if (pl.active(s)) qbytes += (uint32_t)BM * D * 2;
             if (AK && tab_head[s] >= 0) qbytes += (uint32_t)p.npad_k * D * 2;
         }
-        ptx::mbar_expect_tx_w(bar(B_Q_FULL), qbytes);
+        ptx::mbar_expect_tx_w(q_full, qbytes);
         for (int s = 0; s < 2; ++s) {
             if (pl.active(s)) {
                 const uint32_t sQ = sh.base + p.off_q[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d_w(sQ + blk * BM * 128, tm_q, bar(B_Q_FULL), blk * 64,
+                    ptx::tma_load_3d_w(sQ + blk * BM * 128, tm_q, q_full, blk * 64,
                                      it.qt[s] * BM, it.bh[s]);
             }
             if (AK && tab_head[s] >= 0) {
                 const uint32_t sAK = sh.base + p.off_ak[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d_w(sAK + blk * p.npad_k * 128, tm_ak, bar(B_Q_FULL), blk * 64, 0,
+                    ptx::tma_load_3d_w(sAK + blk * p.npad_k * 128, tm_ak, q_full, blk * 64, 0,
                                      tab_head[s]);
             }
         }
@@ -403,7 +431,7 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
                 if (!pl.entry(g, e, isK, j, mask, src)) continue;
                 uint32_t st_u, round;
                 ring_pos(p, kv_it, st_u, round);
-                const int st = (int)st_u;
+                const int st = ring0 + (int)st_u;
                 if (!(ok = wait(bar(B_KV0 + kMaxStages + st), (round & 1u) ^ 1u))) break;
                 const int nbox = pl.load_cols(j, mask) / KB;
                 ptx::mbar_expect_tx_w(bar(B_KV0 + st), (uint32_t)nbox * KB * D * 2);
@@ -427,18 +455,18 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
         }
         if (!ok) break;
         if (AV) {
-            if (!(ok = wait(bar(B_AV_EMPTY), (av_it & 1u) ^ 1u))) break;
+            if (!(ok = wait(av_empty, (av_it & 1u) ^ 1u))) break;
             ++av_it;
             uint32_t vbytes = 0;
             for (int s = 0; s < 2; ++s)
                 if (tab_head[s] >= 0) vbytes += (uint32_t)p.kpad_v * D * 2;
-            ptx::mbar_expect_tx_w(bar(B_AV_FULL), vbytes);
+            ptx::mbar_expect_tx_w(av_full, vbytes);
             for (int s = 0; s < 2; ++s) {
                 if (tab_head[s] < 0) continue;
                 const uint32_t sAV = sh.base + p.off_av[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
-                    ptx::tma_load_3d_w(sAV + blk * p.kpad_v * 128, tm_av, bar(B_AV_FULL), blk * 64, 0,
+                    ptx::tma_load_3d_w(sAV + blk * p.kpad_v * 128, tm_av, av_full, blk * 64, 0,
                                      tab_head[s]);
             }
         }
@@ -448,29 +476,36 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
         for (uint32_t i = kv_it > (uint32_t)S ? kv_it - S : 0; i < kv_it; ++i) {
             uint32_t st_u, round;
             ring_pos(p, i, st_u, round);
-            drain_bar(bar(B_KV0 + (int)st_u), round & 1u);
+            drain_bar(bar(B_KV0 + ring0 + (int)st_u), round & 1u);
         }
-        if (q_it) drain_bar(bar(B_Q_FULL), (q_it - 1) & 1u);
-        if (AV && av_it) drain_bar(bar(B_AV_FULL), (av_it - 1) & 1u);
+        if (q_it) drain_bar(q_full, (q_it - 1) & 1u);
+        if (AV && av_it) drain_bar(av_full, (av_it - 1) & 1u);
     }
 }
 
 // ======================================================================= MMA issuers
 // One MMA warp per slot (warps 1 and 2), so the two slots' wait-issue-commit chains run side
-// by side. Both warps walk every item's K/V ring entries in ring order and each releases
-// every entry (a tcgen05 commit after its MMAs on it, or a plain arrive when its slot does
-// not use it): the release barriers count two arrivals. A warp releases an entry, Q or the
-// W^V rows only after waiting for them to be filled, so neither warp can arrive for a later
-// fill than the producer has made. The whole warp runs the role with warp-uniform control
-// flow; one elected lane issues each tcgen05 instruction.
+// by side. Shared feed: both warps walk every item's K/V ring entries in ring order and each
+// releases every entry (a tcgen05 commit after its MMAs on it, or a plain arrive when its
+// slot does not use it): the release barriers count two arrivals. A warp releases an entry,
+// Q or the W^V rows only after waiting for them to be filled, so neither warp can arrive for
+// a later fill than the producer has made. Split feed: each warp walks its own slot's ring
+// and barriers, which count one arrival. The whole warp runs the role with warp-uniform
+// control flow; one elected lane issues each tcgen05 instruction.
 template <int D, bool SG, bool AK, bool AV, bool CAUSAL>
 __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int slot_in) {
     using T = Tm<D, SG>;
     const int slot = __shfl_sync(0xffffffffu, slot_in, 0);  // known warp-uniform from here on
     constexpr bool EARLY_S = !T::P_ALIAS;
+    const bool SPLIT = p.split != 0;
     const uint32_t bars = sh.base + p.off_bar;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     auto sbar = [&](int which) { return bar(B_SLOT0 + kSlotBars * slot + which); };
+    const uint32_t q_full = SPLIT ? sbar(SB_Q_FULL) : bar(B_Q_FULL);
+    const uint32_t q_empty = SPLIT ? sbar(SB_Q_EMPTY) : bar(B_Q_EMPTY);
+    const uint32_t av_full = SPLIT ? sbar(SB_AV_FULL) : bar(B_AV_FULL);
+    const uint32_t av_empty = SPLIT ? sbar(SB_AV_EMPTY) : bar(B_AV_EMPTY);
+    const int ring0 = SPLIT ? slot * p.ring_stages : 0;
     constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
     auto wait = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = wait_bar_ctrl(b, parity, sh, p.err);
@@ -517,13 +552,14 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
         const Item it = decode_item(p, t);
         Plan<CAUSAL, EARLY_S> pl;
         pl.make(p, it);
+        if (SPLIT) pl.keep_only(slot);
         if (pl.Jmax == 0) continue;
         const bool act = pl.active(slot);
-        if (!(ok = wait(bar(B_Q_FULL), q_it & 1u))) break;
+        if (!(ok = wait(q_full, q_it & 1u))) break;
         ++q_it;
         ptx::tc_fence_after();
         int k_left = act ? pl.J[slot] : 0;  // S steps still to issue (Q is read until the last)
-        if (!act) ptx::mbar_arrive_w(bar(B_Q_EMPTY));
+        if (!act) ptx::mbar_arrive_w(q_empty);
         if (AK && act) {  // R = Q W^K^T into the slot's S columns
             if (!(ok = claim_s())) break;
             const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.npad_k, 0);
@@ -540,6 +576,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                 if (!pl.entry(g, e, isK, j, mask, src)) continue;
                 uint32_t stg, round;
                 ring_pos(p, kv_it, stg, round);
+                stg += (uint32_t)ring0;
                 ++kv_it;
                 if (!(ok = wait(bar(B_KV0 + (int)stg), round & 1u))) break;
                 const uint32_t empty = bar(B_KV0 + kMaxStages + (int)stg);
@@ -573,12 +610,12 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                     pv_pending = true;
                 }
                 ptx::tc_commit_w(empty);  // the entry is free once these MMAs are done
-                if (isK && --k_left == 0) ptx::tc_commit_w(bar(B_Q_EMPTY));  // last read of Q
+                if (isK && --k_left == 0) ptx::tc_commit_w(q_empty);  // last read of Q
             }
         }
         if (!ok) break;
         if (AV) {  // O += beta W^V, beta (bf16 pairs) in the upper S columns of the slot
-            if (!(ok = wait(bar(B_AV_FULL), av_it & 1u))) break;
+            if (!(ok = wait(av_full, av_it & 1u))) break;
             ++av_it;
             if (act) {
                 if (!(ok = wait(sbar(SB_BN_FULL), bn_it & 1u))) break;
@@ -592,9 +629,9 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                 ptx::tc_commit_w(sbar(SB_BN_DONE));
                 ++bd_it;
                 bn_pending = true;
-                ptx::tc_commit_w(bar(B_AV_EMPTY));
+                ptx::tc_commit_w(av_empty);
             } else {
-                ptx::mbar_arrive_w(bar(B_AV_EMPTY));
+                ptx::mbar_arrive_w(av_empty);
             }
         }
         if (act) ptx::tc_commit_w(sbar(SB_O_FULL));
@@ -1029,8 +1066,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (which == SB_S_EMPTY || which == SB_P_FULL || which == SB_BN_FULL)
                     cnt = 128;  // the slot's threads
             }
-            // released by both MMA warps
-            if (i == B_Q_EMPTY || i == B_AV_EMPTY || i >= B_KV0 + kMaxStages) cnt = 2;
+            // shared feed: released by both MMA warps
+            if (i == B_Q_EMPTY || i == B_AV_EMPTY || (!p.split && i >= B_KV0 + kMaxStages)) cnt = 2;
             ptx::mbar_init(bars + 8u * (uint32_t)i, cnt);
         }
         *sh.abort_flag = 0;
@@ -1052,10 +1089,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // registers and each such instruction is a single issue.
     if (warp < kSoftWarp0) {
         ptx::reg_dealloc<kCtrlRegs>();
-        if (warp == 0) {
+        if (warp == 0 || (p.split && warp == 3)) {  // split feed: warp 3 feeds slot 1
             (void)__shfl_sync(0xffffffffu, tmem_raw, 0);
             producer_role<D, SG, AK, AV, CAUSAL>(p, sh, &tm_q, &tm_k, &tm_v, &tm_kf, &tm_vf, &tm_ak,
-                                             &tm_av);  // the whole warp; one lane issues
+                                             &tm_av, warp == 3 ? 1 : 0);  // the whole warp; one lane issues
         } else if (warp == 1 || warp == 2) {
             const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_raw, 0);
             mma_role<D, SG, AK, AV, CAUSAL>(p, sh, tmem, warp - 1);  // slot warp - 1; one lane issues

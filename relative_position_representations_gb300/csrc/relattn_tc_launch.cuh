@@ -164,8 +164,11 @@ inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
     p.off_bar = off;
     off += (uint32_t)kNumBars * 8 + 16;
     p.stages = stages;
+    // split feed with two slots: each slot's ring takes half of the stages
+    const int rs = p.split ? stages / 2 : stages;
+    p.ring_stages = rs;
     p.stage_bytes = stage_bytes;
-    p.stage_mul = stages > 0 ? (uint32_t)((0x100000000ull + (uint64_t)stages - 1) / (uint64_t)stages) : 0u;
+    p.stage_mul = rs > 0 ? (uint32_t)((0x100000000ull + (uint64_t)rs - 1) / (uint64_t)rs) : 0u;
     return off + 1024;  // slack to align the base to 1024 bytes
 }
 
@@ -210,30 +213,38 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         p.head_group = (int)(fit < 1 ? 1 : (fit > p.BH ? p.BH : fit));
     }
     // Choose the first configuration that fits shared memory: two query tiles per item
-    // before one, three K/V stages before two.
-    struct Choice { int pair, min_stages; };
+    // before one, three K/V stages before two. Heads of one query tile pair two heads per
+    // item with nothing to share between the slots: they take the split feed first (two
+    // stages per slot).
+    struct Choice { int pair, split, min_stages; };
 #ifndef RELATTN_D128_PAIR_FIRST
 #define RELATTN_D128_PAIR_FIRST 1
 #endif
-    const Choice pair_first[] = {{1, 3}, {1, 2}, {0, 3}, {0, 2}};
-    const Choice single_first[] = {{0, 3}, {0, 2}, {1, 3}, {1, 2}};
+    const Choice pair_first[] = {{1, 1, 4}, {1, 0, 3}, {1, 0, 2}, {0, 0, 3}, {0, 0, 2}};
+    const Choice single_first[] = {{0, 0, 3}, {0, 0, 2}, {1, 0, 3}, {1, 0, 2}, {1, 0, 2}};
     const Choice *choices = (D == 128 && !RELATTN_D128_PAIR_FIRST) ? single_first : pair_first;
     // R rows (fp32): an even stride, so that W - 1 + stride is odd and the banded gathers of
     // the 32 rows of a warp fall in 32 distinct banks
     p.SR = p.W + (p.W & 1);
     uint32_t smem = 0;
     bool found = false;
-    for (int ci = 0; ci < 4; ++ci) {
+    for (int ci = 0; ci < 5; ++ci) {
         const Choice &c = choices[ci];
+        if (c.split && p.n_qtiles != 1) continue;
         Params q = p;
         q.pair = c.pair;
-        // the two tiles of an item belong to different heads only for odd tile counts
-        q.two_tables = (c.pair && (p.n_qtiles & 1) && p.table_heads && (ak || av)) ? 1 : 0;
+        q.split = c.split;
+        // the two tiles of an item belong to different heads only for odd tile counts; with
+        // the split feed each slot loads its own tables anyway
+        q.two_tables = (c.pair && (ak || av) &&
+                        (c.split || ((p.n_qtiles & 1) && p.table_heads))) ? 1 : 0;
         const uint32_t fixed = layout<D>(q, ak, av, t5mode, 0);
-        const int64_t st = ((int64_t)di.smem_optin - (int64_t)fixed) / ((int64_t)BN * D * 2);
+        int64_t st = ((int64_t)di.smem_optin - (int64_t)fixed) / ((int64_t)BN * D * 2);
+        if (st > kMaxStages) st = kMaxStages;
+        if (c.split) st &= ~(int64_t)1;  // two rings of equal size
         if (st < c.min_stages) continue;
         p = q;
-        smem = layout<D>(p, ak, av, t5mode, (int)(st > kMaxStages ? kMaxStages : st));
+        smem = layout<D>(p, ak, av, t5mode, (int)st);
         found = true;
         break;
     }

@@ -133,6 +133,9 @@ BF16_CASES = [
     ("d128_both", 300, 128, 16, False, (50, 300), True, True, False),
     ("d128_key_only_causal", 700, 128, 64, True, None, True, False, False),
     ("d128_k_over_n", 130, 128, 20, False, None, True, True, False),
+    # one query tile per head: two heads per item on the split feed (own ring per slot)
+    ("d128_one_tile_causal", 128, 128, 8, True, None, True, False, False),
+    ("d128_one_tile_both", 97, 128, 8, False, (10, 97), True, True, False),
 ]
 
 
@@ -140,6 +143,14 @@ BF16_CASES = [
 def test_bf16_variants(case):
     w = _bf16_workload(case)
     check(w, seed=w.n + w.clip_k)
+
+
+def test_bf16_one_tile_odd_head_count():
+    """Five one-tile heads: the last item has a tile for one slot only (split feed)."""
+    w = wl.Workload("odd_heads", B=1, H=5, n=64, d=64, dtype="bf16", clip_k=6,
+                    kv_len_range=None, table_std=0.5)
+    check(w, seed=3)
+    check(w.replace(causal=True), seed=4)
 
 
 def _bf16_workload(case):
