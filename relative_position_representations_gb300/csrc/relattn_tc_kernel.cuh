@@ -104,6 +104,10 @@ constexpr int kNumBars = B_KV0 + 2 * kMaxStages;
 struct Params {
     int BH, H, n;
     int n_qtiles, num_items, head_group;
+    int items_full, n_groups;  // items of a whole head group; head groups (the last may be short)
+    int rot_step;              // items_full mod the grid size
+    int snake;                 // items differ in length: alternate the wave direction
+    uint32_t off_list;         // shared-memory offset of the snake-order item list
     float scale_log2;   // scale * log2(e)
     const int *kv_len;  // [B] or null
     int *err;           // device status word
@@ -255,15 +259,55 @@ __device__ __forceinline__ int keys_of(const Params &p, int bh) {
     return max(0, min(p.kv_len[bh / p.H], p.n));
 }
 
+// Work order of a CTA. A head group's items come longest first (decode_item). Items of one
+// length (snake = 0): CTA b takes items b, b + gridDim.x, ... Items that differ in length
+// (causal query tiles of long sequences): the CTAs take a group's items in waves of gridDim.x
+// whose direction alternates from wave to wave, so that a CTA that took one of the longest
+// items of a wave takes one of the shortest of the next, and group g's waves start rotated
+// by g * (items per group mod gridDim.x), so that the partial last waves of successive groups
+// land on different CTAs. Every role of a CTA walks the same order.
+constexpr int kListCap = 256;  // entries of the shared-memory item list (snake order)
+
+// The snake order of this CTA, written once by one thread before the roles start (into a
+// list of kListCap entries ending in -1; the host enables the order only when it fits).
+__device__ __forceinline__ void snake_list(const Params &p, int *list) {
+    const int G = (int)gridDim.x;
+    int n = 0;
+    for (int g = 0; g < p.n_groups; ++g) {
+        const int cnt = g + 1 < p.n_groups ? p.items_full : p.num_items - g * p.items_full;
+        int bg = (int)blockIdx.x - (g * p.rot_step) % G;
+        if (bg < 0) bg += G;
+        // a position past the group's end stays past it in later waves
+        for (int k = 0;; ++k) {
+            const int r = k * G + ((k & 1) ? G - 1 - bg : bg);
+            if (r >= cnt || n + 1 >= kListCap) break;
+            list[n++] = g * p.items_full + r;
+        }
+    }
+    list[n] = -1;
+}
+struct Sched {
+    int i;            // items taken so far
+    const int *list;  // the snake order, or null for CTA b taking b, b + gridDim.x, ...
+    __device__ __forceinline__ Sched(const Params &p, const Shared &sh)
+        : i(0), list(p.snake ? reinterpret_cast<const int *>(sh.ptr + p.off_list) : nullptr) {}
+    __device__ __forceinline__ int next(const Params &p) {
+        if (list) return list[i++];
+        const int t = (int)blockIdx.x + i * (int)gridDim.x;
+        ++i;
+        return t < p.num_items ? t : -1;
+    }
+};
+
 // one slot's share of item t: head, query tile and the allowed keys of that head; not valid
-// past the last item or when the slot has no tile in it
+// past the last item (t < 0 or t >= num_items) or when the slot has no tile in it
 struct SlotItem {
     int bh, qt, nk;
     bool valid;
 };
 __device__ __forceinline__ SlotItem slot_item(const Params &p, int t, int slot) {
     SlotItem r{0, 0, 0, false};
-    if (t < p.num_items) {
+    if (t >= 0 && t < p.num_items) {
         const Item it = decode_item(p, t);
         r.valid = it.valid[slot];
         r.bh = it.bh[slot];
@@ -383,7 +427,8 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
     };
     uint32_t kv_it = 0, q_it = 0, av_it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+    Sched sc(p, sh);
+    for (int t = sc.next(p); t >= 0 && ok; t = sc.next(p)) {
         const Item it = decode_item(p, t);
         Plan<CAUSAL, EARLY_S> pl;
         pl.make(p, it);
@@ -548,7 +593,8 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
         return true;
     };
 
-    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+    Sched sc(p, sh);
+    for (int t = sc.next(p); t >= 0 && ok; t = sc.next(p)) {
         const Item it = decode_item(p, t);
         Plan<CAUSAL, EARLY_S> pl;
         pl.make(p, it);
@@ -730,10 +776,13 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
     auto rel = [&](int idx) -> float { return Rrow[idx]; };  // scaled R value of table row idx
 
     // the next item is decoded and its key count loaded while the current one runs
-    SlotItem nxt = slot_item(p, blockIdx.x, slot);
-    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+    Sched sc(p, sh);
+    int t_next = sc.next(p);
+    SlotItem nxt = slot_item(p, t_next, slot);
+    for (int t = t_next; t >= 0 && ok; t = t_next) {
         const SlotItem cur = nxt;
-        nxt = slot_item(p, t + gridDim.x, slot);
+        t_next = sc.next(p);
+        nxt = slot_item(p, t_next, slot);
         if (!cur.valid) continue;
         const int bh = uni(cur.bh), qt = uni(cur.qt);
         const int i0 = qt * BM, gi = i0 + row, h = bh % p.H;
@@ -1071,6 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars + 8u * (uint32_t)i, cnt);
         }
         *sh.abort_flag = 0;
+        if (p.snake) snake_list(p, reinterpret_cast<int *>(sh.ptr + p.off_list));
         ptx::mbar_init_fence();
         ptx::tma_prefetch_desc(&tm_q);
         ptx::tma_prefetch_desc(&tm_k);

@@ -163,6 +163,8 @@ inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
     }
     p.off_bar = off;
     off += (uint32_t)kNumBars * 8 + 16;
+    p.off_list = off;  // the snake-order item list (used only when p.snake)
+    off += (uint32_t)kListCap * 4;
     p.stages = stages;
     // split feed with two slots: each slot's ring takes half of the stages
     const int rs = p.split ? stages / 2 : stages;
@@ -256,6 +258,15 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
                               (rest ? items_per_group(rest, p.n_qtiles, p.pair) : 0);
         if (items > INT32_MAX) return cudaErrorNotSupported;
         p.num_items = (int)items;
+        p.items_full = items_per_group(G, p.n_qtiles, p.pair);
+        p.n_groups = full + (rest ? 1 : 0);
+        const int grid = p.num_items < di.sms ? p.num_items : di.sms;  // as launched below
+        p.rot_step = grid > 0 ? p.items_full % grid : 0;
+        if ((int64_t)p.n_groups * grid > INT32_MAX) return cudaErrorNotSupported;  // g * rot_step
+        // causal query tiles of one head differ in length when a head has more than one pair;
+        // the order goes through a list of kListCap entries per CTA
+        const int64_t per_cta = grid > 0 ? ((int64_t)p.num_items + grid - 1) / grid + p.n_groups : 0;
+        p.snake = (a.causal && a.kv_len == nullptr && p.n_qtiles > 2 && per_cta + 1 < kListCap) ? 1 : 0;
     }
 
     // ---- TMA descriptors (the output is written with plain stores)
