@@ -266,7 +266,10 @@ __device__ __forceinline__ int keys_of(const Params &p, int bh) {
 // items of a wave takes one of the shortest of the next, and group g's waves start rotated
 // by g * (items per group mod gridDim.x), so that the partial last waves of successive groups
 // land on different CTAs. Every role of a CTA walks the same order.
-constexpr int kListCap = 256;  // entries of the shared-memory item list (snake order)
+constexpr int kListCap = 256;
+// Padding of the T5 offset table on each side: a banded chunk of a warp reaches at most 61
+// offsets beyond the table's ends (31 rows of the warp + 30 keys of the chunk)
+constexpr int kT5Pad = 64;  // entries of the shared-memory item list (snake order)
 
 // The snake order of this CTA, written once by one thread before the roles start (into a
 // list of kListCap entries ending in -1; the host enables the order only when it fits).
@@ -733,7 +736,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
     auto sbar = [&](int which) { return bar(B_SLOT0 + kSlotBars * slot + which); };
     float *Rrow = reinterpret_cast<float *>(sh.ptr + p.off_r[slot]) + row * p.SR;
     float *brow = reinterpret_cast<float *>(sh.ptr + p.off_beta[slot]) + row * p.SB;
-    float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5[slot]);
+    // T5 offset table, indices -kT5Pad .. 2R + kT5Pad (the ends repeat the saturated buckets,
+    // so the banded gather of a chunk never clamps)
+    float *t5tab = reinterpret_cast<float *>(sh.ptr + p.off_t5[slot]) + kT5Pad;
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 >= 0.f;  // raw chunks need max(x * sl2) = sl2 * max(x)
     const int k = p.clip_k;
@@ -802,7 +807,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         }
         if (T5 && h != t5_head) {
             if (!(ok = slot_sync(slot, true))) break;  // every row is done with the old table
-            for (int idx = stid; idx <= 2 * p.t5_R; idx += 128)
+            for (int idx = stid - kT5Pad; idx <= 2 * p.t5_R + kT5Pad; idx += 128)
                 t5tab[idx] = p.bias[t5_bucket(idx - p.t5_R, p.t5) * p.H + h] * kLog2e;
             if (!(ok = slot_sync(slot, true))) break;
             t5_head = h;
@@ -904,8 +909,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                         const int tb = base + R;
 #pragma unroll
                         for (int e = 0; e < KB; e += 2) {
-                            const float2 r = make_float2(t5tab[min(2 * R, max(0, tb + e))],
-                                                         t5tab[min(2 * R, max(0, tb + e + 1))]);
+                            const float2 r = make_float2(t5tab[tb + e], t5tab[tb + e + 1]);
                             put(xc, e, __ffma2_rn(pair(xc, e), dup(sl2), r));
                         }
                     }

@@ -132,7 +132,7 @@ inline uint32_t layout(Params &p, bool ak, bool av, bool t5mode, int stages) {
     const uint32_t stage_bytes = (uint32_t)BN * D * 2;
     const uint32_t r_bytes = round_up((uint32_t)BM * p.SR * 4, 16);
     const uint32_t b_bytes = round_up((uint32_t)BM * p.SB * 4, 16);
-    const uint32_t t_bytes = round_up((uint32_t)(2 * p.t5_R + 1) * 4, 16);
+    const uint32_t t_bytes = round_up((uint32_t)(2 * p.t5_R + 1 + 2 * kT5Pad) * 4, 16);
     uint32_t off = 0;
     // TMA targets first: every size below is a multiple of 1024 bytes
     for (int s = 0; s < 2; ++s) {
