@@ -106,6 +106,7 @@ struct Params {
     int n_qtiles, num_items, head_group;
     int items_full, n_groups;  // items of a whole head group; head groups (the last may be short)
     int rot_step;              // items_full mod the grid size
+    int tail_from;             // first item of the split last wave (num_items if none)
     int snake;                 // items differ in length: alternate the wave direction
     uint32_t off_list;         // shared-memory offset of the snake-order item list
     float scale_log2;   // scale * log2(e)
@@ -216,7 +217,7 @@ __host__ __device__ inline int items_per_group(int gsize, int Q, int pair) {
 // Items of a group of heads: first the leftover (last, longest) query tile of heads with an
 // odd tile count, two heads per item; then pairs (2i+1, 2i) of the same head, i descending.
 // Without pairing an item is one tile, again longest first.
-__device__ __forceinline__ Item decode_item(const Params &p, int t) {
+__device__ __forceinline__ Item decode_pair_item(const Params &p, int t) {
     const int Q = p.n_qtiles, G = p.head_group;
     const int full = items_per_group(G, Q, p.pair);
     const int g = t / full;
@@ -249,6 +250,29 @@ __device__ __forceinline__ Item decode_item(const Params &p, int t) {
         it.qt[1] = 2 * i;
         it.valid[0] = it.valid[1] = true;
         it.shared = true;
+    }
+    return it;
+}
+
+// Item t of the launch. Items from tail_from on split the last, partial wave of two-tile
+// items into one-tile items (the pair item tail_from + u / 2 gives its tile u % 2, run in
+// slot 0), so that wave costs about half a two-tile item on twice as many CTAs.
+__device__ __forceinline__ Item decode_item(const Params &p, int t) {
+    int single = -1;
+    if (t >= p.tail_from) {
+        const int u = t - p.tail_from;
+        t = p.tail_from + (u >> 1);
+        single = u & 1;
+    }
+    Item it = decode_pair_item(p, t);
+    if (single >= 0) {
+        if (single == 1) {
+            it.bh[0] = it.bh[1];
+            it.qt[0] = it.qt[1];
+            it.valid[0] = it.valid[1];
+        }
+        it.valid[1] = false;
+        it.shared = false;
     }
     return it;
 }

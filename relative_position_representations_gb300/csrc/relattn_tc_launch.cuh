@@ -267,6 +267,17 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         // the order goes through a list of kListCap entries per CTA
         const int64_t per_cta = grid > 0 ? ((int64_t)p.num_items + grid - 1) / grid + p.n_groups : 0;
         p.snake = (a.causal && a.kv_len == nullptr && p.n_qtiles > 2 && per_cta + 1 < kListCap) ? 1 : 0;
+        // a last wave of two-tile items that fills at most half of the grid runs as one-tile
+        // items on twice as many CTAs (bidirectional only: a causal pair's tiles differ in
+        // length and measured slower split)
+        p.tail_from = p.num_items;
+        if (p.pair && !a.causal && p.num_items >= di.sms) {
+            const int r = p.num_items % di.sms;
+            if (r > 0 && 2 * r <= di.sms) {
+                p.tail_from = p.num_items - r;
+                p.num_items = p.tail_from + 2 * r;
+            }
+        }
     }
 
     // ---- TMA descriptors (the output is written with plain stores)
