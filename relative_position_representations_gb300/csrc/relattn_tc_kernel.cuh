@@ -61,6 +61,7 @@ constexpr int kLaunchRegs = 168;
 constexpr int kCtrlRegs = 72;
 constexpr int kSoftRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kSoftRegs == kThreads * kLaunchRegs, "register split");
+static_assert(BM == 128 && BN == 128, "the MMA chains (ptx::tc_mma_*_k*) assume 128-row operand tiles");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 // bound of every device wait, in SM clock cycles (about one second at 2 GHz); clock64 is
@@ -664,9 +665,9 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                     if (!(ok = claim_s())) break;
                     const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
                     const uint64_t dk = dk0 + off;
-#pragma unroll 1
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        ptx::tc_mma_w(tS, dq + kstep(kk, BM), dk + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+                    // one chain of D / 16 k-steps (one elect, immediate operand offsets)
+                    if (D == 64) ptx::tc_mma_ss_k64(tS, dq, dk, idS, 0u);
+                    else ptx::tc_mma_ss_k128(tS, dq, dk, idS, 0u);
                     ptx::tc_commit_w(sbar(SB_S_FULL));
                 } else {  // O += P_j V_j
                     if (!(ok = wait(sbar(SB_P_FULL), p_it & 1u))) break;
@@ -674,10 +675,14 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                     ptx::tc_fence_after();
                     const uint64_t dv = dv0 + off;
                     const int nk16 = cols / 16;
+                    if (nk16 == BN / 16) {  // a whole tile: one chain of 8 k-steps
+                        ptx::tc_mma_ts_k128(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
+                    } else {
 #pragma unroll 1
-                    for (int kk = 0; kk < nk16; ++kk)
-                        ptx::tc_mma_ts_w(tO, tP + (uint32_t)(kk * 8), dv + (uint64_t)(kk * 16 * 128 >> 4), idPV,
-                                         (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < nk16; ++kk)
+                            ptx::tc_mma_ts_w(tO, tP + (uint32_t)(kk * 8), dv + (uint64_t)(kk * 16 * 128 >> 4),
+                                             idPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
                     ptx::tc_commit_w(sbar(SB_PV_DONE));
                     ++pv_it;
                     pv_pending = true;

@@ -174,6 +174,59 @@ __device__ __forceinline__ void tc_commit_w(uint32_t bar) {
         : "memory");
 }
 
+// Chains of MMAs issued from one asm block by one elected lane (one elect for the chain;
+// the operand addresses of later steps are immediate offsets from the first).
+// ss_kn: D += A·B over N/16 k-steps, A and B K-major with 128-byte swizzle and 128 rows, so a
+// k-step moves both descriptors by 32 bytes inside a 64-column block and by 128 rows x 128
+// bytes between blocks (descriptor address units of 16 bytes: 2 and 1024).
+#define RELATTN_MMA_SS_STEP(OFF) \
+    "add.s64 a1, %1, " #OFF ";\n\tadd.s64 b1, %2, " #OFF ";\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+__device__ __forceinline__ void tc_mma_ss_k64(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, b1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        RELATTN_MMA_SS_STEP(2) RELATTN_MMA_SS_STEP(4) RELATTN_MMA_SS_STEP(6) "}\n"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(1u)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_ss_k128(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 a1, b1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        RELATTN_MMA_SS_STEP(2) RELATTN_MMA_SS_STEP(4) RELATTN_MMA_SS_STEP(6)
+        RELATTN_MMA_SS_STEP(1024) RELATTN_MMA_SS_STEP(1026) RELATTN_MMA_SS_STEP(1028)
+        RELATTN_MMA_SS_STEP(1030) "}\n"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(1u)
+        : "memory");
+}
+#undef RELATTN_MMA_SS_STEP
+// ts_k128: D += A·B over 128 keys (8 k-steps), A (P, bf16 pairs) in TMEM 8 columns per step,
+// B (V) MN-major with 128-byte swizzle: 16 rows x 128 bytes per step (128 descriptor units)
+#define RELATTN_MMA_TS_STEP(AOFF, BOFF) \
+    "add.u32 a1, %1, " #AOFF ";\n\tadd.s64 b1, %2, " #BOFF ";\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+__device__ __forceinline__ void tc_mma_ts_k128(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        RELATTN_MMA_TS_STEP(8, 128) RELATTN_MMA_TS_STEP(16, 256) RELATTN_MMA_TS_STEP(24, 384)
+        RELATTN_MMA_TS_STEP(32, 512) RELATTN_MMA_TS_STEP(40, 640) RELATTN_MMA_TS_STEP(48, 768)
+        RELATTN_MMA_TS_STEP(56, 896) "}\n"
+        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(1u)
+        : "memory");
+}
+#undef RELATTN_MMA_TS_STEP
+
 // plain arrive by one elected lane (the whole warp calls it)
 __device__ __forceinline__ void mbar_arrive_w(uint32_t bar) {
     asm volatile(
