@@ -665,9 +665,15 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                     if (!(ok = claim_s())) break;
                     const uint32_t idS = ptx::idesc_bf16(BM, (uint32_t)cols, 0);
                     const uint64_t dk = dk0 + off;
-                    // one chain of D / 16 k-steps (one elect, immediate operand offsets)
-                    if (D == 64) ptx::tc_mma_ss_k64(tS, dq, dk, idS, 0u);
-                    else ptx::tc_mma_ss_k128(tS, dq, dk, idS, 0u);
+                    // d = 128: one chain of 8 k-steps (one elect, immediate operand offsets);
+                    // at d = 64 the rolled loop keeps the code small (its items are short)
+                    if (D == 128) {
+                        ptx::tc_mma_ss_k128(tS, dq, dk, idS, 0u);
+                    } else {
+#pragma unroll 1
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            ptx::tc_mma_w(tS, dq + kstep(kk, BM), dk + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+                    }
                     ptx::tc_commit_w(sbar(SB_S_FULL));
                 } else {  // O += P_j V_j
                     if (!(ok = wait(sbar(SB_P_FULL), p_it & 1u))) break;
@@ -675,7 +681,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
                     ptx::tc_fence_after();
                     const uint64_t dv = dv0 + off;
                     const int nk16 = cols / 16;
-                    if (nk16 == BN / 16) {  // a whole tile: one chain of 8 k-steps
+                    if (D == 128 && nk16 == BN / 16) {  // a whole tile: one chain of 8 k-steps
                         ptx::tc_mma_ts_k128(tO, tP, dv, idPV, j > 0 ? 1u : 0u);
                     } else {
 #pragma unroll 1
