@@ -965,8 +965,9 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                 alpha = ptx::ex2(m_ref - rmax);  // 0 while nothing was seen yet
                 m_ref = rmax;
             }
-            // P and O of the slot are free once the previous P . V is done
-            if (j >= 1 && !(ok = wait_pv(pv_it + (uint32_t)j - 1u))) break;
+            // P and O of the slot are free once the previous P . V is done (with P over S that
+            // is already so: S_j was issued only after that P . V had completed)
+            if (!T::P_ALIAS && j >= 1 && !(ok = wait_pv(pv_it + (uint32_t)j - 1u))) break;
             // on the first key tile l, the bins and O hold nothing yet: no rescale needed
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 l *= alpha;
