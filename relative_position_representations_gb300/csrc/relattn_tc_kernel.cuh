@@ -1103,14 +1103,17 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         ptx::tc_fence_after();
         __syncwarp();
         const float inv = l > 0.f ? 1.f / l : 0.f;
+        // the O row in halves of 64 columns (one TMEM wait per half)
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            ptx::tmem_ld32(lane_base + T::O(slot) + (uint32_t)c0, r);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t r[64];
+            ptx::tmem_ld32(lane_base + T::O(slot) + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[32]>(r));
+            ptx::tmem_ld32(lane_base + T::O(slot) + (uint32_t)c0 + 32u,
+                           *reinterpret_cast<uint32_t(*)[32]>(r + 32));
             ptx::tmem_ld_wait();
             if (gi < p.n) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     uint32_t w[4];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
@@ -1119,8 +1122,7 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
                                                     dup(inv));
                         w[h] = pack2(o.x, o.y);
                     }
-                    const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
-                    reinterpret_cast<uint4 *>(orow)[c0 / 8 + q] = v;
+                    reinterpret_cast<uint4 *>(orow)[c0 / 8 + q] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             __syncwarp();
