@@ -53,7 +53,13 @@ def pairs_per_sequence(w, kv_len_b: int) -> int:
 
 
 def algorithmic_flops(w, kv_len) -> float:
-    """4*d per unmasked pair (Q.K^T and P.V) + 2*d*n per reachable table row and term."""
+    """4*d per unmasked pair (Q.K^T and P.V) + 2*d*n per reachable table row and term.
+    Decode step: one query row per (b, h) over its cache_len keys."""
+    if w.kind == "decode":
+        terms = int(w.key_term) + int(w.value_term)
+        rows = sum(min(int(x), w.n) for x in kv_len) * w.H
+        live = sum(1 for x in kv_len if int(x) > 0) * w.H
+        return 4.0 * w.d * rows + 2.0 * w.d * (w.clip_k + 1) * terms * live
     kvs = [None] * w.B if kv_len is None else [int(x) for x in kv_len]
     pairs = sum(pairs_per_sequence(w, kvs[b]) for b in range(w.B)) * w.H
     flops = 4.0 * w.d * pairs
@@ -65,8 +71,14 @@ def algorithmic_flops(w, kv_len) -> float:
 
 
 def algorithmic_bytes(w, kv_len) -> float:
-    """Q and O in full, K and V rows below kv_len, the tables once (bf16 / fp32 elements)."""
+    """Q and O in full, K and V rows below kv_len, the tables once (bf16 / fp32 elements).
+    Decode step: q and out rows, the cached K and V rows below cache_len, table rows 0..k."""
     es = 2 if w.dtype == "bf16" else 4
+    if w.kind == "decode":
+        rows = sum(min(int(x), w.n) for x in kv_len) * w.H
+        Ht = 1 if w.shared_tables else w.H
+        tabs = Ht * (w.clip_k + 1) * w.d * (int(w.key_term) + int(w.value_term))
+        return float(es * (2 * w.B * w.H * w.d + 2 * rows * w.d + tabs) + 4 * w.B)
     BHnd = w.B * w.H * w.n * w.d
     kvs = [w.n] * w.B if kv_len is None else [min(int(x), w.n) for x in kv_len]
     kv_rows = sum(kvs) * w.H
@@ -180,11 +192,54 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------- CPU oracle
+def workload_by_name(name):
+    from relative_position_representations_gb300 import workloads as wl
+    if name in wl.DECODE_WORKLOADS:
+        return wl.DECODE_WORKLOADS[name]
+    return wl.WORKLOADS[name]
+
+
+def draw(w, seed):
+    from relative_position_representations_gb300 import workloads as wl
+    return wl.draw_decode_inputs(w, seed) if w.kind == "decode" else wl.draw_inputs(w, seed)
+
+
+def key_lengths(w, x):
+    key = "cache_len" if w.kind == "decode" else "kv_len"
+    return None if x.get(key) is None else x[key].tolist()
+
+
+def oracle_decode_rows(w, x, batches, nthreads):
+    """The oracle for the decode step of the sequences in `batches` (all heads): row
+    t = cache_len - 1 of the causal forward, one sequence at a time."""
+    import numpy as np
+    import oracle
+    from relative_position_representations_gb300 import workloads as wl
+    out = []
+    for b in batches:
+        L = min(int(x["cache_len"][b]), w.n)
+        if L == 0:
+            continue
+        qf = np.zeros((1, w.H, L, w.d))
+        qf[0, :, L - 1] = x["q"][b].double().numpy()
+        sl = lambda t: None if t is None else t[b:b + 1, :, :L].double().numpy()
+        tab = lambda t: None if t is None else t.double().numpy()
+        rows = [h * L + L - 1 for h in range(w.H)]
+        out.append(oracle.relattn_fwd(qf, sl(x["k"]), sl(x["v"]), tab(x["aK"]), tab(x["aV"]),
+                                      w.clip_k, True, w.softmax_scale,
+                                      table_head_stride=wl.table_head_stride(w), rows=rows,
+                                      nthreads=nthreads))
+    return out
+
+
 def oracle_rows_call(w, x, rows, nthreads):
     import oracle
 
     def np_(t):
         return None if t is None else t.float().numpy()
+
+    if w.kind == "decode":  # rows are sequence indices
+        return oracle_decode_rows(w, x, rows, nthreads)
 
     kv = None if x.get("kv_len") is None else x["kv_len"].numpy()
     if w.kind == "t5":
@@ -199,7 +254,10 @@ def oracle_rows_call(w, x, rows, nthreads):
 
 
 def row_flops(w, kv_len, rows):
-    """Algorithmic FLOPs of a set of flat row ids (same accounting as algorithmic_flops)."""
+    """Algorithmic FLOPs of a set of flat row ids (same accounting as algorithmic_flops);
+    for the decode step the ids are sequences (all heads)."""
+    if w.kind == "decode":
+        return algorithmic_flops(w.replace(B=len(rows)), [kv_len[int(b)] for b in rows])
     total = 0.0
     reach = 0
     if w.kind == "shaw":
@@ -220,8 +278,8 @@ def time_oracle(w, x, budget_s: float, seed: int = 1):
     import oracle
     nthreads = oracle.default_threads()
     rng = np.random.default_rng(seed)
-    total_rows = w.B * w.H * w.n
-    kv = None if x.get("kv_len") is None else x["kv_len"].numpy()
+    total_rows = w.B if w.kind == "decode" else w.B * w.H * w.n
+    kv = key_lengths(w, x)
     # calibrate on a small batch of rows
     count = min(total_rows, max(nthreads * 4, 64))
     while True:
@@ -244,13 +302,19 @@ def time_oracle(w, x, budget_s: float, seed: int = 1):
         if dt >= budget_s or target < total_rows:
             break
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": "%d of %d query rows (random, seed %d) x %d pass(es), fp64 C loop, "
-                      "%.1f s" % (target, total_rows, seed, passes, dt)}, fl, dt
+            "sample": "%d of %d %s (random, seed %d) x %d pass(es), fp64 C loop, "
+                      "%.1f s" % (target, total_rows,
+                                  "sequences (all heads)" if w.kind == "decode" else "query rows",
+                                  seed, passes, dt)}, fl, dt
 
 
 # ----------------------------------------------------------------------- GPU arm
 def gpu_call(rp, w, g, out, stream):
     from relative_position_representations_gb300 import workloads as wl
+    if w.kind == "decode":
+        return rp.relattn_decode_fwd(g["q"], g["k"], g["v"], g["cache_len"], aK=g["aK"],
+                                     aV=g["aV"], clip_k=w.clip_k, scale=w.softmax_scale, out=out,
+                                     table_head_stride=wl.table_head_stride(w), stream=stream)
     if w.kind == "t5":
         return rp.relattn_t5bias_fwd(g["q"], g["k"], g["v"], g["bias"], w.num_buckets,
                                      w.max_distance, w.bidirectional, w.causal, w.softmax_scale,
@@ -273,12 +337,13 @@ def make_event(external: bool):
 def workload_config(w, world: int, l2_note: str) -> dict:
     """The JSON `config` of both arms: the workload by name and shape."""
     return {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
-            "kind": w.kind, "clip_k": w.clip_k if w.kind == "shaw" else None,
+            "kind": w.kind, "clip_k": w.clip_k if w.kind in ("shaw", "decode") else None,
             "causal": w.causal,
             "terms": ("t5 bias" if w.kind == "t5" else
                       "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
                                if on) or "none"),
-            "kv_len": "U{%d..%d} per sequence" % w.kv_len_range if w.kv_len_range else None,
+            ("cache_len" if w.kind == "decode" else "kv_len"):
+                "U{%d..%d} per sequence" % w.kv_len_range if w.kv_len_range else None,
             "parallelism": "dp%d (independent shards, no collective)" % world,
             "l2": l2_note}
 
@@ -308,9 +373,9 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = wl.WORKLOADS[args.workload]
-    x = wl.draw_inputs(w, seed=args.seed + rank)
-    kv_len = None if x.get("kv_len") is None else x["kv_len"].tolist()
+    w = workload_by_name(args.workload)
+    x = draw(w, seed=args.seed + rank)
+    kv_len = key_lengths(w, x)
     flops = algorithmic_flops(w, kv_len)
     byts = algorithmic_bytes(w, kv_len)
 
@@ -448,18 +513,25 @@ def run_ours(args, rank, world, local_rank):
 
 
 def measure_e2e(rp, w, x, dev, stream, flops, args):
-    """Same step through the C ABI with pinned host inputs: H2D copies, launch, D2H copy."""
+    """Same step through the C ABI with pinned host inputs: H2D copies, launch, D2H copy.
+    Decode step: the key/value caches and the tables are resident state (copied once, before
+    timing); each step copies the new queries and the cache lengths."""
     import torch
+    per_step = ("q", "cache_len") if w.kind == "decode" else tuple(x.keys())
     host = {k: (v.pin_memory() if v is not None else None) for k, v in x.items()}
     g = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in x.items()}
+    for k, v in host.items():
+        if v is not None and k not in per_step:
+            g[k].copy_(v)
     out = torch.empty_like(g["q"])
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    h2d = sum(v.numel() * v.element_size() for k, v in host.items()
+              if v is not None and k in per_step)
     d2h = out.numel() * out.element_size()
 
     def step():
         for k, v in host.items():
-            if v is not None:
+            if v is not None and k in per_step:
                 g[k].copy_(v, non_blocking=True)
         gpu_call(rp, w, g, out, stream)
         out_host.copy_(out, non_blocking=True)
@@ -489,8 +561,8 @@ def measure_e2e(rp, w, x, dev, stream, flops, args):
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores, on bounded samples of the workload."""
     from relative_position_representations_gb300 import workloads as wl
-    w = wl.WORKLOADS[args.workload]
-    x = wl.draw_inputs(w, seed=args.seed)
+    w = workload_by_name(args.workload)
+    x = draw(w, seed=args.seed)
     # the whole run stays within about ref_budget seconds whatever --steps is
     per_step = max(0.05, args.ref_budget / max(1, args.steps + args.warmup))
     for i in range(args.warmup):

@@ -105,6 +105,36 @@ RELATTN_API relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, co
                                     void *out, relattn_stream_t stream);
 
 /*
+ * relattn_decode_fwd — one incremental decoding step of a causal decoder: the new token of
+ * every sequence attends to its sequence's key/value cache with the relative terms of
+ * relattn_fwd (paper summary page, section 3.4, eq. 3 and eq. 4 with clip(j - i, k)).
+ * With t = cache_len[b] - 1, the new token's position (its own key and value are already
+ * the cache's row t):
+ *
+ *   e_j = scale * q . (k_j + aK[h][clip(j - t, clip_k) + clip_k]),   j = 0 .. t
+ *   z   = sum_j softmax_j(e)_j * (v_j + aV[h][clip(j - t, clip_k) + clip_k])
+ *
+ * i.e. row t of relattn_fwd with causal = 1 over the sequence's first t + 1 positions.
+ * Only table rows 0 .. clip_k (offsets -k .. 0) are read.
+ *
+ *   q                 [B, H, d] bf16: the new tokens' queries.
+ *   k_cache, v_cache  [B, H, T, d] bf16 caches of capacity T; rows >= cache_len[b] are
+ *                     not read.
+ *   aK, aV, table_head_stride, clip_k, scale   as in relattn_fwd (bf16 tables).
+ *   cache_len         [B] int32 device array, each in 0 .. T (larger values are taken as
+ *                     T); a sequence with cache_len 0 gets zeros.
+ *   out               [B, H, d] bf16; must not alias an input.
+ *
+ * bf16 only, d in {64, 128}; clip_k <= 256 (else RELATTN_ERR_UNSUPPORTED). Appending the
+ * new token's key and value to the cache is the caller's job.
+ */
+RELATTN_API relattn_status_t relattn_decode_fwd(const void *q, const void *k_cache,
+                                    const void *v_cache, const void *aK, const void *aV,
+                                    long long table_head_stride, int clip_k, float scale,
+                                    const int *cache_len, int B, int H, int T, int d,
+                                    void *out, relattn_stream_t stream);
+
+/*
  * relattn_labels — the integer edge label of every (i, j), computed by the same device
  * functions the attention kernels use, written as int32 labels[i * n_k + j].
  *   kind 0: clip row clip(j - i, clip_k) + clip_k (paper summary, section 3.4).

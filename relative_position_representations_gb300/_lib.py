@@ -32,6 +32,9 @@ _lib.relattn_fwd.restype = _I
 _lib.relattn_t5bias_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I,
                                     _I, _I, _I, _P, _P]
 _lib.relattn_t5bias_fwd.restype = _I
+_lib.relattn_decode_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _P,
+                                    _I, _I, _I, _I, _P, _P]
+_lib.relattn_decode_fwd.restype = _I
 _lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
 _lib.relattn_labels.restype = _I
 _lib.relattn_t5_thresholds.argtypes = [_I, _I, _I, ctypes.POINTER(_I), _I, ctypes.POINTER(_I)]
@@ -43,7 +46,8 @@ _lib.relattn_status_string.restype = ctypes.c_char_p
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
-EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_labels", "relattn_t5_thresholds",
+EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_decode_fwd", "relattn_labels",
+            "relattn_t5_thresholds",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
 
@@ -157,6 +161,50 @@ def relattn_t5bias_fwd(q, k, v, bias, num_buckets=32, max_distance=128, bidirect
                                  float(scale), _ptr(kv_len), B, H, n, d, dt, _ptr(out),
                                  _stream(stream))
     _check(st, "relattn_t5bias_fwd")
+    return out
+
+
+def relattn_decode_fwd(q, k_cache, v_cache, cache_len, aK=None, aV=None, clip_k=0, scale=None,
+                       out=None, table_head_stride=None, stream=None):
+    """One causal decoding step with relative terms: row cache_len[b] - 1 of the causal
+    forward over each sequence's cache (paper summary page, section 3.4, eqs. 3-4).
+
+    q: [B, H, d] bf16; k_cache, v_cache: [B, H, T, d] bf16; cache_len: [B] int32 (the new
+    token's key and value already in row cache_len[b] - 1). aK / aV: [H or 1, 2*clip_k+1, d]
+    bf16 or None. Returns out [B, H, d].
+    """
+    _dev(q, "q", torch.bfloat16)
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, d]")
+    B, H, d = q.shape
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, name, torch.bfloat16)
+        if t.dim() != 4 or t.shape[0] != B or t.shape[1] != H or t.shape[3] != d:
+            raise ValueError("%s must be [B, H, T, d]" % name)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must have one shape")
+    T = k_cache.shape[2]
+    W = 2 * int(clip_k) + 1
+    for name, t in (("aK", aK), ("aV", aV)):
+        if t is not None:
+            _dev(t, name, torch.bfloat16)
+            if t.dim() != 3 or t.shape[1] != W or t.shape[2] != d or t.shape[0] not in (1, H):
+                raise ValueError("%s must be [H or 1, 2*clip_k+1, d]" % name)
+    if table_head_stride is None:
+        ref = aK if aK is not None else aV
+        table_head_stride = 0 if (ref is None or ref.shape[0] == 1) else W * d
+    _dev(cache_len, "cache_len", torch.int32)
+    if cache_len.numel() != B:
+        raise ValueError("cache_len must have B entries")
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.bfloat16)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_decode_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(aK), _ptr(aV),
+                                 int(table_head_stride), int(clip_k), float(scale),
+                                 _ptr(cache_len), B, H, T, d, _ptr(out), _stream(stream))
+    _check(st, "relattn_decode_fwd")
     return out
 
 

@@ -136,6 +136,39 @@ relattn_status_t relattn_fwd(const void *q, const void *k, const void *v, const 
     return dispatch_bf16(a, nullptr, s);
 }
 
+relattn_status_t relattn_decode_fwd(const void *q, const void *k_cache, const void *v_cache,
+                                    const void *aK, const void *aV, long long table_head_stride,
+                                    int clip_k, float scale, const int *cache_len, int B, int H,
+                                    int T, int d, void *out, relattn_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !out || !cache_len) return RELATTN_ERR_INVALID_ARG;
+    if (!shapes_ok(B, H, T, d)) return RELATTN_ERR_INVALID_ARG;
+    if (out == q || out == k_cache || out == v_cache || out == aK || out == aV)
+        return RELATTN_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(cache_len, 4))
+        return RELATTN_ERR_INVALID_ARG;
+    if (clip_k < 0 || clip_k > (1 << 20)) return RELATTN_ERR_INVALID_ARG;
+    if (aK || aV) {
+        const long long rows_d = (2LL * clip_k + 1) * d;
+        if (table_head_stride != 0 && table_head_stride < rows_d) return RELATTN_ERR_INVALID_ARG;
+        if ((aK && !aligned(aK, 16)) || (aV && !aligned(aV, 16))) return RELATTN_ERR_INVALID_ARG;
+        if ((table_head_stride % 8) != 0) return RELATTN_ERR_INVALID_ARG;
+    }
+    if (d != 64 && d != 128) return RELATTN_ERR_UNSUPPORTED;
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    relattn::DecodeArgs a{};
+    a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.aK = aK; a.aV = aV;
+    a.ths = table_head_stride;
+    a.clip_k = clip_k;
+    a.scale = scale;
+    a.cache_len = cache_len;
+    a.B = B; a.H = H; a.T = T; a.d = d;
+    a.out = out;
+    return from_cuda(relattn::launch_decode_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
                                     const float *bias, int num_buckets, int max_distance,
                                     int bidirectional, int causal, float scale,

@@ -63,4 +63,17 @@ struct TcArgs {
 cudaError_t launch_tc_bf16_d64(const TcArgs &a, const T5Buckets *t5, int *err, cudaStream_t s);
 cudaError_t launch_tc_bf16_d128(const TcArgs &a, const T5Buckets *t5, int *err, cudaStream_t s);
 
+// ---- bf16 decode step ----------------------------------------------------------------------
+struct DecodeArgs {
+    const void *q, *k_cache, *v_cache, *aK, *aV;
+    long long ths;
+    int clip_k;
+    float scale;
+    const int *cache_len;
+    int B, H, T, d;
+    void *out;
+};
+// cudaErrorNotSupported when clip_k + 1 table rows exceed the kernel's bins
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+
 }  // namespace relattn

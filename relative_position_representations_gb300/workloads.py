@@ -30,7 +30,7 @@ class Workload:
     n: int
     d: int
     dtype: str                      # "bf16" or "f32"
-    kind: str = "shaw"              # "shaw" or "t5"
+    kind: str = "shaw"              # "shaw", "t5" or "decode" (one decoding step)
     clip_k: int = 0
     causal: bool = False
     key_term: bool = True           # a^K present (Shaw)
@@ -81,6 +81,15 @@ WORKLOADS = {
 
 ORDER = ["tiny_fp32", "base_encoder", "big_decoder", "long_keyonly", "t5_bias"]
 
+# One incremental decoding step (kind "decode"): n is the cache capacity T; each sequence's
+# cache holds kv_len_range-drawn entries, the last being the new token (Transformer-big
+# decoder shape, caches of 1K-2K tokens).
+DECODE_WORKLOADS = {
+    "decode_big": Workload("decode_big", B=32, H=16, n=2048, d=64, dtype="bf16", kind="decode",
+                           clip_k=16, causal=True, table_std=0.02, kv_len_range=(1024, 2048),
+                           scale=1.0 / 8),
+}
+
 
 def draw_inputs(w: Workload, seed: int = 0) -> dict:
     """Seeded CPU tensors for workload w (see the module docstring for the recipe)."""
@@ -108,6 +117,28 @@ def draw_inputs(w: Workload, seed: int = 0) -> dict:
         out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
     else:
         out["kv_len"] = None
+    return out
+
+
+def draw_decode_inputs(w: Workload, seed: int = 0) -> dict:
+    """Seeded CPU tensors for a decode step: q [B, H, d], k / v caches [B, H, T, d] with
+    T = w.n, tables, and cache_len [B] int32 (draw order q, k, v, a^K, a^V, cache_len)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    dt = w.torch_dtype
+
+    def normal(shp, std):
+        return (torch.randn(shp, generator=g, dtype=torch.float32) * std).to(dt)
+
+    out = {"q": normal((w.B, w.H, w.d), w.qkv_std),
+           "k": normal((w.B, w.H, w.n, w.d), w.qkv_std),
+           "v": normal((w.B, w.H, w.n, w.d), w.qkv_std)}
+    W = 2 * w.clip_k + 1
+    Ht = 1 if w.shared_tables else w.H
+    out["aK"] = normal((Ht, W, w.d), w.table_std) if w.key_term else None
+    out["aV"] = normal((Ht, W, w.d), w.table_std) if w.value_term else None
+    lo, hi = w.kv_len_range if w.kv_len_range is not None else (w.n, w.n)
+    out["cache_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
     return out
 
 
