@@ -312,9 +312,15 @@ def time_oracle(w, x, budget_s: float, seed: int = 1):
 def gpu_call(rp, w, g, out, stream):
     from relative_position_representations_gb300 import workloads as wl
     if w.kind == "decode":
+        if "ws" not in g:  # the caller's scratch for the split over the cache (made once)
+            import torch
+            nb = rp.relattn_decode_workspace_size(w.B, w.H, w.n, w.d)
+            g["ws"] = (None if NO_DECODE_WORKSPACE else
+                       torch.empty(max(nb, 16), dtype=torch.uint8, device=g["q"].device))
         return rp.relattn_decode_fwd(g["q"], g["k"], g["v"], g["cache_len"], aK=g["aK"],
                                      aV=g["aV"], clip_k=w.clip_k, scale=w.softmax_scale, out=out,
-                                     table_head_stride=wl.table_head_stride(w), stream=stream)
+                                     table_head_stride=wl.table_head_stride(w), workspace=g["ws"],
+                                     stream=stream)
     if w.kind == "t5":
         return rp.relattn_t5bias_fwd(g["q"], g["k"], g["v"], g["bias"], w.num_buckets,
                                      w.max_distance, w.bidirectional, w.causal, w.softmax_scale,
@@ -322,6 +328,17 @@ def gpu_call(rp, w, g, out, stream):
     return rp.relattn_fwd(g["q"], g["k"], g["v"], g["aK"], g["aV"], w.clip_k, w.causal,
                           w.softmax_scale, kv_len=g["kv_len"], out=out,
                           table_head_stride=wl.table_head_stride(w), stream=stream)
+
+
+NO_DECODE_WORKSPACE = False  # --no-decode-workspace: the decode step gets no scratch
+
+
+def launches_per_step(rp, w) -> int:
+    """Kernels one step launches: the fused kernel, or the decode pieces and their combine."""
+    if (w.kind == "decode" and not NO_DECODE_WORKSPACE and
+            rp.relattn_decode_workspace_size(w.B, w.H, w.n, w.d) > 0):
+        return 2
+    return 1
 
 
 def make_event(external: bool):
@@ -506,7 +523,8 @@ def run_ours(args, rank, world, local_rank):
             w, world, "inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > "
                       "4 x %.0f MB L2), replayed from a CUDA graph" % (
                           n_sets, in_bytes / 1e6, n_sets * in_bytes / 1e6, l2 / 1e6)),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": steps * launches_per_step(rp, w),
         "clocks": clocks,
     }
     return line
@@ -595,6 +613,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-decode-workspace", action="store_true",
+                    help="decode workloads: call without a workspace (one CTA per cache)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the CPU baseline")
@@ -606,6 +626,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    global NO_DECODE_WORKSPACE
+    NO_DECODE_WORKSPACE = args.no_decode_workspace
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

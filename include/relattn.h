@@ -125,6 +125,14 @@ RELATTN_API relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, co
  *                     T); a sequence with cache_len 0 gets zeros.
  *   out               [B, H, d] bf16; must not alias an input.
  *
+ *   workspace         caller-owned device scratch of workspace_bytes (16-byte aligned),
+ *                     or NULL. When relattn_decode_workspace_size is not 0 (a small batch:
+ *                     at most 256 sequence-heads, caches longer than 512) and the workspace
+ *                     is that large, each cache is split over several CTAs and combined by
+ *                     a second kernel on the same stream; otherwise one CTA reads a whole
+ *                     cache. The contents are scratch on entry and on return, and two
+ *                     calls running at the same time must not share it.
+ *
  * bf16 only, d in {64, 128}; clip_k <= 256 (else RELATTN_ERR_UNSUPPORTED). Appending the
  * new token's key and value to the cache is the caller's job.
  */
@@ -132,7 +140,15 @@ RELATTN_API relattn_status_t relattn_decode_fwd(const void *q, const void *k_cac
                                     const void *v_cache, const void *aK, const void *aV,
                                     long long table_head_stride, int clip_k, float scale,
                                     const int *cache_len, int B, int H, int T, int d,
+                                    void *workspace, unsigned long long workspace_bytes,
                                     void *out, relattn_stream_t stream);
+
+/*
+ * relattn_decode_workspace_size — host only: the workspace bytes relattn_decode_fwd uses
+ * to split caches of capacity T over several CTAs (0 when it runs one CTA per cache).
+ */
+RELATTN_API relattn_status_t relattn_decode_workspace_size(int B, int H, int T, int d,
+                                               unsigned long long *bytes);
 
 /*
  * relattn_labels — the integer edge label of every (i, j), computed by the same device

@@ -33,8 +33,10 @@ _lib.relattn_t5bias_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_flo
                                     _I, _I, _I, _P, _P]
 _lib.relattn_t5bias_fwd.restype = _I
 _lib.relattn_decode_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _P,
-                                    _I, _I, _I, _I, _P, _P]
+                                    _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P, _P]
 _lib.relattn_decode_fwd.restype = _I
+_lib.relattn_decode_workspace_size.argtypes = [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
+_lib.relattn_decode_workspace_size.restype = _I
 _lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
 _lib.relattn_labels.restype = _I
 _lib.relattn_t5_thresholds.argtypes = [_I, _I, _I, ctypes.POINTER(_I), _I, ctypes.POINTER(_I)]
@@ -46,7 +48,8 @@ _lib.relattn_status_string.restype = ctypes.c_char_p
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
-EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_decode_fwd", "relattn_labels",
+EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_decode_fwd",
+            "relattn_decode_workspace_size", "relattn_labels",
             "relattn_t5_thresholds",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
@@ -164,14 +167,23 @@ def relattn_t5bias_fwd(q, k, v, bias, num_buckets=32, max_distance=128, bidirect
     return out
 
 
+def relattn_decode_workspace_size(B, H, T, d) -> int:
+    """Workspace bytes relattn_decode_fwd uses to split caches of capacity T (host only)."""
+    n = ctypes.c_ulonglong(0)
+    _check(_lib.relattn_decode_workspace_size(int(B), int(H), int(T), int(d), ctypes.byref(n)),
+           "relattn_decode_workspace_size")
+    return int(n.value)
+
+
 def relattn_decode_fwd(q, k_cache, v_cache, cache_len, aK=None, aV=None, clip_k=0, scale=None,
-                       out=None, table_head_stride=None, stream=None):
+                       out=None, table_head_stride=None, workspace=None, stream=None):
     """One causal decoding step with relative terms: row cache_len[b] - 1 of the causal
     forward over each sequence's cache (paper summary page, section 3.4, eqs. 3-4).
 
     q: [B, H, d] bf16; k_cache, v_cache: [B, H, T, d] bf16; cache_len: [B] int32 (the new
     token's key and value already in row cache_len[b] - 1). aK / aV: [H or 1, 2*clip_k+1, d]
-    bf16 or None. Returns out [B, H, d].
+    bf16 or None. workspace: a CUDA tensor of at least relattn_decode_workspace_size bytes
+    (None: one CTA per cache). Returns out [B, H, d].
     """
     _dev(q, "q", torch.bfloat16)
     if q.dim() != 3:
@@ -201,9 +213,14 @@ def relattn_decode_fwd(q, k_cache, v_cache, cache_len, aK=None, aV=None, clip_k=
     _dev(out, "out", torch.bfloat16)
     if scale is None:
         scale = d ** -0.5
+    ws_bytes = 0
+    if workspace is not None:
+        _dev(workspace, "workspace")
+        ws_bytes = workspace.numel() * workspace.element_size()
     st = _lib.relattn_decode_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(aK), _ptr(aV),
                                  int(table_head_stride), int(clip_k), float(scale),
-                                 _ptr(cache_len), B, H, T, d, _ptr(out), _stream(stream))
+                                 _ptr(cache_len), B, H, T, d, _ptr(workspace), ws_bytes, _ptr(out),
+                                 _stream(stream))
     _check(st, "relattn_decode_fwd")
     return out
 

@@ -14,6 +14,13 @@
 // the block takes the chunk's maximum, then the warps accumulate P V with 16-byte loads
 // that each cover whole rows of V (d/8 lanes per row, 4 or 2 rows per warp load), with an
 // online rescale between chunks. HBM-bound: K and V of the cache are read once.
+//
+// With few heads (at most kSplitMaxHeads) and a workspace the cache of a head is split into
+// pieces of kSplit keys, one CTA each (grid x = heads, y = pieces), so that a small batch
+// still fills the GPU; each piece writes its maximum, row sum and unnormalised P V into the
+// workspace, and
+// a second kernel combines the pieces of a head (rescaled to the common maximum) and adds
+// the value bins, whose k single-key logits it recomputes from q and the cached keys.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -28,6 +35,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 2048;     // keys whose logits are held in shared memory at a time
 constexpr int kMaxBins = 257;    // table rows 0 .. clip_k (clip_k <= 256)
+constexpr int kSplit = 512;      // keys per CTA with a workspace
+constexpr int kSplitMaxHeads = 256;  // more heads than this fill the GPU without a split
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
@@ -38,6 +47,8 @@ struct Params {
     const int *cache_len;
     int B, H, T;
     __nv_bfloat16 *out;
+    float *ws;   // workspace: per (head, piece) {max, row sum, P V[D]}, or null
+    int npiece;  // pieces per head with a workspace
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -75,7 +86,7 @@ __device__ __forceinline__ float block_max(float v, float *red) {
     return r;
 }
 
-template <int D, bool AK, bool AV>
+template <int D, bool AK, bool AV, bool SPLIT>
 __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p) {
     // P V: a row of V is LPR lanes x 16 bytes; a warp load covers KPW keys
     constexpr int LPR = D / 8, KPW = 32 / LPR;
@@ -97,6 +108,18 @@ __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p
     }
     const int t = len - 1, k = p.clip_k;
     const int band0 = t - k;  // keys j >= band0 + 1 have their own bin, j <= band0 share bin 0
+    // keys of this CTA: the whole cache, or piece blockIdx.y of kSplit keys
+    const int j_lo = SPLIT ? (int)blockIdx.y * kSplit : 0;
+    const int j_hi = SPLIT ? min(t + 1, j_lo + kSplit) : t + 1;
+    float *part = SPLIT ? p.ws + ((long long)bh * p.npiece + blockIdx.y) * (D + 2) : nullptr;
+    if (SPLIT && j_lo >= j_hi) {  // past the end of this cache: an empty piece
+        if (tid == 0) {
+            part[0] = -INFINITY;
+            part[1] = 0.f;
+        }
+        for (int c = tid; c < D; c += kThreads) part[2 + c] = 0.f;
+        return;
+    }
     const __nv_bfloat16 *qrow = p.q + (long long)bh * D;
     for (int c = tid; c < D; c += kThreads) qs[c] = __bfloat162float(qrow[c]) * p.scale_log2;
     __syncthreads();
@@ -114,8 +137,8 @@ __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.f;
 
-    for (int j0 = 0; j0 <= t; j0 += kChunk) {
-        const int cnt = min(kChunk, t + 1 - j0);
+    for (int j0 = j_lo; j0 < j_hi; j0 += kChunk) {
+        const int cnt = min(kChunk, j_hi - j0);
         // ---- logits of the chunk, one cached key row per thread
         float tmax = -INFINITY;
         for (int u = tid; u < cnt; u += kThreads) {
@@ -123,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p
             float e = dot_row<D>(kbase + (long long)j * D, qs);
             if (AK) e += rel[max(0, j - band0)];
             e_s[u] = e;
-            if (j >= band0) band[j - band0] = e;  // bin of key j (band0 may be negative)
+            if (!SPLIT && j >= band0) band[j - band0] = e;  // bin of key j (band0 may be < 0)
             tmax = fmaxf(tmax, e);
         }
         const float cmax = block_max(tmax, red);  // also orders the e_s writes before reads
@@ -136,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p
         for (int c = 0; c < 8; ++c) acc[c] *= alpha;
         // ---- P V: warp w takes keys w*KPW + ks, then every kWarps*KPW-th; lane cg owns
         // columns 8cg .. 8cg+7 of its key's row (16-byte loads, KPW whole rows per load)
-#pragma unroll 2
+#pragma unroll 8
         for (int u = warp * KPW + ks; u < cnt; u += kWarps * KPW) {
             const float pj = exp2f(e_s[u] - m);
             const uint4 w = __ldg(reinterpret_cast<const uint4 *>(vbase + (long long)(j0 + u) * D) + cg);
@@ -168,6 +191,19 @@ __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p
     float l = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) l += lw_s[w];
+    if (SPLIT) {  // this piece's maximum, row sum and unnormalised P V
+        if (tid == 0) {
+            part[0] = m;
+            part[1] = l;
+        }
+        for (int c = tid; c < D; c += kThreads) {
+            float o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) o += acc_s[w][c];
+            part[2 + c] = o;
+        }
+        return;
+    }
     const float inv = 1.f / l;
     for (int c = tid; c < D; c += kThreads) {
         float o = 0.f;
@@ -192,6 +228,79 @@ __global__ void __launch_bounds__(kThreads) relattn_decode_kernel(const Params p
     }
 }
 
+// The pieces of one head: common maximum M, row sum and P V rescaled to it, then the value
+// bins (keys t-k+1 .. t one each, bin 0 what the row sum leaves) and the normalisation.
+template <int D, bool AK, bool AV>
+__global__ void __launch_bounds__(128) relattn_decode_combine(const Params p) {
+    __shared__ float qs[D];
+    __shared__ float band[kMaxBins];
+    __shared__ float scl[64];
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H, tid = threadIdx.x;
+    const int len = min(max(p.cache_len[b], 0), p.T);
+    __nv_bfloat16 *orow = p.out + (long long)bh * D;
+    if (len == 0) {
+        for (int c = tid; c < D; c += 128) orow[c] = __float2bfloat16(0.f);
+        return;
+    }
+    const int t = len - 1, k = p.clip_k, band0 = t - k;
+    const int np = min(p.npiece, (t + kSplit) / kSplit);  // pieces holding keys
+    const float *part = p.ws + (long long)bh * p.npiece * (D + 2);
+    float M = -INFINITY;
+    for (int i = 0; i < np; ++i) M = fmaxf(M, part[(long long)i * (D + 2)]);
+    if (tid < np && tid < 64) scl[tid] = exp2f(part[(long long)tid * (D + 2)] - M);
+    const __nv_bfloat16 *qrow = p.q + (long long)bh * D;
+    for (int c = tid; c < D; c += 128) qs[c] = __bfloat162float(qrow[c]) * p.scale_log2;
+    __syncthreads();
+    float L = 0.f;
+    for (int i = 0; i < np; ++i)
+        L = fmaf(part[(long long)i * (D + 2) + 1], i < 64 ? scl[i] : exp2f(part[(long long)i * (D + 2)] - M), L);
+    const long long tab = (long long)h * p.ths;
+    if (AV) {  // logits of the single-key bins 1 .. k (keys band0 + 1 .. t)
+        const __nv_bfloat16 *kbase = p.k + (long long)bh * p.T * D;
+        for (int r = 1 + tid; r <= k; r += 128) {
+            const int j = band0 + r;
+            if (j < 0) continue;
+            float e = dot_row<D>(kbase + (long long)j * D, qs);
+            if (AK) e += dot_row<D>(p.aK + tab + (long long)r * D, qs);
+            band[r] = e;
+        }
+    }
+    __syncthreads();
+    const float inv = 1.f / L;
+    for (int c = tid; c < D; c += 128) {
+        float o = 0.f;
+        for (int i = 0; i < np; ++i)
+            o = fmaf(part[(long long)i * (D + 2) + 2 + c], i < 64 ? scl[i] : exp2f(part[(long long)i * (D + 2)] - M), o);
+        if (AV) {
+            const __nv_bfloat16 *wv = p.aV + tab;
+            float s_band = 0.f, ov = 0.f;
+            for (int r = 1; r <= k; ++r) {
+                if (band0 + r < 0) continue;
+                const float pr = exp2f(band[r] - M);
+                s_band += pr;
+                ov = fmaf(pr, __bfloat162float(wv[(long long)r * D + c]), ov);
+            }
+            ov = fmaf(fmaxf(0.f, L - s_band), __bfloat162float(wv[c]), ov);
+            o += ov;
+        }
+        orow[c] = __float2bfloat16(o * inv);
+    }
+}
+
+template <int D, bool AK, bool AV>
+cudaError_t launch_variant(const Params &p, bool split, cudaStream_t s) {
+    if (!split) {
+        relattn_decode_kernel<D, AK, AV, false><<<dim3((unsigned)(p.B * p.H)), kThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    relattn_decode_kernel<D, AK, AV, true>
+        <<<dim3((unsigned)(p.B * p.H), (unsigned)p.npiece), kThreads, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    relattn_decode_combine<D, AK, AV><<<dim3((unsigned)(p.B * p.H)), 128, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const DecodeArgs &a, cudaStream_t s) {
     Params p;
@@ -208,15 +317,25 @@ cudaError_t launch_d(const DecodeArgs &a, cudaStream_t s) {
     p.H = a.H;
     p.T = a.T;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
-    const dim3 grid((unsigned)(a.B * a.H));
-    if (a.aK && a.aV) relattn_decode_kernel<D, true, true><<<grid, kThreads, 0, s>>>(p);
-    else if (a.aK) relattn_decode_kernel<D, true, false><<<grid, kThreads, 0, s>>>(p);
-    else if (a.aV) relattn_decode_kernel<D, false, true><<<grid, kThreads, 0, s>>>(p);
-    else relattn_decode_kernel<D, false, false><<<grid, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    p.npiece = (a.T + kSplit - 1) / kSplit;
+    const unsigned long long need = decode_workspace_bytes(a.B, a.H, a.T, a.d);
+    const bool split = need > 0 && a.workspace && a.workspace_bytes >= need;
+    p.ws = split ? static_cast<float *>(a.workspace) : nullptr;
+    if (a.aK && a.aV) return launch_variant<D, true, true>(p, split, s);
+    if (a.aK) return launch_variant<D, true, false>(p, split, s);
+    if (a.aV) return launch_variant<D, false, true>(p, split, s);
+    return launch_variant<D, false, false>(p, split, s);
 }
 
 }  // namespace decode
+
+unsigned long long decode_workspace_bytes(int B, int H, int T, int d) {
+    const long long pieces = (T + decode::kSplit - 1) / decode::kSplit;
+    // one piece, or enough heads to fill the GPU: the single-pass kernel needs nothing (with
+    // 512 heads of 1K-2K keys it measured faster than the split)
+    if (pieces <= 1 || (long long)B * H > decode::kSplitMaxHeads) return 0;
+    return (unsigned long long)B * H * pieces * (d + 2) * sizeof(float);
+}
 
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     if (a.clip_k + 1 > decode::kMaxBins) return cudaErrorNotSupported;

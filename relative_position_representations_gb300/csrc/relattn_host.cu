@@ -136,16 +136,25 @@ relattn_status_t relattn_fwd(const void *q, const void *k, const void *v, const 
     return dispatch_bf16(a, nullptr, s);
 }
 
+relattn_status_t relattn_decode_workspace_size(int B, int H, int T, int d,
+                                               unsigned long long *bytes) {
+    if (!bytes || !shapes_ok(B, H, T, d)) return RELATTN_ERR_INVALID_ARG;
+    *bytes = relattn::decode_workspace_bytes(B, H, T, d);
+    return RELATTN_OK;
+}
+
 relattn_status_t relattn_decode_fwd(const void *q, const void *k_cache, const void *v_cache,
                                     const void *aK, const void *aV, long long table_head_stride,
                                     int clip_k, float scale, const int *cache_len, int B, int H,
-                                    int T, int d, void *out, relattn_stream_t stream) {
+                                    int T, int d, void *workspace,
+                                    unsigned long long workspace_bytes, void *out,
+                                    relattn_stream_t stream) {
     if (!q || !k_cache || !v_cache || !out || !cache_len) return RELATTN_ERR_INVALID_ARG;
     if (!shapes_ok(B, H, T, d)) return RELATTN_ERR_INVALID_ARG;
     if (out == q || out == k_cache || out == v_cache || out == aK || out == aV)
         return RELATTN_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(cache_len, 4))
+        !aligned(cache_len, 4) || (workspace && !aligned(workspace, 16)))
         return RELATTN_ERR_INVALID_ARG;
     if (clip_k < 0 || clip_k > (1 << 20)) return RELATTN_ERR_INVALID_ARG;
     if (aK || aV) {
@@ -166,6 +175,8 @@ relattn_status_t relattn_decode_fwd(const void *q, const void *k_cache, const vo
     a.cache_len = cache_len;
     a.B = B; a.H = H; a.T = T; a.d = d;
     a.out = out;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace ? workspace_bytes : 0;
     return from_cuda(relattn::launch_decode_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

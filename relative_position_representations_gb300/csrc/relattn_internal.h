@@ -72,8 +72,13 @@ struct DecodeArgs {
     const int *cache_len;
     int B, H, T, d;
     void *out;
+    void *workspace;  // device scratch for the split over the cache, or null
+    unsigned long long workspace_bytes;
 };
-// cudaErrorNotSupported when clip_k + 1 table rows exceed the kernel's bins
+// bytes of workspace the split over the cache uses (0: the cache fits one CTA's piece)
+unsigned long long decode_workspace_bytes(int B, int H, int T, int d);
+// cudaErrorNotSupported when clip_k + 1 table rows exceed the kernel's bins; without a large
+// enough workspace the single-pass kernel runs
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 
 }  // namespace relattn

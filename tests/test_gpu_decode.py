@@ -51,11 +51,18 @@ def oracle_decode(w, x):
     return ref
 
 
-def run_decode(w, x):
+def run_decode(w, x, split=False):
+    """split: pass a workspace, so caches longer than one piece go over several CTAs."""
+    rp = _rp()
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
-    out = _rp().relattn_decode_fwd(g["q"], g["k"], g["v"], g["cache_len"], aK=g["aK"], aV=g["aV"],
-                                   clip_k=w.clip_k, scale=w.softmax_scale,
-                                   table_head_stride=wl.table_head_stride(w))
+    ws = None
+    if split:
+        nb = rp.relattn_decode_workspace_size(w.B, w.H, w.n, w.d)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=DEV)
+        ws.fill_(0xFF)  # scratch contents must not matter (0xFFFF... floats are NaN)
+    out = rp.relattn_decode_fwd(g["q"], g["k"], g["v"], g["cache_len"], aK=g["aK"], aV=g["aV"],
+                                clip_k=w.clip_k, scale=w.softmax_scale,
+                                table_head_stride=wl.table_head_stride(w), workspace=ws)
     torch.cuda.synchronize()
     return out.float().cpu().numpy()
 
@@ -74,8 +81,9 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("split", [False, True], ids=["one_cta", "split"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_decode_matches_oracle(case):
+def test_decode_matches_oracle(case, split):
     name, B, H, T, d, k, lens, key, val, shared = case
     w = wl.Workload(name, B=B, H=H, n=T, d=d, dtype="bf16", kind="decode", clip_k=k,
                     causal=True, key_term=key, value_term=val, shared_tables=shared,
@@ -83,20 +91,32 @@ def test_decode_matches_oracle(case):
     x = wl.draw_decode_inputs(w, seed=T + k)
     if lens is not None:
         x["cache_len"] = torch.tensor(lens, dtype=torch.int32)
-    got = run_decode(w, x)
+    got = run_decode(w, x, split)
     ref = oracle_decode(w, x)
     tol = 1e-2 * float(np.abs(ref).max()) + 1e-3
     assert np.isfinite(got).all()
     assert float(np.abs(got - ref).max()) <= tol, (float(np.abs(got - ref).max()), tol)
 
 
-def test_decode_step_workload_sampled():
+@pytest.mark.parametrize("split", [False, True], ids=["one_cta", "split"])
+def test_decode_step_workload(split):
     w = wl.DECODE_WORKLOADS["decode_big"]
     x = wl.draw_decode_inputs(w, seed=0)
-    got = run_decode(w, x)
+    got = run_decode(w, x, split)
     ref = oracle_decode(w, x)
     tol = 1e-2 * float(np.abs(ref).max()) + 1e-3
     assert float(np.abs(got - ref).max()) <= tol
+
+
+def test_decode_split_repeats_bitwise():
+    """The split path gives the same bits on every call (no order-dependent sums)."""
+    w = wl.Workload("split_rep", B=2, H=4, n=3000, d=64, dtype="bf16", kind="decode",
+                    clip_k=16, causal=True, table_std=0.5, kv_len_range=(1500, 3000))
+    assert _rp().relattn_decode_workspace_size(w.B, w.H, w.n, w.d) > 0
+    x = wl.draw_decode_inputs(w, seed=3)
+    a = run_decode(w, x, True)
+    for _ in range(3):
+        assert np.array_equal(run_decode(w, x, True), a)
 
 
 def test_decode_relative_terms_matter():
