@@ -144,6 +144,22 @@ RELATTN_API relattn_status_t relattn_decode_fwd(const void *q, const void *k_cac
                                     void *out, relattn_stream_t stream);
 
 /*
+ * relattn_decode_fwd_noalloc — relattn_decode_fwd for callers that provide no device
+ * scratch: the same arguments without workspace / workspace_bytes, run with a 4 MiB scratch
+ * buffer that is part of the library's device image (a file-scope device array, so nothing
+ * is allocated at any call). That buffer is one per device and shared by every call of
+ * this entry point on the device, so such calls must not run at the same time (calls on
+ * one stream are ordered). The pages describe no counterpart of this entry point: it is an
+ * interface convenience, not part of the method.
+ */
+RELATTN_API relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
+                                            const void *v_cache, const void *aK,
+                                            const void *aV, long long table_head_stride,
+                                            int clip_k, float scale, const int *cache_len,
+                                            int B, int H, int T, int d, void *out,
+                                            relattn_stream_t stream);
+
+/*
  * relattn_decode_workspace_size — host only: the workspace bytes relattn_decode_fwd uses
  * to split caches of capacity T over several CTAs (0 when it runs one CTA per cache).
  */

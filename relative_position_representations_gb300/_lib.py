@@ -35,6 +35,9 @@ _lib.relattn_t5bias_fwd.restype = _I
 _lib.relattn_decode_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _P,
                                     _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P, _P]
 _lib.relattn_decode_fwd.restype = _I
+_lib.relattn_decode_fwd_noalloc.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I,
+                                            ctypes.c_float, _P, _I, _I, _I, _I, _P, _P]
+_lib.relattn_decode_fwd_noalloc.restype = _I
 _lib.relattn_decode_workspace_size.argtypes = [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.relattn_decode_workspace_size.restype = _I
 _lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
@@ -49,7 +52,7 @@ _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
 EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_decode_fwd",
-            "relattn_decode_workspace_size", "relattn_labels",
+            "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_labels",
             "relattn_t5_thresholds",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
@@ -164,6 +167,29 @@ def relattn_t5bias_fwd(q, k, v, bias, num_buckets=32, max_distance=128, bidirect
                                  float(scale), _ptr(kv_len), B, H, n, d, dt, _ptr(out),
                                  _stream(stream))
     _check(st, "relattn_t5bias_fwd")
+    return out
+
+
+def relattn_decode_fwd_noalloc(q, k_cache, v_cache, cache_len, aK=None, aV=None, clip_k=0,
+                               scale=None, out=None, table_head_stride=None, stream=None):
+    """relattn_decode_fwd with the library's built-in device scratch (no workspace argument;
+    calls on different streams must not overlap). Same arguments and result."""
+    B, H, d = q.shape
+    T = k_cache.shape[2]
+    W = 2 * int(clip_k) + 1
+    if table_head_stride is None:
+        ref = aK if aK is not None else aV
+        table_head_stride = 0 if (ref is None or ref.shape[0] == 1) else W * d
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", torch.bfloat16)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_decode_fwd_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(aK),
+                                         _ptr(aV), int(table_head_stride), int(clip_k),
+                                         float(scale), _ptr(cache_len), B, H, T, d, _ptr(out),
+                                         _stream(stream))
+    _check(st, "relattn_decode_fwd_noalloc")
     return out
 
 

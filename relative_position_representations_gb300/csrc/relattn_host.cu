@@ -29,6 +29,25 @@ int *status_word_for_current_device() {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// device scratch of relattn_decode_fwd_noalloc: part of the module image, never allocated
+constexpr unsigned long long kStaticScratchBytes = 4ull << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+// its address on the current device, looked up once per device with that device current
+void *static_scratch_for_current_device() {
+    static void *addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 // compute capability of the current device (major*10 + minor), or -1
 int current_cc() {
     int dev = 0, ma = 0, mi = 0;
@@ -178,6 +197,17 @@ relattn_status_t relattn_decode_fwd(const void *q, const void *k_cache, const vo
     a.workspace = workspace;
     a.workspace_bytes = workspace ? workspace_bytes : 0;
     return from_cuda(relattn::launch_decode_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
+                                            const void *v_cache, const void *aK, const void *aV,
+                                            long long table_head_stride, int clip_k, float scale,
+                                            const int *cache_len, int B, int H, int T, int d,
+                                            void *out, relattn_stream_t stream) {
+    void *ws = static_scratch_for_current_device();
+    if (!ws) return RELATTN_ERR_CUDA;
+    return relattn_decode_fwd(q, k_cache, v_cache, aK, aV, table_head_stride, clip_k, scale,
+                              cache_len, B, H, T, d, ws, kStaticScratchBytes, out, stream);
 }
 
 relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
