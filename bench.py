@@ -38,6 +38,8 @@ if ROOT not in sys.path:
 
 METRIC = ("fused rel-attn fwd TFLOP/s (bf16) and % of GB300 tensor/HBM roofline vs CPU oracle")
 DEFAULT_WORKLOAD = "base_encoder"
+# fp32 FMA peak of the SIMT units: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (max SM clock)
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -54,7 +56,11 @@ def pairs_per_sequence(w, kv_len_b: int) -> int:
 
 def algorithmic_flops(w, kv_len) -> float:
     """4*d per unmasked pair (Q.K^T and P.V) + 2*d*n per reachable table row and term.
-    Decode step: one query row per (b, h) over its cache_len keys."""
+    Decode step: one query row per (b, h) over its cache_len keys. Gradients: 2.5 times the
+    forward's count (Q.K^T, dP = dZ.V^T, dQ, dK, dV against Q.K^T and P.V; the same ratio
+    for the table terms)."""
+    if w.kind == "bwd":
+        return 2.5 * algorithmic_flops(w.replace(kind="shaw"), kv_len)
     if w.kind == "decode":
         terms = int(w.key_term) + int(w.value_term)
         rows = sum(min(int(x), w.n) for x in kv_len) * w.H
@@ -74,6 +80,11 @@ def algorithmic_bytes(w, kv_len) -> float:
     """Q and O in full, K and V rows below kv_len, the tables once (bf16 / fp32 elements).
     Decode step: q and out rows, the cached K and V rows below cache_len, table rows 0..k."""
     es = 2 if w.dtype == "bf16" else 4
+    if w.kind == "bwd":  # reads q, k, v, dout and the tables; writes fp32 dq, dk, dv, dtables
+        Ht = 1 if w.shared_tables else w.H
+        tab = Ht * (2 * w.clip_k + 1) * w.d * (int(w.key_term) + int(w.value_term))
+        return float(4 * w.B * w.H * w.n * w.d * es + 3 * w.B * w.H * w.n * w.d * 4 +
+                     tab * (es + 4))
     if w.kind == "decode":
         rows = sum(min(int(x), w.n) for x in kv_len) * w.H
         Ht = 1 if w.shared_tables else w.H
@@ -102,16 +113,30 @@ def read_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# the sources each measured kernel is built from (argument structs in relattn_internal.h
+# and the host entry points do not change the kernels' code)
+KERNEL_SOURCES = {
+    "fused": ["device_common.cuh", "relattn_tc_d128.cu", "relattn_tc_d64.cu",
+              "relattn_tc_kernel.cuh", "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
+    "decode": ["relattn_decode.cu"],
+    "bwd": ["relattn_bwd.cu"],
+}
+
+
+def kernel_family(w) -> str:
+    return {"decode": "decode", "bwd": "bwd"}.get(w.kind, "fused")
+
+
+def kernel_source_hash(family: str = "fused") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "relative_position_representations_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[family]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, family: str = "fused"):
     """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
@@ -119,7 +144,7 @@ def profiled_traffic(workload: str):
             for line in f:
                 parts = line.split()
                 if len(parts) == 3 and not line.startswith("#") and parts[0] == workload:
-                    if parts[1] == kernel_source_hash():
+                    if parts[1] == kernel_source_hash(family):
                         return float(parts[2])
     except Exception:
         pass
@@ -196,12 +221,34 @@ def workload_by_name(name):
     from relative_position_representations_gb300 import workloads as wl
     if name in wl.DECODE_WORKLOADS:
         return wl.DECODE_WORKLOADS[name]
+    if name in wl.BWD_WORKLOADS:
+        return wl.BWD_WORKLOADS[name]
     return wl.WORKLOADS[name]
 
 
 def draw(w, seed):
     from relative_position_representations_gb300 import workloads as wl
-    return wl.draw_decode_inputs(w, seed) if w.kind == "decode" else wl.draw_inputs(w, seed)
+    if w.kind == "decode":
+        return wl.draw_decode_inputs(w, seed)
+    if w.kind == "bwd":
+        return wl.draw_bwd_inputs(w, seed)
+    return wl.draw_inputs(w, seed)
+
+
+def oracle_bwd_batches(w, x, batches):
+    """The gradient oracle on the sequences in `batches` (all heads), one at a time."""
+    from oracle import backward
+    from relative_position_representations_gb300 import workloads as wl
+    out = []
+    for b in batches:
+        sl = lambda t: None if t is None else t[b:b + 1].double().numpy()
+        tab = lambda t: None if t is None else t.double().numpy()
+        kv = None if x["kv_len"] is None else x["kv_len"][b:b + 1].numpy()
+        out.append(backward.relattn_bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), tab(x["aK"]),
+                                        tab(x["aV"]), sl(x["dout"]), w.clip_k, w.causal,
+                                        w.softmax_scale, kv_len=kv,
+                                        table_head_stride=wl.table_head_stride(w)))
+    return out
 
 
 def key_lengths(w, x):
@@ -240,6 +287,8 @@ def oracle_rows_call(w, x, rows, nthreads):
 
     if w.kind == "decode":  # rows are sequence indices
         return oracle_decode_rows(w, x, rows, nthreads)
+    if w.kind == "bwd":  # rows are sequence indices
+        return oracle_bwd_batches(w, x, rows)
 
     kv = None if x.get("kv_len") is None else x["kv_len"].numpy()
     if w.kind == "t5":
@@ -256,8 +305,9 @@ def oracle_rows_call(w, x, rows, nthreads):
 def row_flops(w, kv_len, rows):
     """Algorithmic FLOPs of a set of flat row ids (same accounting as algorithmic_flops);
     for the decode step the ids are sequences (all heads)."""
-    if w.kind == "decode":
-        return algorithmic_flops(w.replace(B=len(rows)), [kv_len[int(b)] for b in rows])
+    if w.kind in ("decode", "bwd"):
+        return algorithmic_flops(w.replace(B=len(rows)),
+                                 None if kv_len is None else [kv_len[int(b)] for b in rows])
     total = 0.0
     reach = 0
     if w.kind == "shaw":
@@ -278,7 +328,7 @@ def time_oracle(w, x, budget_s: float, seed: int = 1):
     import oracle
     nthreads = oracle.default_threads()
     rng = np.random.default_rng(seed)
-    total_rows = w.B if w.kind == "decode" else w.B * w.H * w.n
+    total_rows = w.B if w.kind in ("decode", "bwd") else w.B * w.H * w.n
     kv = key_lengths(w, x)
     # calibrate on a small batch of rows
     count = min(total_rows, max(nthreads * 4, 64))
@@ -302,15 +352,27 @@ def time_oracle(w, x, budget_s: float, seed: int = 1):
         if dt >= budget_s or target < total_rows:
             break
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-            "sample": "%d of %d %s (random, seed %d) x %d pass(es), fp64 C loop, "
+            "sample": "%d of %d %s (random, seed %d) x %d pass(es), fp64 %s, "
                       "%.1f s" % (target, total_rows,
-                                  "sequences (all heads)" if w.kind == "decode" else "query rows",
-                                  seed, passes, dt)}, fl, dt
+                                  "sequences (all heads)" if w.kind in ("decode", "bwd")
+                                  else "query rows",
+                                  seed, passes,
+                                  "numpy gradient oracle" if w.kind == "bwd" else "C loop",
+                                  dt)}, fl, dt
 
 
 # ----------------------------------------------------------------------- GPU arm
 def gpu_call(rp, w, g, out, stream):
     from relative_position_representations_gb300 import workloads as wl
+    if w.kind == "bwd":
+        if "ws" not in g:  # the caller's workspace (made once)
+            import torch
+            nb = rp.relattn_bwd_workspace_size(w.B, w.H, w.n, w.d, w.clip_k)
+            g["ws"] = torch.empty(max(nb, 4), dtype=torch.uint8, device=g["q"].device)
+        return rp.relattn_bwd(g["q"], g["k"], g["v"], g["dout"], aK=g["aK"], aV=g["aV"],
+                              clip_k=w.clip_k, causal=w.causal, scale=w.softmax_scale,
+                              kv_len=g["kv_len"], table_head_stride=wl.table_head_stride(w),
+                              workspace=g["ws"], stream=stream)
     if w.kind == "decode":
         if "ws" not in g:  # the caller's scratch for the split over the cache (made once)
             import torch
@@ -338,6 +400,8 @@ def launches_per_step(rp, w) -> int:
     if (w.kind == "decode" and not NO_DECODE_WORKSPACE and
             rp.relattn_decode_workspace_size(w.B, w.H, w.n, w.d) > 0):
         return 2
+    if w.kind == "bwd":  # rows, keys, tables (the two table memsets are not kernels of ours)
+        return 3 if (w.key_term or w.value_term) else 2
     return 1
 
 
@@ -354,7 +418,7 @@ def make_event(external: bool):
 def workload_config(w, world: int, l2_note: str) -> dict:
     """The JSON `config` of both arms: the workload by name and shape."""
     return {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
-            "kind": w.kind, "clip_k": w.clip_k if w.kind in ("shaw", "decode") else None,
+            "kind": w.kind, "clip_k": w.clip_k if w.kind in ("shaw", "decode", "bwd") else None,
             "causal": w.causal,
             "terms": ("t5 bias" if w.kind == "t5" else
                       "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
@@ -492,9 +556,17 @@ def run_ours(args, rank, world, local_rank):
     e2e = None if args.no_e2e else measure_e2e(rp, w, x, dev, stream, flops, args)
 
     peaks, peak_src = read_peaks()
-    t_roof_compute = flops / (peaks["bf16_tflops"] * 1e12)
+    # the gradients run on the SIMT units: their compute roof is the fp32 FMA rate
+    alu = w.kind == "bwd"
+    compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
+    t_roof_compute = flops / (compute_peak * 1e12)
     t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
-    if t_roof_mem >= t_roof_compute:
+    if alu and t_roof_compute > t_roof_mem:
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": FP32_SIMT_TFLOPS,
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_SIMT_TFLOPS, 4),
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 flop x 2.07 GHz"}
+    elif t_roof_mem >= t_roof_compute:
         achieved = byts / (kern_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -504,7 +576,7 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "peak_source": peak_src + " (cuBLAS bf16 burst)"}
-    roof["traffic"] = profiled_traffic(w.name)
+    roof["traffic"] = profiled_traffic(w.name, kernel_family(w))
     roof["kernel_ms"] = round(kern_ms, 5)
     roof["kernel_time_source"] = kern_src
     roof["algorithmic_flops"] = flops
@@ -542,22 +614,26 @@ def measure_e2e(rp, w, x, dev, stream, flops, args):
         if v is not None and k not in per_step:
             g[k].copy_(v)
     out = torch.empty_like(g["q"])
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for k, v in host.items()
               if v is not None and k in per_step)
-    d2h = out.numel() * out.element_size()
+    back = []  # pinned host buffers for the step's results (the gradients for "bwd")
 
     def step():
         for k, v in host.items():
             if v is not None and k in per_step:
                 g[k].copy_(v, non_blocking=True)
-        gpu_call(rp, w, g, out, stream)
-        out_host.copy_(out, non_blocking=True)
+        res = gpu_call(rp, w, g, out, stream)
+        res = [t for t in res if t is not None] if isinstance(res, tuple) else [res]
+        if not back:
+            back.extend(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in res)
+        for hb, t in zip(back, res):
+            hb.copy_(t, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
             step()
     stream.synchronize()
+    d2h = sum(t.numel() * t.element_size() for t in back)
     n = max(5, min(200, args.steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):

@@ -167,6 +167,44 @@ RELATTN_API relattn_status_t relattn_decode_workspace_size(int B, int H, int T, 
                                                unsigned long long *bytes);
 
 /*
+ * relattn_bwd — gradients of relattn_fwd (Shaw relation-aware attention) for training. The
+ * pages state only the forward pass (paper summary page, section 3.4, eq. 3 and eq. 4);
+ * these are the chain rule through it:
+ *
+ *   dp_ij = dz_i . (v_j + aV_r),  de_ij = p_ij (dp_ij - sum_j' p_ij' dp_ij'),
+ *   dq_i = scale sum_j de_ij (k_j + aK_r),  dk_j = scale sum_i de_ij q_i,
+ *   dv_j = sum_i p_ij dz_i,  daK_r = scale sum_{r_ij = r} de_ij q_i,
+ *   daV_r = sum_{r_ij = r} p_ij dz_i,     r = r_ij = clip(j - i, clip_k) + clip_k,
+ *
+ * with p the forward's softmax over the same allowed keys (causal, kv_len).
+ *
+ *   q, k, v, aK, aV, table_head_stride, clip_k, causal, scale, kv_len, B, H, n, d, dtype
+ *                     as in relattn_fwd (bf16 or fp32; any 1 <= d <= 128).
+ *   dout              [B, H, n, d] of `dtype`: the gradient of the loss with respect to out.
+ *   dq, dk, dv        [B, H, n, d] fp32, written (not accumulated).
+ *   daK, daV          fp32 tables laid out like aK / aV (head stride table_head_stride;
+ *                     with 0 one table receives every head's gradient); written (not
+ *                     accumulated); required when the matching table is given, ignored
+ *                     otherwise.
+ *   workspace         caller-owned device scratch of at least relattn_bwd_workspace_size
+ *                     bytes (4-byte aligned); its contents are scratch.
+ *
+ * Arithmetic is fp32 on the SIMT units (three kernels: one warp per query row, one warp per
+ * key, one CTA per table row), so it is a first, correct version rather than a fast one.
+ * 2*clip_k + 1 <= 257.
+ */
+RELATTN_API relattn_status_t relattn_bwd(const void *q, const void *k, const void *v,
+                             const void *aK, const void *aV, long long table_head_stride,
+                             int clip_k, int causal, float scale, const int *kv_len, int B,
+                             int H, int n, int d, int dtype, const void *dout, float *dq,
+                             float *dk, float *dv, float *daK, float *daV, void *workspace,
+                             unsigned long long workspace_bytes, relattn_stream_t stream);
+
+/* relattn_bwd_workspace_size — host only: the workspace bytes relattn_bwd needs. */
+RELATTN_API relattn_status_t relattn_bwd_workspace_size(int B, int H, int n, int d, int clip_k,
+                                            unsigned long long *bytes);
+
+/*
  * relattn_labels — the integer edge label of every (i, j), computed by the same device
  * functions the attention kernels use, written as int32 labels[i * n_k + j].
  *   kind 0: clip row clip(j - i, clip_k) + clip_k (paper summary, section 3.4).

@@ -38,6 +38,11 @@ _lib.relattn_decode_fwd.restype = _I
 _lib.relattn_decode_fwd_noalloc.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I,
                                             ctypes.c_float, _P, _I, _I, _I, _I, _P, _P]
 _lib.relattn_decode_fwd_noalloc.restype = _I
+_lib.relattn_bwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, _I, ctypes.c_float, _P, _I,
+                             _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_ulonglong, _P]
+_lib.relattn_bwd.restype = _I
+_lib.relattn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
+_lib.relattn_bwd_workspace_size.restype = _I
 _lib.relattn_decode_workspace_size.argtypes = [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.relattn_decode_workspace_size.restype = _I
 _lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
@@ -52,7 +57,8 @@ _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
 EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_decode_fwd",
-            "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_labels",
+            "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
+            "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
@@ -191,6 +197,53 @@ def relattn_decode_fwd_noalloc(q, k_cache, v_cache, cache_len, aK=None, aV=None,
                                          _stream(stream))
     _check(st, "relattn_decode_fwd_noalloc")
     return out
+
+
+def relattn_bwd_workspace_size(B, H, n, d, clip_k) -> int:
+    """Workspace bytes relattn_bwd needs (host only)."""
+    nb = ctypes.c_ulonglong(0)
+    _check(_lib.relattn_bwd_workspace_size(int(B), int(H), int(n), int(d), int(clip_k),
+                                           ctypes.byref(nb)), "relattn_bwd_workspace_size")
+    return int(nb.value)
+
+
+def relattn_bwd(q, k, v, dout, aK=None, aV=None, clip_k=0, causal=False, scale=None, kv_len=None,
+                table_head_stride=None, workspace=None, stream=None):
+    """Gradients of relattn_fwd: returns (dq, dk, dv, daK, daV), fp32 (daK / daV None when
+    the table is None). workspace: a CUDA tensor of at least relattn_bwd_workspace_size
+    bytes, or None to make one."""
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    _dev(dout, "dout", q.dtype)
+    if dout.shape != q.shape:
+        raise ValueError("dout must be [B, H, n, d] like q")
+    W = 2 * int(clip_k) + 1
+    for name, t in (("aK", aK), ("aV", aV)):
+        if t is not None:
+            _dev(t, name, q.dtype)
+            if t.dim() != 3 or t.shape[1] != W or t.shape[2] != d or t.shape[0] not in (1, H):
+                raise ValueError("%s must be [H or 1, 2*clip_k+1, d]" % name)
+    if table_head_stride is None:
+        ref = aK if aK is not None else aV
+        table_head_stride = 0 if (ref is None or ref.shape[0] == 1) else W * d
+    _dev(kv_len, "kv_len", torch.int32)
+    if scale is None:
+        scale = d ** -0.5
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dv = (torch.empty(q.shape, **f32) for _ in range(3))
+    daK = None if aK is None else torch.empty(aK.shape, **f32)
+    daV = None if aV is None else torch.empty(aV.shape, **f32)
+    need = relattn_bwd_workspace_size(B, H, n, d, clip_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4), dtype=torch.uint8, device=q.device)
+    _dev(workspace, "workspace")
+    st = _lib.relattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(aK), _ptr(aV), int(table_head_stride),
+                          int(clip_k), int(bool(causal)), float(scale), _ptr(kv_len), B, H, n, d,
+                          dt, _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(daK), _ptr(daV),
+                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                          _stream(stream))
+    _check(st, "relattn_bwd")
+    return dq, dk, dv, daK, daV
 
 
 def relattn_decode_workspace_size(B, H, T, d) -> int:

@@ -210,6 +210,53 @@ relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
                               cache_len, B, H, T, d, ws, kStaticScratchBytes, out, stream);
 }
 
+relattn_status_t relattn_bwd_workspace_size(int B, int H, int n, int d, int clip_k,
+                                            unsigned long long *bytes) {
+    if (!bytes || !shapes_ok(B, H, n, d) || clip_k < 0 || clip_k > (1 << 20))
+        return RELATTN_ERR_INVALID_ARG;
+    *bytes = relattn::bwd_workspace_bytes(B, H, n, clip_k);
+    return RELATTN_OK;
+}
+
+relattn_status_t relattn_bwd(const void *q, const void *k, const void *v, const void *aK,
+                             const void *aV, long long table_head_stride, int clip_k, int causal,
+                             float scale, const int *kv_len, int B, int H, int n, int d,
+                             int dtype, const void *dout, float *dq, float *dk, float *dv,
+                             float *daK, float *daV, void *workspace,
+                             unsigned long long workspace_bytes, relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, dq, B, H, n, d, dtype);
+    if (st != RELATTN_OK && st != RELATTN_ERR_UNSUPPORTED) return st;
+    if (!dout || !dk || !dv || !workspace) return RELATTN_ERR_INVALID_ARG;
+    if (d > 128) return RELATTN_ERR_UNSUPPORTED;
+    if (clip_k < 0 || clip_k > (1 << 20) || (causal != 0 && causal != 1)) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    const uintptr_t al = dtype == RELATTN_BF16 ? 2 : 4;
+    if (!aligned(dout, al) || !aligned(dk, 4) || !aligned(dv, 4) || !aligned(workspace, 4))
+        return RELATTN_ERR_INVALID_ARG;
+    if ((aK && !daK) || (aV && !daV)) return RELATTN_ERR_INVALID_ARG;
+    if (aK || aV) {
+        const long long rows_d = (2LL * clip_k + 1) * d;
+        if (table_head_stride != 0 && table_head_stride < rows_d) return RELATTN_ERR_INVALID_ARG;
+        if ((daK && !aligned(daK, 4)) || (daV && !aligned(daV, 4))) return RELATTN_ERR_INVALID_ARG;
+    }
+    if (workspace_bytes < relattn::bwd_workspace_bytes(B, H, n, clip_k)) return RELATTN_ERR_INVALID_ARG;
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    relattn::BwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.aK = aK; a.aV = aV; a.dout = dout;
+    a.ths = table_head_stride;
+    a.clip_k = clip_k;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.daK = daK; a.daV = daV;
+    a.workspace = workspace;
+    return from_cuda(relattn::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
                                     const float *bias, int num_buckets, int max_distance,
                                     int bidirectional, int causal, float scale,

@@ -81,4 +81,20 @@ unsigned long long decode_workspace_bytes(int B, int H, int T, int d);
 // enough workspace the single-pass kernel runs
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 
+// ---- gradients (SIMT, fp32 arithmetic) ---------------------------------------------------
+struct BwdArgs {
+    const void *q, *k, *v, *aK, *aV, *dout;
+    long long ths;
+    int clip_k, causal;
+    float scale;
+    const int *kv_len;
+    int B, H, n, d;
+    int bf16;  // 1: q, k, v, tables and dout are bf16; 0: fp32
+    float *dq, *dk, *dv, *daK, *daV;
+    void *workspace;  // at least bwd_workspace_bytes
+};
+unsigned long long bwd_workspace_bytes(int B, int H, int n, int clip_k);
+// cudaErrorNotSupported when 2k+1 > 257 or d > 128
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s);
+
 }  // namespace relattn

@@ -30,7 +30,7 @@ class Workload:
     n: int
     d: int
     dtype: str                      # "bf16" or "f32"
-    kind: str = "shaw"              # "shaw", "t5" or "decode" (one decoding step)
+    kind: str = "shaw"              # "shaw", "t5", "decode" (one decoding step), "bwd" (gradients)
     clip_k: int = 0
     causal: bool = False
     key_term: bool = True           # a^K present (Shaw)
@@ -81,6 +81,14 @@ WORKLOADS = {
 
 ORDER = ["tiny_fp32", "base_encoder", "big_decoder", "long_keyonly", "t5_bias"]
 
+# Gradients of the base encoder (kind "bwd"): the forward's inputs plus dout ~ N(0, 1) drawn
+# after them.
+BWD_WORKLOADS = {
+    "bwd_base_encoder": Workload("bwd_base_encoder", B=64, H=8, n=128, d=64, dtype="bf16",
+                                 kind="bwd", clip_k=16, table_std=0.02, kv_len_range=(32, 128),
+                                 scale=1.0 / 8),
+}
+
 # One incremental decoding step (kind "decode"): n is the cache capacity T; each sequence's
 # cache holds kv_len_range-drawn entries, the last being the new token (Transformer-big
 # decoder shape, caches of 1K-2K tokens).
@@ -118,6 +126,16 @@ def draw_inputs(w: Workload, seed: int = 0) -> dict:
     else:
         out["kv_len"] = None
     return out
+
+
+def draw_bwd_inputs(w: Workload, seed: int = 0) -> dict:
+    """The forward inputs of a Shaw workload, then dout [B, H, n, d] ~ N(0, 1)."""
+    x = draw_inputs(w.replace(kind="shaw"), seed)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 7919)
+    x["dout"] = torch.randn((w.B, w.H, w.n, w.d), generator=g,
+                            dtype=torch.float32).to(w.torch_dtype)
+    return x
 
 
 def draw_decode_inputs(w: Workload, seed: int = 0) -> dict:
