@@ -15,6 +15,10 @@ the tables are zero, the k = 0 closed forms, the causal first row, shift invaria
 the relative-only dependence, the brute-force materialised form, bin sums, key-only
 equivalence, T5 constant-bias reduction, the clip examples and label counts printed on
 the pages, and a hand-computed 2-token sign check.
+Pins of the scalar offset biases (ALiBi, the clipped per-offset table) are in
+tests/test_oracle_offset_bias.py: library attention with the bias grid as an additive mask,
+ALiBi as the T5 path with a linear table, the zero-query closed form of the ALiBi weights,
+a hand-computed 2-token sign check of the clipped table, and the softmax's shift invariance.
 """
 from __future__ import annotations
 
@@ -139,6 +143,76 @@ def t5bias_fwd(q, k, v, bias, num_buckets, max_distance, bidirectional, causal, 
     if rc != 0:
         raise RuntimeError("oracle thread start failed")
     return out if rows is not None else out.reshape(B, H, n, d)
+
+
+def offset_bias_fwd(q, k, v, bias_of_offset, causal, scale, kv_len=None, rows=None,
+                    nthreads=None):
+    """Attention with a scalar bias per relative offset, fp64:
+
+        e_ij = scale * q_i . k_j + bias_of_offset[h, (j - i) + n - 1]
+
+    ("Relative position embeddings" page: the T5 form of section "T5" with the bucketing
+    left out, which is what section "Placement in the taxonomy" varies). bias_of_offset:
+    [H, 2n - 1], the bias of every offset of the sequence. The C loop runs it as the T5
+    loop in which every offset is its own bucket.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, n, d = q.shape
+    bo = np.asarray(bias_of_offset, dtype=np.float64)
+    if bo.shape != (H, 2 * n - 1):
+        raise ValueError("bias_of_offset must be [H, 2n - 1]")
+    bias = np.ascontiguousarray(bo.T)                       # [2n - 1 "buckets", H]
+    ident = np.ascontiguousarray(np.arange(2 * n - 1, dtype=np.int32))
+    kvl = None if kv_len is None else np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32))
+    r, nrows = _rows_arg(rows, B, H, n)
+    out = np.zeros((nrows, d), dtype=np.float64)
+    rc = _load().oracle_t5bias_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(ident),
+                                    int(bool(causal)), float(scale), _ptr(kvl), B, H, n, d,
+                                    _ptr(r), nrows, _ptr(out),
+                                    int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle thread start failed")
+    return out if rows is not None else out.reshape(B, H, n, d)
+
+
+def alibi_bias_of_offset(n: int, slopes) -> np.ndarray:
+    """ALiBi as a bias per offset: b_h(delta) = -m_h * |delta| ("Relative position
+    embeddings", section "Placement in the taxonomy"). Returns [H, 2n - 1], index
+    delta + n - 1."""
+    m = np.asarray(slopes, dtype=np.float64).reshape(-1)
+    delta = np.arange(-(n - 1), n, dtype=np.float64)
+    return -m[:, None] * np.abs(delta)[None, :]
+
+
+def clipped_bias_of_offset(n: int, table, radius: int, heads: int) -> np.ndarray:
+    """A learned scalar per offset, clipped at `radius` like the Shaw tables:
+    b_h(delta) = table[h, clip(delta, radius) + radius]. table: [heads or 1, 2*radius + 1]
+    (one row shared by every head). Returns [heads, 2n - 1], index delta + n - 1."""
+    t = np.asarray(table, dtype=np.float64)
+    if t.ndim != 2 or t.shape[1] != 2 * radius + 1 or t.shape[0] not in (1, heads):
+        raise ValueError("table must be [heads or 1, 2*radius + 1]")
+    out = np.empty((heads, 2 * n - 1), dtype=np.float64)
+    for h in range(heads):
+        row = t[h if t.shape[0] == heads else 0]
+        for idx in range(2 * n - 1):
+            out[h, idx] = row[clip(idx - (n - 1), radius) + radius]
+    return out
+
+
+def alibi_fwd(q, k, v, slopes, causal, scale, kv_len=None, rows=None, nthreads=None):
+    """ALiBi attention forward, fp64: e_ij = scale * q_i . k_j - m_h |j - i|."""
+    n = np.shape(q)[2]
+    return offset_bias_fwd(q, k, v, alibi_bias_of_offset(n, slopes), causal, scale,
+                           kv_len=kv_len, rows=rows, nthreads=nthreads)
+
+
+def offset_table_fwd(q, k, v, table, radius, causal, scale, kv_len=None, rows=None,
+                     nthreads=None):
+    """Clipped per-offset scalar bias forward, fp64: e_ij = scale * q_i . k_j +
+    table[h, clip(j - i, radius) + radius]."""
+    H, n = np.shape(q)[1], np.shape(q)[2]
+    return offset_bias_fwd(q, k, v, clipped_bias_of_offset(n, table, radius, H), causal, scale,
+                           kv_len=kv_len, rows=rows, nthreads=nthreads)
 
 
 def clip_labels(n_q: int, n_k: int, clip_k: int) -> np.ndarray:
