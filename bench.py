@@ -94,11 +94,15 @@ def algorithmic_bytes(w, kv_len) -> float:
     kvs = [w.n] * w.B if kv_len is None else [min(int(x), w.n) for x in kv_len]
     kv_rows = sum(kvs) * w.H
     byt = es * (2 * BHnd + 2 * kv_rows * w.d)
+    Ht = 1 if w.shared_tables else w.H
     if w.kind == "shaw":
-        Ht = 1 if w.shared_tables else w.H
         byt += es * Ht * (2 * w.clip_k + 1) * w.d * (int(w.key_term) + int(w.value_term))
-    else:
+    elif w.kind == "t5":
         byt += 4 * w.num_buckets * w.H
+    elif w.kind == "alibi":  # the slopes
+        byt += 4 * w.H
+    else:  # "offset": the clipped per-offset table
+        byt += 4 * Ht * (2 * w.clip_k + 1)
     return float(byt)
 
 
@@ -223,6 +227,8 @@ def workload_by_name(name):
         return wl.DECODE_WORKLOADS[name]
     if name in wl.BWD_WORKLOADS:
         return wl.BWD_WORKLOADS[name]
+    if name in wl.BIAS_WORKLOADS:
+        return wl.BIAS_WORKLOADS[name]
     return wl.WORKLOADS[name]
 
 
@@ -295,6 +301,14 @@ def oracle_rows_call(w, x, rows, nthreads):
         return oracle.t5bias_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), x["bias"].numpy(),
                                  w.num_buckets, w.max_distance, w.bidirectional, w.causal,
                                  w.softmax_scale, kv_len=kv, rows=rows, nthreads=nthreads)
+    if w.kind == "alibi":
+        return oracle.alibi_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), x["slopes"].numpy(),
+                                w.causal, w.softmax_scale, kv_len=kv, rows=rows,
+                                nthreads=nthreads)
+    if w.kind == "offset":
+        return oracle.offset_table_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), x["table"].numpy(),
+                                       w.clip_k, w.causal, w.softmax_scale, kv_len=kv,
+                                       rows=rows, nthreads=nthreads)
     from relative_position_representations_gb300 import workloads as wl
     return oracle.relattn_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), np_(x["aK"]), np_(x["aV"]),
                               w.clip_k, w.causal, w.softmax_scale, kv_len=kv,
@@ -387,6 +401,13 @@ def gpu_call(rp, w, g, out, stream):
         return rp.relattn_t5bias_fwd(g["q"], g["k"], g["v"], g["bias"], w.num_buckets,
                                      w.max_distance, w.bidirectional, w.causal, w.softmax_scale,
                                      kv_len=g.get("kv_len"), out=out, stream=stream)
+    if w.kind == "alibi":
+        return rp.relattn_alibi_fwd(g["q"], g["k"], g["v"], g["slopes"], w.causal,
+                                    w.softmax_scale, kv_len=g["kv_len"], out=out, stream=stream)
+    if w.kind == "offset":
+        return rp.relattn_offset_bias_fwd(g["q"], g["k"], g["v"], g["table"], w.clip_k,
+                                          w.causal, w.softmax_scale, kv_len=g["kv_len"],
+                                          out=out, stream=stream)
     return rp.relattn_fwd(g["q"], g["k"], g["v"], g["aK"], g["aV"], w.clip_k, w.causal,
                           w.softmax_scale, kv_len=g["kv_len"], out=out,
                           table_head_stride=wl.table_head_stride(w), stream=stream)
@@ -418,9 +439,13 @@ def make_event(external: bool):
 def workload_config(w, world: int, l2_note: str) -> dict:
     """The JSON `config` of both arms: the workload by name and shape."""
     return {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "d": w.d,
-            "kind": w.kind, "clip_k": w.clip_k if w.kind in ("shaw", "decode", "bwd") else None,
+            "kind": w.kind,
+            "clip_k": w.clip_k if w.kind in ("shaw", "decode", "bwd", "offset") else None,
             "causal": w.causal,
             "terms": ("t5 bias" if w.kind == "t5" else
+                      "alibi bias (slopes 2^(-%g(h+1)/H))" % w.alibi_max_bias
+                      if w.kind == "alibi" else
+                      "per-offset scalar bias, radius %d" % w.clip_k if w.kind == "offset" else
                       "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
                                if on) or "none"),
             ("cache_len" if w.kind == "decode" else "kv_len"):

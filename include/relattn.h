@@ -105,6 +105,46 @@ RELATTN_API relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, co
                                     void *out, relattn_stream_t stream);
 
 /*
+ * relattn_alibi_fwd — ALiBi: the scalar relative bias with the T5 table replaced by a
+ * fixed line per head ("Relative position embeddings", section "Placement in the taxonomy"):
+ *
+ *   e_ij = scale * q_i . k_j - slopes[h] * |j - i|
+ *
+ * softmax, masks, empty rows and output as in relattn_fwd (no edge vector on the values).
+ * slopes is a [H] fp32 device array (the method fixes them, e.g. 2^(-8(h+1)/H); any values
+ * are accepted). The bias is formed in fp32 (slope times the exact distance).
+ *
+ * bf16 limit (else RELATTN_ERR_UNSUPPORTED): the kernel holds the bias of every offset of
+ * the sequence in shared memory, 4 * (2n + 127) bytes per query tile in flight; n up to
+ * about 20000 fits. fp32 (SIMT) has no such limit.
+ */
+RELATTN_API relattn_status_t relattn_alibi_fwd(const void *q, const void *k, const void *v,
+                                   const float *slopes, int causal, float scale,
+                                   const int *kv_len, int B, int H, int n, int d, int dtype,
+                                   void *out, relattn_stream_t stream);
+
+/*
+ * relattn_offset_bias_fwd — a learned scalar per relative offset, clipped like the Shaw
+ * tables: the T5 form ("Relative position embeddings", section "T5") with one table entry
+ * per offset instead of per bucket (the 1-D case of the offset-indexed table of section
+ * "Two-dimensional variants"), read at clip(j - i, radius):
+ *
+ *   e_ij = scale * q_i . k_j + table[h * table_head_stride + clip(j - i, radius) + radius]
+ *
+ * softmax, masks, empty rows and output as in relattn_fwd. table is an fp32 device array
+ * [H|1, 2*radius + 1], entry r holding the bias of offset r - radius.
+ *   table_head_stride  elements between heads' rows; 0 = one row shared by every head,
+ *                      else >= 2*radius + 1.
+ *   radius             0 <= radius <= 2^20 (radius >= n - 1 means no clipping).
+ * bf16 limit (else RELATTN_ERR_UNSUPPORTED): as relattn_alibi_fwd, with min(radius, n - 1)
+ * in place of n - 1.
+ */
+RELATTN_API relattn_status_t relattn_offset_bias_fwd(const void *q, const void *k, const void *v,
+                                   const float *table, long long table_head_stride, int radius,
+                                   int causal, float scale, const int *kv_len, int B, int H,
+                                   int n, int d, int dtype, void *out, relattn_stream_t stream);
+
+/*
  * relattn_decode_fwd — one incremental decoding step of a causal decoder: the new token of
  * every sequence attends to its sequence's key/value cache with the relative terms of
  * relattn_fwd (paper summary page, section 3.4, eq. 3 and eq. 4 with clip(j - i, k)).

@@ -32,6 +32,12 @@ _lib.relattn_fwd.restype = _I
 _lib.relattn_t5bias_fwd.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P, _I, _I,
                                     _I, _I, _I, _P, _P]
 _lib.relattn_t5bias_fwd.restype = _I
+_lib.relattn_alibi_fwd.argtypes = [_P, _P, _P, _P, _I, ctypes.c_float, _P, _I, _I, _I, _I, _I,
+                                   _P, _P]
+_lib.relattn_alibi_fwd.restype = _I
+_lib.relattn_offset_bias_fwd.argtypes = [_P, _P, _P, _P, ctypes.c_longlong, _I, _I,
+                                         ctypes.c_float, _P, _I, _I, _I, _I, _I, _P, _P]
+_lib.relattn_offset_bias_fwd.restype = _I
 _lib.relattn_decode_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _P,
                                     _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P, _P]
 _lib.relattn_decode_fwd.restype = _I
@@ -56,7 +62,8 @@ _lib.relattn_status_string.restype = ctypes.c_char_p
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
-EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_decode_fwd",
+EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
+            "relattn_offset_bias_fwd", "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds",
@@ -173,6 +180,59 @@ def relattn_t5bias_fwd(q, k, v, bias, num_buckets=32, max_distance=128, bidirect
                                  float(scale), _ptr(kv_len), B, H, n, d, dt, _ptr(out),
                                  _stream(stream))
     _check(st, "relattn_t5bias_fwd")
+    return out
+
+
+def relattn_alibi_fwd(q, k, v, slopes, causal=False, scale=None, kv_len=None, out=None,
+                      stream=None):
+    """ALiBi attention: e_ij = scale * q_i . k_j - slopes[h] * |j - i| ("Relative position
+    embeddings", section "Placement in the taxonomy").
+
+    slopes: [H] fp32 CUDA tensor. scale defaults to 1/sqrt(d). Returns out.
+    """
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    _dev(slopes, "slopes", torch.float32)
+    if slopes.shape != (H,):
+        raise ValueError("slopes must be [H]")
+    _dev(kv_len, "kv_len", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_alibi_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), int(bool(causal)),
+                                float(scale), _ptr(kv_len), B, H, n, d, dt, _ptr(out),
+                                _stream(stream))
+    _check(st, "relattn_alibi_fwd")
+    return out
+
+
+def relattn_offset_bias_fwd(q, k, v, table, radius, causal=False, scale=None, kv_len=None,
+                            out=None, stream=None):
+    """Scalar bias per relative offset, clipped at `radius`: e_ij = scale * q_i . k_j +
+    table[h, clip(j - i, radius) + radius].
+
+    table: [H or 1, 2*radius + 1] fp32 CUDA tensor (one row: shared by every head).
+    scale defaults to 1/sqrt(d). Returns out.
+    """
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    _dev(table, "table", torch.float32)
+    W = 2 * int(radius) + 1
+    if table.dim() != 2 or table.shape[1] != W or table.shape[0] not in (1, H):
+        raise ValueError("table must be [H or 1, 2*radius + 1]")
+    ths = 0 if (table.shape[0] == 1 and H > 1) else W
+    _dev(kv_len, "kv_len", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_offset_bias_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(table), int(ths),
+                                      int(radius), int(bool(causal)), float(scale),
+                                      _ptr(kv_len), B, H, n, d, dt, _ptr(out), _stream(stream))
+    _check(st, "relattn_offset_bias_fwd")
     return out
 
 

@@ -27,4 +27,14 @@ __device__ __forceinline__ int t5_bucket(int delta, const T5Buckets &t) {
     return offset + b;
 }
 
+// Scalar bias of offset delta = j - i for head h: a T5 bucket's table entry, ALiBi's
+// -m_h |delta| ("Placement in the taxonomy": the T5 table replaced by a line), or the entry
+// clip(delta, R) + R of a per-offset table (R the table's radius, hs its head stride).
+__device__ __forceinline__ float scalar_bias(const float *bias, int kind, int H, int R,
+                                             long long hs, const T5Buckets &t, int delta, int h) {
+    if (kind == kBiasAlibi) return -bias[h] * (float)(delta < 0 ? -delta : delta);
+    if (kind == kBiasTable) return bias[(long long)h * hs + clip_offset(delta, R) + R];
+    return bias[(long long)t5_bucket(delta, t) * H + h];
+}
+
 }  // namespace relattn

@@ -102,6 +102,52 @@ relattn_status_t dispatch_bf16(const relattn::TcArgs &a, const relattn::T5Bucket
     return from_cuda(e);
 }
 
+// Forward with a scalar bias per offset (T5 buckets, ALiBi or a clipped per-offset table):
+// shared checks, then the fp32 SIMT path or the bf16 tcgen05 path.
+relattn_status_t scalar_bias_fwd(const void *q, const void *k, const void *v, const float *bias,
+                                 int kind, int radius, long long head_stride,
+                                 const relattn::T5Buckets *t5, int causal, float scale,
+                                 const int *kv_len, int B, int H, int n, int d, int dtype,
+                                 void *out, relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, out, B, H, n, d, dtype);
+    if (st != RELATTN_OK) return st;
+    if (!bias || !aligned(bias, 4)) return RELATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    relattn::T5Buckets none{};
+    const relattn::T5Buckets *tb = t5 ? t5 : &none;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == RELATTN_F32) {
+        relattn::SimtArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.causal = causal;
+        a.scale = scale;
+        a.kv_len = kv_len;
+        a.bias = bias;
+        a.bias_kind = kind;
+        a.bias_R = radius;
+        a.bias_hs = head_stride;
+        a.B = B; a.H = H; a.n = n; a.d = d;
+        a.out = static_cast<float *>(out);
+        return from_cuda(relattn::launch_simt_f32(a, tb, s));
+    }
+    relattn::TcArgs a{};
+    a.q = q; a.k = k; a.v = v;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.bias = bias;
+    a.bias_kind = kind;
+    a.bias_R = radius;
+    a.bias_hs = head_stride;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.out = out;
+    a.mode = relattn::kT5;
+    return dispatch_bf16(a, tb, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -262,39 +308,31 @@ relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
                                     int bidirectional, int causal, float scale,
                                     const int *kv_len, int B, int H, int n, int d, int dtype,
                                     void *out, relattn_stream_t stream) {
-    relattn_status_t st = check_qkv(q, k, v, out, B, H, n, d, dtype);
-    if (st != RELATTN_OK) return st;
-    if (!bias || !aligned(bias, 4)) return RELATTN_ERR_INVALID_ARG;
-    if ((causal != 0 && causal != 1) || (bidirectional != 0 && bidirectional != 1))
-        return RELATTN_ERR_INVALID_ARG;
-    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    if (bidirectional != 0 && bidirectional != 1) return RELATTN_ERR_INVALID_ARG;
     relattn::T5Buckets t5{};
     if (!relattn::t5_make_buckets(num_buckets, max_distance, bidirectional, &t5))
         return RELATTN_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dtype == RELATTN_F32) {
-        relattn::SimtArgs a{};
-        a.q = static_cast<const float *>(q);
-        a.k = static_cast<const float *>(k);
-        a.v = static_cast<const float *>(v);
-        a.causal = causal;
-        a.scale = scale;
-        a.kv_len = kv_len;
-        a.bias = bias;
-        a.B = B; a.H = H; a.n = n; a.d = d;
-        a.out = static_cast<float *>(out);
-        return from_cuda(relattn::launch_simt_f32(a, &t5, s));
-    }
-    relattn::TcArgs a{};
-    a.q = q; a.k = k; a.v = v;
-    a.causal = causal;
-    a.scale = scale;
-    a.kv_len = kv_len;
-    a.bias = bias;
-    a.B = B; a.H = H; a.n = n; a.d = d;
-    a.out = out;
-    a.mode = relattn::kT5;
-    return dispatch_bf16(a, &t5, s);
+    return scalar_bias_fwd(q, k, v, bias, relattn::kBiasBuckets, 0, 0, &t5, causal, scale,
+                           kv_len, B, H, n, d, dtype, out, stream);
+}
+
+relattn_status_t relattn_alibi_fwd(const void *q, const void *k, const void *v,
+                                   const float *slopes, int causal, float scale,
+                                   const int *kv_len, int B, int H, int n, int d, int dtype,
+                                   void *out, relattn_stream_t stream) {
+    return scalar_bias_fwd(q, k, v, slopes, relattn::kBiasAlibi, 0, 0, nullptr, causal, scale,
+                           kv_len, B, H, n, d, dtype, out, stream);
+}
+
+relattn_status_t relattn_offset_bias_fwd(const void *q, const void *k, const void *v,
+                                         const float *table, long long table_head_stride,
+                                         int radius, int causal, float scale,
+                                         const int *kv_len, int B, int H, int n, int d,
+                                         int dtype, void *out, relattn_stream_t stream) {
+    if (radius < 0 || radius > (1 << 20)) return RELATTN_ERR_INVALID_ARG;
+    if (table_head_stride != 0 && table_head_stride < 2LL * radius + 1) return RELATTN_ERR_INVALID_ARG;
+    return scalar_bias_fwd(q, k, v, table, relattn::kBiasTable, radius, table_head_stride,
+                           nullptr, causal, scale, kv_len, B, H, n, d, dtype, out, stream);
 }
 
 relattn_status_t relattn_labels(int kind, int clip_k, int num_buckets, int max_distance,

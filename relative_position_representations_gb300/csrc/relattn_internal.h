@@ -24,6 +24,11 @@ struct T5Buckets {
 // invalid parameters. Exact integer arithmetic.
 bool t5_make_buckets(int num_buckets, int max_distance, int bidirectional, T5Buckets *b);
 
+// Scalar bias per relative offset ("Relative position embeddings" page, sections "T5" and
+// "Placement in the taxonomy"): T5 buckets of a [num_buckets, H] table, ALiBi -m_h |delta|
+// from a [H] slope array, or a [H|1, 2R+1] table read at clip(delta, R) + R.
+enum BiasKind : int { kBiasBuckets = 0, kBiasAlibi = 1, kBiasTable = 2 };
+
 // Device status word (one per device), set by bounded waits that run out.
 int *device_error_word();  // device address of the word for the current device, or null
 
@@ -34,10 +39,14 @@ struct SimtArgs {
     int clip_k, causal;
     float scale;
     const int *kv_len;
-    const float *bias;  // T5 [nb, H] or null
+    const float *bias;  // scalar bias (see bias_kind) or null
+    int bias_kind;      // BiasKind
+    int bias_R;         // kBiasTable: the table's clip radius
+    long long bias_hs;  // kBiasTable: elements between heads' rows (0 = one shared row)
     int B, H, n, d;
     float *out;
 };
+// t5 non-null: the scalar-bias variant (bias_kind says which bias; t5 is read for buckets)
 cudaError_t launch_simt_f32(const SimtArgs &a, const T5Buckets *t5, cudaStream_t s);
 
 // ---- label kernel ----------------------------------------------------------------------
@@ -53,10 +62,13 @@ struct TcArgs {
     int clip_k, causal;
     float scale;
     const int *kv_len;
-    const float *bias;
+    const float *bias;  // kT5 mode: the scalar bias of bias_kind
+    int bias_kind;      // BiasKind
+    int bias_R;         // kBiasTable: the table's clip radius
+    long long bias_hs;  // kBiasTable: elements between heads' rows (0 = one shared row)
     int B, H, n, d;
     void *out;
-    int mode;
+    int mode;           // kShaw, or kT5 for every scalar offset bias
 };
 // Returns cudaErrorNotSupported for combinations the kernel does not cover (checked
 // before any launch), cudaErrorInvalidValue for bad tensor-map parameters.

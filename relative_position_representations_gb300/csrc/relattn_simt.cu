@@ -21,8 +21,9 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Shaw (paper summary section 3.4, eqs. 3 and 4) or T5 ("Relative position embeddings",
-// section "T5") forward for one query row per warp.
+// Shaw (paper summary section 3.4, eqs. 3 and 4) or a scalar offset bias ("Relative
+// position embeddings", sections "T5" and "Placement in the taxonomy") forward for one
+// query row per warp.
 template <bool T5>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     simt_f32_kernel(const SimtArgs a, const T5Buckets t5) {
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
             }
         }
         float e = warp_sum(part) * a.scale;
-        if (T5) e += a.bias[(long long)t5_bucket(j - i, t5) * a.H + h];
+        if (T5) e += scalar_bias(a.bias, a.bias_kind, a.H, a.bias_R, a.bias_hs, t5, j - i, h);
         const float m_new = fmaxf(m, e);
         const float corr = expf(m - m_new);  // m = -inf on the first key -> 0
         const float p = expf(e - m_new);

@@ -5,7 +5,10 @@
 //   e_ij = scale * (q_i . k_j + R_i[clip(j-i,k)+k]),    R = Q W^K^T  ([BM x (2k+1)] per tile),
 // and eq. 3 split in two sums,
 //   z_i = sum_j a_ij v_j + sum_r beta_ir w^V_r,   beta_ir = sum_{j: clip(j-i,k)+k = r} a_ij.
-// T5 variant ("Relative position embeddings", section "T5"): e_ij = scale*q_i.k_j + b[bucket].
+// Scalar-bias variant ("Relative position embeddings", sections "T5" and "Placement in the
+// taxonomy"): e_ij = scale*q_i.k_j + b_h(j - i), with b a T5 bucket's table entry, ALiBi's
+// -m_h |j - i|, or a per-offset table clipped at its radius; the kernel reads b from a
+// shared-memory table over the offsets (constant beyond its radius).
 //
 // One persistent CTA per SM. A work item is two query tiles of 128 rows ("slots" 0 and 1):
 // normally two neighbouring tiles of the same head, which then share every K/V tile, or,
@@ -123,8 +126,11 @@ struct Params {
     int kpad_v;         // W rounded up to 16: K of the beta W^V MMA
     int table_heads;    // 1: tables indexed by head, 0: one shared table
     int two_tables;     // the two slots may belong to different heads: own table buffers
-    const float *bias;  // T5 [num_buckets, H]
-    int t5_R;           // T5 offset-table radius (bucket is constant beyond it)
+    const float *bias;  // scalar bias: T5 [num_buckets, H], ALiBi slopes [H] or [H|1, 2R+1]
+    int bias_kind;      // BiasKind
+    int bias_R;         // kBiasTable: the table's clip radius
+    long long bias_hs;  // kBiasTable: head stride of the table (0 = shared)
+    int t5_R;           // offset-table radius (the bias is constant beyond it)
     T5Buckets t5;
     uint32_t off_q[2], off_kv, off_ak[2], off_av[2], off_r[2], off_beta[2], off_t5[2], off_bar;
     // Two ways to feed the slots. Shared: one producer warp, one K/V ring whose entries may
@@ -291,10 +297,10 @@ __device__ __forceinline__ int keys_of(const Params &p, int bh) {
 // items of a wave takes one of the shortest of the next, and group g's waves start rotated
 // by g * (items per group mod gridDim.x), so that the partial last waves of successive groups
 // land on different CTAs. Every role of a CTA walks the same order.
-constexpr int kListCap = 256;
-// Padding of the T5 offset table on each side: a banded chunk of a warp reaches at most 61
+constexpr int kListCap = 256;  // entries of the shared-memory item list (snake order)
+// Padding of the offset-bias table on each side: a banded chunk of a warp reaches at most 61
 // offsets beyond the table's ends (31 rows of the warp + 30 keys of the chunk)
-constexpr int kT5Pad = 64;  // entries of the shared-memory item list (snake order)
+constexpr int kT5Pad = 64;
 
 // The snake order of this CTA, written once by one thread before the roles start (into a
 // list of kListCap entries ending in -1; the host enables the order only when it fits).
@@ -843,7 +849,8 @@ __device__ void softmax_role(const Params &p, const Shared &sh, uint32_t tmem, i
         if (T5 && h != t5_head) {
             if (!(ok = slot_sync(slot, true))) break;  // every row is done with the old table
             for (int idx = stid - kT5Pad; idx <= 2 * p.t5_R + kT5Pad; idx += 128)
-                t5tab[idx] = p.bias[t5_bucket(idx - p.t5_R, p.t5) * p.H + h] * kLog2e;
+                t5tab[idx] = scalar_bias(p.bias, p.bias_kind, p.H, p.bias_R, p.bias_hs, p.t5,
+                                         idx - p.t5_R, h) * kLog2e;
             if (!(ok = slot_sync(slot, true))) break;
             t5_head = h;
         }

@@ -201,9 +201,24 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
     p.table_heads = a.ths != 0 ? 1 : 0;
     p.bias = a.bias;
     if (t5mode) {
-        p.t5 = *t5;
-        p.t5_R = t5->sat;
+        // the shared-memory table covers offsets -t5_R .. t5_R; beyond them the bias is
+        // constant (T5: the saturated buckets; a clipped table: its end entries). ALiBi never
+        // saturates: its table spans every offset of the sequence.
+        p.bias_kind = a.bias_kind;
+        p.bias_R = a.bias_R;
+        p.bias_hs = a.bias_hs;
+        if (a.bias_kind == kBiasBuckets) {
+            if (!t5) return cudaErrorInvalidValue;
+            p.t5 = *t5;
+            p.t5_R = t5->sat;
+        } else if (a.bias_kind == kBiasAlibi) {
+            p.t5_R = a.n - 1;
+        } else {
+            p.t5_R = a.bias_R < a.n - 1 ? a.bias_R : a.n - 1;
+        }
     }
+    // no shared-memory table over 2^17 offsets fits (and 2 * t5_R stays in range)
+    if (t5mode && (p.t5_R < 0 || p.t5_R > (1 << 16))) return cudaErrorNotSupported;
     if (p.BH == 0 || p.n_qtiles == 0) return cudaSuccess;
 
     const DeviceInfo di = device_info();

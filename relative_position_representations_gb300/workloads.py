@@ -11,7 +11,8 @@ embeddings" page, section "T5": 32 buckets, max_distance 128). No dataset is rea
 every value is drawn from a torch CPU generator seeded by the caller.
 
 Draw order (fp32 draws, then a round-to-nearest-even cast to the workload dtype):
-Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. N(0, s^2) means s * randn.
+Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. ALiBi: q, k, v, kv_len (the slopes are
+fixed, not drawn). Clipped offset table: q, k, v, table, kv_len. N(0, s^2) means s * randn.
 """
 from __future__ import annotations
 
@@ -30,8 +31,9 @@ class Workload:
     n: int
     d: int
     dtype: str                      # "bf16" or "f32"
-    kind: str = "shaw"              # "shaw", "t5", "decode" (one decoding step), "bwd" (gradients)
-    clip_k: int = 0
+    kind: str = "shaw"              # "shaw", "t5", "alibi", "offset" (clipped per-offset scalar
+                                    # table), "decode" (one decoding step), "bwd" (gradients)
+    clip_k: int = 0                 # Shaw clip distance; the table radius for "offset"
     causal: bool = False
     key_term: bool = True           # a^K present (Shaw)
     value_term: bool = True         # a^V present (Shaw)
@@ -44,6 +46,7 @@ class Workload:
     max_distance: int = 128
     bidirectional: bool = True
     bias_std: float = 1.0
+    alibi_max_bias: float = 8.0     # ALiBi slopes m_h = 2^(-alibi_max_bias * (h + 1) / H)
 
     @property
     def softmax_scale(self) -> float:
@@ -81,6 +84,17 @@ WORKLOADS = {
 
 ORDER = ["tiny_fp32", "base_encoder", "big_decoder", "long_keyonly", "t5_bias"]
 
+# Scalar offset biases through the T5 form ("Relative position embeddings" page, sections
+# "T5" and "Placement in the taxonomy"), on the T5 case's shape: ALiBi in a causal decoder
+# (q, k, v ~ N(0, 1), 1/sqrt(d)), and a learned per-head scalar per offset clipped at 128
+# (the T5 case's max_distance) in a bidirectional encoder.
+BIAS_WORKLOADS = {
+    "alibi_decoder": Workload("alibi_decoder", B=8, H=12, n=2048, d=64, dtype="bf16",
+                              kind="alibi", causal=True, scale=1.0 / 8),
+    "offset_bias": Workload("offset_bias", B=8, H=12, n=2048, d=64, dtype="bf16",
+                            kind="offset", clip_k=128, scale=1.0 / 8, bias_std=1.0),
+}
+
 # Gradients of the base encoder (kind "bwd"): the forward's inputs plus dout ~ N(0, 1) drawn
 # after them.
 BWD_WORKLOADS = {
@@ -115,6 +129,18 @@ def draw_inputs(w: Workload, seed: int = 0) -> dict:
         out["bias"] = torch.randn((w.num_buckets, w.H), generator=g,
                                   dtype=torch.float32) * w.bias_std
         out["kv_len"] = None
+        return out
+    if w.kind in ("alibi", "offset"):
+        if w.kind == "alibi":
+            out["slopes"] = alibi_slopes(w)
+        else:
+            Ht = 1 if w.shared_tables else w.H
+            out["table"] = torch.randn((Ht, 2 * w.clip_k + 1), generator=g,
+                                       dtype=torch.float32) * w.bias_std
+        out["kv_len"] = None
+        if w.kv_len_range is not None:
+            lo, hi = w.kv_len_range
+            out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
         return out
     W = 2 * w.clip_k + 1
     Ht = 1 if w.shared_tables else w.H
@@ -158,6 +184,12 @@ def draw_decode_inputs(w: Workload, seed: int = 0) -> dict:
     lo, hi = w.kv_len_range if w.kv_len_range is not None else (w.n, w.n)
     out["cache_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
     return out
+
+
+def alibi_slopes(w: Workload) -> torch.Tensor:
+    """The fixed ALiBi slopes, a geometric sequence over the heads: [H] fp32."""
+    return torch.tensor([2.0 ** (-w.alibi_max_bias * (h + 1) / w.H) for h in range(w.H)],
+                        dtype=torch.float32)
 
 
 def table_head_stride(w: Workload) -> int:

@@ -96,3 +96,28 @@ def test_invalid_arguments_rejected_before_any_launch(lib):
                           ctypes.c_void_p(0x200000), None)
     assert bad_t5 == 1                                   # max_distance inside the exact range
     assert lib.raw_call("relattn_labels", 5, 0, 32, 128, 1, 4, 4, FAKE, None) == 1
+
+
+def test_offset_bias_arguments_rejected_before_any_launch(lib):
+    TAB = ctypes.c_void_p(0x300000)
+    OUT = ctypes.c_void_p(0x200000)
+
+    def offs(table=TAB, ths=0, radius=4, causal=0, dtype=0, d=64):
+        return lib.raw_call("relattn_offset_bias_fwd", FAKE, FAKE, FAKE, table,
+                            ctypes.c_longlong(ths), radius, causal, ctypes.c_float(1.0), None,
+                            1, 2, 16, d, dtype, OUT, None)
+
+    def alibi(slopes=TAB, causal=0, d=64):
+        return lib.raw_call("relattn_alibi_fwd", FAKE, FAKE, FAKE, slopes, causal,
+                            ctypes.c_float(1.0), None, 1, 2, 16, d, 0, OUT, None)
+
+    assert offs(radius=-1) == 1
+    assert offs(radius=(1 << 20) + 1) == 1
+    assert offs(ths=5) == 1                               # head stride below 2*radius + 1
+    assert offs(table=None) == 1
+    assert offs(table=ctypes.c_void_p(0x300002)) == 1      # fp32 table: 4-byte alignment
+    assert offs(causal=3) == 1
+    assert offs(d=96) == 2
+    assert alibi(slopes=None) == 1
+    assert alibi(causal=-1) == 1
+    assert alibi(d=32) == 2
