@@ -19,6 +19,10 @@ Pins of the scalar offset biases (ALiBi, the clipped per-offset table) are in
 tests/test_oracle_offset_bias.py: library attention with the bias grid as an additive mask,
 ALiBi as the T5 path with a linear table, the zero-query closed form of the ALiBi weights,
 a hand-computed 2-token sign check of the clipped table, and the softmax's shift invariance.
+Pins of the labelled-edge form (labeled_fwd) are in tests/test_oracle_labeled.py: clip
+labels reproduce the Shaw forward, random labels match the numpy materialised form, a
+2-token hand computation with asymmetric labels, constant-label closed forms, per-sequence
+independence; test_oracle_mutations.py plants a transposed and a batch-blind label read.
 """
 from __future__ import annotations
 
@@ -59,6 +63,11 @@ def _configure(lib):
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, P, ctypes.c_longlong, P, ctypes.c_int]
     lib.oracle_t5bias_rows.restype = ctypes.c_int
+    lib.oracle_labeled_rows.argtypes = [P, P, P, P, P, ctypes.c_longlong, P, ctypes.c_longlong,
+                                        ctypes.c_int, ctypes.c_double, P, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                                        ctypes.c_longlong, P, ctypes.c_int]
+    lib.oracle_labeled_rows.restype = ctypes.c_int
     return lib
 
 
@@ -140,6 +149,48 @@ def t5bias_fwd(q, k, v, bias, num_buckets, max_distance, bidirectional, causal, 
                                     int(bool(causal)), float(scale), _ptr(kvl), B, H, n, d,
                                     _ptr(r), nrows, _ptr(out),
                                     int(nthreads or default_threads()))
+    if rc != 0:
+        raise RuntimeError("oracle thread start failed")
+    return out if rows is not None else out.reshape(B, H, n, d)
+
+
+def labeled_fwd(q, k, v, aK, aV, labels, causal, scale, kv_len=None, table_head_stride=None,
+                rows=None, nthreads=None):
+    """Relation-aware attention over arbitrary labelled edges, fp64 (paper summary page,
+    section "Relation-Aware Self-Attention: The Core Modification", eqs. 3 and 4 with
+    a^K_ij = w^K[L_b[i, j]] and a^V_ij = w^V[L_b[i, j]]).
+
+    labels: uint8 [n, n] (one label matrix for every sequence) or [B, n, n]; every value
+    must index a table row. aK / aV: [H_t, num_labels, d] or None. table_head_stride:
+    elements between heads' tables (default num_labels * d, 0 = shared).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, n, d = q.shape
+    aK, aV = _f64(aK), _f64(aV)
+    lab = np.ascontiguousarray(np.asarray(labels, dtype=np.uint8))
+    if lab.shape == (n, n):
+        lbs = 0
+    elif lab.shape == (B, n, n):
+        lbs = n * n
+    else:
+        raise ValueError("labels must be [n, n] or [B, n, n]")
+    ref = aK if aK is not None else aV
+    if ref is not None:
+        if ref.ndim != 3 or ref.shape[2] != d:
+            raise ValueError("tables must be [H_t, num_labels, d]")
+        if lab.size and int(lab.max()) >= ref.shape[1]:
+            raise ValueError("a label has no table row")
+        if table_head_stride is None:
+            table_head_stride = ref.shape[1] * d
+    else:
+        table_head_stride = 0
+    kvl = None if kv_len is None else np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32))
+    r, nrows = _rows_arg(rows, B, H, n)
+    out = np.zeros((nrows, d), dtype=np.float64)
+    rc = _load().oracle_labeled_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(aK), _ptr(aV),
+                                     int(table_head_stride), _ptr(lab), lbs,
+                                     int(bool(causal)), float(scale), _ptr(kvl), B, H, n, d,
+                                     _ptr(r), nrows, _ptr(out), int(nthreads or default_threads()))
     if rc != 0:
         raise RuntimeError("oracle thread start failed")
     return out if rows is not None else out.reshape(B, H, n, d)

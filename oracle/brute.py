@@ -52,19 +52,28 @@ def _softmax_rows(e, ok):
     return np.where(l > 0, p / np.where(l > 0, l, 1.0), 0.0)
 
 
-def materialised(q, k, v, aK, aV, clip_k, causal, scale, kv_len=None, table_head_stride=None):
+def materialised(q, k, v, aK, aV, clip_k, causal, scale, kv_len=None, table_head_stride=None,
+                 labels=None, num_labels=None):
+    """labels: optional edge labels ([n, n] or [B, n, n]) in place of clip(j - i, k) + k, for
+    tables of num_labels rows (the general labelled graph of the paper summary's section
+    "Relation-Aware Self-Attention: The Core Modification")."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     B, H, n, d = q.shape
-    ths = (2 * clip_k + 1) * d if table_head_stride is None else table_head_stride
-    lab = _labels(n, clip_k)
+    rows = 2 * clip_k + 1 if labels is None else int(num_labels)
+    ths = rows * d if table_head_stride is None else table_head_stride
     out = np.zeros_like(q)
     idx = np.arange(n)
     for b in range(B):
+        if labels is None:
+            lab = _labels(n, clip_k)
+        else:
+            L = np.asarray(labels, dtype=np.int64)
+            lab = L if L.ndim == 2 else L[b]
         valid = n if kv_len is None else min(int(kv_len[b]), n)
         ok = _allowed(n, idx, idx, causal, valid)
         for h in range(H):
-            wK = _tables(aK, h, ths, 2 * clip_k + 1, d)
-            wV = _tables(aV, h, ths, 2 * clip_k + 1, d)
+            wK = _tables(aK, h, ths, rows, d)
+            wV = _tables(aV, h, ths, rows, d)
             AK = wK[lab] if wK is not None else np.zeros((n, n, d))   # [i, j, d]
             AV = wV[lab] if wV is not None else np.zeros((n, n, d))
             keys = k[b, h][None, :, :] + AK                            # k_j + a^K_ij

@@ -21,6 +21,11 @@
  *   maximum; this is the same number as exp(e_ij) / sum exp(e_ik) (the factor exp(-m)
  *   cancels) and only keeps exp() finite.
  *
+ *   Arbitrary labelled edges (paper summary page, section "Relation-Aware Self-Attention:
+ *   The Core Modification": the input is a graph whose edge (i, j) carries a_ij; section
+ *   3.4 then specialises the label to clip(j - i, k) + k): the same two equations with
+ *   a^K_ij = w^K[L[b][i][j]], a^V_ij = w^V[L[b][i][j]] for a given label matrix L.
+ *
  *   T5 scalar bias ("Relative position embeddings" page, section "T5"):
  *     e_ij = scale * q_i . k_j + b[bucket(j - i), h]
  *   The bucket of each offset is computed exactly by oracle/t5.py and handed in as a
@@ -40,6 +45,8 @@ typedef struct {
     const double *aK, *aV;            /* Shaw: [*, 2k+1, d] with head stride ths, or NULL */
     long long ths;                    /* table head stride, in elements (0 = shared) */
     int clip_k;
+    const unsigned char *labels;      /* labelled edges: [*, n, n] or NULL (clip labels) */
+    long long label_bstride;          /* elements between batches' label matrices (0 = shared) */
     const double *bias;               /* T5: [num_buckets, H] */
     const int *bucket_of_offset;      /* T5: [2n - 1], index (j - i) + (n - 1) */
     int causal;
@@ -58,6 +65,13 @@ static long long clip_ll(long long x, long long k) {
     if (x < -k) return -k;
     if (x > k) return k;
     return x;
+}
+
+/* table row of edge (i, j) of sequence b: the given label, else clip(j - i, k) + k */
+static long long edge_label(const job_t *J, long long b, long long i, long long j) {
+    if (J->labels)
+        return (long long)J->labels[b * J->label_bstride + i * (long long)J->n + j];
+    return clip_ll(j - i, J->clip_k) + J->clip_k;
 }
 
 static void one_row(const job_t *J, long long row, double *out_row, double *e, char *ok) {
@@ -85,7 +99,7 @@ static void one_row(const job_t *J, long long row, double *out_row, double *e, c
             const int bucket = J->bucket_of_offset[(j - i) + (n - 1)];
             e[j] = J->scale * s + J->bias[(long long)bucket * H + h];
         } else {
-            const long long r = clip_ll(j - i, J->clip_k) + J->clip_k;
+            const long long r = edge_label(J, b, i, j);
             const double *ak = J->aK ? J->aK + h * J->ths + r * d : NULL;
             for (int c = 0; c < d; ++c) s += qi[c] * (kj[c] + (ak ? ak[c] : 0.0));
             e[j] = J->scale * s;
@@ -104,7 +118,7 @@ static void one_row(const job_t *J, long long row, double *out_row, double *e, c
         const double *vj = J->v + (bh * n + j) * d;
         const double *av = NULL;
         if (!J->t5 && J->aV) {
-            const long long r = clip_ll(j - i, J->clip_k) + J->clip_k;
+            const long long r = edge_label(J, b, i, j);
             av = J->aV + h * J->ths + r * d;
         }
         for (int c = 0; c < d; ++c) out_row[c] += alpha * (vj[c] + (av ? av[c] : 0.0));
@@ -153,6 +167,23 @@ int oracle_relattn_rows(const double *q, const double *k, const double *v,
     memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.aK = aK; J.aV = aV; J.ths = table_head_stride;
     J.clip_k = clip_k; J.causal = causal; J.scale = scale; J.kv_len = kv_len;
+    J.B = B; J.H = H; J.n = n; J.d = d; J.rows = rows; J.nrows = nrows; J.out = out;
+    J.t5 = 0;
+    return run(&J, nthreads);
+}
+
+/* Labelled edges: table rows from labels[b * label_bstride + i * n + j] (values below the
+ * tables' row count; the caller checks). aK / aV may be NULL. */
+int oracle_labeled_rows(const double *q, const double *k, const double *v,
+                        const double *aK, const double *aV, long long table_head_stride,
+                        const unsigned char *labels, long long label_bstride, int causal,
+                        double scale, const int *kv_len, int B, int H, int n, int d,
+                        const long long *rows, long long nrows, double *out, int nthreads) {
+    job_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.aK = aK; J.aV = aV; J.ths = table_head_stride;
+    J.labels = labels; J.label_bstride = label_bstride;
+    J.causal = causal; J.scale = scale; J.kv_len = kv_len;
     J.B = B; J.H = H; J.n = n; J.d = d; J.rows = rows; J.nrows = nrows; J.out = out;
     J.t5 = 0;
     return run(&J, nthreads);

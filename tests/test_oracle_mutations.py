@@ -8,6 +8,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_labeled as labeled
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "relattn_oracle.c")
@@ -17,9 +18,12 @@ MUTANTS = [
     ("offset sign i-j", "clip_ll(j - i, J->clip_k)", "clip_ll(i - j, J->clip_k)"),
     ("key edge dropped", "(kj[c] + (ak ? ak[c] : 0.0))", "(kj[c])"),
     ("value edge dropped", "(vj[c] + (av ? av[c] : 0.0))", "(vj[c])"),
-    ("table order reversed", "const long long r = clip_ll(j - i, J->clip_k) + J->clip_k;\n"
-     "            const double *ak", "const long long r = J->clip_k - clip_ll(j - i, J->clip_k);\n"
-     "            const double *ak"),
+    ("table order reversed", "return clip_ll(j - i, J->clip_k) + J->clip_k;",
+     "return J->clip_k - clip_ll(j - i, J->clip_k);"),
+    ("label matrix transposed", "J->labels[b * J->label_bstride + i * (long long)J->n + j]",
+     "J->labels[b * J->label_bstride + j * (long long)J->n + i]"),
+    ("label batch stride ignored", "J->labels[b * J->label_bstride + i",
+     "J->labels[i"),
     ("key row uses i", "const double *kj = J->k + (bh * n + j) * d;",
      "const double *kj = J->k + (bh * n + i) * d;"),
     ("causal off by one", "(!J->causal || j <= i)", "(!J->causal || j < i)"),
@@ -43,6 +47,9 @@ PIN_TESTS = [
     lambda: [pins.test_t5_constant_bias_per_head_reduces_to_library_attention(c)
              for c in (False, True)],
     lambda: pins.test_t5_bias_equals_shaw_style_materialised_bias(),
+    lambda: labeled.test_two_token_asymmetric_labels_by_hand(),
+    lambda: [labeled.test_random_labels_match_materialised_numpy(c, kv, per_batch)
+             for (c, kv, per_batch) in labeled.RANDOM_CASES],
 ]
 
 
