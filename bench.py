@@ -69,8 +69,9 @@ def algorithmic_flops(w, kv_len) -> float:
     kvs = [None] * w.B if kv_len is None else [int(x) for x in kv_len]
     pairs = sum(pairs_per_sequence(w, kvs[b]) for b in range(w.B)) * w.H
     flops = 4.0 * w.d * pairs
-    if w.kind == "shaw":
-        reach = (w.clip_k + 1) if w.causal else (2 * w.clip_k + 1)
+    if w.kind in ("shaw", "labeled"):
+        reach = (w.num_labels if w.kind == "labeled" else
+                 (w.clip_k + 1) if w.causal else (2 * w.clip_k + 1))
         terms = int(w.key_term) + int(w.value_term)
         flops += 2.0 * w.d * w.n * reach * terms * w.B * w.H
     return flops
@@ -101,6 +102,9 @@ def algorithmic_bytes(w, kv_len) -> float:
         byt += 4 * w.num_buckets * w.H
     elif w.kind == "alibi":  # the slopes
         byt += 4 * w.H
+    elif w.kind == "labeled":  # the tables and the uint8 label matrices
+        byt += es * Ht * w.num_labels * w.d * (int(w.key_term) + int(w.value_term))
+        byt += (w.B if w.labels_per_sequence else 1) * w.n * w.n
     else:  # "offset": the clipped per-offset table
         byt += 4 * Ht * (2 * w.clip_k + 1)
     return float(byt)
@@ -124,11 +128,12 @@ KERNEL_SOURCES = {
               "relattn_tc_kernel.cuh", "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
     "decode": ["relattn_decode.cu"],
     "bwd": ["relattn_bwd.cu"],
+    "labeled": ["device_common.cuh", "relattn_labeled.cu"],
 }
 
 
 def kernel_family(w) -> str:
-    return {"decode": "decode", "bwd": "bwd"}.get(w.kind, "fused")
+    return {"decode": "decode", "bwd": "bwd", "labeled": "labeled"}.get(w.kind, "fused")
 
 
 def kernel_source_hash(family: str = "fused") -> str:
@@ -229,6 +234,8 @@ def workload_by_name(name):
         return wl.BWD_WORKLOADS[name]
     if name in wl.BIAS_WORKLOADS:
         return wl.BIAS_WORKLOADS[name]
+    if name in wl.LABELED_WORKLOADS:
+        return wl.LABELED_WORKLOADS[name]
     return wl.WORKLOADS[name]
 
 
@@ -309,6 +316,12 @@ def oracle_rows_call(w, x, rows, nthreads):
         return oracle.offset_table_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), x["table"].numpy(),
                                        w.clip_k, w.causal, w.softmax_scale, kv_len=kv,
                                        rows=rows, nthreads=nthreads)
+    if w.kind == "labeled":
+        from relative_position_representations_gb300 import workloads as wl
+        return oracle.labeled_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), np_(x["aK"]),
+                                  np_(x["aV"]), x["labels"].numpy(), w.causal, w.softmax_scale,
+                                  kv_len=kv, table_head_stride=wl.table_head_stride(w),
+                                  rows=rows, nthreads=nthreads)
     from relative_position_representations_gb300 import workloads as wl
     return oracle.relattn_fwd(np_(x["q"]), np_(x["k"]), np_(x["v"]), np_(x["aK"]), np_(x["aV"]),
                               w.clip_k, w.causal, w.softmax_scale, kv_len=kv,
@@ -327,6 +340,8 @@ def row_flops(w, kv_len, rows):
     if w.kind == "shaw":
         reach = ((w.clip_k + 1) if w.causal else (2 * w.clip_k + 1)) * (
             int(w.key_term) + int(w.value_term))
+    elif w.kind == "labeled":
+        reach = w.num_labels * (int(w.key_term) + int(w.value_term))
     for r in rows:
         bh, i = divmod(int(r), w.n)
         b = bh // w.H
@@ -404,6 +419,11 @@ def gpu_call(rp, w, g, out, stream):
     if w.kind == "alibi":
         return rp.relattn_alibi_fwd(g["q"], g["k"], g["v"], g["slopes"], w.causal,
                                     w.softmax_scale, kv_len=g["kv_len"], out=out, stream=stream)
+    if w.kind == "labeled":
+        return rp.relattn_labeled_fwd(g["q"], g["k"], g["v"], g["labels"], aK=g["aK"], aV=g["aV"],
+                                      causal=w.causal, scale=w.softmax_scale, kv_len=g["kv_len"],
+                                      out=out, table_head_stride=wl.table_head_stride(w),
+                                      stream=stream)
     if w.kind == "offset":
         return rp.relattn_offset_bias_fwd(g["q"], g["k"], g["v"], g["table"], w.clip_k,
                                           w.causal, w.softmax_scale, kv_len=g["kv_len"],
@@ -446,6 +466,10 @@ def workload_config(w, world: int, l2_note: str) -> dict:
                       "alibi bias (slopes 2^(-%g(h+1)/H))" % w.alibi_max_bias
                       if w.kind == "alibi" else
                       "per-offset scalar bias, radius %d" % w.clip_k if w.kind == "offset" else
+                      "%s with %d labels (uint8 label matrix %s)" % (
+                          "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term)) if on),
+                          w.num_labels, "per sequence" if w.labels_per_sequence else "shared")
+                      if w.kind == "labeled" else
                       "+".join(t for t, on in (("aK", w.key_term), ("aV", w.value_term))
                                if on) or "none"),
             ("cache_len" if w.kind == "decode" else "kv_len"):
@@ -581,8 +605,9 @@ def run_ours(args, rank, world, local_rank):
     e2e = None if args.no_e2e else measure_e2e(rp, w, x, dev, stream, flops, args)
 
     peaks, peak_src = read_peaks()
-    # the gradients run on the SIMT units: their compute roof is the fp32 FMA rate
-    alu = w.kind == "bwd"
+    # the gradients and the labelled edges run on the SIMT units: their compute roof is the
+    # fp32 FMA rate
+    alu = w.kind in ("bwd", "labeled")
     compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
     t_roof_compute = flops / (compute_peak * 1e12)
     t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
@@ -615,7 +640,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(t_max / steps, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        # the arithmetic type: the tensor-core kernels multiply bf16, the SIMT kernels fp32
+        "dtype": "bf16" if (w.dtype == "bf16" and not alu) else "f32", "data": "synthetic",
         "config": workload_config(
             w, world, "inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > "
                       "4 x %.0f MB L2), replayed from a CUDA graph" % (

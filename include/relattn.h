@@ -145,6 +145,36 @@ RELATTN_API relattn_status_t relattn_offset_bias_fwd(const void *q, const void *
                                    int n, int d, int dtype, void *out, relattn_stream_t stream);
 
 /*
+ * relattn_labeled_fwd — relation-aware attention over arbitrary labelled edges (paper
+ * summary page, section "Relation-Aware Self-Attention: The Core Modification": every edge
+ * (i, j) of the input graph carries its own a^K_ij and a^V_ij; section 3.4 specialises the
+ * label to clip(j - i, k) + k, which relattn_fwd computes without a label matrix):
+ *
+ *   e_ij = scale * q_i . (k_j + aK[h][L])
+ *   z_i  = sum_j softmax_j(e)_ij * (v_j + aV[h][L]),     L = labels[b * label_batch_stride + i * n + j]
+ *
+ * masks, empty rows and output as in relattn_fwd.
+ *   aK, aV              tables [*, num_labels, d] of `dtype` (16-byte aligned); NULL drops
+ *                       that term (both NULL: plain attention, labels unused and may be NULL).
+ *   table_head_stride   elements between heads' tables; 0 = shared; else >= num_labels * d
+ *                       and a multiple of 8 (bf16) / 4 (fp32).
+ *   num_labels          1 .. 256.
+ *   labels              uint8 device array of labels, [B|1, n, n] row-major.
+ *   label_batch_stride  elements between sequences' label matrices; 0 = one matrix for
+ *                       every sequence, else >= n * n.
+ * A label >= num_labels is not checked on the host: the kernel reads it as the last table
+ * row and sets the device status word to RELATTN_ERR_INVALID_ARG (relattn_get_device_error).
+ * Runs on the SIMT units with fp32 arithmetic for bf16 and fp32 inputs alike; d <= 128 and a
+ * multiple of 8 (bf16) / 4 (fp32), else RELATTN_ERR_UNSUPPORTED.
+ */
+RELATTN_API relattn_status_t relattn_labeled_fwd(const void *q, const void *k, const void *v,
+                                     const void *aK, const void *aV, long long table_head_stride,
+                                     int num_labels, const unsigned char *labels,
+                                     long long label_batch_stride, int causal, float scale,
+                                     const int *kv_len, int B, int H, int n, int d, int dtype,
+                                     void *out, relattn_stream_t stream);
+
+/*
  * relattn_decode_fwd — one incremental decoding step of a causal decoder: the new token of
  * every sequence attends to its sequence's key/value cache with the relative terms of
  * relattn_fwd (paper summary page, section 3.4, eq. 3 and eq. 4 with clip(j - i, k)).
@@ -265,9 +295,9 @@ RELATTN_API relattn_status_t relattn_t5_thresholds(int num_buckets, int max_dist
 
 /*
  * relattn_get_device_error — synchronises `stream`, then reads and clears the device
- * status word of the current device: RELATTN_OK, or RELATTN_ERR_TIMEOUT if a bounded
- * device wait ran out since the last call. RELATTN_ERR_CUDA if the stream reports an
- * error.
+ * status word of the current device: RELATTN_OK, RELATTN_ERR_TIMEOUT if a bounded
+ * device wait ran out since the last call, or RELATTN_ERR_INVALID_ARG if relattn_labeled_fwd
+ * met a label without a table row. RELATTN_ERR_CUDA if the stream reports an error.
  */
 RELATTN_API relattn_status_t relattn_get_device_error(relattn_stream_t stream);
 

@@ -38,6 +38,10 @@ _lib.relattn_alibi_fwd.restype = _I
 _lib.relattn_offset_bias_fwd.argtypes = [_P, _P, _P, _P, ctypes.c_longlong, _I, _I,
                                          ctypes.c_float, _P, _I, _I, _I, _I, _I, _P, _P]
 _lib.relattn_offset_bias_fwd.restype = _I
+_lib.relattn_labeled_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, _P,
+                                     ctypes.c_longlong, _I, ctypes.c_float, _P, _I, _I, _I, _I,
+                                     _I, _P, _P]
+_lib.relattn_labeled_fwd.restype = _I
 _lib.relattn_decode_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _P,
                                     _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P, _P]
 _lib.relattn_decode_fwd.restype = _I
@@ -63,7 +67,7 @@ _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
 EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
-            "relattn_offset_bias_fwd", "relattn_decode_fwd",
+            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds",
@@ -233,6 +237,52 @@ def relattn_offset_bias_fwd(q, k, v, table, radius, causal=False, scale=None, kv
                                       int(radius), int(bool(causal)), float(scale),
                                       _ptr(kv_len), B, H, n, d, dt, _ptr(out), _stream(stream))
     _check(st, "relattn_offset_bias_fwd")
+    return out
+
+
+def relattn_labeled_fwd(q, k, v, labels, aK=None, aV=None, causal=False, scale=None,
+                        kv_len=None, out=None, table_head_stride=None, stream=None):
+    """Relation-aware attention over labelled edges: the table rows of edge (i, j) are picked
+    by labels[b, i, j] (paper summary, "Relation-Aware Self-Attention: The Core
+    Modification").
+
+    labels: uint8 CUDA tensor [n, n] (shared by every sequence) or [B, n, n]. aK / aV:
+    [H or 1, num_labels, d] of q's dtype, or None. scale defaults to 1/sqrt(d). Returns out.
+    """
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    ref = aK if aK is not None else aV
+    num_labels = 0
+    lbs = 0
+    if ref is not None:
+        for t, nm in ((aK, "aK"), (aV, "aV")):
+            _dev(t, nm, q.dtype)
+        if ref.dim() != 3 or ref.shape[2] != d:
+            raise ValueError("tables must be [H or 1, num_labels, d]")
+        num_labels = int(ref.shape[1])
+        if table_head_stride is None:
+            table_head_stride = 0 if (ref.shape[0] == 1 and H > 1) else num_labels * d
+        _dev(labels, "labels", torch.uint8)
+        if labels.shape == (n, n):
+            lbs = 0
+        elif labels.shape == (B, n, n):
+            lbs = n * n
+        else:
+            raise ValueError("labels must be [n, n] or [B, n, n]")
+    else:
+        table_head_stride = 0
+    _dev(kv_len, "kv_len", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_labeled_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(aK), _ptr(aV),
+                                  int(table_head_stride), num_labels,
+                                  _ptr(labels) if ref is not None else None, int(lbs),
+                                  int(bool(causal)), float(scale), _ptr(kv_len), B, H, n, d, dt,
+                                  _ptr(out), _stream(stream))
+    _check(st, "relattn_labeled_fwd")
     return out
 
 

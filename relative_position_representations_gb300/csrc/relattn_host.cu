@@ -245,6 +245,52 @@ relattn_status_t relattn_decode_fwd(const void *q, const void *k_cache, const vo
     return from_cuda(relattn::launch_decode_bf16(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+relattn_status_t relattn_labeled_fwd(const void *q, const void *k, const void *v,
+                                     const void *aK, const void *aV, long long table_head_stride,
+                                     int num_labels, const unsigned char *labels,
+                                     long long label_batch_stride, int causal, float scale,
+                                     const int *kv_len, int B, int H, int n, int d, int dtype,
+                                     void *out, relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, out, B, H, n, d, dtype);
+    // this path takes any head dimension up to 128 whose rows are whole 16-byte vectors
+    if (st != RELATTN_OK && st != RELATTN_ERR_UNSUPPORTED) return st;
+    if (!shapes_ok(B, H, n, d)) return RELATTN_ERR_INVALID_ARG;
+    const int vec = dtype == RELATTN_BF16 ? 8 : 4;
+    if (d > 128 || d % vec != 0) return RELATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return RELATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    if (aK || aV) {
+        if (num_labels < 1 || num_labels > 256 || !labels) return RELATTN_ERR_INVALID_ARG;
+        if ((aK && !aligned(aK, 16)) || (aV && !aligned(aV, 16))) return RELATTN_ERR_INVALID_ARG;
+        if (table_head_stride != 0 &&
+            (table_head_stride < (long long)num_labels * d || table_head_stride % vec != 0))
+            return RELATTN_ERR_INVALID_ARG;
+        if (label_batch_stride != 0 && label_batch_stride < (long long)n * n)
+            return RELATTN_ERR_INVALID_ARG;
+    }
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    int *err = status_word_for_current_device();
+    if (!err) return RELATTN_ERR_CUDA;
+    relattn::LabeledArgs a{};
+    a.q = q; a.k = k; a.v = v; a.aK = aK; a.aV = aV;
+    a.ths = table_head_stride;
+    a.num_labels = (aK || aV) ? num_labels : 0;
+    a.labels = labels;
+    a.lbs = label_batch_stride;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
+    a.out = out;
+    a.err = err;
+    return from_cuda(relattn::launch_labeled(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
                                             const void *v_cache, const void *aK, const void *aV,
                                             long long table_head_stride, int clip_k, float scale,

@@ -93,6 +93,26 @@ unsigned long long decode_workspace_bytes(int B, int H, int T, int d);
 // enough workspace the single-pass kernel runs
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 
+// ---- labelled edges (SIMT, fp32 arithmetic) ----------------------------------------------
+constexpr int kMaxLabels = 256;      // uint8 labels
+constexpr int kLabelOutOfRange = 1;  // device status word value (RELATTN_ERR_INVALID_ARG)
+struct LabeledArgs {
+    const void *q, *k, *v, *aK, *aV;
+    long long ths;            // elements between heads' tables (0 = shared)
+    int num_labels;           // table rows
+    const uint8_t *labels;    // [*, n, n]
+    long long lbs;            // elements between sequences' label matrices (0 = shared)
+    int causal;
+    float scale;
+    const int *kv_len;
+    int B, H, n, d;
+    int bf16;                 // 1: q, k, v, tables and out are bf16; 0: fp32
+    void *out;
+    int *err;                 // device status word (a label without a table row)
+};
+// cudaErrorNotSupported when d > 128 or more than 256 labels
+cudaError_t launch_labeled(const LabeledArgs &a, cudaStream_t s);
+
 // ---- gradients (SIMT, fp32 arithmetic) ---------------------------------------------------
 struct BwdArgs {
     const void *q, *k, *v, *aK, *aV, *dout;

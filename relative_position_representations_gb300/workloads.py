@@ -12,7 +12,8 @@ every value is drawn from a torch CPU generator seeded by the caller.
 
 Draw order (fp32 draws, then a round-to-nearest-even cast to the workload dtype):
 Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. ALiBi: q, k, v, kv_len (the slopes are
-fixed, not drawn). Clipped offset table: q, k, v, table, kv_len. N(0, s^2) means s * randn.
+fixed, not drawn). Clipped offset table: q, k, v, table, kv_len. Labelled edges: q, k, v, a^K, a^V (num_labels
+rows), labels ~ U{0..num_labels-1} per pair (uint8), kv_len. N(0, s^2) means s * randn.
 """
 from __future__ import annotations
 
@@ -32,7 +33,8 @@ class Workload:
     d: int
     dtype: str                      # "bf16" or "f32"
     kind: str = "shaw"              # "shaw", "t5", "alibi", "offset" (clipped per-offset scalar
-                                    # table), "decode" (one decoding step), "bwd" (gradients)
+                                    # table), "labeled" (label matrix), "decode" (one decoding
+                                    # step), "bwd" (gradients)
     clip_k: int = 0                 # Shaw clip distance; the table radius for "offset"
     causal: bool = False
     key_term: bool = True           # a^K present (Shaw)
@@ -47,6 +49,8 @@ class Workload:
     bidirectional: bool = True
     bias_std: float = 1.0
     alibi_max_bias: float = 8.0     # ALiBi slopes m_h = 2^(-alibi_max_bias * (h + 1) / H)
+    num_labels: int = 16            # "labeled": table rows (labels are uint8)
+    labels_per_sequence: bool = True  # "labeled": one label matrix per sequence, else shared
 
     @property
     def softmax_scale(self) -> float:
@@ -93,6 +97,14 @@ BIAS_WORKLOADS = {
                               kind="alibi", causal=True, scale=1.0 / 8),
     "offset_bias": Workload("offset_bias", B=8, H=12, n=2048, d=64, dtype="bf16",
                             kind="offset", clip_k=128, scale=1.0 / 8, bias_std=1.0),
+}
+
+# Labelled edges (paper summary, "Relation-Aware Self-Attention: The Core Modification"): a
+# random graph with 16 edge types over 512 tokens per sequence, Transformer-base heads.
+LABELED_WORKLOADS = {
+    "labeled_graph": Workload("labeled_graph", B=16, H=8, n=512, d=64, dtype="bf16",
+                              kind="labeled", num_labels=16, table_std=0.02, scale=1.0 / 8,
+                              kv_len_range=(256, 512)),
 }
 
 # Gradients of the base encoder (kind "bwd"): the forward's inputs plus dout ~ N(0, 1) drawn
@@ -142,10 +154,14 @@ def draw_inputs(w: Workload, seed: int = 0) -> dict:
             lo, hi = w.kv_len_range
             out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
         return out
-    W = 2 * w.clip_k + 1
+    W = w.num_labels if w.kind == "labeled" else 2 * w.clip_k + 1
     Ht = 1 if w.shared_tables else w.H
     out["aK"] = normal((Ht, W, w.d), w.table_std) if w.key_term else None
     out["aV"] = normal((Ht, W, w.d), w.table_std) if w.value_term else None
+    if w.kind == "labeled":
+        shape_l = (w.B, w.n, w.n) if w.labels_per_sequence else (w.n, w.n)
+        out["labels"] = torch.randint(0, w.num_labels, shape_l, generator=g,
+                                      dtype=torch.int32).to(torch.uint8)
     if w.kv_len_range is not None:
         lo, hi = w.kv_len_range
         out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
@@ -193,4 +209,5 @@ def alibi_slopes(w: Workload) -> torch.Tensor:
 
 
 def table_head_stride(w: Workload) -> int:
-    return 0 if w.shared_tables else (2 * w.clip_k + 1) * w.d
+    rows = w.num_labels if w.kind == "labeled" else 2 * w.clip_k + 1
+    return 0 if w.shared_tables else rows * w.d

@@ -121,3 +121,26 @@ def test_offset_bias_arguments_rejected_before_any_launch(lib):
     assert alibi(slopes=None) == 1
     assert alibi(causal=-1) == 1
     assert alibi(d=32) == 2
+
+
+def test_labeled_arguments_rejected_before_any_launch(lib):
+    TAB = ctypes.c_void_p(0x300000)
+    LAB = ctypes.c_void_p(0x400000)
+    OUT = ctypes.c_void_p(0x200000)
+
+    def lab(aK=TAB, aV=None, ths=0, L=8, labels=LAB, lbs=0, causal=0, n=16, d=64, dtype=0):
+        return lib.raw_call("relattn_labeled_fwd", FAKE, FAKE, FAKE, aK, aV,
+                            ctypes.c_longlong(ths), L, labels, ctypes.c_longlong(lbs), causal,
+                            ctypes.c_float(1.0), None, 1, 2, n, d, dtype, OUT, None)
+
+    assert lab(L=0) == 1
+    assert lab(L=257) == 1
+    assert lab(labels=None) == 1
+    assert lab(lbs=100) == 1                       # below n * n
+    assert lab(ths=8 * 64 - 8) == 1                # below num_labels * d
+    assert lab(ths=8 * 64 + 4) == 1                # bf16 rows: a multiple of 8 elements
+    assert lab(aK=ctypes.c_void_p(0x300008)) == 1  # tables 16-byte aligned
+    assert lab(causal=2) == 1
+    assert lab(d=36) == 2                          # bf16: d a multiple of 8
+    assert lab(d=136) == 2
+    assert lab(dtype=1, d=130) == 2
