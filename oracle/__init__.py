@@ -23,6 +23,8 @@ Pins of the labelled-edge form (labeled_fwd) are in tests/test_oracle_labeled.py
 labels reproduce the Shaw forward, random labels match the numpy materialised form, a
 2-token hand computation with asymmetric labels, constant-label closed forms, per-sequence
 independence; test_oracle_mutations.py plants a transposed and a batch-blind label read.
+oracle/txl.py states the Transformer-XL four-term score (pinned in tests/test_oracle_txl.py
+against library attention, the Shaw loop with an unclipped table, and the offset-bias loop).
 """
 from __future__ import annotations
 
