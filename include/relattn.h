@@ -5,7 +5,10 @@
  * Representations" (paper summary page, section 3.4: eq. 3 for the output, eq. 4 for the
  * compatibility, clip(j - i, k) and the 2k+1 edge vectors w_{-k}..w_{k}; section
  * "Efficient Implementation" for the eq. 5 split). T5 variant: "Relative position
- * embeddings" page, section "T5".
+ * embeddings" page, section "T5"; ALiBi and the per-offset scalar table: the same page,
+ * sections "Placement in the taxonomy" and "Two-dimensional variants". Labelled edges: the
+ * paper summary's section "Relation-Aware Self-Attention: The Core Modification". Also a
+ * decode step against a key/value cache and the gradients of relattn_fwd.
  *
  * Conventions shared by every entry point
  *   - Tensors q, k, v, out are [B, H, n, d], contiguous, d fastest (row-major).

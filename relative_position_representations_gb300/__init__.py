@@ -1,4 +1,5 @@
-"""relation-aware self-attention forward on GB300 (sm_103a).
+"""relation-aware self-attention on GB300 (sm_103a): the Shaw forward, T5 / ALiBi /
+per-offset scalar biases, labelled edges, a decode step and the Shaw gradients.
 
 The compute lives in librelattn.so (C ABI, include/relattn.h); this package holds its
 ctypes binding (`_lib`), the in-tree build script (`build`) and the named workloads with
