@@ -139,3 +139,72 @@ def test_t5_bias_gradient_sums_to_zero_per_head():
     _, _, _, db = backward.t5bias_bwd(q, kk, v, bias, dz, 32, 16, True, True, 1.0)
     np.testing.assert_allclose(db.sum(axis=0), np.zeros(H), atol=1e-12)
     assert float(np.abs(db).max()) > 1e-3  # not trivially zero
+
+
+@pytest.mark.parametrize("causal,kvl,per_seq", [(False, None, True), (True, None, False),
+                                                (False, [3, 8], True)])
+def test_labeled_gradients_match_finite_differences(causal, kvl, per_seq):
+    rng = np.random.default_rng(21)
+    B, H, n, d, L = 2, 2, 8, 3, 5
+    q, kk, v, dz = (rng.standard_normal((B, H, n, d)) for _ in range(4))
+    aK = rng.standard_normal((H, L, d)) * 0.7
+    aV = rng.standard_normal((H, L, d)) * 0.7
+    lab = rng.integers(0, L, size=(B, n, n) if per_seq else (n, n)).astype(np.uint8)
+    kv = None if kvl is None else np.asarray(kvl, dtype=np.int32)
+
+    def fwd():
+        return oracle.labeled_fwd(q, kk, v, aK, aV, lab, causal, 0.8, kv_len=kv, nthreads=1)
+
+    dq, dk, dv, daK, daV = backward.labeled_bwd(q, kk, v, aK, aV, dz, lab, causal, 0.8,
+                                                kv_len=kv)
+    _close(dq, _fd(fwd, q, dz))
+    _close(dk, _fd(fwd, kk, dz))
+    _close(dv, _fd(fwd, v, dz))
+    _close(daK, _fd(fwd, aK, dz))
+    _close(daV, _fd(fwd, aV, dz))
+
+
+def test_labeled_gradients_with_clip_labels_are_the_shaw_gradients():
+    rng = np.random.default_rng(22)
+    B, H, n, d, k = 2, 2, 9, 4, 2
+    q, kk, v, dz = (rng.standard_normal((B, H, n, d)) for _ in range(4))
+    aK = rng.standard_normal((H, 2 * k + 1, d))
+    aV = rng.standard_normal((H, 2 * k + 1, d))
+    lab = oracle.clip_labels(n, n, k)
+    got = backward.labeled_bwd(q, kk, v, aK, aV, dz, lab, True, 0.5)
+    ref = backward.relattn_bwd(q, kk, v, aK, aV, dz, k, True, 0.5)
+    for a, b in zip(got, ref):
+        np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("R,shared,causal", [(2, False, False), (0, True, True), (20, False, True)])
+def test_offset_table_gradients_match_finite_differences(R, shared, causal):
+    rng = np.random.default_rng(23)
+    B, H, n, d = 2, 2, 7, 3
+    q, kk, v, dz = (rng.standard_normal((B, H, n, d)) for _ in range(4))
+    table = rng.standard_normal((1 if shared else H, 2 * R + 1))
+
+    def fwd():
+        return oracle.offset_table_fwd(q, kk, v, table, R, causal, 0.6, nthreads=1)
+
+    dq, dk, dv, dt = backward.offset_table_bwd(q, kk, v, table, R, dz, causal, 0.6)
+    _close(dq, _fd(fwd, q, dz))
+    _close(dk, _fd(fwd, kk, dz))
+    _close(dv, _fd(fwd, v, dz))
+    _close(dt, _fd(fwd, table, dz))
+
+
+def test_alibi_gradients_match_finite_differences():
+    rng = np.random.default_rng(24)
+    B, H, n, d = 2, 2, 8, 3
+    q, kk, v, dz = (rng.standard_normal((B, H, n, d)) for _ in range(4))
+    slopes = np.array([0.5, 0.125])
+
+    def fwd():
+        return oracle.alibi_fwd(q, kk, v, slopes, False, 0.7, kv_len=[8, 5], nthreads=1)
+
+    dq, dk, dv, dm = backward.alibi_slope_bwd(q, kk, v, slopes, dz, False, 0.7, kv_len=[8, 5])
+    _close(dq, _fd(fwd, q, dz))
+    _close(dk, _fd(fwd, kk, dz))
+    _close(dv, _fd(fwd, v, dz))
+    _close(dm, _fd(fwd, slopes, dz))
