@@ -7,7 +7,7 @@
  * "Efficient Implementation" for the eq. 5 split). T5 variant: "Relative position
  * embeddings" page, section "T5"; ALiBi and the per-offset scalar table: the same page,
  * sections "Placement in the taxonomy" and "Two-dimensional variants". Labelled edges: the
- * paper summary's section "Relation-Aware Self-Attention: The Core Modification". Also a
+ * section "Relation-Aware Self-Attention: The Core Modification" of the same page. Also a
  * decode step against a key/value cache and the gradients of relattn_fwd.
  *
  * Conventions shared by every entry point
@@ -180,7 +180,7 @@ RELATTN_API relattn_status_t relattn_labeled_fwd(const void *q, const void *k, c
 /*
  * relattn_decode_fwd — one incremental decoding step of a causal decoder: the new token of
  * every sequence attends to its sequence's key/value cache with the relative terms of
- * relattn_fwd (paper summary page, section 3.4, eq. 3 and eq. 4 with clip(j - i, k)).
+ * relattn_fwd ("Self-Attention with Relative Position Representations" page, section 3.4, eq. 3 and eq. 4 with clip(j - i, k)).
  * With t = cache_len[b] - 1, the new token's position (its own key and value are already
  * the cache's row t):
  *
@@ -241,7 +241,7 @@ RELATTN_API relattn_status_t relattn_decode_workspace_size(int B, int H, int T, 
 
 /*
  * relattn_bwd — gradients of relattn_fwd (Shaw relation-aware attention) for training. The
- * pages state only the forward pass (paper summary page, section 3.4, eq. 3 and eq. 4);
+ * pages state only the forward pass ("Self-Attention with Relative Position Representations" page, section 3.4, eq. 3 and eq. 4);
  * these are the chain rule through it:
  *
  *   dp_ij = dz_i . (v_j + aV_r),  de_ij = p_ij (dp_ij - sum_j' p_ij' dp_ij'),
@@ -280,7 +280,7 @@ RELATTN_API relattn_status_t relattn_bwd_workspace_size(int B, int H, int n, int
 /*
  * relattn_labels — the integer edge label of every (i, j), computed by the same device
  * functions the attention kernels use, written as int32 labels[i * n_k + j].
- *   kind 0: clip row clip(j - i, clip_k) + clip_k (paper summary, section 3.4).
+ *   kind 0: clip row clip(j - i, clip_k) + clip_k ("Self-Attention with Relative Position Representations" page, section 3.4).
  *   kind 1: T5 bucket(j - i) with (num_buckets, max_distance, bidirectional).
  * labels is caller-owned device memory of n_q * n_k int32.
  */

@@ -106,7 +106,7 @@ def _rows_arg(rows, B, H, n):
 
 
 def clip(x, k):
-    """clip(x, k) = max(-k, min(k, x)) (paper summary, "Relative Position Representations")."""
+    """clip(x, k) = max(-k, min(k, x)) ("Self-Attention with Relative Position Representations" page, section "Relative Position Representations")."""
     return max(-k, min(k, x))
 
 
@@ -158,7 +158,7 @@ def t5bias_fwd(q, k, v, bias, num_buckets, max_distance, bidirectional, causal, 
 
 def labeled_fwd(q, k, v, aK, aV, labels, causal, scale, kv_len=None, table_head_stride=None,
                 rows=None, nthreads=None):
-    """Relation-aware attention over arbitrary labelled edges, fp64 (paper summary page,
+    """Relation-aware attention over arbitrary labelled edges, fp64 ("Self-Attention with Relative Position Representations" page,
     section "Relation-Aware Self-Attention: The Core Modification", eqs. 3 and 4 with
     a^K_ij = w^K[L_b[i, j]] and a^V_ij = w^V[L_b[i, j]]).
 

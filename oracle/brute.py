@@ -2,7 +2,7 @@
 
 TEST INFRASTRUCTURE ONLY (same rule as the rest of oracle/).
 
-materialised(): the naive form the paper summary calls prohibitive ("Efficient
+materialised(): the naive form the "Self-Attention with Relative Position Representations" page calls prohibitive ("Efficient
 Implementation: How the Method Scales", opening paragraph): build the n x n x d edge
 tensors a^K_ij = w^K[clip(j-i,k)+k] and a^V_ij = w^V[clip(j-i,k)+k] explicitly, add them
 to the keys and values, and apply eq. 4, the softmax and eq. 3 as written.
@@ -55,7 +55,7 @@ def _softmax_rows(e, ok):
 def materialised(q, k, v, aK, aV, clip_k, causal, scale, kv_len=None, table_head_stride=None,
                  labels=None, num_labels=None):
     """labels: optional edge labels ([n, n] or [B, n, n]) in place of clip(j - i, k) + k, for
-    tables of num_labels rows (the general labelled graph of the paper summary's section
+    tables of num_labels rows (the general labelled graph of the "Self-Attention with Relative Position Representations" page, section
     "Relation-Aware Self-Attention: The Core Modification")."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     B, H, n, d = q.shape

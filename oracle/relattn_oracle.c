@@ -21,7 +21,7 @@
  *   maximum; this is the same number as exp(e_ij) / sum exp(e_ik) (the factor exp(-m)
  *   cancels) and only keeps exp() finite.
  *
- *   Arbitrary labelled edges (paper summary page, section "Relation-Aware Self-Attention:
+ *   Arbitrary labelled edges (the same page, section "Relation-Aware Self-Attention:
  *   The Core Modification": the input is a graph whose edge (i, j) carries a_ij; section
  *   3.4 then specialises the label to clip(j - i, k) + k): the same two equations with
  *   a^K_ij = w^K[L[b][i][j]], a^V_ij = w^V[L[b][i][j]] for a given label matrix L.

@@ -133,7 +133,8 @@ def _qkv(q, k, v):
 
 def relattn_fwd(q, k, v, aK=None, aV=None, clip_k=0, causal=False, scale=None, kv_len=None,
                 out=None, table_head_stride=None, stream=None):
-    """Shaw relation-aware attention forward (paper summary page, section 3.4, eqs. 3-4).
+    """Shaw relation-aware attention forward ("Self-Attention with Relative Position Representations"
+    page, section 3.4, eqs. 3-4).
 
     q, k, v: [B, H, n, d] bf16 or fp32 CUDA tensors. aK / aV: [H or 1, 2*clip_k+1, d]
     (None drops the term). kv_len: [B] int32 CUDA tensor or None. Returns out.
@@ -243,8 +244,8 @@ def relattn_offset_bias_fwd(q, k, v, table, radius, causal=False, scale=None, kv
 def relattn_labeled_fwd(q, k, v, labels, aK=None, aV=None, causal=False, scale=None,
                         kv_len=None, out=None, table_head_stride=None, stream=None):
     """Relation-aware attention over labelled edges: the table rows of edge (i, j) are picked
-    by labels[b, i, j] (paper summary, "Relation-Aware Self-Attention: The Core
-    Modification").
+    by labels[b, i, j] ("Self-Attention with Relative Position Representations" page, section
+    "Relation-Aware Self-Attention: The Core Modification").
 
     labels: uint8 CUDA tensor [n, n] (shared by every sequence) or [B, n, n]. aK / aV:
     [H or 1, num_labels, d] of q's dtype, or None. scale defaults to 1/sqrt(d). Returns out.
@@ -367,7 +368,8 @@ def relattn_decode_workspace_size(B, H, T, d) -> int:
 def relattn_decode_fwd(q, k_cache, v_cache, cache_len, aK=None, aV=None, clip_k=0, scale=None,
                        out=None, table_head_stride=None, workspace=None, stream=None):
     """One causal decoding step with relative terms: row cache_len[b] - 1 of the causal
-    forward over each sequence's cache (paper summary page, section 3.4, eqs. 3-4).
+    forward over each sequence's cache ("Self-Attention with Relative Position Representations"
+    page, section 3.4, eqs. 3-4).
 
     q: [B, H, d] bf16; k_cache, v_cache: [B, H, T, d] bf16; cache_len: [B] int32 (the new
     token's key and value already in row cache_len[b] - 1). aK / aV: [H or 1, 2*clip_k+1, d]

@@ -1,7 +1,8 @@
 // Gradients of the Shaw relation-aware attention forward: dq, dk, dv, dw^K, dw^V.
 //
-// The pages give only the forward pass (paper summary page, section 3.4: eq. 3, eq. 4 and
-// the softmax). The gradients are the chain rule through it:
+// The pages give only the forward pass ("Self-Attention with Relative Position
+// Representations" page, section 3.4: eq. 3, eq. 4 and the softmax). The gradients are the
+// chain rule through it:
 //   dp_ij = dz_i . (v_j + w^V_r),  de_ij = p_ij (dp_ij - D_i),  D_i = sum_j p_ij dp_ij,
 //   dq_i = scale sum_j de_ij (k_j + w^K_r),  dk_j = scale sum_i de_ij q_i,
 //   dv_j = sum_i p_ij dz_i,  dw^K_r = scale sum_{r_ij = r} de_ij q_i,

@@ -1,7 +1,8 @@
-// Relation-aware attention over arbitrary labelled edges (paper summary page, section
-// "Relation-Aware Self-Attention: The Core Modification": every edge (i, j) of the input
-// graph carries its own a^K_ij, a^V_ij; here they are rows of two tables picked by a label
-// matrix, the general form that section 3.4 specialises to clip(j - i, k) + k):
+// Relation-aware attention over arbitrary labelled edges ("Self-Attention with Relative
+// Position Representations" page, section "Relation-Aware Self-Attention: The Core
+// Modification": every edge (i, j) of the input graph carries its own a^K_ij, a^V_ij; here
+// they are rows of two tables picked by a label matrix, the general form that section 3.4
+// specialises to clip(j - i, k) + k):
 //
 //   e_ij = scale * q_i . (k_j + w^K[L_b[i, j]])         (eq. 4)
 //   z_i  = sum_j softmax_j(e)_ij * (v_j + w^V[L_b[i, j]]) (eq. 3)

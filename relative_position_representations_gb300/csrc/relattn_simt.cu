@@ -21,9 +21,9 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Shaw (paper summary section 3.4, eqs. 3 and 4) or a scalar offset bias ("Relative
-// position embeddings", sections "T5" and "Placement in the taxonomy") forward for one
-// query row per warp.
+// Shaw ("Self-Attention with Relative Position Representations" page, section 3.4, eqs. 3
+// and 4) or a scalar offset bias ("Relative position embeddings", sections "T5" and
+// "Placement in the taxonomy") forward for one query row per warp.
 template <bool T5>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     simt_f32_kernel(const SimtArgs a, const T5Buckets t5) {

@@ -4,16 +4,17 @@ This module holds shapes, distributions and random draws only: none of the atten
 arithmetic. Both the CUDA path (through bench.py and the GPU tests) and the CPU oracle are
 fed from here, so the two see bit-identical inputs.
 
-Shapes follow the translation Transformer configurations on the paper summary page
-(section 5, "Evaluation Methodology": base d_z = 64 with 8 heads and clip k = 16,
-big d_z = 64 with 16 heads), plus a long-sequence key-only case and the T5 bias case ("Relative position
-embeddings" page, section "T5": 32 buckets, max_distance 128). No dataset is read:
+Shapes follow the translation Transformer configurations on the "Self-Attention with
+Relative Position Representations" page (section 5, "Evaluation Methodology": base d_z = 64
+with 8 heads and clip k = 16, big d_z = 64 with 16 heads), plus a long-sequence key-only
+case and the T5 bias case ("Relative position embeddings" page, section "T5": 32 buckets,
+max_distance 128). No dataset is read:
 every value is drawn from a torch CPU generator seeded by the caller.
 
 Draw order (fp32 draws, then a round-to-nearest-even cast to the workload dtype):
 Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. ALiBi: q, k, v, kv_len (the slopes are
-fixed, not drawn). Clipped offset table: q, k, v, table, kv_len. Labelled edges: q, k, v, a^K, a^V (num_labels
-rows), labels ~ U{0..num_labels-1} per pair (uint8), kv_len. N(0, s^2) means s * randn.
+fixed, not drawn). Clipped offset table: q, k, v, table, kv_len. Labelled edges: q, k, v,
+a^K, a^V (num_labels rows), labels ~ U{0..num_labels-1} per pair (uint8), kv_len. N(0, s^2) means s * randn.
 """
 from __future__ import annotations
 
@@ -99,7 +100,8 @@ BIAS_WORKLOADS = {
                             kind="offset", clip_k=128, scale=1.0 / 8, bias_std=1.0),
 }
 
-# Labelled edges (paper summary, "Relation-Aware Self-Attention: The Core Modification"): a
+# Labelled edges ("Self-Attention with Relative Position Representations" page, section
+# "Relation-Aware Self-Attention: The Core Modification"): a
 # random graph with 16 edge types over 512 tokens per sequence, Transformer-base heads.
 LABELED_WORKLOADS = {
     "labeled_graph": Workload("labeled_graph", B=16, H=8, n=512, d=64, dtype="bf16",

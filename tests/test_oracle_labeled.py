@@ -1,8 +1,9 @@
 """Pins for the labelled-edge oracle (oracle.labeled_fwd).
 
-The paper summary's general form ("Relation-Aware Self-Attention: The Core Modification")
-gives every edge (i, j) of an input graph its own a_ij; its section 3.4 specialises the
-edge to a table row picked by clip(j - i, k). With an explicit label matrix L the rows are
+The general form on the "Self-Attention with Relative Position Representations" page
+(section "Relation-Aware Self-Attention: The Core Modification") gives every edge (i, j) of
+an input graph its own a_ij; its section 3.4 specialises the edge to a table row picked by
+clip(j - i, k). With an explicit label matrix L the rows are
 w[L_b[i, j]]. What fixes the expected values:
   * L = clip(j - i, k) + k reproduces the Shaw forward (pinned on its own in
     test_oracle_pins.py);
