@@ -2,15 +2,18 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step is one forward pass over one batch of the named workload (default: the
-Transformer-base encoder shape, B=64 H=8 n=128 d=64 k=16 bf16 with per-sequence key
-padding): a single kernel launch through the C ABI. Inputs are seeded and synthetic
-(workloads.py) and resident in HBM; to keep L2 (126 MB) from serving them, the timed
-steps rotate over enough input sets to exceed 4x L2 and are replayed from a CUDA graph
-(the kernel is a few microseconds long, so host launch overhead would otherwise dominate).
+One step is one forward pass over one batch of the named workload (default: the long
+key-only causal case, B=4 H=16 n=4096 d=128 k=64 bf16, the largest configuration): a single
+kernel launch through the C ABI. Inputs are seeded and synthetic (workloads.py) and
+resident in HBM; to keep L2 from serving them, the timed steps rotate over enough input
+sets to exceed 4x L2, and exactly --steps launches are replayed from one CUDA graph (the
+short workloads are a few microseconds long, so host launch overhead would otherwise
+dominate). The other forward configurations (--also) are timed the same way in the same
+run and reported as compact lines under "workloads".
 
 Printed (rank 0, one JSON line): the whole-job TFLOP/s over the timed steps; the per-launch
-kernel time measured with CUDA events on the launching stream and its roofline fraction;
+kernel time measured with CUDA events on the launching stream (mean, p10, p90, and for the
+HBM-bound workloads a single launch after an L2 flush) and its roofline fraction;
 an end-to-end number through the same C ABI with host (pinned) buffers and the
 host<->device copies inside the timed region; the fp64 CPU oracle timed on a bounded
 sample of the same workload; SM clocks sampled while the timed region runs.
@@ -37,7 +40,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = ("fused rel-attn fwd TFLOP/s (bf16) and % of GB300 tensor/HBM roofline vs CPU oracle")
-DEFAULT_WORKLOAD = "base_encoder"
+# the largest single-GPU configuration (the compute-bound one); the other forward
+# configurations are measured in the same run as compact lines under "workloads"
+DEFAULT_WORKLOAD = "long_keyonly"
+ALSO_WORKLOADS = "base_encoder,big_decoder,t5_bias"
 # fp32 FMA peak of the SIMT units: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (max SM clock)
 FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -351,11 +357,11 @@ def row_flops(w, kv_len, rows):
     return total
 
 
-def time_oracle(w, x, budget_s: float, seed: int = 1):
+def time_oracle(w, x, budget_s: float, seed: int = 1, nthreads=None):
     """Run the oracle on random rows of the workload for about budget_s seconds."""
     import numpy as np
     import oracle
-    nthreads = oracle.default_threads()
+    nthreads = nthreads or oracle.default_threads()
     rng = np.random.default_rng(seed)
     total_rows = w.B if w.kind in ("decode", "bwd") else w.B * w.H * w.n
     kv = key_lengths(w, x)
@@ -494,12 +500,165 @@ def whole_job(elapsed_ms: float, work: float, world: int, device) -> tuple:
     return float(tt.item()), float(ww.item())
 
 
+def input_sets(w, x, dev):
+    """Enough resident copies of the inputs (distinct buffers, same values) that a pass over
+    them exceeds 4x L2, so the timed reads come from HBM."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    in_bytes = sum(t.numel() * t.element_size() for t in x.values() if t is not None)
+    n_sets = max(1, min(64, math.ceil(4 * l2 / max(in_bytes, 1))))
+    sets = []
+    for s in range(n_sets):
+        g = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in x.items()}
+        if s > 0:
+            g = {kk: (vv.clone() if vv is not None else None) for kk, vv in g.items()}
+        sets.append((g, torch.empty_like(g["q"])))
+    note = ("inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > 4 x %.0f MB "
+            "L2), replayed from a CUDA graph" % (n_sets, in_bytes / 1e6, n_sets * in_bytes / 1e6,
+                                                 l2 / 1e6))
+    return sets, l2, note
+
+
+def percentile(xs, q):
+    ys = sorted(xs)
+    if not ys:
+        return None
+    k = (len(ys) - 1) * q
+    lo, hi = int(math.floor(k)), int(math.ceil(k))
+    return ys[lo] + (ys[hi] - ys[lo]) * (k - lo)
+
+
+class DeviceTimer:
+    """One CUDA graph of exactly `steps` launches over the rotating input sets, with an
+    external CUDA event recorded on the launching stream before each launch and after the
+    last, so that one replay gives the timed region and every launch's duration."""
+
+    def __init__(self, rp, w, sets, stream, steps, warmup):
+        import torch
+        self.stream = stream
+        self.steps = steps
+        with torch.cuda.stream(stream):  # warm-up, also sets the kernel attributes
+            for i in range(max(warmup, 1)):
+                g, o = sets[i % len(sets)]
+                gpu_call(rp, w, g, o, stream)
+        stream.synchronize()
+        probe = make_event(True)
+        self.use_events = probe is not None
+        self.evs = [make_event(True) for _ in range(steps + 1)] if self.use_events else []
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            for s in range(steps):
+                if self.use_events:
+                    self.evs[s].record(stream)
+                g, o = sets[s % len(sets)]
+                gpu_call(rp, w, g, o, stream)
+            if self.use_events:
+                self.evs[steps].record(stream)
+        with torch.cuda.stream(stream):
+            self.graph.replay()  # untimed replay
+        stream.synchronize()
+
+    def replay(self):
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+
+    def timed(self):
+        """(elapsed ms of one replay, per-launch ms list)."""
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            self.graph.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        per = ([self.evs[s].elapsed_time(self.evs[s + 1]) for s in range(self.steps)]
+               if self.use_events else [])
+        return e0.elapsed_time(e1), per
+
+
+def l2_flushed_launch_ms(rp, w, g, o, dev, stream, reps=20):
+    """Single launches, each after a write of a buffer twice the L2 size (torch fill, not
+    timed): CUDA events on the launching stream around the kernel alone; the median."""
+    import torch
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=dev)
+    ts = []
+    with torch.cuda.stream(stream):
+        for r in range(reps + 2):
+            flush.fill_(float(r))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gpu_call(rp, w, g, o, stream)
+            e1.record(stream)
+            stream.synchronize()
+            if r >= 2:
+                ts.append(e0.elapsed_time(e1))
+    del flush
+    return statistics.median(ts)
+
+
+def roofline(w, flops, byts, kern_ms, peaks, peak_src):
+    """Bound, achieved and fraction of the dominant roof for one launch of kern_ms."""
+    alu = w.kind in ("bwd", "labeled")
+    compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
+    t_roof_compute = flops / (compute_peak * 1e12)
+    t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
+    if alu and t_roof_compute > t_roof_mem:
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        return {"bound": "alu", "achieved": round(achieved, 2), "peak": FP32_SIMT_TFLOPS,
+                "unit": "TFLOP/s", "frac": round(achieved / FP32_SIMT_TFLOPS, 4),
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 flop x 2.07 GHz"}
+    if t_roof_mem >= t_roof_compute:
+        achieved = byts / (kern_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": peak_src + " (STREAM-style copy)"}
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "peak_source": peak_src + " (cuBLAS bf16 burst)"}
+
+
+def measure_also(rp, name, args, dev, stream, peaks, peak_src):
+    """A compact device-timed line for another workload: the same graph timing (--steps
+    launches over rotating input sets), roofline and profiled traffic; no e2e, no oracle."""
+    import torch
+    w = workload_by_name(name)
+    x = draw(w, seed=args.seed)
+    kv_len = key_lengths(w, x)
+    flops, byts = algorithmic_flops(w, kv_len), algorithmic_bytes(w, kv_len)
+    sets, _, note = input_sets(w, x, dev)
+    tm = DeviceTimer(rp, w, sets, stream, args.steps, args.warmup)
+    elapsed_ms, per = tm.timed()
+    status = rp.relattn_get_device_error(stream)
+    if status != 0:
+        raise RuntimeError("device status word set while timing %s: %s"
+                           % (name, rp.relattn_status_string(status)))
+    kern_ms = statistics.mean(per) if per else elapsed_ms / args.steps
+    roof = roofline(w, flops, byts, kern_ms, peaks, peak_src)
+    roof["traffic"] = profiled_traffic(w.name, kernel_family(w))
+    roof["kernel_ms"] = round(kern_ms, 5)
+    if per:
+        roof["kernel_ms_p10"] = round(percentile(per, 0.1), 5)
+        roof["kernel_ms_p90"] = round(percentile(per, 0.9), 5)
+    if roof["bound"] == "hbm":
+        roof["kernel_ms_l2_flushed"] = round(
+            l2_flushed_launch_ms(rp, w, sets[0][0], sets[0][1], dev, stream), 5)
+    line = {"workload": name, "value": round(flops * args.steps / (elapsed_ms * 1e-3) / 1e12, 3),
+            "unit": "TFLOP/s", "steps": args.steps, "ms_per_step": round(elapsed_ms / args.steps, 6),
+            "config": workload_config(w, 1, note), "roofline": roof,
+            "gpu_launches": args.steps * launches_per_step(rp, w)}
+    del tm, sets
+    torch.cuda.synchronize()
+    return line
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
     import relative_position_representations_gb300 as rp
-    from relative_position_representations_gb300 import workloads as wl
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -508,91 +667,46 @@ def run_ours(args, rank, world, local_rank):
     kv_len = key_lengths(w, x)
     flops = algorithmic_flops(w, kv_len)
     byts = algorithmic_bytes(w, kv_len)
-
-    # rotate over enough resident input sets that the timed reads come from HBM
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    in_bytes = sum(t.numel() * t.element_size() for t in x.values() if t is not None)
-    n_sets = max(1, min(64, math.ceil(4 * l2 / max(in_bytes, 1))))
-    sets = []
-    for s in range(n_sets):
-        g = {kk: (vv.to(dev) if vv is not None else None) for kk, vv in x.items()}
-        if s > 0:  # distinct buffers with the same values
-            g = {kk: (vv.clone() if vv is not None else None) for kk, vv in g.items()}
-        sets.append((g, torch.empty_like(g["q"])))
+    sets, l2, l2_note = input_sets(w, x, dev)
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
-
-    # warm-up (also sets the kernel attributes before graph capture)
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 1)):
-            g, o = sets[i % n_sets]
-            gpu_call(rp, w, g, o, stream)
-    stream.synchronize()
-
-    # one graph = one pass over all input sets, with external timing events between launches
-    probe = make_event(True)
-    use_events = probe is not None
-    graph = torch.cuda.CUDAGraph()
-    evs = [make_event(True) for _ in range(n_sets + 1)] if use_events else []
-    with torch.cuda.graph(graph, stream=stream):
-        for s in range(n_sets):
-            if use_events:
-                evs[s].record(stream)
-            g, o = sets[s]
-            gpu_call(rp, w, g, o, stream)
-        if use_events:
-            evs[n_sets].record(stream)
-    reps = max(1, math.ceil(args.steps / n_sets))
-    steps = reps * n_sets
-    with torch.cuda.stream(stream):
-        graph.replay()  # untimed replay
-    stream.synchronize()
+    steps = args.steps
+    tm = DeviceTimer(rp, w, sets, stream, steps, args.warmup)
 
     # clocks sampled around and during the timed region, with the same launches running
     sampler = ClockSampler(local_rank)
     soak = 0.0 if args.no_clocks else 0.6
+
+    def soak_for(sec):
+        until = time.time() + sec
+        while time.time() < until:
+            tm.replay()
+            stream.synchronize()
+
     if soak:
         sampler.start()
-    soak_until = time.time() + soak
-    with torch.cuda.stream(stream):
-        while time.time() < soak_until:
-            graph.replay()
-            stream.synchronize()
+        soak_for(soak)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_start_wall = time.time()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    kernel_ms = []
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for r in range(reps):
-            graph.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
+    elapsed_ms, kernel_ms = tm.timed()
     t_end_wall = time.time()
-    if use_events:
-        # the in-graph events hold the timestamps of the last timed replay
-        kernel_ms = [evs[s].elapsed_time(evs[s + 1]) for s in range(n_sets)]
     if world > 1:
         dist.barrier()
-    soak_until = time.time() + soak
-    with torch.cuda.stream(stream):
-        while time.time() < soak_until:
-            graph.replay()
-            stream.synchronize()
+    if soak:
+        soak_for(soak)
     sampler.stop()
     # a bounded device wait that ran out voids the timing (and the outputs)
     status = rp.relattn_get_device_error(stream)
     if status != 0:
         raise RuntimeError("device status word set during the timed region: %s"
                            % rp.relattn_status_string(status))
-    elapsed_ms = e0.elapsed_time(e1)
     clocks = sampler.summary(t_start_wall - soak, t_end_wall + soak) if soak else None
-    if use_events and any(m > 0 for m in kernel_ms):
+    if kernel_ms and any(m > 0 for m in kernel_ms):
         kern_ms = statistics.mean(kernel_ms)
-        kern_src = ("cuda events between the launches of the last timed graph replay "
-                    "(%d launches)" % len(kernel_ms))
+        kern_src = ("cuda events on the launching stream between the %d launches of the timed "
+                    "graph replay" % len(kernel_ms))
     else:
         kern_ms = elapsed_ms / steps
         kern_src = "timed-region elapsed / steps (events in graphs unavailable)"
@@ -601,40 +715,40 @@ def run_ours(args, rank, world, local_rank):
     t_max, total_flops = whole_job(elapsed_ms, flops * steps, world, dev)
     value = total_flops / (t_max * 1e-3) / 1e12
 
-    # end to end through the C ABI with pinned host buffers
-    e2e = None if args.no_e2e else measure_e2e(rp, w, x, dev, stream, flops, args)
-
     peaks, peak_src = read_peaks()
-    # the gradients and the labelled edges run on the SIMT units: their compute roof is the
-    # fp32 FMA rate
-    alu = w.kind in ("bwd", "labeled")
-    compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
-    t_roof_compute = flops / (compute_peak * 1e12)
-    t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
-    if alu and t_roof_compute > t_roof_mem:
-        achieved = flops / (kern_ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": FP32_SIMT_TFLOPS,
-                "unit": "TFLOP/s", "frac": round(achieved / FP32_SIMT_TFLOPS, 4),
-                "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 flop x 2.07 GHz"}
-    elif t_roof_mem >= t_roof_compute:
-        achieved = byts / (kern_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_source": peak_src + " (STREAM-style copy)"}
-    else:
-        achieved = flops / (kern_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "peak_source": peak_src + " (cuBLAS bf16 burst)"}
+    roof = roofline(w, flops, byts, kern_ms, peaks, peak_src)
     roof["traffic"] = profiled_traffic(w.name, kernel_family(w))
     roof["kernel_ms"] = round(kern_ms, 5)
+    if kernel_ms:
+        roof["kernel_ms_p10"] = round(percentile(kernel_ms, 0.1), 5)
+        roof["kernel_ms_p90"] = round(percentile(kernel_ms, 0.9), 5)
+    if roof["bound"] == "hbm" and w.kind not in ("decode",):
+        roof["kernel_ms_l2_flushed"] = round(
+            l2_flushed_launch_ms(rp, w, sets[0][0], sets[0][1], dev, stream), 5)
     roof["kernel_time_source"] = kern_src
     roof["algorithmic_flops"] = flops
     roof["algorithmic_bytes"] = byts
+    del tm, sets
+    torch.cuda.synchronize()
 
+    # end to end through the C ABI with pinned host buffers
+    e2e = None if args.no_e2e else measure_e2e(rp, w, x, dev, stream, flops, args)
+
+    # the other forward configurations, device-timed the same way (rank 0, one GPU)
+    also = []
+    if rank == 0 and world == 1 and args.also:
+        for name in [a for a in args.also.split(",") if a and a != w.name]:
+            also.append(measure_also(rp, name, args, dev, stream, peaks, peak_src))
+
+    alu = w.kind in ("bwd", "labeled")
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(w, x, args.cpu_budget)
+        cpu["model"] = host_cpu_model()
+        # the small configurations also get a 1-thread figure
+        if w.name in ("tiny_fp32", "base_encoder", "big_decoder"):
+            one, _, _ = time_oracle(w, x, min(args.cpu_budget, 4.0), nthreads=1)
+            cpu["single_thread"] = {"value": one["value"], "sample": one["sample"]}
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -642,15 +756,33 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         # the arithmetic type: the tensor-core kernels multiply bf16, the SIMT kernels fp32
         "dtype": "bf16" if (w.dtype == "bf16" and not alu) else "f32", "data": "synthetic",
-        "config": workload_config(
-            w, world, "inputs larger than L2: %d rotating input sets of %.1f MB (%.0f MB > "
-                      "4 x %.0f MB L2), replayed from a CUDA graph" % (
-                          n_sets, in_bytes / 1e6, n_sets * in_bytes / 1e6, l2 / 1e6)),
+        "config": workload_config(w, world, l2_note),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": steps * launches_per_step(rp, w),
         "clocks": clocks,
     }
+    if also:
+        line["workloads"] = also
     return line
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
 
 
 def measure_e2e(rp, w, x, dev, stream, flops, args):
@@ -750,6 +882,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip clock sampling and its soak")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--also", default=ALSO_WORKLOADS,
+                    help="comma-separated workloads also device-timed in the same run ('' = none)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

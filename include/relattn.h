@@ -217,13 +217,29 @@ RELATTN_API relattn_status_t relattn_decode_fwd(const void *q, const void *k_cac
                                     void *out, relattn_stream_t stream);
 
 /*
- * relattn_decode_fwd_noalloc — relattn_decode_fwd for callers that provide no device
- * scratch: the same arguments without workspace / workspace_bytes, run with a 4 MiB scratch
- * buffer that is part of the library's device image (a file-scope device array, so nothing
- * is allocated at any call). That buffer is one per device and shared by every call of
- * this entry point on the device, so such calls must not run at the same time (calls on
- * one stream are ordered). The pages describe no counterpart of this entry point: it is an
- * interface convenience, not part of the method.
+ * relattn_decode_fwd_noalloc — relattn_decode_fwd for callers that cannot allocate device
+ * memory: a host runtime that reserves its whole device budget at start-up and forbids
+ * allocations afterwards, or a plugin inside another engine that is handed tensors but no
+ * allocator. cudaMalloc may also synchronise the device, which a latency-bound decoding loop
+ * cannot afford. The arguments are those of relattn_decode_fwd without workspace /
+ * workspace_bytes; the scratch is a 4 MiB array that is part of the library's device image
+ * (a file-scope __device__ array, held by every device that loads the library until the
+ * process exits), so no call allocates anything.
+ *
+ *   - When the split over the cache would need more than 4 MiB
+ *     (relattn_decode_workspace_size > 4 MiB, e.g. 256 sequence-heads of d = 128 with
+ *     T > 15872), the call runs without the split, one CTA per cache, and uses no scratch.
+ *   - The array is one per device and shared by every call of this entry point on that
+ *     device: calls that overlap on the GPU (different streams, no ordering) race on it and
+ *     give wrong results; calls on one stream are ordered. Each call writes every scratch
+ *     value it later reads, so nothing has to be cleared between calls.
+ *   - The first call on a device, with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress) and keeps it for the process; make that first call
+ *     before any stream capture. The kept address is not valid after cudaDeviceReset: do not
+ *     use the library across a reset.
+ *
+ * The pages describe no counterpart of this entry point: it is an interface convenience,
+ * not part of the method.
  */
 RELATTN_API relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
                                             const void *v_cache, const void *aK,
@@ -303,6 +319,28 @@ RELATTN_API relattn_status_t relattn_t5_thresholds(int num_buckets, int max_dist
  * met a label without a table row. RELATTN_ERR_CUDA if the stream reports an error.
  */
 RELATTN_API relattn_status_t relattn_get_device_error(relattn_stream_t stream);
+
+/*
+ * relattn_set_wait_limit — the bound of every device-side wait of the tensor-core forward
+ * kernels (relattn_fwd, relattn_t5bias_fwd, relattn_alibi_fwd, relattn_offset_bias_fwd on
+ * bf16), in SM clock cycles; the default is 2e9 (about one second at 2 GHz). A wait that
+ * runs out makes every warp of the kernel stop, wait (again bounded) for its copies and
+ * tensor-core operations in flight, release its tensor memory and exit; the call's output is
+ * then undefined and relattn_get_device_error reports RELATTN_ERR_TIMEOUT. The setting is
+ * process-wide and applies to launches made after the call. 1000 <= cycles <= 2^40, else
+ * RELATTN_ERR_INVALID_ARG. Host only; not part of the method (the pages have no
+ * counterpart): failure detection of the library.
+ */
+RELATTN_API relattn_status_t relattn_set_wait_limit(long long cycles);
+
+/*
+ * relattn_debug_withhold_first_load — test hook for the timeout path: with on = 1, each
+ * producer warp of the tensor-core forward kernels announces the Q tiles of its first work
+ * item to their barrier but never loads them, so the tensor-core warp's bounded wait for
+ * them runs out (no fault, no trap: the kernel exits through its abort path). on = 0
+ * (the default) restores normal launches. Process-wide; never set it in production.
+ */
+RELATTN_API relattn_status_t relattn_debug_withhold_first_load(int on);
 
 /* Static English text for a status code. */
 RELATTN_API const char *relattn_status_string(relattn_status_t s);

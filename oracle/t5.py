@@ -13,7 +13,7 @@ logarithmic after that,
                                                                     otherwise,
     clamped to B - 1.
 
-Readings taken where the page is garbled or silent (each listed in the design doc):
+Readings taken where the page is garbled or silent:
   * bidirectional: the B buckets split into two halves of B/2, one per sign; inside a
     half B_exact = (B/2)/2 and the formula uses the half's size B/2 in place of B.
     Offsets j - i > 0 use the upper half (bucket + B/2), offsets <= 0 the lower half.

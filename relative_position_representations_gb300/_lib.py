@@ -63,6 +63,10 @@ _lib.relattn_get_device_error.argtypes = [_P]
 _lib.relattn_get_device_error.restype = _I
 _lib.relattn_status_string.argtypes = [_I]
 _lib.relattn_status_string.restype = ctypes.c_char_p
+_lib.relattn_set_wait_limit.argtypes = [ctypes.c_longlong]
+_lib.relattn_set_wait_limit.restype = _I
+_lib.relattn_debug_withhold_first_load.argtypes = [_I]
+_lib.relattn_debug_withhold_first_load.restype = _I
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
@@ -70,7 +74,8 @@ EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
-            "relattn_t5_thresholds",
+            "relattn_t5_thresholds", "relattn_set_wait_limit",
+            "relattn_debug_withhold_first_load",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
 
@@ -448,6 +453,20 @@ def relattn_t5_thresholds(num_buckets=32, max_distance=128, bidirectional=True):
 def relattn_get_device_error(stream=None) -> int:
     """Synchronise the stream; return (and clear) the device status word."""
     return int(_lib.relattn_get_device_error(_stream(stream)))
+
+
+def relattn_set_wait_limit(cycles: int) -> None:
+    """Bound of every device wait of the tensor-core forward kernels, in SM clock cycles."""
+    st = int(_lib.relattn_set_wait_limit(int(cycles)))
+    if st != OK:
+        raise RelattnError(st, "relattn_set_wait_limit")
+
+
+def relattn_debug_withhold_first_load(on: bool) -> None:
+    """Test hook: the tensor-core forward kernels withhold their first Q load (timeout test)."""
+    st = int(_lib.relattn_debug_withhold_first_load(1 if on else 0))
+    if st != OK:
+        raise RelattnError(st, "relattn_debug_withhold_first_load")
 
 
 def raw_call(name, *args):

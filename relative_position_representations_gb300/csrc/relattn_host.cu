@@ -1,6 +1,7 @@
 // Public C ABI of librelattn.so (declared in include/relattn.h): argument validation,
 // dispatch to the fp32 SIMT path or the bf16 tcgen05 path, device status word.
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -90,13 +91,21 @@ relattn_status_t check_qkv(const void *q, const void *k, const void *v, const vo
     return RELATTN_OK;
 }
 
-relattn_status_t dispatch_bf16(const relattn::TcArgs &a, const relattn::T5Buckets *t5,
+// bound of the fused kernel's device waits (SM clock cycles) and the timeout-test hook,
+// read at each launch
+std::atomic<long long> g_wait_limit{2000000000ll};
+std::atomic<int> g_withhold_q{0};
+
+relattn_status_t dispatch_bf16(const relattn::TcArgs &args, const relattn::T5Buckets *t5,
                                cudaStream_t s) {
     const int cc = current_cc();
     if (cc < 0) return RELATTN_ERR_CUDA;
     if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
     int *err = status_word_for_current_device();
     if (!err) return RELATTN_ERR_CUDA;
+    relattn::TcArgs a = args;
+    a.wait_limit = g_wait_limit.load();
+    a.withhold_q = g_withhold_q.load();
     const cudaError_t e = a.d == 64 ? relattn::launch_tc_bf16_d64(a, t5, err, s)
                                     : relattn::launch_tc_bf16_d128(a, t5, err, s);
     return from_cuda(e);
@@ -436,6 +445,18 @@ const char *relattn_status_string(relattn_status_t s) {
     return "unknown status";
 }
 
-int relattn_version(void) { return 100; }
+relattn_status_t relattn_set_wait_limit(long long cycles) {
+    if (cycles < 1000 || cycles > (1ll << 40)) return RELATTN_ERR_INVALID_ARG;
+    g_wait_limit.store(cycles);
+    return RELATTN_OK;
+}
+
+relattn_status_t relattn_debug_withhold_first_load(int on) {
+    if (on != 0 && on != 1) return RELATTN_ERR_INVALID_ARG;
+    g_withhold_q.store(on);
+    return RELATTN_OK;
+}
+
+int relattn_version(void) { return 101; }
 
 }  // extern "C"

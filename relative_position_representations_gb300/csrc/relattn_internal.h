@@ -69,6 +69,8 @@ struct TcArgs {
     int B, H, n, d;
     void *out;
     int mode;           // kShaw, or kT5 for every scalar offset bias
+    long long wait_limit;  // bound of every device wait in SM clock cycles (<= 0: 2e9)
+    int withhold_q;        // test hook: withhold the first Q load of each producer (timeout test)
 };
 // Returns cudaErrorNotSupported for combinations the kernel does not cover (checked
 // before any launch), cudaErrorInvalidValue for bad tensor-map parameters.

@@ -67,9 +67,9 @@ static_assert(128 * kCtrlRegs + 256 * kSoftRegs == kThreads * kLaunchRegs, "regi
 static_assert(BM == 128 && BN == 128, "the MMA chains (ptx::tc_mma_*_k*) assume 128-row operand tiles");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
-// bound of every device wait, in SM clock cycles (about one second at 2 GHz); clock64 is
-// read only after a wait did not succeed at once and then every 256 polls
-constexpr long long kWaitLimitCycles = 2000000000ll;
+// Every device wait is bounded by Params::wait_limit SM clock cycles (the library default
+// is 2e9, about one second at 2 GHz); clock64 is read only after a wait did not succeed at
+// once and then every 256 polls.
 
 // TMEM columns of slot s. D = 64: S at 128 s, O at 256 + 64 s, P at 384 + 64 s. D = 128 with
 // two tiles per item: S at 128 s, O at 256 + 128 s, P over the first half of the slot's S.
@@ -139,6 +139,8 @@ struct Params {
     // own producer warp, its own half of the ring and its own Q and W^V barriers, so the two
     // slots run their items independently.
     int split;
+    long long wait_limit;  // bound of every wait, SM clock cycles
+    int withhold_q;        // test hook: the producer issues no Q load for its first item
     int stages;
     int ring_stages;     // stages of one ring: all of them (shared feed) or half (split feed)
     uint32_t stage_bytes;
@@ -156,18 +158,19 @@ struct Shared {
     uint32_t base;  // 1024-aligned shared address
     uint8_t *ptr;   // generic pointer to the same byte
     volatile int *abort_flag;
+    long long limit;  // bound of every wait (cycles)
 };
 
 // slow path of a bounded wait (polls, with an abort check and a cycle limit every 256 polls)
 __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                           int *err) {
+                                           int *err, long long limit) {
     const long long t0 = clock64();
     uint32_t spins = 0;
     while (true) {
         if (ptx::mbar_try(bar, parity)) return true;
         if ((++spins & 255u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 atomicCAS(err, 0, 4 /* RELATTN_ERR_TIMEOUT */);
                 return false;
@@ -179,25 +182,26 @@ __device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, vol
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Shared &sh,
                                          int *err) {
     if (ptx::mbar_try(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, sh.abort_flag, err);
+    return wait_bar_slow(bar, parity, sh.abort_flag, err, sh.limit);
 }
 
 // the same for the producer and MMA warps, with the slow path out of line (those warps have
 // registers to spare for a call, and their many waits would otherwise each carry a copy)
 static __device__ __noinline__ bool wait_bar_slow_call(uint32_t bar, uint32_t parity,
-                                                volatile int *abort_flag, int *err) {
-    return wait_bar_slow(bar, parity, abort_flag, err);
+                                                volatile int *abort_flag, int *err,
+                                                long long limit) {
+    return wait_bar_slow(bar, parity, abort_flag, err, limit);
 }
 __device__ __forceinline__ bool wait_bar_ctrl(uint32_t bar, uint32_t parity, const Shared &sh,
                                               int *err) {
     if (ptx::mbar_try(bar, parity)) return true;
-    return wait_bar_slow_call(bar, parity, sh.abort_flag, err);
+    return wait_bar_slow_call(bar, parity, sh.abort_flag, err, sh.limit);
 }
 
 // bounded poll of a barrier during teardown (no abort check)
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, long long limit) {
     const long long t0 = clock64();
-    while (!ptx::mbar_try(bar, parity) && clock64() - t0 < kWaitLimitCycles) {
+    while (!ptx::mbar_try(bar, parity) && clock64() - t0 < limit) {
     }
 }
 
@@ -487,8 +491,11 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
             if (AK && tab_head[s] >= 0) qbytes += (uint32_t)p.npad_k * D * 2;
         }
         ptx::mbar_expect_tx_w(q_full, qbytes);
+        // test hook: the first item's Q tiles are announced but never loaded, so the MMA warp's
+        // bounded wait for them runs out (the device status word reports the timeout)
+        const bool hold = p.withhold_q && q_it == 1;
         for (int s = 0; s < 2; ++s) {
-            if (pl.active(s)) {
+            if (pl.active(s) && !hold) {
                 const uint32_t sQ = sh.base + p.off_q[s];
 #pragma unroll
                 for (int blk = 0; blk < DB; ++blk)
@@ -550,16 +557,16 @@ __device__ void producer_role(const Params &p, const Shared &sh, const CUtensorM
             }
         }
     }
-    if (!ok) {
-        // drain: wait (bounded) for copies already issued into shared memory
-        for (uint32_t i = kv_it > (uint32_t)S ? kv_it - S : 0; i < kv_it; ++i) {
-            uint32_t st_u, round;
-            ring_pos(p, i, st_u, round);
-            drain_bar(bar(B_KV0 + ring0 + (int)st_u), round & 1u);
-        }
-        if (q_it) drain_bar(q_full, (q_it - 1) & 1u);
-        if (AV && av_it) drain_bar(av_full, (av_it - 1) & 1u);
+    // drain: wait (bounded) for the copies issued into shared memory, so that none is still
+    // in flight when the CTA exits (normally they were all consumed already; after an abort
+    // the consumers may have given up on some)
+    for (uint32_t i = kv_it > (uint32_t)S ? kv_it - S : 0; i < kv_it; ++i) {
+        uint32_t st_u, round;
+        ring_pos(p, i, st_u, round);
+        drain_bar(bar(B_KV0 + ring0 + (int)st_u), round & 1u, sh.limit);
     }
+    if (q_it) drain_bar(q_full, (q_it - 1) & 1u, sh.limit);
+    if (AV && av_it) drain_bar(av_full, (av_it - 1) & 1u, sh.limit);
 }
 
 // ======================================================================= MMA issuers
@@ -728,7 +735,7 @@ __device__ void mma_role(const Params &p, const Shared &sh, uint32_t tmem, int s
     }
     // every MMA issued by this warp completes before TMEM is released
     ptx::tc_commit_w(sbar(SB_DRAIN));
-    drain_bar(sbar(SB_DRAIN), 0);
+    drain_bar(sbar(SB_DRAIN), 0, sh.limit);
 }
 
 // ======================================================================= softmax / epilogue
@@ -1153,6 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar_ptr = reinterpret_cast<uint64_t *>(sh.ptr + p.off_bar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_ptr + kNumBars);
     sh.abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    sh.limit = p.wait_limit;
     const int warp = threadIdx.x >> 5;
     const uint32_t bars = sh.base + p.off_bar;
 

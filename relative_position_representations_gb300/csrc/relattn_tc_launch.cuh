@@ -266,6 +266,8 @@ cudaError_t launch_tc(const TcArgs &a, const T5Buckets *t5, int *err_word, cudaS
         break;
     }
     if (!found || smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
+    p.wait_limit = a.wait_limit > 0 ? a.wait_limit : 2000000000ll;
+    p.withhold_q = a.withhold_q;
     {
         const int G = p.head_group;
         const int full = p.BH / G, rest = p.BH - full * G;

@@ -48,6 +48,15 @@ def test_status_strings_and_version(lib):
     assert lib.relattn_status_string(99) == "unknown status"
 
 
+def test_wait_limit_and_hook_arguments_checked_on_the_host(lib):
+    """Host-only checks of the failure-detection settings (no launch)."""
+    assert lib.raw_call("relattn_set_wait_limit", 10) == 1  # below 1000 cycles
+    assert lib.raw_call("relattn_set_wait_limit", 1 << 41) == 1
+    assert lib.raw_call("relattn_debug_withhold_first_load", 2) == 1
+    assert lib.raw_call("relattn_set_wait_limit", 2000000000) == 0  # the default
+    assert lib.raw_call("relattn_debug_withhold_first_load", 0) == 0
+
+
 @pytest.mark.parametrize("nb,md,bidir", [(32, 128, True), (32, 128, False), (16, 40, True),
                                          (64, 1000, True), (8, 5, False), (4, 3, True),
                                          (256, 100000, True), (200, 7000, False)])

@@ -298,28 +298,12 @@ def test_bf16_unsupported_and_invalid_status():
 
 
 # ------------------------------------------------------------------- full-size workloads
-def _sample_rows(w, count, seed):
-    rng = np.random.default_rng(seed)
-    BH = w.B * w.H
-    bh = rng.integers(0, BH, count)
-    i = rng.integers(0, w.n, count)
-    # tile edges and sequence ends for a few heads
-    edges = np.array([0, 1, 126, 127, 128, 129, w.n - 2, w.n - 1])
-    edges = edges[(edges >= 0) & (edges < w.n)]
-    extra_bh = np.repeat(rng.integers(0, BH, 4), len(edges))
-    extra_i = np.tile(edges, 4)
-    return np.unique(np.concatenate([bh * w.n + i, extra_bh * w.n + extra_i]))
-
-
-@pytest.mark.parametrize("name", ["base_encoder", "big_decoder"])
+@pytest.mark.parametrize("name", ["base_encoder", "big_decoder", "long_keyonly", "t5_bias"])
 def test_full_workload_all_rows(name):
+    """Every output row of the full-size workload, element by element, against the oracle
+    (at most a few seconds of oracle work on the host cores): every (head, query tile) of
+    the launch that bench.py times is compared."""
     check(wl.WORKLOADS[name])
-
-
-@pytest.mark.parametrize("name,count", [("long_keyonly", 1500), ("t5_bias", 3000)])
-def test_full_workload_sampled_rows(name, count):
-    w = wl.WORKLOADS[name]
-    check(w, rows=_sample_rows(w, count, 7))
 
 
 @pytest.mark.parametrize("name,reps", [("base_encoder", 400), ("big_decoder", 400),
