@@ -134,7 +134,8 @@ KERNEL_SOURCES = {
               "relattn_tc_kernel.cuh", "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
     "decode": ["relattn_decode.cu"],
     "bwd": ["relattn_bwd.cu"],
-    "labeled": ["device_common.cuh", "relattn_labeled.cu"],
+    "labeled": ["relattn_labeled_tc.cuh", "relattn_labeled_tc.cu", "relattn_tc_kernel.cuh",
+                "sm103_ptx.cuh"],
 }
 
 
@@ -600,7 +601,9 @@ def l2_flushed_launch_ms(rp, w, g, o, dev, stream, reps=20):
 
 def roofline(w, flops, byts, kern_ms, peaks, peak_src):
     """Bound, achieved and fraction of the dominant roof for one launch of kern_ms."""
-    alu = w.kind in ("bwd", "labeled")
+    # the gradients run on the SIMT units (fp32 FMA roof); labelled edges on the tensor cores
+    # for bf16 (the fp32 inputs take the SIMT kernel)
+    alu = w.kind == "bwd" or (w.kind == "labeled" and w.dtype != "bf16")
     compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
     t_roof_compute = flops / (compute_peak * 1e12)
     t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
@@ -740,7 +743,9 @@ def run_ours(args, rank, world, local_rank):
         for name in [a for a in args.also.split(",") if a and a != w.name]:
             also.append(measure_also(rp, name, args, dev, stream, peaks, peak_src))
 
-    alu = w.kind in ("bwd", "labeled")
+    # the gradients run on the SIMT units (fp32 FMA roof); labelled edges on the tensor cores
+    # for bf16 (the fp32 inputs take the SIMT kernel)
+    alu = w.kind == "bwd" or (w.kind == "labeled" and w.dtype != "bf16")
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(w, x, args.cpu_budget)

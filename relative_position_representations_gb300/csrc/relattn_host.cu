@@ -297,7 +297,15 @@ relattn_status_t relattn_labeled_fwd(const void *q, const void *k, const void *v
     a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
     a.out = out;
     a.err = err;
-    return from_cuda(relattn::launch_labeled(a, reinterpret_cast<cudaStream_t>(stream)));
+    a.wait_limit = g_wait_limit.load();
+    // bf16 with d = 64 or 128 runs on the tensor cores when the kernel fits the shapes (at
+    // most 128 labels); the SIMT kernel takes everything else
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (a.bf16 && (d == 64 || d == 128)) {
+        const cudaError_t e = relattn::launch_labeled_tc(a, cs);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    return from_cuda(relattn::launch_labeled(a, cs));
 }
 
 relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,

@@ -111,9 +111,13 @@ struct LabeledArgs {
     int bf16;                 // 1: q, k, v, tables and out are bf16; 0: fp32
     void *out;
     int *err;                 // device status word (a label without a table row)
+    long long wait_limit;     // tensor-core path: bound of every device wait (cycles, <= 0: 2e9)
 };
-// cudaErrorNotSupported when d > 128 or more than 256 labels
+// SIMT kernel; cudaErrorNotSupported when d > 128 or more than 256 labels
 cudaError_t launch_labeled(const LabeledArgs &a, cudaStream_t s);
+// tensor-core kernel (bf16, d = 64 or 128, at most 128 labels); cudaErrorNotSupported for any
+// other combination, checked before any launch
+cudaError_t launch_labeled_tc(const LabeledArgs &a, cudaStream_t s);
 
 // ---- gradients (SIMT, fp32 arithmetic) ---------------------------------------------------
 struct BwdArgs {

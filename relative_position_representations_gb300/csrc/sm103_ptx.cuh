@@ -101,6 +101,19 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool
         : "memory");
     return r != 0;
 }
+// the same with an OR reduction
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -225,6 +238,33 @@ __device__ __forceinline__ void tc_mma_ts_k128(uint32_t d, uint32_t a_tmem, uint
         ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(1u)
         : "memory");
 }
+// ts_k128_2: the same over 128 keys whose A operand sits in two TMEM blocks of 32 columns:
+// keys 0..63 (k-steps 0..3) at a_lo, keys 64..127 (k-steps 4..7) at a_hi
+__device__ __forceinline__ void tc_mma_ts_k128_2(uint32_t d, uint32_t a_lo, uint32_t a_hi, uint64_t b,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 t, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %4, p;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.s64 b1, %3, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "add.u32 a1, %1, 16;\n\tadd.s64 b1, %3, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "add.u32 a1, %1, 24;\n\tadd.s64 b1, %3, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "add.u32 a1, %2, 0;\n\tadd.s64 b1, %3, 512;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "add.u32 a1, %2, 8;\n\tadd.s64 b1, %3, 640;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "add.u32 a1, %2, 16;\n\tadd.s64 b1, %3, 768;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "add.u32 a1, %2, 24;\n\tadd.s64 b1, %3, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, t;\n\t"
+        "}\n"
+        ::"r"(d), "r"(a_lo), "r"(a_hi), "l"(b), "r"(idesc), "r"(accumulate), "r"(1u)
+        : "memory");
+}
 #undef RELATTN_MMA_TS_STEP
 
 // plain arrive by one elected lane (the whole warp calls it)
@@ -330,6 +370,15 @@ __device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float *r) {
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
         "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         RELATTN_WF8(0), RELATTN_WF8(8)
+        : "memory");
+}
+// same as tmem_st32, from fp32 registers holding the 32-bit patterns to store
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        RELATTN_WF8(0), RELATTN_WF8(8), RELATTN_WF8(16), RELATTN_WF8(24)
         : "memory");
 }
 #undef RELATTN_WF8

@@ -63,6 +63,14 @@ def check(w, seed=0, rows=None):
     ("bf16", 129, 128, 256, False, None, True, False, True, True),
     ("bf16", 70, 32, 3, False, (1, 70), True, False, True, False),
     ("bf16", 90, 64, 9, True, None, True, False, False, True),
+    # the tensor-core kernel (bf16, d = 64 or 128, at most 128 labels): label rows read as
+    # 16-byte vectors (n a multiple of 16) or byte by byte, several key tiles, padding, causal
+    ("bf16", 512, 64, 16, False, (200, 512), True, False, True, True),
+    ("bf16", 384, 128, 40, True, None, True, True, True, True),
+    ("bf16", 250, 128, 128, False, (1, 250), False, False, True, True),
+    ("bf16", 160, 64, 1, True, (30, 160), True, False, True, True),
+    ("bf16", 256, 64, 5, False, None, False, False, False, True),
+    ("bf16", 300, 128, 64, True, (100, 300), True, False, True, False),
     ("f32", 77, 32, 5, False, None, False, False, True, True),
     ("f32", 64, 128, 33, True, (10, 64), True, True, True, True),
     ("f32", 45, 20, 4, False, None, True, False, True, True),
