@@ -167,8 +167,11 @@ RELATTN_API relattn_status_t relattn_offset_bias_fwd(const void *q, const void *
  *                       every sequence, else >= n * n.
  * A label >= num_labels is not checked on the host: the kernel reads it as the last table
  * row and sets the device status word to RELATTN_ERR_INVALID_ARG (relattn_get_device_error).
- * Runs on the SIMT units with fp32 arithmetic for bf16 and fp32 inputs alike; d <= 128 and a
- * multiple of 8 (bf16) / 4 (fp32), else RELATTN_ERR_UNSUPPORTED.
+ * bf16 with d = 64 or 128 and at most 128 labels (when the tables' rows fit shared memory)
+ * runs on the tensor cores: R = Q aK^T over the labels per query tile, gathered by label into
+ * the scores, and per-label bins of the probabilities times aV, fp32 accumulation. Every other
+ * supported shape runs on the SIMT units with fp32 arithmetic; d <= 128 and a multiple of
+ * 8 (bf16) / 4 (fp32), else RELATTN_ERR_UNSUPPORTED.
  */
 RELATTN_API relattn_status_t relattn_labeled_fwd(const void *q, const void *k, const void *v,
                                      const void *aK, const void *aV, long long table_head_stride,
