@@ -67,6 +67,9 @@ def algorithmic_flops(w, kv_len) -> float:
     for the table terms)."""
     if w.kind == "bwd":
         return 2.5 * algorithmic_flops(w.replace(kind="shaw"), kv_len)
+    if w.kind == "txl":  # (q + u).k_j, (q + v).r_ij and p v_j: 3 x 2 d per unmasked pair
+        kvs = [None] * w.B if kv_len is None else [int(x) for x in kv_len]
+        return 6.0 * w.d * sum(pairs_per_sequence(w, kvs[b]) for b in range(w.B)) * w.H
     if w.kind == "decode":
         terms = int(w.key_term) + int(w.value_term)
         rows = sum(min(int(x), w.n) for x in kv_len) * w.H
@@ -108,6 +111,8 @@ def algorithmic_bytes(w, kv_len) -> float:
         byt += 4 * w.num_buckets * w.H
     elif w.kind == "alibi":  # the slopes
         byt += 4 * w.H
+    elif w.kind == "txl":  # the projected offset encodings and the two bias vectors
+        byt += es * Ht * (2 * w.n - 1 + 2) * w.d
     elif w.kind == "labeled":  # the tables and the uint8 label matrices
         byt += es * Ht * w.num_labels * w.d * (int(w.key_term) + int(w.value_term))
         byt += (w.B if w.labels_per_sequence else 1) * w.n * w.n
@@ -136,11 +141,12 @@ KERNEL_SOURCES = {
     "bwd": ["relattn_bwd.cu"],
     "labeled": ["relattn_labeled_tc.cuh", "relattn_labeled_tc.cu", "relattn_tc_kernel.cuh",
                 "sm103_ptx.cuh"],
+    "txl": ["relattn_txl.cu"],
 }
 
 
 def kernel_family(w) -> str:
-    return {"decode": "decode", "bwd": "bwd", "labeled": "labeled"}.get(w.kind, "fused")
+    return {"decode": "decode", "bwd": "bwd", "labeled": "labeled", "txl": "txl"}.get(w.kind, "fused")
 
 
 def kernel_source_hash(family: str = "fused") -> str:
@@ -243,6 +249,8 @@ def workload_by_name(name):
         return wl.BIAS_WORKLOADS[name]
     if name in wl.LABELED_WORKLOADS:
         return wl.LABELED_WORKLOADS[name]
+    if name in wl.TXL_WORKLOADS:
+        return wl.TXL_WORKLOADS[name]
     return wl.WORKLOADS[name]
 
 
@@ -268,6 +276,23 @@ def oracle_bwd_batches(w, x, batches):
                                         tab(x["aV"]), sl(x["dout"]), w.clip_k, w.causal,
                                         w.softmax_scale, kv_len=kv,
                                         table_head_stride=wl.table_head_stride(w)))
+    return out
+
+
+def oracle_txl_batches(w, x, batches):
+    """The Transformer-XL oracle on the sequences in `batches` (all heads), one at a time."""
+    import numpy as np
+    from oracle import txl
+    f = lambda t: t.double().numpy()
+    rel, u, vb = f(x["rel"]), f(x["u"]), f(x["vb"])
+    if rel.shape[0] == 1 and w.H > 1:
+        rel, u, vb = (np.repeat(t, w.H, axis=0) for t in (rel, u, vb))
+    out = []
+    for b in batches:
+        sl = lambda t: t[b:b + 1].double().numpy()
+        kv = None if x["kv_len"] is None else x["kv_len"][b:b + 1].numpy()
+        out.append(txl.txl_fwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), rel, u, vb, w.causal,
+                               w.softmax_scale, kv_len=kv))
     return out
 
 
@@ -309,6 +334,8 @@ def oracle_rows_call(w, x, rows, nthreads):
         return oracle_decode_rows(w, x, rows, nthreads)
     if w.kind == "bwd":  # rows are sequence indices
         return oracle_bwd_batches(w, x, rows)
+    if w.kind == "txl":  # rows are sequence indices
+        return oracle_txl_batches(w, x, rows)
 
     kv = None if x.get("kv_len") is None else x["kv_len"].numpy()
     if w.kind == "t5":
@@ -339,7 +366,7 @@ def oracle_rows_call(w, x, rows, nthreads):
 def row_flops(w, kv_len, rows):
     """Algorithmic FLOPs of a set of flat row ids (same accounting as algorithmic_flops);
     for the decode step the ids are sequences (all heads)."""
-    if w.kind in ("decode", "bwd"):
+    if w.kind in ("decode", "bwd", "txl"):
         return algorithmic_flops(w.replace(B=len(rows)),
                                  None if kv_len is None else [kv_len[int(b)] for b in rows])
     total = 0.0
@@ -364,7 +391,7 @@ def time_oracle(w, x, budget_s: float, seed: int = 1, nthreads=None):
     import oracle
     nthreads = nthreads or oracle.default_threads()
     rng = np.random.default_rng(seed)
-    total_rows = w.B if w.kind in ("decode", "bwd") else w.B * w.H * w.n
+    total_rows = w.B if w.kind in ("decode", "bwd", "txl") else w.B * w.H * w.n
     kv = key_lengths(w, x)
     # calibrate on a small batch of rows
     count = min(total_rows, max(nthreads * 4, 64))
@@ -390,10 +417,11 @@ def time_oracle(w, x, budget_s: float, seed: int = 1, nthreads=None):
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
             "sample": "%d of %d %s (random, seed %d) x %d pass(es), fp64 %s, "
                       "%.1f s" % (target, total_rows,
-                                  "sequences (all heads)" if w.kind in ("decode", "bwd")
+                                  "sequences (all heads)" if w.kind in ("decode", "bwd", "txl")
                                   else "query rows",
                                   seed, passes,
-                                  "numpy gradient oracle" if w.kind == "bwd" else "C loop",
+                                  "numpy gradient oracle" if w.kind == "bwd" else
+                                  "numpy Transformer-XL oracle" if w.kind == "txl" else "C loop",
                                   dt)}, fl, dt
 
 
@@ -426,6 +454,10 @@ def gpu_call(rp, w, g, out, stream):
     if w.kind == "alibi":
         return rp.relattn_alibi_fwd(g["q"], g["k"], g["v"], g["slopes"], w.causal,
                                     w.softmax_scale, kv_len=g["kv_len"], out=out, stream=stream)
+    if w.kind == "txl":
+        return rp.relattn_txl_fwd(g["q"], g["k"], g["v"], g["rel"], g["u"], g["vb"],
+                                  causal=w.causal, scale=w.softmax_scale, kv_len=g["kv_len"],
+                                  out=out, stream=stream)
     if w.kind == "labeled":
         return rp.relattn_labeled_fwd(g["q"], g["k"], g["v"], g["labels"], aK=g["aK"], aV=g["aV"],
                                       causal=w.causal, scale=w.softmax_scale, kv_len=g["kv_len"],
@@ -470,6 +502,7 @@ def workload_config(w, world: int, l2_note: str) -> dict:
             "clip_k": w.clip_k if w.kind in ("shaw", "decode", "bwd", "offset") else None,
             "causal": w.causal,
             "terms": ("t5 bias" if w.kind == "t5" else
+                      "Transformer-XL (q+u).k + (q+v).r over every offset" if w.kind == "txl" else
                       "alibi bias (slopes 2^(-%g(h+1)/H))" % w.alibi_max_bias
                       if w.kind == "alibi" else
                       "per-offset scalar bias, radius %d" % w.clip_k if w.kind == "offset" else
@@ -603,7 +636,7 @@ def roofline(w, flops, byts, kern_ms, peaks, peak_src):
     """Bound, achieved and fraction of the dominant roof for one launch of kern_ms."""
     # the gradients run on the SIMT units (fp32 FMA roof); labelled edges on the tensor cores
     # for bf16 (the fp32 inputs take the SIMT kernel)
-    alu = w.kind == "bwd" or (w.kind == "labeled" and w.dtype != "bf16")
+    alu = w.kind in ("bwd", "txl") or (w.kind == "labeled" and w.dtype != "bf16")
     compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
     t_roof_compute = flops / (compute_peak * 1e12)
     t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
@@ -745,7 +778,7 @@ def run_ours(args, rank, world, local_rank):
 
     # the gradients run on the SIMT units (fp32 FMA roof); labelled edges on the tensor cores
     # for bf16 (the fp32 inputs take the SIMT kernel)
-    alu = w.kind == "bwd" or (w.kind == "labeled" and w.dtype != "bf16")
+    alu = w.kind in ("bwd", "txl") or (w.kind == "labeled" and w.dtype != "bf16")
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(w, x, args.cpu_budget)

@@ -181,6 +181,31 @@ RELATTN_API relattn_status_t relattn_labeled_fwd(const void *q, const void *k, c
                                      void *out, relattn_stream_t stream);
 
 /*
+ * relattn_txl_fwd — Transformer-XL relative attention ("Relative Position Encoding in
+ * Transformer-XL" page: the four-term score and the roles of the global biases u and v;
+ * "Relative position embeddings" page, section "Transformer-XL"):
+ *
+ *   A_ij = q_i . k_j + q_i . r_ij + u . k_j + v . r_ij,    r_ij = rel[h][j - i + n - 1]
+ *   z_i  = sum_j softmax_j(scale * A)_ij v_j
+ *
+ * over the allowed keys (j < kv_len[b], and j <= i if causal); a row with no allowed key is
+ * written as zeros. Unlike relattn_fwd the offsets are not clipped and there is no value term.
+ *   q, k, v           [B, H, n, d] of `dtype` (16-byte aligned).
+ *   rel               [H, 2n - 1, d] of `dtype` (16-byte aligned): row o holds the projected
+ *                     encoding of the offset j - i = o - (n - 1), i.e. W_{k,R} r(j - i).
+ *   u, vb             [H, d] of `dtype`: the global content bias u and position bias v.
+ *   shared            1: rel, u and vb are a single set ([1, 2n - 1, d], [1, d]) for all heads.
+ *   causal, scale, kv_len, B, H, n, d, dtype, out, stream   as in relattn_fwd; d <= 128 and a
+ *                     multiple of 8 (bf16) / 4 (fp32), else RELATTN_ERR_UNSUPPORTED.
+ * Runs on the SIMT units with fp32 arithmetic: one warp per query row, the two dot products
+ * (q_i + u) . k_j and (q_i + v) . r_ij per key.
+ */
+RELATTN_API relattn_status_t relattn_txl_fwd(const void *q, const void *k, const void *v,
+                                 const void *rel, const void *u, const void *vb, int shared,
+                                 int causal, float scale, const int *kv_len, int B, int H, int n,
+                                 int d, int dtype, void *out, relattn_stream_t stream);
+
+/*
  * relattn_decode_fwd — one incremental decoding step of a causal decoder: the new token of
  * every sequence attends to its sequence's key/value cache with the relative terms of
  * relattn_fwd ("Self-Attention with Relative Position Representations" page, section 3.4, eq. 3 and eq. 4 with clip(j - i, k)).

@@ -42,6 +42,9 @@ _lib.relattn_labeled_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, 
                                      ctypes.c_longlong, _I, ctypes.c_float, _P, _I, _I, _I, _I,
                                      _I, _P, _P]
 _lib.relattn_labeled_fwd.restype = _I
+_lib.relattn_txl_fwd.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, ctypes.c_float, _P, _I, _I, _I,
+                                 _I, _I, _P, _P]
+_lib.relattn_txl_fwd.restype = _I
 _lib.relattn_decode_fwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, ctypes.c_float, _P,
                                     _I, _I, _I, _I, _P, ctypes.c_ulonglong, _P, _P]
 _lib.relattn_decode_fwd.restype = _I
@@ -71,7 +74,7 @@ _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
 EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
-            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_decode_fwd",
+            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_txl_fwd", "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
@@ -243,6 +246,36 @@ def relattn_offset_bias_fwd(q, k, v, table, radius, causal=False, scale=None, kv
                                       int(radius), int(bool(causal)), float(scale),
                                       _ptr(kv_len), B, H, n, d, dt, _ptr(out), _stream(stream))
     _check(st, "relattn_offset_bias_fwd")
+    return out
+
+
+def relattn_txl_fwd(q, k, v, rel, u, vb, causal=False, scale=None, kv_len=None, out=None,
+                    stream=None):
+    """Transformer-XL relative attention: score (q_i + u) . k_j + (q_i + v) . rel[j - i + n - 1]
+    ("Relative Position Encoding in Transformer-XL" page, the four-term score).
+
+    rel: [H or 1, 2n - 1, d], u and vb: [H or 1, d], all of q's dtype (one set for every head
+    when the first dimension is 1 and H > 1). scale defaults to 1/sqrt(d). Returns out.
+    """
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    for t, nm in ((rel, "rel"), (u, "u"), (vb, "vb")):
+        _dev(t, nm, q.dtype)
+    if rel.dim() != 3 or rel.shape[1:] != (2 * n - 1, d) or u.dim() != 2 or vb.dim() != 2:
+        raise ValueError("rel must be [H or 1, 2n - 1, d], u and vb [H or 1, d]")
+    shared = 1 if (rel.shape[0] == 1 and H > 1) else 0
+    if rel.shape[0] != (1 if shared else H) or u.shape != (rel.shape[0], d) or vb.shape != u.shape:
+        raise ValueError("rel, u and vb must have one entry per head, or one for all")
+    _dev(kv_len, "kv_len", torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    _dev(out, "out", q.dtype)
+    if scale is None:
+        scale = d ** -0.5
+    st = _lib.relattn_txl_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(rel), _ptr(u), _ptr(vb), shared,
+                              int(bool(causal)), float(scale), _ptr(kv_len), B, H, n, d, dt,
+                              _ptr(out), _stream(stream))
+    _check(st, "relattn_txl_fwd")
     return out
 
 

@@ -308,6 +308,39 @@ relattn_status_t relattn_labeled_fwd(const void *q, const void *k, const void *v
     return from_cuda(relattn::launch_labeled(a, cs));
 }
 
+relattn_status_t relattn_txl_fwd(const void *q, const void *k, const void *v, const void *rel,
+                                 const void *u, const void *vb, int shared, int causal, float scale,
+                                 const int *kv_len, int B, int H, int n, int d, int dtype,
+                                 void *out, relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, out, B, H, n, d, dtype);
+    // this path takes any head dimension up to 128 whose rows are whole 16-byte vectors
+    if (st != RELATTN_OK && st != RELATTN_ERR_UNSUPPORTED) return st;
+    if (!shapes_ok(B, H, n, d)) return RELATTN_ERR_INVALID_ARG;
+    if ((long long)H * (2LL * n - 1) * d > (1LL << 40)) return RELATTN_ERR_INVALID_ARG;
+    const int vec = dtype == RELATTN_BF16 ? 8 : 4;
+    if (d > 128 || d % vec != 0) return RELATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return RELATTN_ERR_INVALID_ARG;
+    if (!rel || !u || !vb || !aligned(rel, 16)) return RELATTN_ERR_INVALID_ARG;
+    const uintptr_t el = dtype == RELATTN_BF16 ? 2 : 4;
+    if (!aligned(u, el) || !aligned(vb, el)) return RELATTN_ERR_INVALID_ARG;
+    if ((shared != 0 && shared != 1) || (causal != 0 && causal != 1)) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    relattn::TxlArgs a{};
+    a.q = q; a.k = k; a.v = v; a.rel = rel; a.u = u; a.vb = vb;
+    a.shared = shared;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
+    a.out = out;
+    return from_cuda(relattn::launch_txl(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
                                             const void *v_cache, const void *aK, const void *aV,
                                             long long table_head_stride, int clip_k, float scale,

@@ -119,6 +119,22 @@ cudaError_t launch_labeled(const LabeledArgs &a, cudaStream_t s);
 // other combination, checked before any launch
 cudaError_t launch_labeled_tc(const LabeledArgs &a, cudaStream_t s);
 
+// ---- Transformer-XL relative attention (SIMT, fp32 arithmetic) -----------------------------
+struct TxlArgs {
+    const void *q, *k, *v;   // [B, H, n, d]
+    const void *rel;         // [H|1, 2n - 1, d]: the projected encoding of offset j - i at row j - i + n - 1
+    const void *u, *vb;      // [H|1, d]: the global content and position biases
+    int shared;              // 1: rel, u and vb are one set for every head
+    int causal;
+    float scale;
+    const int *kv_len;
+    int B, H, n, d;
+    int bf16;
+    void *out;
+};
+// cudaErrorNotSupported when d > 128
+cudaError_t launch_txl(const TxlArgs &a, cudaStream_t s);
+
 // ---- gradients (SIMT, fp32 arithmetic) ---------------------------------------------------
 struct BwdArgs {
     const void *q, *k, *v, *aK, *aV, *dout;

@@ -12,7 +12,7 @@ max_distance 128). No dataset is read:
 every value is drawn from a torch CPU generator seeded by the caller.
 
 Draw order (fp32 draws, then a round-to-nearest-even cast to the workload dtype):
-Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. ALiBi: q, k, v, kv_len (the slopes are
+Shaw: q, k, v, a^K, a^V, kv_len. T5: q, k, v, bias. Transformer-XL: q, k, v, rel, u, v, kv_len. ALiBi: q, k, v, kv_len (the slopes are
 fixed, not drawn). Clipped offset table: q, k, v, table, kv_len. Labelled edges: q, k, v,
 a^K, a^V (num_labels rows), labels ~ U{0..num_labels-1} per pair (uint8), kv_len. N(0, s^2) means s * randn.
 """
@@ -34,8 +34,8 @@ class Workload:
     d: int
     dtype: str                      # "bf16" or "f32"
     kind: str = "shaw"              # "shaw", "t5", "alibi", "offset" (clipped per-offset scalar
-                                    # table), "labeled" (label matrix), "decode" (one decoding
-                                    # step), "bwd" (gradients)
+                                    # table), "labeled" (label matrix), "txl" (Transformer-XL),
+                                    # "decode" (one decoding step), "bwd" (gradients)
     clip_k: int = 0                 # Shaw clip distance; the table radius for "offset"
     causal: bool = False
     key_term: bool = True           # a^K present (Shaw)
@@ -109,6 +109,14 @@ LABELED_WORKLOADS = {
                               kv_len_range=(256, 512)),
 }
 
+# Transformer-XL ("Relative Position Encoding in Transformer-XL" page): a causal decoder of
+# the T5 case's shape with projected encodings of every offset and the global biases u and v
+# (all N(0, 0.5^2): large enough that every term moves the output).
+TXL_WORKLOADS = {
+    "txl_decoder": Workload("txl_decoder", B=8, H=12, n=1024, d=64, dtype="bf16", kind="txl",
+                            causal=True, table_std=0.5, scale=1.0 / 8),
+}
+
 # Gradients of the base encoder (kind "bwd"): the forward's inputs plus dout ~ N(0, 1) drawn
 # after them.
 BWD_WORKLOADS = {
@@ -143,6 +151,16 @@ def draw_inputs(w: Workload, seed: int = 0) -> dict:
         out["bias"] = torch.randn((w.num_buckets, w.H), generator=g,
                                   dtype=torch.float32) * w.bias_std
         out["kv_len"] = None
+        return out
+    if w.kind == "txl":  # projected offset encodings [H|1, 2n-1, d], then u and v [H|1, d]
+        Ht = 1 if w.shared_tables else w.H
+        out["rel"] = normal((Ht, 2 * w.n - 1, w.d), w.table_std)
+        out["u"] = normal((Ht, w.d), w.table_std)
+        out["vb"] = normal((Ht, w.d), w.table_std)
+        out["kv_len"] = None
+        if w.kv_len_range is not None:
+            lo, hi = w.kv_len_range
+            out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int32)
         return out
     if w.kind in ("alibi", "offset"):
         if w.kind == "alibi":

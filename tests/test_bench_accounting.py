@@ -90,3 +90,11 @@ def test_labelled_row_counts_add_up_to_the_launch():
                     causal=True)
     rows = np.arange(w.B * w.H * w.n)
     assert bench.row_flops(w, [9, 4], rows) == pytest.approx(bench.algorithmic_flops(w, [9, 4]))
+
+
+def test_txl_counts_three_dot_products_per_pair_and_the_offset_table():
+    # B=1, H=1, n=3, d=2, causal: pairs 1 + 2 + 3 = 6; FLOPs 6 d per pair = 72. Bytes (bf16):
+    # q, out 2 * 6 elements, k, v 2 * 6, rel (2n - 1) * d = 10 and u, v 2 * d = 4 -> 38 * 2
+    w = wl.Workload("x", B=1, H=1, n=3, d=2, dtype="bf16", kind="txl", causal=True)
+    assert bench.algorithmic_flops(w, None) == 72.0
+    assert bench.algorithmic_bytes(w, None) == 76.0

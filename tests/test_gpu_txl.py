@@ -1,0 +1,72 @@
+"""GPU parity of relattn_txl_fwd (Transformer-XL relative attention) against the fp64 oracle
+oracle/txl.py, on the same seeded inputs. Tolerances as elsewhere: bf16 inputs with fp32
+arithmetic max|gpu - ref| <= 1e-2 * max|ref| + 1e-3; fp32 <= 1e-5 * max|ref|."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import txl
+from relative_position_representations_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def _rp():
+    import relative_position_representations_gb300 as rp
+    return rp
+
+
+def run_case(w, seed):
+    rp = _rp()
+    x = wl.draw_inputs(w, seed)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    got = rp.relattn_txl_fwd(g["q"], g["k"], g["v"], g["rel"], g["u"], g["vb"], causal=w.causal,
+                             scale=w.softmax_scale, kv_len=g["kv_len"])
+    torch.cuda.synchronize()
+    f = lambda t: t.double().numpy()
+    H = w.H
+    rel, u, vb = f(x["rel"]), f(x["u"]), f(x["vb"])
+    if rel.shape[0] == 1 and H > 1:  # one set for every head
+        rel, u, vb = (np.repeat(t, H, axis=0) for t in (rel, u, vb))
+    ref = txl.txl_fwd(f(x["q"]), f(x["k"]), f(x["v"]), rel, u, vb, w.causal, w.softmax_scale,
+                      kv_len=None if x["kv_len"] is None else x["kv_len"].numpy())
+    got = got.float().cpu().numpy()
+    m = float(np.abs(ref).max())
+    tol = 1e-5 * m if w.dtype == "f32" else 1e-2 * m + 1e-3
+    assert np.isfinite(got).all()
+    err = float(np.abs(got - ref).max())
+    assert err <= tol, "%s: max|err| %.3e > tol %.3e" % (w.name, err, tol)
+    assert rp.relattn_get_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype,n,d,causal,kv,shared", [
+    ("bf16", 200, 64, True, None, False),
+    ("bf16", 129, 128, False, (1, 129), False),
+    ("bf16", 64, 32, False, None, True),
+    ("f32", 77, 32, True, (10, 77), False),
+    ("f32", 50, 128, False, None, True),
+    ("f32", 1, 8, True, None, False),
+])
+def test_txl_matches_the_oracle(dtype, n, d, causal, kv, shared):
+    w = wl.Workload("txl_case", B=2, H=3, n=n, d=d, dtype=dtype, kind="txl", causal=causal,
+                    kv_len_range=kv, shared_tables=shared, table_std=0.5, qkv_std=0.7)
+    run_case(w, seed=n + d)
+
+
+def test_txl_decoder_workload():
+    run_case(wl.TXL_WORKLOADS["txl_decoder"].replace(B=2), seed=3)
+
+
+def test_txl_sign_of_the_offset_matters():
+    """Reversing the offset table (o -> 2n - 2 - o, i.e. j - i -> i - j) changes the output:
+    the kernel reads rel at j - i + n - 1, not at i - j + n - 1."""
+    rp = _rp()
+    w = wl.Workload("txl_sign", B=1, H=2, n=96, d=64, dtype="f32", kind="txl", table_std=0.5)
+    x = wl.draw_inputs(w, 11)
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    a = rp.relattn_txl_fwd(g["q"], g["k"], g["v"], g["rel"], g["u"], g["vb"]).cpu()
+    b = rp.relattn_txl_fwd(g["q"], g["k"], g["v"], g["rel"].flip(1).contiguous(), g["u"],
+                           g["vb"]).cpu()
+    assert float((a - b).abs().max()) > 1e-2
