@@ -370,6 +370,16 @@ RELATTN_API relattn_status_t relattn_set_wait_limit(long long cycles);
  */
 RELATTN_API relattn_status_t relattn_debug_withhold_first_load(int on);
 
+/*
+ * relattn_set_short_kernel — routing switch of the bf16 forward. With on = 1 (the default),
+ * relattn_fwd calls with n <= 256, d = 64 and at most 64 staged table rows (clip_k + 1
+ * causal, 2*clip_k + 1 otherwise) run on the short-sequence kernel, which keeps all of a
+ * query tile's keys on chip and runs two CTAs per SM; on = 0 sends them to the general
+ * kernel. Both compute the same eq. 3 / eq. 4 (results agree to rounding). Process-wide,
+ * read at each call; any other value is RELATTN_ERR_INVALID_ARG.
+ */
+RELATTN_API relattn_status_t relattn_set_short_kernel(int on);
+
 /* Static English text for a status code. */
 RELATTN_API const char *relattn_status_string(relattn_status_t s);
 

@@ -70,6 +70,8 @@ _lib.relattn_set_wait_limit.argtypes = [ctypes.c_longlong]
 _lib.relattn_set_wait_limit.restype = _I
 _lib.relattn_debug_withhold_first_load.argtypes = [_I]
 _lib.relattn_debug_withhold_first_load.restype = _I
+_lib.relattn_set_short_kernel.argtypes = [_I]
+_lib.relattn_set_short_kernel.restype = _I
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
@@ -78,7 +80,7 @@ EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
-            "relattn_debug_withhold_first_load",
+            "relattn_debug_withhold_first_load", "relattn_set_short_kernel",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
 
@@ -500,6 +502,13 @@ def relattn_debug_withhold_first_load(on: bool) -> None:
     st = int(_lib.relattn_debug_withhold_first_load(1 if on else 0))
     if st != OK:
         raise RelattnError(st, "relattn_debug_withhold_first_load")
+
+
+def relattn_set_short_kernel(on: bool) -> None:
+    """Route bf16 forwards of at most 256 keys with d = 64 to the short-sequence kernel (default)."""
+    st = int(_lib.relattn_set_short_kernel(1 if on else 0))
+    if st != OK:
+        raise RelattnError(st, "relattn_set_short_kernel")
 
 
 def raw_call(name, *args):

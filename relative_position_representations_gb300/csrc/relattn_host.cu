@@ -95,6 +95,7 @@ relattn_status_t check_qkv(const void *q, const void *k, const void *v, const vo
 // read at each launch
 std::atomic<long long> g_wait_limit{2000000000ll};
 std::atomic<int> g_withhold_q{0};
+std::atomic<int> g_short_kernel{1};
 
 relattn_status_t dispatch_bf16(const relattn::TcArgs &args, const relattn::T5Buckets *t5,
                                cudaStream_t s) {
@@ -106,6 +107,10 @@ relattn_status_t dispatch_bf16(const relattn::TcArgs &args, const relattn::T5Buc
     relattn::TcArgs a = args;
     a.wait_limit = g_wait_limit.load();
     a.withhold_q = g_withhold_q.load();
+    if (g_short_kernel.load() && relattn::short_kernel_covers(a)) {
+        const cudaError_t e = relattn::launch_short_bf16(a, err, s);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
     const cudaError_t e = a.d == 64 ? relattn::launch_tc_bf16_d64(a, t5, err, s)
                                     : relattn::launch_tc_bf16_d128(a, t5, err, s);
     return from_cuda(e);
@@ -498,6 +503,12 @@ relattn_status_t relattn_debug_withhold_first_load(int on) {
     return RELATTN_OK;
 }
 
-int relattn_version(void) { return 101; }
+relattn_status_t relattn_set_short_kernel(int on) {
+    if (on != 0 && on != 1) return RELATTN_ERR_INVALID_ARG;
+    g_short_kernel.store(on);
+    return RELATTN_OK;
+}
+
+int relattn_version(void) { return 102; }
 
 }  // extern "C"

@@ -76,6 +76,11 @@ struct TcArgs {
 // before any launch), cudaErrorInvalidValue for bad tensor-map parameters.
 cudaError_t launch_tc_bf16_d64(const TcArgs &a, const T5Buckets *t5, int *err, cudaStream_t s);
 cudaError_t launch_tc_bf16_d128(const TcArgs &a, const T5Buckets *t5, int *err, cudaStream_t s);
+// Sequences of at most 256 keys with d = 64 and the Shaw tables (at most 64 staged rows):
+// the short-sequence kernel. short_kernel_covers says whether it takes the call;
+// launch_short_bf16 returns cudaErrorNotSupported for anything else (checked before any launch).
+bool short_kernel_covers(const TcArgs &a);
+cudaError_t launch_short_bf16(const TcArgs &a, int *err, cudaStream_t s);
 
 // ---- bf16 decode step ----------------------------------------------------------------------
 struct DecodeArgs {

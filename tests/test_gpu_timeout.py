@@ -6,7 +6,9 @@ announce the Q tiles of its first work item without loading them, so the tensor-
 wait for them runs out: the kernel then takes its abort path (every role stops at its next
 wait, waits for its copies and tensor-core operations in flight, frees its tensor memory and
 exits). The host must read RELATTN_ERR_TIMEOUT once (the read clears it), and a normal launch
-on the same context must still match the oracle.
+on the same context must still match the oracle. Each case runs with the short-sequence
+kernel enabled and disabled (the split-feed case is the one it takes; the other two shapes
+stay on the general kernel either way).
 """
 import numpy as np
 import pytest
@@ -62,18 +64,21 @@ def _oracle(w, x):
                               table_head_stride=wl.table_head_stride(w))
 
 
+@pytest.mark.parametrize("short", [True, False], ids=["short_on", "short_off"])
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_withheld_load_times_out_and_the_context_stays_usable(w):
+def test_withheld_load_times_out_and_the_context_stays_usable(w, short):
     rp = _rp()
     x = wl.draw_inputs(w, seed=3)
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     assert rp.relattn_get_device_error() == 0
     rp.relattn_set_wait_limit(1_000_000)
     rp.relattn_debug_withhold_first_load(True)
+    rp.relattn_set_short_kernel(short)
     try:
         _call(rp, w, g)
         status = rp.relattn_get_device_error()
     finally:
+        rp.relattn_set_short_kernel(True)
         rp.relattn_debug_withhold_first_load(False)
         rp.relattn_set_wait_limit(2_000_000_000)
     assert status == TIMEOUT, "expected the timeout status, got %d" % status
