@@ -139,6 +139,7 @@ KERNEL_SOURCES = {
               "relattn_tc_kernel.cuh", "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
     "decode": ["relattn_decode.cu"],
     "bwd": ["relattn_bwd.cu"],
+    "bwd_tc": ["relattn_bwd_tc.cu", "relattn_tc_kernel.cuh", "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
     "labeled": ["relattn_labeled_tc.cuh", "relattn_labeled_tc.cu", "relattn_tc_kernel.cuh",
                 "sm103_ptx.cuh"],
     "txl": ["relattn_txl.cu"],
@@ -147,8 +148,23 @@ KERNEL_SOURCES = {
 }
 
 
+def bwd_on_tensor_cores(w) -> bool:
+    """The library routes bf16 gradients with d = 64 / 128 and at most 128 staged table rows
+    to its tensor-core kernels (the others run on the SIMT kernels)."""
+    rows = w.clip_k + 1 if w.causal else 2 * w.clip_k + 1
+    return w.kind == "bwd" and w.dtype == "bf16" and w.d in (64, 128) and rows <= 128
+
+
+def simt_roof(w) -> bool:
+    """Workloads whose kernels run on the SIMT units (roof: the derived fp32 FMA rate)."""
+    return (w.kind == "txl" or (w.kind == "bwd" and not bwd_on_tensor_cores(w)) or
+            (w.kind == "labeled" and w.dtype != "bf16"))
+
+
 def kernel_family(w) -> str:
     fam = {"decode": "decode", "bwd": "bwd", "labeled": "labeled", "txl": "txl"}.get(w.kind, "fused")
+    if fam == "bwd" and bwd_on_tensor_cores(w):
+        fam = "bwd_tc"
     if fam == "fused" and w.kind == "shaw" and w.dtype == "bf16" and w.d == 64 and w.n <= 256:
         rows = (w.clip_k + 1 if w.causal else 2 * w.clip_k + 1) if (w.key_term or w.value_term) else 1
         if rows <= 64:  # the library routes these to the short-sequence kernel
@@ -660,9 +676,7 @@ def l2_flushed_launch_ms(rp, w, g, o, dev, stream, reps=20):
 
 def roofline(w, flops, byts, kern_ms, peaks, peak_src):
     """Bound, achieved and fraction of the dominant roof for one launch of kern_ms."""
-    # the gradients run on the SIMT units (fp32 FMA roof); labelled edges on the tensor cores
-    # for bf16 (the fp32 inputs take the SIMT kernel)
-    alu = w.kind in ("bwd", "txl") or (w.kind == "labeled" and w.dtype != "bf16")
+    alu = simt_roof(w)
     compute_peak = FP32_SIMT_TFLOPS if alu else peaks["bf16_tflops"]
     t_roof_compute = flops / (compute_peak * 1e12)
     t_roof_mem = byts / (peaks["hbm_gbs"] * 1e9)
@@ -802,9 +816,7 @@ def run_ours(args, rank, world, local_rank):
         for name in [a for a in args.also.split(",") if a and a != w.name]:
             also.append(measure_also(rp, name, args, dev, stream, peaks, peak_src))
 
-    # the gradients run on the SIMT units (fp32 FMA roof); labelled edges on the tensor cores
-    # for bf16 (the fp32 inputs take the SIMT kernel)
-    alu = w.kind in ("bwd", "txl") or (w.kind == "labeled" and w.dtype != "bf16")
+    alu = simt_roof(w)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu, _, _ = time_oracle(w, x, args.cpu_budget)

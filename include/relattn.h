@@ -304,11 +304,21 @@ RELATTN_API relattn_status_t relattn_decode_workspace_size(int B, int H, int T, 
  *                     accumulated); required when the matching table is given, ignored
  *                     otherwise.
  *   workspace         caller-owned device scratch of at least relattn_bwd_workspace_size
- *                     bytes (4-byte aligned); its contents are scratch.
+ *                     bytes (4-byte aligned; 256-byte aligned for the tensor-core path);
+ *                     its contents are scratch (per query row: the softmax statistics, the
+ *                     relative terms R and Rv with them folded in, the bins).
  *
- * Arithmetic is fp32 on the SIMT units (three kernels: one warp per query row, one warp per
- * key, one CTA per table row), so it is a first, correct version rather than a fast one.
- * 2*clip_k + 1 <= 257.
+ * Two paths (relattn_set_bwd_tensor_cores chooses). Tensor cores, for bf16 with d = 64 or
+ * 128 and at most 128 staged table rows (clip_k + 1 causal, 2*clip_k + 1 otherwise): a
+ * query-tile kernel forms S = Q K^T and dP = dZ V^T on tcgen05 and takes each row's softmax
+ * statistics and bins; a key-tile kernel recomputes S^T and dP^T, forms P and dS and
+ * accumulates dV = P^T dZ and dK = dS^T Q in tensor memory, adding dQ = dS K into dq with
+ * atomic adds; a SIMT kernel adds the table terms of dq and the table gradients. P, dS and
+ * the bins enter the products as bf16 (fp32 accumulation). SIMT, for everything else
+ * (fp32 inputs, any 1 <= d <= 128, 2*clip_k + 1 <= 257): fp32 arithmetic from the exact
+ * inputs, three kernels (one warp per query row, one warp per key, one CTA per table row).
+ * Device waits of the tensor-core path are bounded as in relattn_fwd (relattn_set_wait_limit;
+ * RELATTN_ERR_TIMEOUT through relattn_get_device_error).
  */
 RELATTN_API relattn_status_t relattn_bwd(const void *q, const void *k, const void *v,
                              const void *aK, const void *aV, long long table_head_stride,
@@ -379,6 +389,17 @@ RELATTN_API relattn_status_t relattn_debug_withhold_first_load(int on);
  * read at each call; any other value is RELATTN_ERR_INVALID_ARG.
  */
 RELATTN_API relattn_status_t relattn_set_short_kernel(int on);
+
+/*
+ * relattn_set_bwd_tensor_cores — routing switch of relattn_bwd. With on = 1 (the default),
+ * bf16 calls with d = 64 or 128, at most 128 staged table rows (clip_k + 1 causal,
+ * 2*clip_k + 1 otherwise) and a workspace aligned to 256 bytes run on the tensor-core
+ * kernels; on = 0 sends them to the SIMT kernels (fp32 arithmetic from the exact inputs).
+ * Both compute the same gradients, the tensor-core path with bf16 operands in its products
+ * (P, dS and the bins rounded to bf16). Process-wide, read at each call; any other value
+ * is RELATTN_ERR_INVALID_ARG.
+ */
+RELATTN_API relattn_status_t relattn_set_bwd_tensor_cores(int on);
 
 /* Static English text for a status code. */
 RELATTN_API const char *relattn_status_string(relattn_status_t s);

@@ -15,6 +15,7 @@ _BINDING = ("relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
             "relattn_debug_withhold_first_load", "relattn_set_short_kernel",
+            "relattn_set_bwd_tensor_cores",
             "relattn_get_device_error", "relattn_status_string", "relattn_version",
             "RelattnError")
 

@@ -72,6 +72,8 @@ _lib.relattn_debug_withhold_first_load.argtypes = [_I]
 _lib.relattn_debug_withhold_first_load.restype = _I
 _lib.relattn_set_short_kernel.argtypes = [_I]
 _lib.relattn_set_short_kernel.restype = _I
+_lib.relattn_set_bwd_tensor_cores.argtypes = [_I]
+_lib.relattn_set_bwd_tensor_cores.restype = _I
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
@@ -80,7 +82,7 @@ EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
-            "relattn_debug_withhold_first_load", "relattn_set_short_kernel",
+            "relattn_debug_withhold_first_load", "relattn_set_short_kernel", "relattn_set_bwd_tensor_cores",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
 
 
@@ -509,6 +511,13 @@ def relattn_set_short_kernel(on: bool) -> None:
     st = int(_lib.relattn_set_short_kernel(1 if on else 0))
     if st != OK:
         raise RelattnError(st, "relattn_set_short_kernel")
+
+
+def relattn_set_bwd_tensor_cores(on: bool) -> None:
+    """Route eligible bf16 gradient calls to the tensor-core kernels (default) or the SIMT ones."""
+    st = int(_lib.relattn_set_bwd_tensor_cores(1 if on else 0))
+    if st != OK:
+        raise RelattnError(st, "relattn_set_bwd_tensor_cores")
 
 
 def raw_call(name, *args):

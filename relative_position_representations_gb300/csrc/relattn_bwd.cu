@@ -312,7 +312,9 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t s) {
 }  // namespace bwd
 
 unsigned long long bwd_workspace_bytes(int B, int H, int n, int clip_k) {
-    return (unsigned long long)B * H * n * bwd::rec_floats(2 * clip_k + 1) * sizeof(float);
+    const unsigned long long simt = (unsigned long long)B * H * n * bwd::rec_floats(2 * clip_k + 1) * sizeof(float);
+    const unsigned long long tc = bwd_tc_workspace_bytes(B, H, n, clip_k);
+    return simt > tc ? simt : tc;
 }
 
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s) {

@@ -1,0 +1,901 @@
+// Gradients of the Shaw relation-aware attention forward on the tensor cores (bf16 inputs,
+// head dimension 64 or 128, fp32 gradients).
+//
+// The pages state only the forward pass ("Self-Attention with Relative Position
+// Representations" page, section 3.4: eq. 3, eq. 4 and the softmax); the gradients are the
+// chain rule through it, with r = r_ij = clip(j - i, k) + k and c = scale * log2(e):
+//   x_ij  = c (q_i . k_j + R_ir),            R = Q W^K^T          (log2-domain logit)
+//   p_ij  = 2^(x_ij - lse_i),                 lse_i = log2 sum_j 2^x_ij
+//   dp_ij = dz_i . v_j + Rv_ir,               Rv = dZ W^V^T
+//   ds_ij = p_ij (dp_ij - D_i),               D_i = sum_j p_ij dp_ij
+//   dq_i  = scale (sum_j ds_ij k_j + sum_r gamma_ir w^K_r),   dk_j = scale sum_i ds_ij q_i,
+//   dv_j  = sum_i p_ij dz_i,   dw^K_r = scale sum_i gamma_ir q_i,   dw^V_r = sum_i beta_ir dz_i,
+// with the bins beta_ir = sum_{j: r_ij = r} p_ij and gamma_ir = sum_{j: r_ij = r} ds_ij.
+//
+// Three kernels, in stream order:
+//   stats   one CTA per (head, 128-row query tile): R and Rv by MMA, then S_j = Q K_j^T and
+//           dP_j = dZ V_j^T per key tile (tcgen05, fp32 in TMEM) and an online softmax over
+//           the tile's keys that yields lse_i, D_i and the bins: the two end bins (offsets at
+//           or beyond -k and +k) as rescaled sums, and the interior bins, each of which holds
+//           exactly one key of the row, as that key's logit and dp value. Per row it writes
+//           R'_ir = c R_ir - lse_i and Rv'_ir = Rv_ir - D_i (so that the next kernel needs no
+//           other row statistic) and zeroes dq.
+//   keys    one CTA per (head, 128-key tile), looping over the query tiles that see it:
+//           S^T = K Q_i^T and dP^T = V dZ_i^T (lanes = keys), then per element
+//           p = 2^(c s + R'[r]) and ds = p (dp + Rv'[r]); P^T (bf16) goes back into TMEM and
+//           dS (bf16) into shared memory, and three more MMAs follow: dV += P^T dZ_i,
+//           dK += dS^T Q_i (both accumulated in TMEM over the query tiles) and
+//           dQ_i = dS K (added into dq with vector atomics).
+//   tables  SIMT, one CTA per (head, query tile): the bins from the stats kernel's records,
+//           dq_i += scale sum_r gamma_ir w^K_r and the table gradients (atomic adds).
+// No n x n or n x n x d tensor reaches memory; the workspace holds per-row values only.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "relattn_internal.h"
+#include "relattn_tc_launch.cuh"
+
+namespace relattn {
+namespace btc {
+
+using tc::BM;
+using tc::BN;
+using tc::kLog2e;
+using tc::Shared;
+
+constexpr int kThreads = 192;   // warp 0 loads, warp 1 issues MMAs, warps 2-5 one row each
+constexpr int kRowWarp0 = 2;
+constexpr int kMaxW = 128;      // staged table rows (k + 1 causal, 2k + 1 otherwise)
+constexpr int kRec = 8;         // floats per row record
+constexpr int kMaxStages = 2;
+
+// row record: lse, D, then beta and gamma of the two end bins
+enum : int { kRecLse = 0, kRecD = 1, kRecBL = 2, kRecGL = 3, kRecBR = 4, kRecGR = 5 };
+
+struct Params {
+    int B, H, n, BH, n_tiles;
+    int clip_k, causal, W, Wp;   // staged rows W, rounded up to 16 (N of R = Q W^K^T)
+    int ak, av, bins;            // tables present; bins = ak || av
+    int SK, SV, SR;              // row strides (floats): R' and Rv' rows, shared R rows
+    int table_heads;
+    float c, scale;
+    const int *kv_len;
+    int *err;
+    float *dq, *dk, *dv;
+    float *ws_rk, *ws_rv, *ws_x, *ws_dp, *ws_rec;
+    uint32_t off_q, off_dz, off_k, off_v, off_wk, off_wv, off_r, off_rv, off_ds, off_bar;
+    uint32_t stage_bytes;        // stats: one K (or V) stage; keys: one Q/dZ/R'/Rv' stage
+    int stages;
+    long long wait_limit;
+};
+
+__device__ __forceinline__ int keys_of(const Params &p, int bh) {
+    return p.kv_len ? max(0, min(p.kv_len[bh / p.H], p.n)) : p.n;
+}
+
+// K-major operand with 128-byte swizzle, k-step kk of 16: 64-column block kk / 4 (rows x 128
+// bytes apart), 32 bytes per step inside the block (descriptor units of 16 bytes)
+__device__ __forceinline__ uint64_t kstep(int kk, int rows) {
+    return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+}
+// MN-major operand with 128-byte swizzle, k-step kk of 16 rows: 16 x 128 bytes
+__device__ __forceinline__ uint64_t mnstep(int kk) { return (uint64_t)(kk * 16 * 128 >> 4); }
+
+// instruction descriptor, kind::f16 with A MN-major as well (bit 15)
+__host__ __device__ constexpr uint32_t idesc_amn(uint32_t M, uint32_t N) {
+    return ptx::idesc_bf16(M, N, 1) | (1u << 15);
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}\n"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float *dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+struct Smem {
+    Shared sh;
+    uint32_t bar0;
+    uint32_t tmem_slot;
+};
+
+__device__ __forceinline__ Smem setup_smem(uint8_t *smem_raw, const Params &p) {
+    Smem s;
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    s.sh.base = (raw + 1023u) & ~1023u;
+    s.sh.ptr = smem_raw + (s.sh.base - raw);
+    s.bar0 = s.sh.base + p.off_bar;
+    s.tmem_slot = s.bar0 + 8u * 32u;
+    s.sh.abort_flag = reinterpret_cast<volatile int *>(s.sh.ptr + p.off_bar + 8 * 32 + 4);
+    s.sh.limit = p.wait_limit;
+    return s;
+}
+
+// ============================================================================ stats kernel
+enum : int {
+    A_LD0 = 0, A_R_FULL, A_R_EMPTY, A_S_FULL, A_S_EMPTY, A_DRAIN,
+    A_KV_FULL = 6, A_KV_EMPTY = A_KV_FULL + kMaxStages, kABars = A_KV_EMPTY + kMaxStages
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_stats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
+                     const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = setup_smem(smem_raw, p);
+    const Shared &sh = sm.sh;
+    auto bar = [&](int i) { return sm.bar0 + 8u * (uint32_t)i; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // causal: longest rows first
+    const int qt = p.n_tiles - 1 - (int)blockIdx.x / p.BH, bh = (int)blockIdx.x % p.BH;
+    const int i0 = qt * BM;
+    const int nk = keys_of(p, bh);
+    const int nkc = p.causal ? min(nk, i0 + BM) : nk;
+    const int J = (nkc + BN - 1) / BN;
+    const int th = p.table_heads ? bh % p.H : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kABars; ++i)
+            ptx::mbar_init(bar(i), (i == A_R_EMPTY || i == A_S_EMPTY) ? 128u : 1u);
+        *sh.abort_flag = 0;
+        ptx::mbar_init_fence();
+    }
+    if (warp == 1) ptx::tmem_alloc(sm.tmem_slot, 256);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t *>(sh.ptr + p.off_bar + 8 * 32), 0);
+
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = tc::wait_bar_ctrl(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+
+    if (warp == 0) {
+        // ---------------- loads: Q, dZ and the table rows, then the K/V ring
+        bool ok = true;
+        uint32_t bytes = 2u * BM * D * 2;
+        if (p.ak) bytes += (uint32_t)p.Wp * D * 2;
+        if (p.av) bytes += (uint32_t)p.Wp * D * 2;
+        ptx::mbar_expect_tx_w(bar(A_LD0), bytes);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+            ptx::tma_load_3d_w(sh.base + p.off_q + (uint32_t)(h * BM * 128), &tm_q, bar(A_LD0), 64 * h, i0, bh);
+            ptx::tma_load_3d_w(sh.base + p.off_dz + (uint32_t)(h * BM * 128), &tm_dz, bar(A_LD0), 64 * h, i0, bh);
+            if (p.ak)
+                ptx::tma_load_3d_w(sh.base + p.off_wk + (uint32_t)(h * p.Wp * 128), &tm_wk, bar(A_LD0), 64 * h, 0, th);
+            if (p.av)
+                ptx::tma_load_3d_w(sh.base + p.off_wv + (uint32_t)(h * p.Wp * 128), &tm_wv, bar(A_LD0), 64 * h, 0, th);
+        }
+        int issued = 0;
+        for (int j = 0; j < J && ok; ++j) {
+            const int s = j % p.stages;
+            const uint32_t round = (uint32_t)(j / p.stages);
+            if (!(ok = wait_w(bar(A_KV_EMPTY + s), (round & 1u) ^ 1u))) break;
+            ptx::mbar_expect_tx_w(bar(A_KV_FULL + s), 2u * BN * D * 2);
+            const uint32_t ks = sh.base + p.off_k + (uint32_t)s * p.stage_bytes;
+            const uint32_t vs = sh.base + p.off_v + (uint32_t)s * p.stage_bytes;
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                ptx::tma_load_3d_w(ks + (uint32_t)(h * BN * 128), &tm_k, bar(A_KV_FULL + s), 64 * h, j * BN, bh);
+                ptx::tma_load_3d_w(vs + (uint32_t)(h * BN * 128), &tm_v, bar(A_KV_FULL + s), 64 * h, j * BN, bh);
+            }
+            issued = j + 1;
+        }
+        // drain: no copy may still be in flight when the CTA exits
+        tc::drain_bar(bar(A_LD0), 0, sh.limit);
+        for (int j = issued > p.stages ? issued - p.stages : 0; j < issued; ++j)
+            tc::drain_bar(bar(A_KV_FULL + j % p.stages), (uint32_t)(j / p.stages) & 1u, sh.limit);
+    } else if (warp == 1) {
+        // ---------------- MMA issue
+        const uint64_t dq = ptx::sdesc_sw128(sh.base + p.off_q, 16, 1024);
+        const uint64_t ddz = ptx::sdesc_sw128(sh.base + p.off_dz, 16, 1024);
+        bool ok = wait_w(bar(A_LD0), 0);
+        if (ok) {
+            ptx::tc_fence_after();
+            const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.Wp, 0);
+            if (p.ak) {
+                const uint64_t dw = ptx::sdesc_sw128(sh.base + p.off_wk, 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::tc_mma_w(tmem, dq + kstep(kk, BM), dw + kstep(kk, p.Wp), idR, kk > 0 ? 1u : 0u);
+            }
+            if (p.av) {
+                const uint64_t dw = ptx::sdesc_sw128(sh.base + p.off_wv, 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::tc_mma_w(tmem + 128, ddz + kstep(kk, BM), dw + kstep(kk, p.Wp), idR, kk > 0 ? 1u : 0u);
+            }
+            ptx::tc_commit_w(bar(A_R_FULL));
+            ok = wait_w(bar(A_R_EMPTY), 0);
+        }
+        constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0);
+        for (int j = 0; j < J && ok; ++j) {
+            const int s = j % p.stages;
+            const uint32_t round = (uint32_t)(j / p.stages);
+            if (!(ok = wait_w(bar(A_KV_FULL + s), round & 1u))) break;
+            if (j > 0 && !(ok = wait_w(bar(A_S_EMPTY), (uint32_t)(j - 1) & 1u))) break;
+            ptx::tc_fence_after();
+            const uint64_t dk = ptx::sdesc_sw128(sh.base + p.off_k + (uint32_t)s * p.stage_bytes, 16, 1024);
+            const uint64_t dv = ptx::sdesc_sw128(sh.base + p.off_v + (uint32_t)s * p.stage_bytes, 16, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::tc_mma_w(tmem, dq + kstep(kk, BM), dk + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::tc_mma_w(tmem + 128, ddz + kstep(kk, BM), dv + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+            ptx::tc_commit_w(bar(A_S_FULL));
+            ptx::tc_commit_w(bar(A_KV_EMPTY + s));
+        }
+        ptx::tc_commit_w(bar(A_DRAIN));
+        tc::drain_bar(bar(A_DRAIN), 0, sh.limit);
+    } else if (warp >= kRowWarp0) {
+        // ---------------- one thread per query row (TMEM lane = row)
+        const int quarter = warp & 3;
+        const int il = 32 * quarter + lane, i = i0 + il;
+        const bool row_ok = i < p.n;
+        const long long row = (long long)bh * p.n + i;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+        float *Rs = reinterpret_cast<float *>(sh.ptr + p.off_r) + il * p.SR;
+        float *Rvs = reinterpret_cast<float *>(sh.ptr + p.off_rv) + il * p.SR;
+        const int k = p.clip_k, W = p.W;
+        const bool bidir = !p.causal;
+        const int khi = p.causal ? 0 : k;  // largest offset with a staged row
+        bool ok = tc::wait_bar(bar(A_R_FULL), 0, sh, p.err);
+        ok = __all_sync(0xffffffffu, ok) != 0;
+        if (ok) {
+            ptx::tc_fence_after();
+            for (int c0 = 0; c0 < p.Wp; c0 += 16) {
+                float x[16], y[16];
+                if (p.ak) ptx::tmem_ld16p(lane_base + (uint32_t)c0, reinterpret_cast<uint32_t *>(x));
+                if (p.av) ptx::tmem_ld16p(lane_base + 128u + (uint32_t)c0, reinterpret_cast<uint32_t *>(y));
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    if (c0 + t < W) {
+                        if (p.ak) Rs[c0 + t] = x[t];
+                        if (p.av) Rvs[c0 + t] = y[t];
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(A_R_EMPTY));
+        }
+        float m = -INFINITY, l = 0.f, Dacc = 0.f, Lb = 0.f, Ld = 0.f, Rb = 0.f, Rd = 0.f;
+        for (int j = 0; j < J && ok; ++j) {
+            ok = tc::wait_bar(bar(A_S_FULL), (uint32_t)j & 1u, sh, p.err);
+            if (!(ok = __all_sync(0xffffffffu, ok) != 0)) break;
+            ptx::tc_fence_after();
+            const int j0 = j * BN;
+            // pass 1: logits (log2 domain) back over the scores, and their maximum
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float s[32];
+                ptx::tmem_ld32f(lane_base + (uint32_t)(32 * ch), s);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int jj = j0 + 32 * ch + t, dl = jj - i;
+                    const bool valid = jj < nk && (!p.causal || dl <= 0);
+                    const int r = min(max(dl, -k), khi) + k;
+                    const float x = valid ? p.c * (s[t] + (p.ak ? Rs[r] : 0.f)) : -INFINITY;
+                    mx = fmaxf(mx, x);
+                    s[t] = x;
+                }
+                __syncwarp();
+                ptx::tmem_st32f(lane_base + (uint32_t)(32 * ch), s);
+            }
+            ptx::tmem_st_wait();
+            if (mx > -INFINITY) {
+                const float mn = fmaxf(m, mx);
+                const float al = ptx::ex2(m - mn);  // m = -inf: 0 (the sums are still 0)
+                l *= al; Dacc *= al; Lb *= al; Ld *= al; Rb *= al; Rd *= al;
+                m = mn;
+                // pass 2: probabilities (unnormalised), D and the bins
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    float x[32], dp[32];
+                    ptx::tmem_ld32f(lane_base + (uint32_t)(32 * ch), x);
+                    ptx::tmem_ld32f(lane_base + 128u + (uint32_t)(32 * ch), dp);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int jj = j0 + 32 * ch + t, dl = jj - i;
+                        const int r = min(max(dl, -k), khi) + k;
+                        const float pt = x[t] == -INFINITY ? 0.f : ptx::ex2(x[t] - m);
+                        const float dpf = dp[t] + (p.av ? Rvs[r] : 0.f);
+                        const float tt = pt * dpf;
+                        l += pt;
+                        Dacc += tt;
+                        if (p.bins) {
+                            if (r == 0) {
+                                Lb += pt;
+                                Ld += tt;
+                            } else if (bidir && r == 2 * k) {
+                                Rb += pt;
+                                Rd += tt;
+                            } else if (x[t] != -INFINITY && row_ok) {
+                                // interior bin: exactly one key of the row
+                                p.ws_x[row * W + r] = x[t];
+                                p.ws_dp[row * W + r] = dpf;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(A_S_EMPTY));
+        }
+        if (ok && row_ok) {
+            const float lse = l > 0.f ? m + __log2f(l) : INFINITY;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float Dv = Dacc * inv;
+            float *rec = p.ws_rec + row * kRec;
+            rec[kRecLse] = lse;
+            rec[kRecD] = Dv;
+            rec[kRecBL] = Lb * inv;
+            rec[kRecGL] = Ld * inv - Dv * (Lb * inv);
+            rec[kRecBR] = Rb * inv;
+            rec[kRecGR] = Rd * inv - Dv * (Rb * inv);
+            float *rk = p.ws_rk + row * p.SK;
+            if (p.ak) {
+                for (int r = 0; r < W; ++r) rk[r] = p.c * Rs[r] - lse;
+            } else {
+                rk[0] = -lse;
+            }
+            float *rv = p.ws_rv + row * p.SV;
+            if (p.av) {
+                for (int r = 0; r < W; ++r) rv[r] = Rvs[r] - Dv;
+            } else {
+                rv[0] = -Dv;
+            }
+            float4 *dqr = reinterpret_cast<float4 *>(p.dq + row * D);
+#pragma unroll 4
+            for (int c4 = 0; c4 < D / 4; ++c4) dqr[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 256);
+    }
+}
+
+// ============================================================================= keys kernel
+enum : int {
+    B_KV = 0, B_S_FULL, B_P_FULL, B_DQ_FULL, B_DQ_EMPTY, B_MMA_DONE, B_DKV, B_DRAIN,
+    B_Q_FULL = 8, B_Q_EMPTY = B_Q_FULL + kMaxStages, kBBars = B_Q_EMPTY + kMaxStages
+};
+
+// shared-memory layout of one query stage: Q tile, dZ tile, R' rows, Rv' rows
+template <int D>
+struct QStage {
+    static constexpr uint32_t kTile = (uint32_t)BM * D * 2;
+    static __device__ __forceinline__ uint32_t q(const Params &p, int s) { return p.off_q + (uint32_t)s * p.stage_bytes; }
+    static __device__ __forceinline__ uint32_t dz(const Params &p, int s) { return q(p, s) + kTile; }
+    static __device__ __forceinline__ uint32_t rk(const Params &p, int s) { return q(p, s) + 2 * kTile; }
+    static __device__ __forceinline__ uint32_t rv(const Params &p, int s) {
+        return rk(p, s) + (uint32_t)BM * p.SK * 4;
+    }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_keys_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = setup_smem(smem_raw, p);
+    const Shared &sh = sm.sh;
+    auto bar = [&](int i) { return sm.bar0 + 8u * (uint32_t)i; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // causal: the key tiles with the most query tiles first
+    const int jt = (int)blockIdx.x / p.BH, bh = (int)blockIdx.x % p.BH;
+    const int j0 = jt * BN;
+    const int nk = keys_of(p, bh);
+    const int qs = p.causal ? jt : 0;
+    const int NQ = j0 < nk ? p.n_tiles - qs : 0;
+    using QS = QStage<D>;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kBBars; ++i)
+            ptx::mbar_init(bar(i), (i == B_P_FULL || i == B_DQ_EMPTY) ? 128u : 1u);
+        *sh.abort_flag = 0;
+        ptx::mbar_init_fence();
+    }
+    if (warp == 1) ptx::tmem_alloc(sm.tmem_slot, 512);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t *>(sh.ptr + p.off_bar + 8 * 32), 0);
+    // TMEM columns: S^T (then P^T) at 0, dP^T (then dQ) at 128, dK at 256, dV at 256 + D
+    constexpr uint32_t tS = 0, tDP = 128, tDK = 256, tDV = 256 + D;
+
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = tc::wait_bar_ctrl(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+
+    if (warp == 0) {
+        // ---------------- loads: K and V of this tile once, then Q, dZ, R', Rv' per query tile
+        bool ok = true;
+        int issued = 0;
+        if (NQ > 0) {
+            ptx::mbar_expect_tx_w(bar(B_KV), 2u * BN * D * 2);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                ptx::tma_load_3d_w(sh.base + p.off_k + (uint32_t)(h * BN * 128), &tm_k, bar(B_KV), 64 * h, j0, bh);
+                ptx::tma_load_3d_w(sh.base + p.off_v + (uint32_t)(h * BN * 128), &tm_v, bar(B_KV), 64 * h, j0, bh);
+            }
+        }
+        for (int pi = 0; pi < NQ && ok; ++pi) {
+            const int qt = qs + pi, i0 = qt * BM;
+            const int s = pi % p.stages;
+            const uint32_t round = (uint32_t)(pi / p.stages);
+            if (!(ok = wait_w(bar(B_Q_EMPTY + s), (round & 1u) ^ 1u))) break;
+            const int rows = min(BM, p.n - i0);
+            const uint32_t rk_bytes = (uint32_t)rows * p.SK * 4, rv_bytes = (uint32_t)rows * p.SV * 4;
+            ptx::mbar_expect_tx_w(bar(B_Q_FULL + s), 2u * BM * D * 2 + rk_bytes + rv_bytes);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                ptx::tma_load_3d_w(sh.base + QS::q(p, s) + (uint32_t)(h * BM * 128), &tm_q, bar(B_Q_FULL + s),
+                                   64 * h, i0, bh);
+                ptx::tma_load_3d_w(sh.base + QS::dz(p, s) + (uint32_t)(h * BM * 128), &tm_dz, bar(B_Q_FULL + s),
+                                   64 * h, i0, bh);
+            }
+            const long long row0 = (long long)bh * p.n + i0;
+            bulk_load(sh.base + QS::rk(p, s), p.ws_rk + row0 * p.SK, rk_bytes, bar(B_Q_FULL + s));
+            bulk_load(sh.base + QS::rv(p, s), p.ws_rv + row0 * p.SV, rv_bytes, bar(B_Q_FULL + s));
+            issued = pi + 1;
+        }
+        if (NQ > 0) tc::drain_bar(bar(B_KV), 0, sh.limit);
+        for (int pi = issued > p.stages ? issued - p.stages : 0; pi < issued; ++pi)
+            tc::drain_bar(bar(B_Q_FULL + pi % p.stages), (uint32_t)(pi / p.stages) & 1u, sh.limit);
+    } else if (warp == 1) {
+        // ---------------- MMA issue
+        bool ok = NQ > 0 ? wait_w(bar(B_KV), 0) : true;
+        const uint64_t dk_k = ptx::sdesc_sw128(sh.base + p.off_k, 16, 1024);            // K, K-major
+        const uint64_t dv_k = ptx::sdesc_sw128(sh.base + p.off_v, 16, 1024);            // V, K-major
+        const uint64_t dk_mn = ptx::sdesc_sw128(sh.base + p.off_k, BN * 128, 1024);     // K, MN-major
+        const uint64_t ds_k = ptx::sdesc_sw128(sh.base + p.off_ds, 16, 1024);           // dS^T, K-major
+        const uint64_t ds_mn = ptx::sdesc_sw128(sh.base + p.off_ds, BN * 128, 1024);    // dS, MN-major
+        constexpr uint32_t idS = ptx::idesc_bf16(BN, BM, 0);
+        constexpr uint32_t idG = ptx::idesc_bf16(BN, D, 1);    // dV, dK: B MN-major
+        constexpr uint32_t idQ = idesc_amn(BM, D);             // dQ: A and B MN-major
+        for (int pi = 0; pi < NQ && ok; ++pi) {
+            const int s = pi % p.stages;
+            const uint32_t round = (uint32_t)(pi / p.stages);
+            if (!(ok = wait_w(bar(B_Q_FULL + s), round & 1u))) break;
+            if (pi > 0) {
+                // the previous tile's P^T and dS are read, and its dQ is out of TMEM
+                if (!(ok = wait_w(bar(B_MMA_DONE), (uint32_t)(pi - 1) & 1u))) break;
+                if (!(ok = wait_w(bar(B_DQ_EMPTY), (uint32_t)(pi - 1) & 1u))) break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t dq_k = ptx::sdesc_sw128(sh.base + QS::q(p, s), 16, 1024);
+            const uint64_t ddz_k = ptx::sdesc_sw128(sh.base + QS::dz(p, s), 16, 1024);
+            const uint64_t dq_mn = ptx::sdesc_sw128(sh.base + QS::q(p, s), BM * 128, 1024);
+            const uint64_t ddz_mn = ptx::sdesc_sw128(sh.base + QS::dz(p, s), BM * 128, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)  // S^T = K Q^T
+                ptx::tc_mma_w(tmem + tS, dk_k + kstep(kk, BN), dq_k + kstep(kk, BM), idS, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dZ^T
+                ptx::tc_mma_w(tmem + tDP, dv_k + kstep(kk, BN), ddz_k + kstep(kk, BM), idS, kk > 0 ? 1u : 0u);
+            ptx::tc_commit_w(bar(B_S_FULL));
+            if (!(ok = wait_w(bar(B_P_FULL), (uint32_t)pi & 1u))) break;
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dZ (P^T bf16 pairs in TMEM)
+                ptx::tc_mma_ts_w(tmem + tDV, tmem + tS + (uint32_t)(kk * 8), ddz_mn + mnstep(kk), idG,
+                                 (pi > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q
+                ptx::tc_mma_w(tmem + tDK, ds_k + kstep(kk, BN), dq_mn + mnstep(kk), idG,
+                              (pi > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < BN / 16; ++kk)  // dQ = dS K
+                ptx::tc_mma_w(tmem + tDP, ds_mn + mnstep(kk), dk_mn + mnstep(kk), idQ, kk > 0 ? 1u : 0u);
+            ptx::tc_commit_w(bar(B_DQ_FULL));
+            ptx::tc_commit_w(bar(B_Q_EMPTY + s));
+            ptx::tc_commit_w(bar(B_MMA_DONE));
+        }
+        if (NQ > 0) ptx::tc_commit_w(bar(B_DKV));
+        ptx::tc_commit_w(bar(B_DRAIN));
+        tc::drain_bar(bar(B_DRAIN), 0, sh.limit);
+    } else if (warp >= kRowWarp0) {
+        // ---------------- one thread per key (TMEM lane = key) for P and dS, per query row for dQ
+        const int quarter = warp & 3;
+        const int jl = 32 * quarter + lane, j = j0 + jl;
+        const bool kvalid = j < nk;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+        const int k = p.clip_k;
+        const int khi = p.causal ? 0 : k;  // largest offset with a staged row
+        uint8_t *ds_row = sh.ptr + p.off_ds + jl * 128;
+        const uint32_t sw = (uint32_t)(jl & 7);
+        bool ok = true;
+        for (int pi = 0; pi < NQ && ok; ++pi) {
+            const int qt = qs + pi, i0 = qt * BM;
+            const int s = pi % p.stages;
+            ok = tc::wait_bar(bar(B_S_FULL), (uint32_t)pi & 1u, sh, p.err);
+            if (!(ok = __all_sync(0xffffffffu, ok) != 0)) break;
+            ptx::tc_fence_after();
+            const float *rk = reinterpret_cast<const float *>(sh.ptr + QS::rk(p, s));
+            const float *rv = reinterpret_cast<const float *>(sh.ptr + QS::rv(p, s));
+#pragma unroll 1
+            for (int ch = 0; ch < BM / 32; ++ch) {
+                float sv[32], dpv[32];
+                ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), sv);
+                ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dpv);
+                ptx::tmem_ld_wait();
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int t2 = 0; t2 < 16; ++t2) {
+                    float pe[2], de[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = 2 * t2 + h;
+                        const int il = 32 * ch + t, i = i0 + il, dl = j - i;
+                        const bool valid = kvalid && i < p.n && (!p.causal || dl <= 0);
+                        const int r = min(max(dl, -k), khi) + k;
+                        const float x = p.c * sv[t] + rk[il * p.SK + (p.ak ? r : 0)];
+                        // rows beyond n hold stale R', Rv': select, never multiply by 0
+                        const float pr = valid ? ptx::ex2(x) : 0.f;
+                        const float dr = dpv[t] + rv[il * p.SV + (p.av ? r : 0)];
+                        pe[h] = pr;
+                        de[h] = valid ? pr * dr : 0.f;
+                    }
+                    pp[t2] = ptx::pack_bf16x2(pe[0], pe[1]);
+                    dd[t2] = ptx::pack_bf16x2(de[0], de[1]);
+                }
+                __syncwarp();
+                // P^T over the columns of S^T already read
+                ptx::tmem_st16(lane_base + tS + (uint32_t)(16 * ch), pp);
+                // dS^T row jl, queries 32 ch .. 32 ch + 31: 128-byte swizzled rows, two 64-query blocks
+                const uint32_t blk = (uint32_t)(ch >> 1) * (BN * 128);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t u = (uint32_t)((ch & 1) * 4 + w);
+                    *reinterpret_cast<uint4 *>(ds_row + blk + ((u ^ sw) << 4)) =
+                        make_uint4(dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
+                }
+            }
+            ptx::tmem_st_wait();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(B_P_FULL));
+            // dQ rows (TMEM lane = query row of the tile)
+            ok = tc::wait_bar(bar(B_DQ_FULL), (uint32_t)pi & 1u, sh, p.err);
+            if (!(ok = __all_sync(0xffffffffu, ok) != 0)) break;
+            ptx::tc_fence_after();
+            const int qi = i0 + jl;
+            float *dqr = p.dq + ((long long)bh * p.n + qi) * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float v[32];
+                ptx::tmem_ld32f(lane_base + tDP + (uint32_t)c0, v);
+                ptx::tmem_ld_wait();
+                if (qi < p.n) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        red_add_v4(dqr + c0 + 4 * u, p.scale * v[4 * u], p.scale * v[4 * u + 1],
+                                   p.scale * v[4 * u + 2], p.scale * v[4 * u + 3]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(B_DQ_EMPTY));
+        }
+        // dK and dV of this key tile
+        if (ok && NQ > 0) {
+            ok = tc::wait_bar(bar(B_DKV), 0, sh, p.err);
+            ok = __all_sync(0xffffffffu, ok) != 0;
+            if (ok) ptx::tc_fence_after();
+        }
+        if (ok) {
+            const long long krow = (long long)bh * p.n + j;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float a[32], b[32];
+                if (NQ > 0) {
+                    ptx::tmem_ld32f(lane_base + tDK + (uint32_t)c0, a);
+                    ptx::tmem_ld32f(lane_base + tDV + (uint32_t)c0, b);
+                    ptx::tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) a[t] = b[t] = 0.f;
+                }
+                if (j < p.n) {
+                    float4 *dkr = reinterpret_cast<float4 *>(p.dk + krow * D + c0);
+                    float4 *dvr = reinterpret_cast<float4 *>(p.dv + krow * D + c0);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        dkr[u] = make_float4(p.scale * a[4 * u], p.scale * a[4 * u + 1], p.scale * a[4 * u + 2],
+                                             p.scale * a[4 * u + 3]);
+                        dvr[u] = make_float4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// =========================================================================== tables kernel
+constexpr int kTabThreads = 256;
+
+__device__ __forceinline__ float ldf(const __nv_bfloat16 *p, long long i) { return __bfloat162float(p[i]); }
+
+// one CTA per (head, query tile): the bins of its rows, dq += scale gamma W^K, and the tile's
+// share of dW^K = scale gamma^T Q and dW^V = beta^T dZ (atomic adds into the table gradients)
+__global__ void __launch_bounds__(kTabThreads)
+    bwd_tables_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *dz, const __nv_bfloat16 *aK,
+                      float *daK, float *daV, long long ths, int D, const Params p) {
+    extern __shared__ float tsm[];
+    const int W = p.W, k = p.clip_k;
+    const int qt = (int)blockIdx.x / p.BH, bh = (int)blockIdx.x % p.BH;
+    const int i0 = qt * BM, h = bh % p.H;
+    const int nk = keys_of(p, bh);
+    const long long th = p.table_heads ? (long long)h * ths : 0;
+    const int rows = min(BM, p.n - i0);
+    const int SW = W + 1;
+    float *g = tsm;                 // [BM][W + 1]
+    float *be = g + BM * SW;        // [BM][W + 1]
+    float *wk = be + BM * SW;       // [W][D] (ak)
+    for (int e = threadIdx.x; e < rows * W; e += blockDim.x) {
+        const int il = e / W, r = e - il * W, i = i0 + il;
+        const long long row = (long long)bh * p.n + i;
+        const float *rec = p.ws_rec + row * kRec;
+        const float lse = rec[kRecLse], Dv = rec[kRecD];
+        float bb = 0.f, gg = 0.f;
+        if (lse < INFINITY) {
+            if (r == 0) {
+                bb = rec[kRecBL];
+                gg = rec[kRecGL];
+            } else if (!p.causal && r == 2 * k) {
+                bb = rec[kRecBR];
+                gg = rec[kRecGR];
+            } else {
+                const int jj = i + r - k;
+                if (jj >= 0 && jj < nk && (!p.causal || jj <= i)) {
+                    bb = ptx::ex2(p.ws_x[row * W + r] - lse);
+                    gg = bb * (p.ws_dp[row * W + r] - Dv);
+                }
+            }
+        }
+        g[il * SW + r] = gg;
+        be[il * SW + r] = bb;
+    }
+    if (p.ak)
+        for (int e = threadIdx.x; e < W * D; e += blockDim.x) wk[e] = ldf(aK, th + e);
+    __syncthreads();
+    if (p.ak) {  // dq_i += scale sum_r gamma_ir w^K_r
+        for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
+            const int il = e / D, cc = e - il * D;
+            float acc = 0.f;
+            for (int r = 0; r < W; ++r) acc = fmaf(g[il * SW + r], wk[r * D + cc], acc);
+            float *dst = p.dq + ((long long)bh * p.n + i0 + il) * D + cc;
+            *dst += p.scale * acc;
+        }
+    }
+    const long long base = ((long long)bh * p.n + i0) * D;
+    for (int e = threadIdx.x; e < W * D; e += blockDim.x) {
+        const int r = e / D, cc = e - r * D;
+        float ak = 0.f, av = 0.f;
+        for (int il = 0; il < rows; ++il) {
+            if (p.ak) ak = fmaf(g[il * SW + r], ldf(q, base + (long long)il * D + cc), ak);
+            if (p.av) av = fmaf(be[il * SW + r], ldf(dz, base + (long long)il * D + cc), av);
+        }
+        if (p.ak) atomicAdd(daK + th + e, p.scale * ak);
+        if (p.av) atomicAdd(daV + th + e, av);
+    }
+}
+
+// ==================================================================================== host
+
+inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+inline unsigned long long round_up_ull(unsigned long long x, unsigned long long a) { return (x + a - 1) / a * a; }
+
+// workspace floats per row and layout (each array 256-byte aligned)
+inline unsigned long long ws_layout(const BwdArgs &a, int W, int SK, int SV, Params *p) {
+    const unsigned long long rows = (unsigned long long)a.B * a.H * a.n;
+    unsigned long long off = 0;
+    auto take = [&](unsigned long long floats) {
+        const unsigned long long o = off;
+        off = round_up_ull(off + floats * 4, 256);
+        return o;
+    };
+    const unsigned long long o_rk = take(rows * SK), o_rv = take(rows * SV);
+    const unsigned long long o_x = take(rows * W), o_dp = take(rows * W), o_rec = take(rows * kRec);
+    if (p) {
+        char *b = static_cast<char *>(a.workspace);
+        p->ws_rk = reinterpret_cast<float *>(b + o_rk);
+        p->ws_rv = reinterpret_cast<float *>(b + o_rv);
+        p->ws_x = reinterpret_cast<float *>(b + o_x);
+        p->ws_dp = reinterpret_cast<float *>(b + o_dp);
+        p->ws_rec = reinterpret_cast<float *>(b + o_rec);
+    }
+    return off;
+}
+
+template <typename K>
+cudaError_t opt_in(K kern, std::mutex &mu, bool (&opted)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!opted[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::device_info().smem_optin);
+        if (e != cudaSuccess) return e;
+        opted[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
+    const bool ak = a.aK != nullptr, av = a.aV != nullptr;
+    const int W = a.causal ? a.clip_k + 1 : 2 * a.clip_k + 1;
+    if ((ak || av) && W > kMaxW) return cudaErrorNotSupported;
+    const tc::DeviceInfo di = tc::device_info();
+    if (di.sms <= 0 || di.smem_optin <= 0) return cudaErrorInvalidDevice;
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.B = a.B;
+    p.H = a.H;
+    p.n = a.n;
+    p.BH = a.B * a.H;
+    p.n_tiles = (a.n + BM - 1) / BM;
+    p.clip_k = a.clip_k;
+    p.causal = a.causal;
+    p.W = W;
+    p.Wp = (int)round_up((uint32_t)W, 16);
+    p.ak = ak;
+    p.av = av;
+    p.bins = ak || av;
+    p.SK = (int)round_up((uint32_t)(ak ? W : 1), 4);
+    p.SV = (int)round_up((uint32_t)(av ? W : 1), 4);
+    p.SR = (W + 1) & ~1;  // even: the band gather of a warp's 32 rows (stride SR - 1) hits 32 banks
+    p.table_heads = a.ths != 0 ? 1 : 0;
+    p.c = a.scale * kLog2e;
+    p.scale = a.scale;
+    p.kv_len = a.kv_len;
+    p.err = a.err;
+    p.dq = a.dq;
+    p.dk = a.dk;
+    p.dv = a.dv;
+    p.wait_limit = a.wait_limit > 0 ? a.wait_limit : 2000000000ll;
+    if (p.BH == 0 || a.n == 0) return cudaSuccess;
+    if ((long long)p.BH * p.n_tiles > INT32_MAX) return cudaErrorNotSupported;
+    if (reinterpret_cast<uintptr_t>(a.workspace) % 256 != 0) return cudaErrorNotSupported;
+    ws_layout(a, W, p.SK, p.SV, &p);
+
+    // stats kernel shared memory: Q, dZ, K/V stages, table rows (TMA targets, 1024-aligned),
+    // then the R and Rv rows and the barriers
+    const uint32_t tile = (uint32_t)BM * D * 2;
+    const uint32_t tab = (uint32_t)p.Wp * D * 2;
+    auto layout_a = [&](Params &q, int stages) {
+        uint32_t off = 0;
+        q.off_q = off; off += tile;
+        q.off_dz = off; off += tile;
+        q.off_k = off; off += (uint32_t)stages * tile;
+        q.off_v = off; off += (uint32_t)stages * tile;
+        q.off_wk = off; if (ak) off += round_up(tab, 1024);
+        q.off_wv = off; if (av) off += round_up(tab, 1024);
+        q.off_r = off; if (ak) off += (uint32_t)BM * q.SR * 4;
+        q.off_rv = off; if (av) off += (uint32_t)BM * q.SR * 4;
+        off = round_up(off, 16);
+        q.off_bar = off; off += 8 * 32 + 16;
+        q.stage_bytes = tile;
+        q.stages = stages;
+        return off + 1024;  // slack to align the base to 1024 bytes
+    };
+    // keys kernel shared memory: K, V, dS (MMA operands, 1024-aligned), the query stages
+    // (Q, dZ, R' rows, Rv' rows), barriers
+    auto layout_b = [&](Params &q, int stages) {
+        uint32_t off = 0;
+        q.off_k = off; off += tile;
+        q.off_v = off; off += tile;
+        q.off_ds = off; off += (uint32_t)BN * BM * 2;
+        q.stage_bytes = round_up(2 * tile + (uint32_t)BM * (q.SK + q.SV) * 4, 1024);
+        q.off_q = off; off += (uint32_t)stages * q.stage_bytes;
+        q.off_bar = off; off += 8 * 32 + 16;
+        q.stages = stages;
+        return off + 1024;
+    };
+    const uint32_t optin = (uint32_t)di.smem_optin;
+    Params pa = p, pb = p;
+    uint32_t sma = layout_a(pa, 2);
+    if (sma > optin) sma = layout_a(pa, 1);
+    uint32_t smb = layout_b(pb, 2);
+    if (smb > optin) smb = layout_b(pb, 1);
+    if (sma > optin || smb > optin) return cudaErrorNotSupported;
+    const uint32_t smc = (uint32_t)(2 * BM * (W + 1) + (ak ? W * D : 0)) * 4;
+    if (smc > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
+
+    // TMA descriptors
+    CUtensorMap tm[6];
+    const uint64_t d = (uint64_t)D, n = (uint64_t)a.n, BH = (uint64_t)p.BH;
+    const uint64_t rs = d * 2, hs = n * d * 2;
+    if (!tc::make_map(&tm[0], a.q, d, n, BH, rs, hs, BM) || !tc::make_map(&tm[1], a.dout, d, n, BH, rs, hs, BM) ||
+        !tc::make_map(&tm[2], a.k, d, n, BH, rs, hs, BN) || !tc::make_map(&tm[3], a.v, d, n, BH, rs, hs, BN))
+        return cudaErrorInvalidValue;
+    tm[4] = tm[0];
+    tm[5] = tm[0];
+    const uint64_t Ht = p.table_heads ? (uint64_t)a.H : 1;
+    const uint64_t rows_mem = (uint64_t)(2 * a.clip_k + 1);
+    const uint64_t ths_bytes = p.table_heads ? (uint64_t)a.ths * 2 : rows_mem * d * 2;
+    if (ak && !tc::make_map(&tm[4], a.aK, d, rows_mem, Ht, rs, ths_bytes, (uint32_t)p.Wp)) return cudaErrorInvalidValue;
+    if (av && !tc::make_map(&tm[5], a.aV, d, rows_mem, Ht, rs, ths_bytes, (uint32_t)p.Wp)) return cudaErrorInvalidValue;
+
+    static std::mutex mu;
+    static bool opted_a[64] = {}, opted_b[64] = {}, opted_c[64] = {};
+    cudaError_t e;
+    if ((e = opt_in(bwd_stats_kernel<D>, mu, opted_a)) != cudaSuccess) return e;
+    if ((e = opt_in(bwd_keys_kernel<D>, mu, opted_b)) != cudaSuccess) return e;
+    if ((e = opt_in(bwd_tables_kernel, mu, opted_c)) != cudaSuccess) return e;
+
+    const int Htab = p.table_heads ? a.H : 1;
+    const size_t tab_bytes = (size_t)((long long)(Htab - 1) * a.ths + (long long)(2 * a.clip_k + 1) * a.d) * sizeof(float);
+    if (ak && (e = cudaMemsetAsync(a.daK, 0, tab_bytes, s)) != cudaSuccess) return e;
+    if (av && (e = cudaMemsetAsync(a.daV, 0, tab_bytes, s)) != cudaSuccess) return e;
+    const unsigned tiles = (unsigned)(p.BH * p.n_tiles);
+    bwd_stats_kernel<D><<<tiles, kThreads, sma, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_keys_kernel<D><<<tiles, kThreads, smb, s>>>(tm[0], tm[1], tm[2], tm[3], pb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (ak || av) {
+        bwd_tables_kernel<<<tiles, kTabThreads, smc, s>>>(
+            static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.dout),
+            static_cast<const __nv_bfloat16 *>(a.aK), a.daK, a.daV, a.ths, D, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace btc
+
+unsigned long long bwd_tc_workspace_bytes(int B, int H, int n, int clip_k) {
+    BwdArgs a{};
+    a.B = B;
+    a.H = H;
+    a.n = n;
+    const int W = 2 * clip_k + 1;
+    const int S4 = (int)btc::round_up((uint32_t)W, 4);
+    return btc::ws_layout(a, W, S4, S4, nullptr);
+}
+
+bool bwd_tc_covers(const BwdArgs &a) {
+    if (!a.bf16 || (a.d != 64 && a.d != 128)) return false;
+    const int W = a.causal ? a.clip_k + 1 : 2 * a.clip_k + 1;
+    if ((a.aK || a.aV) && W > btc::kMaxW) return false;
+    return reinterpret_cast<uintptr_t>(a.workspace) % 256 == 0;
+}
+
+cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s) {
+    if (!bwd_tc_covers(a)) return cudaErrorNotSupported;
+    return a.d == 64 ? btc::launch<64>(a, s) : btc::launch<128>(a, s);
+}
+
+}  // namespace relattn

@@ -96,6 +96,7 @@ relattn_status_t check_qkv(const void *q, const void *k, const void *v, const vo
 std::atomic<long long> g_wait_limit{2000000000ll};
 std::atomic<int> g_withhold_q{0};
 std::atomic<int> g_short_kernel{1};
+std::atomic<int> g_bwd_tensor_cores{1};
 
 relattn_status_t dispatch_bf16(const relattn::TcArgs &args, const relattn::T5Buckets *t5,
                                cudaStream_t s) {
@@ -401,7 +402,15 @@ relattn_status_t relattn_bwd(const void *q, const void *k, const void *v, const 
     a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
     a.dq = dq; a.dk = dk; a.dv = dv; a.daK = daK; a.daV = daV;
     a.workspace = workspace;
-    return from_cuda(relattn::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)));
+    a.wait_limit = g_wait_limit.load();
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (g_bwd_tensor_cores.load() && relattn::bwd_tc_covers(a)) {
+        a.err = status_word_for_current_device();
+        if (!a.err) return RELATTN_ERR_CUDA;
+        const cudaError_t e = relattn::launch_bwd_tc(a, s);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    return from_cuda(relattn::launch_bwd(a, s));
 }
 
 relattn_status_t relattn_t5bias_fwd(const void *q, const void *k, const void *v,
@@ -506,6 +515,12 @@ relattn_status_t relattn_debug_withhold_first_load(int on) {
 relattn_status_t relattn_set_short_kernel(int on) {
     if (on != 0 && on != 1) return RELATTN_ERR_INVALID_ARG;
     g_short_kernel.store(on);
+    return RELATTN_OK;
+}
+
+relattn_status_t relattn_set_bwd_tensor_cores(int on) {
+    if (on != 0 && on != 1) return RELATTN_ERR_INVALID_ARG;
+    g_bwd_tensor_cores.store(on);
     return RELATTN_OK;
 }
 

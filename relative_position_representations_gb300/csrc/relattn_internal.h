@@ -151,9 +151,17 @@ struct BwdArgs {
     int bf16;  // 1: q, k, v, tables and dout are bf16; 0: fp32
     float *dq, *dk, *dv, *daK, *daV;
     void *workspace;  // at least bwd_workspace_bytes
+    int *err;               // tensor-core path: device status word
+    long long wait_limit;   // tensor-core path: bound of every device wait (cycles, <= 0: 2e9)
 };
+// the larger of the two paths' needs
 unsigned long long bwd_workspace_bytes(int B, int H, int n, int clip_k);
-// cudaErrorNotSupported when 2k+1 > 257 or d > 128
+// SIMT kernels; cudaErrorNotSupported when 2k+1 > 257 or d > 128
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s);
+// tensor-core kernels (bf16, d = 64 or 128, at most 128 staged table rows, workspace aligned
+// to 256 bytes); bwd_tc_covers says whether they take the call
+unsigned long long bwd_tc_workspace_bytes(int B, int H, int n, int clip_k);
+bool bwd_tc_covers(const BwdArgs &a);
+cudaError_t launch_bwd_tc(const BwdArgs &a, cudaStream_t s);
 
 }  // namespace relattn

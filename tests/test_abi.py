@@ -58,6 +58,9 @@ def test_wait_limit_and_hook_arguments_checked_on_the_host(lib):
     assert lib.raw_call("relattn_set_short_kernel", 2) == 1
     assert lib.raw_call("relattn_set_short_kernel", 0) == 0
     assert lib.raw_call("relattn_set_short_kernel", 1) == 0  # the default
+    assert lib.raw_call("relattn_set_bwd_tensor_cores", 2) == 1
+    assert lib.raw_call("relattn_set_bwd_tensor_cores", 0) == 0
+    assert lib.raw_call("relattn_set_bwd_tensor_cores", 1) == 0  # the default
 
 
 @pytest.mark.parametrize("nb,md,bidir", [(32, 128, True), (32, 128, False), (16, 40, True),
