@@ -15,19 +15,20 @@
 // Three kernels, in stream order:
 //   stats   one CTA per (head, 128-row query tile): R and Rv by MMA, then S_j = Q K_j^T and
 //           dP_j = dZ V_j^T per key tile (tcgen05, fp32 in TMEM) and an online softmax over
-//           the tile's keys that yields lse_i, D_i and the bins: the two end bins (offsets at
-//           or beyond -k and +k) as rescaled sums, and the interior bins, each of which holds
-//           exactly one key of the row, as that key's logit and dp value. Per row it writes
-//           R'_ir = c R_ir - lse_i and Rv'_ir = Rv_ir - D_i (so that the next kernel needs no
-//           other row statistic) and zeroes dq.
+//           the tile's keys that yields lse_i, D_i and the two end bins (offsets at or
+//           beyond -k and +k, rescaled sums). Per row it writes R'_ir = c R_ir - lse_i and
+//           Rv'_ir = Rv_ir - D_i (so that the next kernel needs no other row statistic).
 //   keys    one CTA per (head, 128-key tile), looping over the query tiles that see it:
 //           S^T = K Q_i^T and dP^T = V dZ_i^T (lanes = keys), then per element
 //           p = 2^(c s + R'[r]) and ds = p (dp + Rv'[r]); P^T (bf16) goes back into TMEM and
 //           dS (bf16) into shared memory, and three more MMAs follow: dV += P^T dZ_i,
 //           dK += dS^T Q_i (both accumulated in TMEM over the query tiles) and
-//           dQ_i = dS K (added into dq with vector atomics).
-//   tables  SIMT, one CTA per (head, query tile): the bins from the stats kernel's records,
-//           dq_i += scale sum_r gamma_ir w^K_r and the table gradients (atomic adds).
+//           dQ_i = dS K (added into dq with vector atomics). An interior bin (-k < j - i < k)
+//           holds exactly one key of its row, so the thread of that key stores its p and ds
+//           as the bin (the 32 lanes of a warp store consecutive bins of one row).
+//   tables  one CTA per (head, query tile): the bins as bf16 tiles, then dq_i += scale
+//           sum_r gamma_ir w^K_r, dW^K += scale Gamma^T Q and dW^V += Beta^T dZ on tcgen05
+//           (the table gradients by vector atomic adds).
 // No n x n or n x n x d tensor reaches memory; the workspace holds per-row values only.
 #include <cstdint>
 #include <cstring>
@@ -60,13 +61,14 @@ struct Params {
     int B, H, n, BH, n_tiles;
     int clip_k, causal, W, Wp;   // staged rows W, rounded up to 16 (N of R = Q W^K^T)
     int ak, av, bins;            // tables present; bins = ak || av
-    int SK, SV, SR;              // row strides (floats): R' and Rv' rows, shared R rows
+    int SK, SV;                  // row strides (floats) of R' and Rv' in the workspace
+    int SRk, SRv;                // row strides (floats) of the R and Rv rows in shared memory
     int table_heads;
     float c, scale;
     const int *kv_len;
     int *err;
     float *dq, *dk, *dv;
-    float *ws_rk, *ws_rv, *ws_x, *ws_dp, *ws_rec;
+    float *ws_rk, *ws_rv, *ws_bb, *ws_gg, *ws_rec;  // ws_bb, ws_gg: interior bins [row][W]
     uint32_t off_q, off_dz, off_k, off_v, off_wk, off_wv, off_r, off_rv, off_ds, off_bar;
     uint32_t stage_bytes;        // stats: one K (or V) stage; keys: one Q/dZ/R'/Rv' stage
     int stages;
@@ -129,7 +131,7 @@ enum : int {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     bwd_stats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
@@ -152,6 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(i), (i == A_R_EMPTY || i == A_S_EMPTY) ? 128u : 1u);
         *sh.abort_flag = 0;
         ptx::mbar_init_fence();
+    } else if (threadIdx.x == 32) {
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_dz);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
+        if (p.ak) ptx::tma_prefetch_desc(&tm_wk);
+        if (p.av) ptx::tma_prefetch_desc(&tm_wv);
     }
     if (warp == 1) ptx::tmem_alloc(sm.tmem_slot, 256);
     ptx::tc_fence_before();
@@ -249,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = i < p.n;
         const long long row = (long long)bh * p.n + i;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
-        float *Rs = reinterpret_cast<float *>(sh.ptr + p.off_r) + il * p.SR;
-        float *Rvs = reinterpret_cast<float *>(sh.ptr + p.off_rv) + il * p.SR;
+        float *Rs = reinterpret_cast<float *>(sh.ptr + p.off_r) + il * p.SRk;
+        float *Rvs = reinterpret_cast<float *>(sh.ptr + p.off_rv) + il * p.SRv;
         const int k = p.clip_k, W = p.W;
         const bool bidir = !p.causal;
         const int khi = p.causal ? 0 : k;  // largest offset with a staged row
@@ -321,19 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float tt = pt * dpf;
                         l += pt;
                         Dacc += tt;
-                        if (p.bins) {
-                            if (r == 0) {
-                                Lb += pt;
-                                Ld += tt;
-                            } else if (bidir && r == 2 * k) {
-                                Rb += pt;
-                                Rd += tt;
-                            } else if (x[t] != -INFINITY && row_ok) {
-                                // interior bin: exactly one key of the row
-                                p.ws_x[row * W + r] = x[t];
-                                p.ws_dp[row * W + r] = dpf;
-                            }
-                        }
+                        // the end bins (every key at or beyond -k, or +k); the interior
+                        // bins, one key each, are written by the keys kernel
+                        const bool isL = r == 0, isR = bidir && r == 2 * k && !isL;
+                        Lb += isL ? pt : 0.f;
+                        Ld += isL ? tt : 0.f;
+                        Rb += isR ? pt : 0.f;
+                        Rd += isR ? tt : 0.f;
                     }
                     __syncwarp();
                 }
@@ -341,36 +344,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(A_S_EMPTY));
         }
+        // per row: lse, D and the end bins; R' = c R - lse and Rv' = Rv - D in place over the
+        // shared-memory rows, then copied out by whole rows (coalesced)
         if (ok && row_ok) {
             const float lse = l > 0.f ? m + __log2f(l) : INFINITY;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float Dv = Dacc * inv;
-            float *rec = p.ws_rec + row * kRec;
-            rec[kRecLse] = lse;
-            rec[kRecD] = Dv;
-            rec[kRecBL] = Lb * inv;
-            rec[kRecGL] = Ld * inv - Dv * (Lb * inv);
-            rec[kRecBR] = Rb * inv;
-            rec[kRecGR] = Rd * inv - Dv * (Rb * inv);
-            float *rk = p.ws_rk + row * p.SK;
+            float4 *rec = reinterpret_cast<float4 *>(p.ws_rec + row * kRec);
+            rec[0] = make_float4(lse, Dv, Lb * inv, Ld * inv - Dv * (Lb * inv));
+            rec[1] = make_float4(Rb * inv, Rd * inv - Dv * (Rb * inv), 0.f, 0.f);
             if (p.ak) {
-                for (int r = 0; r < W; ++r) rk[r] = p.c * Rs[r] - lse;
+                for (int r = 0; r < W; ++r) Rs[r] = p.c * Rs[r] - lse;
             } else {
-                rk[0] = -lse;
+                Rs[0] = -lse;
             }
-            float *rv = p.ws_rv + row * p.SV;
             if (p.av) {
-                for (int r = 0; r < W; ++r) rv[r] = Rvs[r] - Dv;
+                for (int r = 0; r < W; ++r) Rvs[r] = Rvs[r] - Dv;
             } else {
-                rv[0] = -Dv;
+                Rvs[0] = -Dv;
             }
-            float4 *dqr = reinterpret_cast<float4 *>(p.dq + row * D);
-#pragma unroll 4
-            for (int c4 = 0; c4 < D / 4; ++c4) dqr[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // every row thread gets here (its waits are bounded), so the named barrier cannot hang
+        if (ptx::bar_red_and(1, 128, ok)) {
+            const int rows = min(BM, p.n - i0);
+            const int wk = p.ak ? W : 1, wv = p.av ? W : 1;
+            const float *Rs0 = reinterpret_cast<const float *>(sh.ptr + p.off_r);
+            const float *Rvs0 = reinterpret_cast<const float *>(sh.ptr + p.off_rv);
+            const long long row0 = (long long)bh * p.n + i0;
+            for (int rr = quarter; rr < rows; rr += 4) {
+                float *dk = p.ws_rk + (row0 + rr) * p.SK;
+                float *dv = p.ws_rv + (row0 + rr) * p.SV;
+                for (int e = lane; e < p.SK; e += 32) dk[e] = e < wk ? Rs0[rr * p.SRk + e] : 0.f;
+                for (int e = lane; e < p.SV; e += 32) dv[e] = e < wv ? Rvs0[rr * p.SRv + e] : 0.f;
+            }
         }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_barrier();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 256);
@@ -418,6 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(i), (i == B_P_FULL || i == B_DQ_EMPTY) ? 128u : 1u);
         *sh.abort_flag = 0;
         ptx::mbar_init_fence();
+    } else if (threadIdx.x == 32) {
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_dz);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
     }
     if (warp == 1) ptx::tmem_alloc(sm.tmem_slot, 512);
     ptx::tc_fence_before();
@@ -545,6 +560,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dpv);
                 ptx::tmem_ld_wait();
                 uint32_t pp[16], dd[16];
+                // do the warp's 32 keys and this chunk's 32 queries reach an interior bin
+                // (|j - i| < k)? Then each element of one is stored, fp32, as the bin of row i
+                const int dmax = j0 + 32 * quarter + 31 - (i0 + 32 * ch);
+                const int dmin = j0 + 32 * quarter - (i0 + 32 * ch + 31);
+                // interior offsets: -k < j - i < k, or -k < j - i <= 0 causal
+                const int dhi = p.causal ? 1 : k;
+                const bool band = p.bins && dmax > -k && dmin < dhi;
+                const long long brow0 = ((long long)bh * p.n + i0 + 32 * ch) * p.W;
 #pragma unroll
                 for (int t2 = 0; t2 < 16; ++t2) {
                     float pe[2], de[2];
@@ -560,6 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float dr = dpv[t] + rv[il * p.SV + (p.av ? r : 0)];
                         pe[h] = pr;
                         de[h] = valid ? pr * dr : 0.f;
+                        if (band && valid && dl > -k && dl < dhi) {  // interior bin r of row i
+                            p.ws_bb[brow0 + t * p.W + r] = pr;
+                            p.ws_gg[brow0 + t * p.W + r] = de[h];
+                        }
                     }
                     pp[t2] = ptx::pack_bf16x2(pe[0], pe[1]);
                     dd[t2] = ptx::pack_bf16x2(de[0], de[1]);
@@ -634,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_barrier();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
@@ -642,72 +669,201 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // =========================================================================== tables kernel
-constexpr int kTabThreads = 256;
+// One CTA per (head, query tile). The row threads build the tile's bins as bf16 MMA operands,
+// gamma and beta [BM rows][128 table rows] (two 64-column blocks, 128-byte swizzle, zero beyond
+// W): the end bins from the stats kernel's records, the interior bins from the keys kernel.
+// Then three MMAs:
+//   dQ_tab = Gamma W^K      (M = rows, K = table rows, N = D; added into dq times scale)
+//   dW^K  += Gamma^T Q      (M = table rows, K = rows; A MN-major over the same tile)
+//   dW^V  += Beta^T dZ
+// and the tile's share of the table gradients goes out by vector atomic adds.
+enum : int { C_LD = 0, C_G_FULL, C_MMA_DONE, C_DRAIN, kCBars };
 
-__device__ __forceinline__ float ldf(const __nv_bfloat16 *p, long long i) { return __bfloat162float(p[i]); }
-
-// one CTA per (head, query tile): the bins of its rows, dq += scale gamma W^K, and the tile's
-// share of dW^K = scale gamma^T Q and dW^V = beta^T dZ (atomic adds into the table gradients)
-__global__ void __launch_bounds__(kTabThreads)
-    bwd_tables_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *dz, const __nv_bfloat16 *aK,
-                      float *daK, float *daV, long long ths, int D, const Params p) {
-    extern __shared__ float tsm[];
-    const int W = p.W, k = p.clip_k;
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tables_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
+                      const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ Params p,
+                      float *daK, float *daV, long long ths) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = setup_smem(smem_raw, p);
+    const Shared &sh = sm.sh;
+    auto bar = [&](int i) { return sm.bar0 + 8u * (uint32_t)i; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = (int)blockIdx.x / p.BH, bh = (int)blockIdx.x % p.BH;
     const int i0 = qt * BM, h = bh % p.H;
-    const int nk = keys_of(p, bh);
-    const long long th = p.table_heads ? (long long)h * ths : 0;
+    const int th = p.table_heads ? h : 0;
+    const long long tho = p.table_heads ? (long long)h * ths : 0;
+    const int W = p.W, k = p.clip_k;
     const int rows = min(BM, p.n - i0);
-    const int SW = W + 1;
-    float *g = tsm;                 // [BM][W + 1]
-    float *be = g + BM * SW;        // [BM][W + 1]
-    float *wk = be + BM * SW;       // [W][D] (ak)
-    for (int e = threadIdx.x; e < rows * W; e += blockDim.x) {
-        const int il = e / W, r = e - il * W, i = i0 + il;
-        const long long row = (long long)bh * p.n + i;
-        const float *rec = p.ws_rec + row * kRec;
-        const float lse = rec[kRecLse], Dv = rec[kRecD];
-        float bb = 0.f, gg = 0.f;
-        if (lse < INFINITY) {
-            if (r == 0) {
-                bb = rec[kRecBL];
-                gg = rec[kRecGL];
-            } else if (!p.causal && r == 2 * k) {
-                bb = rec[kRecBR];
-                gg = rec[kRecGR];
-            } else {
-                const int jj = i + r - k;
-                if (jj >= 0 && jj < nk && (!p.causal || jj <= i)) {
-                    bb = ptx::ex2(p.ws_x[row * W + r] - lse);
-                    gg = bb * (p.ws_dp[row * W + r] - Dv);
+    const long long row0 = (long long)bh * p.n + i0;
+    constexpr uint32_t kCols = D == 64 ? 256u : 512u;  // dQ_tab, dW^K, dW^V: D columns each
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kCBars; ++i) ptx::mbar_init(bar(i), i == C_G_FULL ? 128u : 1u);
+        *sh.abort_flag = 0;
+        ptx::mbar_init_fence();
+    } else if (threadIdx.x == 32) {
+        if (p.ak) ptx::tma_prefetch_desc(&tm_q);
+        if (p.ak) ptx::tma_prefetch_desc(&tm_wk);
+        if (p.av) ptx::tma_prefetch_desc(&tm_dz);
+    }
+    if (warp == 1) ptx::tmem_alloc(sm.tmem_slot, kCols);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t *>(sh.ptr + p.off_bar + 8 * 32), 0);
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = tc::wait_bar_ctrl(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+
+    if (warp == 0) {
+        uint32_t bytes = 0;
+        if (p.ak) bytes += (uint32_t)BM * D * 2 + (uint32_t)p.Wp * D * 2;
+        if (p.av) bytes += (uint32_t)BM * D * 2;
+        ptx::mbar_expect_tx_w(bar(C_LD), bytes);
+#pragma unroll
+        for (int hh = 0; hh < D / 64; ++hh) {
+            if (p.ak) {
+                ptx::tma_load_3d_w(sh.base + p.off_q + (uint32_t)(hh * BM * 128), &tm_q, bar(C_LD), 64 * hh, i0, bh);
+                ptx::tma_load_3d_w(sh.base + p.off_wk + (uint32_t)(hh * p.Wp * 128), &tm_wk, bar(C_LD), 64 * hh, 0, th);
+            }
+            if (p.av)
+                ptx::tma_load_3d_w(sh.base + p.off_dz + (uint32_t)(hh * BM * 128), &tm_dz, bar(C_LD), 64 * hh, i0, bh);
+        }
+        tc::drain_bar(bar(C_LD), 0, sh.limit);
+    } else if (warp == 1) {
+        bool ok = wait_w(bar(C_LD), 0) && wait_w(bar(C_G_FULL), 0);
+        if (ok) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idT = ptx::idesc_bf16(BM, D, 1);  // A K-major, B MN-major
+            constexpr uint32_t idW = idesc_amn(BM, D);           // A and B MN-major
+            if (p.ak) {
+                const uint64_t dg_k = ptx::sdesc_sw128(sh.base + p.off_k, 16, 1024);
+                const uint64_t dg_mn = ptx::sdesc_sw128(sh.base + p.off_k, BM * 128, 1024);
+                const uint64_t dwk = ptx::sdesc_sw128(sh.base + p.off_wk, (uint32_t)p.Wp * 128, 1024);
+                const uint64_t dq_mn = ptx::sdesc_sw128(sh.base + p.off_q, BM * 128, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < p.Wp / 16; ++kk)  // dQ_tab = Gamma W^K
+                    ptx::tc_mma_w(tmem, dg_k + kstep(kk, BM), dwk + mnstep(kk), idT, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+                for (int kk = 0; kk < BM / 16; ++kk)  // dW^K = Gamma^T Q
+                    ptx::tc_mma_w(tmem + D, dg_mn + mnstep(kk), dq_mn + mnstep(kk), idW, kk > 0 ? 1u : 0u);
+            }
+            if (p.av) {
+                const uint64_t db_mn = ptx::sdesc_sw128(sh.base + p.off_v, BM * 128, 1024);
+                const uint64_t ddz_mn = ptx::sdesc_sw128(sh.base + p.off_dz, BM * 128, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < BM / 16; ++kk)  // dW^V = Beta^T dZ
+                    ptx::tc_mma_w(tmem + 2 * D, db_mn + mnstep(kk), ddz_mn + mnstep(kk), idW, kk > 0 ? 1u : 0u);
+            }
+            ptx::tc_commit_w(bar(C_MMA_DONE));
+        }
+        ptx::tc_commit_w(bar(C_DRAIN));
+        tc::drain_bar(bar(C_DRAIN), 0, sh.limit);
+    } else if (warp >= kRowWarp0) {
+        const int quarter = warp & 3;
+        const int il = 32 * quarter + lane, i = i0 + il;
+        const long long row = row0 + il;
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+        const int nk = keys_of(p, bh);
+        // this row's bins, bf16, 8 table rows per 16-byte chunk
+        float4 e0 = make_float4(0.f, 0.f, 0.f, 0.f), e1 = e0;
+        bool live = false;
+        if (il < rows) {
+            const float4 *rec = reinterpret_cast<const float4 *>(p.ws_rec + row * kRec);
+            e0 = rec[0];
+            e1 = rec[1];
+            live = e0.x < INFINITY;
+        }
+        uint8_t *grow = sh.ptr + p.off_k + il * 128;  // gamma tile (the keys area of the other kernels)
+        uint8_t *brow = sh.ptr + p.off_v + il * 128;  // beta tile
+        const uint32_t sw = (uint32_t)(il & 7);
+        for (int c8 = 0; c8 < 16; ++c8) {
+            uint32_t gp[4], bp[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float gv[2], bv[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 8 * c8 + 2 * e + hh;
+                    float bb = 0.f, gg = 0.f;
+                    if (live && r < W) {
+                        if (r == 0) {
+                            bb = e0.z;
+                            gg = e0.w;
+                        } else if (!p.causal && r == 2 * k) {
+                            bb = e1.x;
+                            gg = e1.y;
+                        } else {
+                            const int jj = i + r - k;  // the one key of an interior bin
+                            if (jj >= 0 && jj < nk && (!p.causal || jj <= i)) {
+                                bb = p.ws_bb[row * W + r];
+                                gg = p.ws_gg[row * W + r];
+                            }
+                        }
+                    }
+                    gv[hh] = gg;
+                    bv[hh] = bb;
+                }
+                gp[e] = ptx::pack_bf16x2(gv[0], gv[1]);
+                bp[e] = ptx::pack_bf16x2(bv[0], bv[1]);
+            }
+            const uint32_t off = (uint32_t)(c8 >> 3) * (BM * 128) + ((((uint32_t)c8 & 7u) ^ sw) << 4);
+            if (p.ak) *reinterpret_cast<uint4 *>(grow + off) = make_uint4(gp[0], gp[1], gp[2], gp[3]);
+            if (p.av) *reinterpret_cast<uint4 *>(brow + off) = make_uint4(bp[0], bp[1], bp[2], bp[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(C_G_FULL));
+        bool ok = tc::wait_bar(bar(C_MMA_DONE), 0, sh, p.err);
+        ok = __all_sync(0xffffffffu, ok) != 0;
+        if (ok) {
+            ptx::tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float v[32], wkv[32], wvv[32];
+                if (p.ak) {
+                    ptx::tmem_ld32f(lane_base + (uint32_t)c0, v);
+                    ptx::tmem_ld32f(lane_base + (uint32_t)(D + c0), wkv);
+                }
+                if (p.av) ptx::tmem_ld32f(lane_base + (uint32_t)(2 * D + c0), wvv);
+                ptx::tmem_ld_wait();
+                if (p.ak && il < rows) {  // TMEM lane = row of the tile
+                    float4 *dst = reinterpret_cast<float4 *>(p.dq + row * D + c0);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        float4 t = dst[u];
+                        t.x += p.scale * v[4 * u];
+                        t.y += p.scale * v[4 * u + 1];
+                        t.z += p.scale * v[4 * u + 2];
+                        t.w += p.scale * v[4 * u + 3];
+                        dst[u] = t;
+                    }
+                }
+                if (il < W) {  // TMEM lane = table row
+                    if (p.ak) {
+                        float *dst = daK + tho + (long long)il * D + c0;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            red_add_v4(dst + 4 * u, p.scale * wkv[4 * u], p.scale * wkv[4 * u + 1],
+                                       p.scale * wkv[4 * u + 2], p.scale * wkv[4 * u + 3]);
+                    }
+                    if (p.av) {
+                        float *dst = daV + tho + (long long)il * D + c0;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            red_add_v4(dst + 4 * u, wvv[4 * u], wvv[4 * u + 1], wvv[4 * u + 2], wvv[4 * u + 3]);
+                    }
                 }
             }
         }
-        g[il * SW + r] = gg;
-        be[il * SW + r] = bb;
     }
-    if (p.ak)
-        for (int e = threadIdx.x; e < W * D; e += blockDim.x) wk[e] = ldf(aK, th + e);
-    __syncthreads();
-    if (p.ak) {  // dq_i += scale sum_r gamma_ir w^K_r
-        for (int e = threadIdx.x; e < rows * D; e += blockDim.x) {
-            const int il = e / D, cc = e - il * D;
-            float acc = 0.f;
-            for (int r = 0; r < W; ++r) acc = fmaf(g[il * SW + r], wk[r * D + cc], acc);
-            float *dst = p.dq + ((long long)bh * p.n + i0 + il) * D + cc;
-            *dst += p.scale * acc;
-        }
-    }
-    const long long base = ((long long)bh * p.n + i0) * D;
-    for (int e = threadIdx.x; e < W * D; e += blockDim.x) {
-        const int r = e / D, cc = e - r * D;
-        float ak = 0.f, av = 0.f;
-        for (int il = 0; il < rows; ++il) {
-            if (p.ak) ak = fmaf(g[il * SW + r], ldf(q, base + (long long)il * D + cc), ak);
-            if (p.av) av = fmaf(be[il * SW + r], ldf(dz, base + (long long)il * D + cc), av);
-        }
-        if (p.ak) atomicAdd(daK + th + e, p.scale * ak);
-        if (p.av) atomicAdd(daV + th + e, av);
+    ptx::tc_fence_before();
+    ptx::cta_barrier();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kCols);
     }
 }
 
@@ -726,13 +882,13 @@ inline unsigned long long ws_layout(const BwdArgs &a, int W, int SK, int SV, Par
         return o;
     };
     const unsigned long long o_rk = take(rows * SK), o_rv = take(rows * SV);
-    const unsigned long long o_x = take(rows * W), o_dp = take(rows * W), o_rec = take(rows * kRec);
+    const unsigned long long o_bb = take(rows * W), o_gg = take(rows * W), o_rec = take(rows * kRec);
     if (p) {
         char *b = static_cast<char *>(a.workspace);
         p->ws_rk = reinterpret_cast<float *>(b + o_rk);
         p->ws_rv = reinterpret_cast<float *>(b + o_rv);
-        p->ws_x = reinterpret_cast<float *>(b + o_x);
-        p->ws_dp = reinterpret_cast<float *>(b + o_dp);
+        p->ws_bb = reinterpret_cast<float *>(b + o_bb);
+        p->ws_gg = reinterpret_cast<float *>(b + o_gg);
         p->ws_rec = reinterpret_cast<float *>(b + o_rec);
     }
     return off;
@@ -776,7 +932,10 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     p.bins = ak || av;
     p.SK = (int)round_up((uint32_t)(ak ? W : 1), 4);
     p.SV = (int)round_up((uint32_t)(av ? W : 1), 4);
-    p.SR = (W + 1) & ~1;  // even: the band gather of a warp's 32 rows (stride SR - 1) hits 32 banks
+    // even strides: the band gather of a warp's 32 rows (address step SR - 1) hits 32 banks;
+    // without the table one slot holds the row's -lse (or -D)
+    p.SRk = ak ? (W + 1) & ~1 : 2;
+    p.SRv = av ? (W + 1) & ~1 : 2;
     p.table_heads = a.ths != 0 ? 1 : 0;
     p.c = a.scale * kLog2e;
     p.scale = a.scale;
@@ -803,8 +962,8 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
         q.off_v = off; off += (uint32_t)stages * tile;
         q.off_wk = off; if (ak) off += round_up(tab, 1024);
         q.off_wv = off; if (av) off += round_up(tab, 1024);
-        q.off_r = off; if (ak) off += (uint32_t)BM * q.SR * 4;
-        q.off_rv = off; if (av) off += (uint32_t)BM * q.SR * 4;
+        q.off_r = off; off += (uint32_t)BM * q.SRk * 4;
+        q.off_rv = off; off += (uint32_t)BM * q.SRv * 4;
         off = round_up(off, 16);
         q.off_bar = off; off += 8 * 32 + 16;
         q.stage_bytes = tile;
@@ -826,13 +985,27 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     };
     const uint32_t optin = (uint32_t)di.smem_optin;
     Params pa = p, pb = p;
-    uint32_t sma = layout_a(pa, 2);
+    // one key tile (n <= 128): one K/V stage, so that two CTAs share an SM
+    uint32_t sma = layout_a(pa, p.n_tiles > 1 ? 2 : 1);
     if (sma > optin) sma = layout_a(pa, 1);
     uint32_t smb = layout_b(pb, 2);
     if (smb > optin) smb = layout_b(pb, 1);
     if (sma > optin || smb > optin) return cudaErrorNotSupported;
-    const uint32_t smc = (uint32_t)(2 * BM * (W + 1) + (ak ? W * D : 0)) * 4;
-    if (smc > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
+    // tables kernel shared memory: Q, dZ, W^K (TMA), the gamma and beta tiles (in the places
+    // of the K and V tiles), barriers
+    Params pc = p;
+    auto layout_c = [&](Params &q) {
+        uint32_t off = 0;
+        q.off_q = off; off += tile;
+        q.off_dz = off; off += tile;
+        q.off_wk = off; off += round_up(tab, 1024);
+        q.off_k = off; off += (uint32_t)BM * 128 * 2;   // gamma: 128 rows x 128 table rows, bf16
+        q.off_v = off; off += (uint32_t)BM * 128 * 2;   // beta
+        q.off_bar = off; off += 8 * 32 + 16;
+        return off + 1024;
+    };
+    const uint32_t smc = layout_c(pc);
+    if (smc > optin) return cudaErrorNotSupported;
 
     // TMA descriptors
     CUtensorMap tm[6];
@@ -854,21 +1027,21 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     cudaError_t e;
     if ((e = opt_in(bwd_stats_kernel<D>, mu, opted_a)) != cudaSuccess) return e;
     if ((e = opt_in(bwd_keys_kernel<D>, mu, opted_b)) != cudaSuccess) return e;
-    if ((e = opt_in(bwd_tables_kernel, mu, opted_c)) != cudaSuccess) return e;
+    if ((e = opt_in(bwd_tables_kernel<D>, mu, opted_c)) != cudaSuccess) return e;
 
     const int Htab = p.table_heads ? a.H : 1;
     const size_t tab_bytes = (size_t)((long long)(Htab - 1) * a.ths + (long long)(2 * a.clip_k + 1) * a.d) * sizeof(float);
     if (ak && (e = cudaMemsetAsync(a.daK, 0, tab_bytes, s)) != cudaSuccess) return e;
     if (av && (e = cudaMemsetAsync(a.daV, 0, tab_bytes, s)) != cudaSuccess) return e;
+    // dq: the keys kernel adds dS K into it, the tables kernel the table term
+    if ((e = cudaMemsetAsync(a.dq, 0, (size_t)p.BH * a.n * D * sizeof(float), s)) != cudaSuccess) return e;
     const unsigned tiles = (unsigned)(p.BH * p.n_tiles);
     bwd_stats_kernel<D><<<tiles, kThreads, sma, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_keys_kernel<D><<<tiles, kThreads, smb, s>>>(tm[0], tm[1], tm[2], tm[3], pb);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ak || av) {
-        bwd_tables_kernel<<<tiles, kTabThreads, smc, s>>>(
-            static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.dout),
-            static_cast<const __nv_bfloat16 *>(a.aK), a.daK, a.daV, a.ths, D, p);
+        bwd_tables_kernel<D><<<tiles, kThreads, smc, s>>>(tm[0], tm[1], tm[4], pc, a.daK, a.daV, a.ths);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

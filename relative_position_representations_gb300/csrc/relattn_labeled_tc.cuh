@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_barrier();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_raw, 512);

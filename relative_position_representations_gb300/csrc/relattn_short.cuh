@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
 
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cta_barrier();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_raw, kTmemCols);

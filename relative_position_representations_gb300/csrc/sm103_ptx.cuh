@@ -117,6 +117,12 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Barrier over the whole CTA that warps may reach from different branches of a role split.
+// The aligned form (__syncthreads, bar.sync) requires every warp to execute the same barrier
+// instruction; after the roles of a warp-specialised kernel the compiler may give each role
+// its own copy of it, and the aligned barrier then released the control warps while the
+// row warps were still working (seen with globaltimer stamps). This is the non-aligned form.
+__device__ __forceinline__ void cta_barrier() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05
 // Per-warpgroup register budget (all four warps of a warpgroup execute the same one).
