@@ -143,6 +143,7 @@ KERNEL_SOURCES = {
     "labeled": ["relattn_labeled_tc.cuh", "relattn_labeled_tc.cu", "relattn_tc_kernel.cuh",
                 "sm103_ptx.cuh"],
     "txl": ["relattn_txl.cu"],
+    "txl_tc": ["relattn_txl_tc.cu", "relattn_tc_kernel.cuh", "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
     "short": ["relattn_short.cuh", "relattn_short.cu", "relattn_tc_kernel.cuh",
               "relattn_tc_launch.cuh", "sm103_ptx.cuh"],
 }
@@ -155,9 +156,15 @@ def bwd_on_tensor_cores(w) -> bool:
     return w.kind == "bwd" and w.dtype == "bf16" and w.d in (64, 128) and rows <= 128
 
 
+def txl_on_tensor_cores(w) -> bool:
+    """bf16 Transformer-XL with d = 64 / 128 runs on the tensor-core kernel."""
+    return w.kind == "txl" and w.dtype == "bf16" and w.d in (64, 128)
+
+
 def simt_roof(w) -> bool:
     """Workloads whose kernels run on the SIMT units (roof: the derived fp32 FMA rate)."""
-    return (w.kind == "txl" or (w.kind == "bwd" and not bwd_on_tensor_cores(w)) or
+    return ((w.kind == "txl" and not txl_on_tensor_cores(w)) or
+            (w.kind == "bwd" and not bwd_on_tensor_cores(w)) or
             (w.kind == "labeled" and w.dtype != "bf16"))
 
 
@@ -165,6 +172,8 @@ def kernel_family(w) -> str:
     fam = {"decode": "decode", "bwd": "bwd", "labeled": "labeled", "txl": "txl"}.get(w.kind, "fused")
     if fam == "bwd" and bwd_on_tensor_cores(w):
         fam = "bwd_tc"
+    if fam == "txl" and txl_on_tensor_cores(w):
+        fam = "txl_tc"
     if fam == "fused" and w.kind == "shaw" and w.dtype == "bf16" and w.d == 64 and w.n <= 256:
         rows = (w.clip_k + 1 if w.causal else 2 * w.clip_k + 1) if (w.key_term or w.value_term) else 1
         if rows <= 64:  # the library routes these to the short-sequence kernel

@@ -197,8 +197,12 @@ RELATTN_API relattn_status_t relattn_labeled_fwd(const void *q, const void *k, c
  *   shared            1: rel, u and vb are a single set ([1, 2n - 1, d], [1, d]) for all heads.
  *   causal, scale, kv_len, B, H, n, d, dtype, out, stream   as in relattn_fwd; d <= 128 and a
  *                     multiple of 8 (bf16) / 4 (fp32), else RELATTN_ERR_UNSUPPORTED.
- * Runs on the SIMT units with fp32 arithmetic: one warp per query row, the two dot products
- * (q_i + u) . k_j and (q_i + v) . r_ij per key.
+ * bf16 with d = 64 or 128 runs on the tensor cores: per (query tile, key tile) S = Q K^T and
+ * T = Q R^T over the 255 offsets the pair spans (R: the table rows of those offsets), T read
+ * along its diagonals, u . k_j and v . r_ij added as per-key and per-offset fp32 scalars,
+ * O += P V with P in bf16, fp32 accumulation. Everything else (fp32, other d) runs on the SIMT
+ * units with fp32 arithmetic: one warp per query row, the two dot products (q_i + u) . k_j and
+ * (q_i + v) . r_ij per key. Device waits of the tensor-core path are bounded as in relattn_fwd.
  */
 RELATTN_API relattn_status_t relattn_txl_fwd(const void *q, const void *k, const void *v,
                                  const void *rel, const void *u, const void *vb, int shared,

@@ -344,7 +344,15 @@ relattn_status_t relattn_txl_fwd(const void *q, const void *k, const void *v, co
     a.B = B; a.H = H; a.n = n; a.d = d;
     a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
     a.out = out;
-    return from_cuda(relattn::launch_txl(a, reinterpret_cast<cudaStream_t>(stream)));
+    a.wait_limit = g_wait_limit.load();
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (relattn::txl_tc_covers(a)) {
+        a.err = status_word_for_current_device();
+        if (!a.err) return RELATTN_ERR_CUDA;
+        const cudaError_t e = relattn::launch_txl_tc(a, s);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+    }
+    return from_cuda(relattn::launch_txl(a, s));
 }
 
 relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,

@@ -136,9 +136,14 @@ struct TxlArgs {
     int B, H, n, d;
     int bf16;
     void *out;
+    int *err;               // tensor-core path: device status word
+    long long wait_limit;   // tensor-core path: bound of every device wait (cycles, <= 0: 2e9)
 };
-// cudaErrorNotSupported when d > 128
+// SIMT kernel; cudaErrorNotSupported when d > 128
 cudaError_t launch_txl(const TxlArgs &a, cudaStream_t s);
+// tensor-core kernel (bf16, d = 64 or 128); txl_tc_covers says whether it takes the call
+bool txl_tc_covers(const TxlArgs &a);
+cudaError_t launch_txl_tc(const TxlArgs &a, cudaStream_t s);
 
 // ---- gradients (SIMT, fp32 arithmetic) ---------------------------------------------------
 struct BwdArgs {

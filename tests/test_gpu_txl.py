@@ -48,6 +48,13 @@ def run_case(w, seed):
     ("f32", 77, 32, True, (10, 77), False),
     ("f32", 50, 128, False, None, True),
     ("f32", 1, 8, True, None, False),
+    # the tensor-core kernel (bf16, d = 64 / 128): several query and key tiles, ragged tails,
+    # empty rows (kv_len 0), one set of encodings for all heads, a single token
+    ("bf16", 300, 64, False, (0, 300), False),
+    ("bf16", 385, 64, True, None, True),
+    ("bf16", 257, 128, True, (100, 257), False),
+    ("bf16", 1, 64, False, None, False),
+    ("bf16", 130, 64, False, None, True),
 ])
 def test_txl_matches_the_oracle(dtype, n, d, causal, kv, shared):
     w = wl.Workload("txl_case", B=2, H=3, n=n, d=d, dtype=dtype, kind="txl", causal=causal,
@@ -59,11 +66,13 @@ def test_txl_decoder_workload():
     run_case(wl.TXL_WORKLOADS["txl_decoder"].replace(B=2), seed=3)
 
 
-def test_txl_sign_of_the_offset_matters():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_txl_sign_of_the_offset_matters(dtype):
     """Reversing the offset table (o -> 2n - 2 - o, i.e. j - i -> i - j) changes the output:
-    the kernel reads rel at j - i + n - 1, not at i - j + n - 1."""
+    the kernels (SIMT for fp32, tensor cores for bf16) read rel at j - i + n - 1, not at
+    i - j + n - 1."""
     rp = _rp()
-    w = wl.Workload("txl_sign", B=1, H=2, n=96, d=64, dtype="f32", kind="txl", table_std=0.5)
+    w = wl.Workload("txl_sign", B=1, H=2, n=96, d=64, dtype=dtype, kind="txl", table_std=0.5)
     x = wl.draw_inputs(w, 11)
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     a = rp.relattn_txl_fwd(g["q"], g["k"], g["v"], g["rel"], g["u"], g["vb"]).cpu()
