@@ -70,9 +70,12 @@ struct Params {
     float *dq, *dk, *dv;
     float *ws_rk, *ws_rv, *ws_bb, *ws_gg, *ws_rec;  // ws_bb, ws_gg: interior bins [row][W]
     uint32_t off_q, off_dz, off_k, off_v, off_wk, off_wv, off_r, off_rv, off_ds, off_bar;
+    uint32_t off_p, off_gb;      // one-tile kernel: the P tile and the gamma|beta tile
     uint32_t stage_bytes;        // stats: one K (or V) stage; keys: one Q/dZ/R'/Rv' stage
     int stages;
     long long wait_limit;
+    float *daK, *daV;            // one-tile kernel: the table gradients (atomic adds)
+    long long ths;               // their head stride (elements; 0 = one table)
 };
 
 __device__ __forceinline__ int keys_of(const Params &p, int bh) {
@@ -314,7 +317,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float al = ptx::ex2(m - mn);  // m = -inf: 0 (the sums are still 0)
                 l *= al; Dacc *= al; Lb *= al; Ld *= al; Rb *= al; Rd *= al;
                 m = mn;
-                // pass 2: probabilities (unnormalised), D and the bins
+            }
+            {
+                // pass 2: probabilities (unnormalised), D and the bins. Every lane runs it (the
+                // TMEM loads are warp-collective); a row with no allowed key so far has only
+                // -inf logits, whose terms are 0
+                const float mm = m == -INFINITY ? 0.f : m;
 #pragma unroll 1
                 for (int ch = 0; ch < BN / 32; ++ch) {
                     float x[32], dp[32];
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int t = 0; t < 32; ++t) {
                         const int jj = j0 + 32 * ch + t, dl = jj - i;
                         const int r = min(max(dl, -k), khi) + k;
-                        const float pt = x[t] == -INFINITY ? 0.f : ptx::ex2(x[t] - m);
+                        const float pt = ptx::ex2(x[t] - mm);  // -inf logits: 0
                         const float dpf = dp[t] + (p.av ? Rvs[r] : 0.f);
                         const float tt = pt * dpf;
                         l += pt;
@@ -867,6 +875,349 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ================================================================== one-tile kernel
+// Sequences of at most 128 keys (d = 64, at most 48 staged table rows): one query tile and
+// one key tile per head, so one CTA does the whole head with no workspace and no atomics on
+// dq, dk, dv. R = Q W^K^T, Rv = dZ W^V^T, S = Q K^T and dP = dZ V^T by MMA; the row threads
+// take the exact row statistics in three passes over TMEM (maximum; row sum and D; then P,
+// dS and the bins) and write P and dS (bf16) and the bins gamma | beta (bf16, one tile:
+// gamma in table columns 0..63, beta in 64..127) into shared memory. Then
+//   dV = P^T dZ, dK = dS^T Q     (A MN-major over the [query][key] tiles)
+//   dQ = dS K + Gamma W^K        (A K-major)
+//   [dW^K; dW^V] = [Gamma | Beta]^T [Q | dZ]   (one M = 128, N = 128 product; its two
+//                                 off-diagonal blocks are not used)
+// and the outputs leave TMEM by row (dq, dk, dv plain stores, the table rows by atomic adds).
+enum : int { S_LD = 0, S_A_FULL, S_G_FULL, S_OUT_FULL, S_DRAIN, kSBars };
+constexpr int kShortMaxW = 48;
+
+__device__ __forceinline__ void st_bf16_tile(uint8_t *tile, int row, int col, float v) {
+    // element (row, col) of a [128 rows][128 cols] bf16 tile in two 64-column blocks with the
+    // 128-byte swizzle
+    const uint32_t off = (uint32_t)(col >> 6) * (BM * 128) + (uint32_t)row * 128 +
+                         ((((uint32_t)(col & 63) >> 3) ^ ((uint32_t)row & 7u)) << 4) + ((uint32_t)(col & 7) << 1);
+    *reinterpret_cast<__nv_bfloat16 *>(tile + off) = __float2bfloat16_rn(v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
+                     const __grid_constant__ Params p) {
+    static_assert(D == 64, "one-tile kernel: d = 64");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const Smem sm = setup_smem(smem_raw, p);
+    const Shared &sh = sm.sh;
+    auto bar = [&](int i) { return sm.bar0 + 8u * (uint32_t)i; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = (int)blockIdx.x;
+    const int nk = keys_of(p, bh);
+    const int th = p.table_heads ? bh % p.H : 0;
+    const long long tho = p.table_heads ? (long long)(bh % p.H) * p.ths : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kSBars; ++i) ptx::mbar_init(bar(i), i == S_G_FULL ? 128u : 1u);
+        *sh.abort_flag = 0;
+        ptx::mbar_init_fence();
+    } else if (threadIdx.x == 32) {
+        ptx::tma_prefetch_desc(&tm_q);
+        ptx::tma_prefetch_desc(&tm_dz);
+        ptx::tma_prefetch_desc(&tm_k);
+        ptx::tma_prefetch_desc(&tm_v);
+        if (p.ak) ptx::tma_prefetch_desc(&tm_wk);
+        if (p.av) ptx::tma_prefetch_desc(&tm_wv);
+    }
+    if (warp == 1) ptx::tmem_alloc(sm.tmem_slot, 512);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t *>(sh.ptr + p.off_bar + 8 * 32), 0);
+    // TMEM columns: S at 0 and dP at 128 (then dV at 0, dK at 64, dQ at 128), R at 256 and Rv
+    // at 384 (then [dW^K | . ; . | dW^V] at 256)
+    constexpr uint32_t tS = 0, tDP = 128, tR = 256, tRv = 384, tDV = 0, tDK = 64, tDQ = 128, tW = 256;
+    auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool r = tc::wait_bar_ctrl(b, parity, sh, p.err);
+        return __all_sync(0xffffffffu, r ? 1 : 0) != 0;
+    };
+
+    if (warp == 0) {
+        uint32_t bytes = 4u * BM * D * 2;
+        if (p.ak) bytes += (uint32_t)p.Wp * D * 2;
+        if (p.av) bytes += (uint32_t)p.Wp * D * 2;
+        ptx::mbar_expect_tx_w(bar(S_LD), bytes);
+        ptx::tma_load_3d_w(sh.base + p.off_q, &tm_q, bar(S_LD), 0, 0, bh);
+        ptx::tma_load_3d_w(sh.base + p.off_dz, &tm_dz, bar(S_LD), 0, 0, bh);
+        ptx::tma_load_3d_w(sh.base + p.off_k, &tm_k, bar(S_LD), 0, 0, bh);
+        ptx::tma_load_3d_w(sh.base + p.off_v, &tm_v, bar(S_LD), 0, 0, bh);
+        if (p.ak) ptx::tma_load_3d_w(sh.base + p.off_wk, &tm_wk, bar(S_LD), 0, 0, th);
+        if (p.av) ptx::tma_load_3d_w(sh.base + p.off_wv, &tm_wv, bar(S_LD), 0, 0, th);
+        tc::drain_bar(bar(S_LD), 0, sh.limit);
+    } else if (warp == 1) {
+        bool ok = wait_w(bar(S_LD), 0);
+        const uint64_t dq_k = ptx::sdesc_sw128(sh.base + p.off_q, 16, 1024);
+        const uint64_t ddz_k = ptx::sdesc_sw128(sh.base + p.off_dz, 16, 1024);
+        if (ok) {
+            ptx::tc_fence_after();
+            const uint32_t idR = ptx::idesc_bf16(BM, (uint32_t)p.Wp, 0);
+            if (p.ak) {
+                const uint64_t dw = ptx::sdesc_sw128(sh.base + p.off_wk, 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::tc_mma_w(tmem + tR, dq_k + kstep(kk, BM), dw + kstep(kk, p.Wp), idR, kk > 0 ? 1u : 0u);
+            }
+            if (p.av) {
+                const uint64_t dw = ptx::sdesc_sw128(sh.base + p.off_wv, 16, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::tc_mma_w(tmem + tRv, ddz_k + kstep(kk, BM), dw + kstep(kk, p.Wp), idR, kk > 0 ? 1u : 0u);
+            }
+            constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0);
+            const uint64_t dk_k = ptx::sdesc_sw128(sh.base + p.off_k, 16, 1024);
+            const uint64_t dv_k = ptx::sdesc_sw128(sh.base + p.off_v, 16, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)  // S = Q K^T
+                ptx::tc_mma_w(tmem + tS, dq_k + kstep(kk, BM), dk_k + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk)  // dP = dZ V^T
+                ptx::tc_mma_w(tmem + tDP, ddz_k + kstep(kk, BM), dv_k + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
+            ptx::tc_commit_w(bar(S_A_FULL));
+            ok = wait_w(bar(S_G_FULL), 0);
+        }
+        if (ok) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idA = idesc_amn(BM, D);       // A and B MN-major, N = D
+            constexpr uint32_t idQ = ptx::idesc_bf16(BM, D, 1);  // A K-major, B MN-major
+            constexpr uint32_t idW = idesc_amn(BM, 2 * D);   // [Gamma | Beta]^T [Q | dZ]
+            const uint64_t dp_mn = ptx::sdesc_sw128(sh.base + p.off_p, BN * 128, 1024);
+            const uint64_t ds_mn = ptx::sdesc_sw128(sh.base + p.off_ds, BN * 128, 1024);
+            const uint64_t ds_k = ptx::sdesc_sw128(sh.base + p.off_ds, 16, 1024);
+            const uint64_t dz_mn = ptx::sdesc_sw128(sh.base + p.off_dz, BM * 128, 1024);
+            const uint64_t dq_mn = ptx::sdesc_sw128(sh.base + p.off_q, BM * 128, 1024);  // [Q | dZ]
+            const uint64_t dk_mn = ptx::sdesc_sw128(sh.base + p.off_k, BN * 128, 1024);
+            const uint64_t dgb_mn = ptx::sdesc_sw128(sh.base + p.off_gb, BM * 128, 1024);
+            const uint64_t dg_k = ptx::sdesc_sw128(sh.base + p.off_gb, 16, 1024);
+#pragma unroll 1
+            for (int kk = 0; kk < BM / 16; ++kk)  // dV = P^T dZ
+                ptx::tc_mma_w(tmem + tDV, dp_mn + mnstep(kk), dz_mn + mnstep(kk), idA, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < BM / 16; ++kk)  // dK = dS^T Q
+                ptx::tc_mma_w(tmem + tDK, ds_mn + mnstep(kk), dq_mn + mnstep(kk), idA, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+            for (int kk = 0; kk < BN / 16; ++kk)  // dQ = dS K
+                ptx::tc_mma_w(tmem + tDQ, ds_k + kstep(kk, BM), dk_mn + mnstep(kk), idQ, kk > 0 ? 1u : 0u);
+            if (p.ak) {  // dQ += Gamma W^K
+                const uint64_t dwk = ptx::sdesc_sw128(sh.base + p.off_wk, (uint32_t)p.Wp * 128, 1024);
+#pragma unroll 1
+                for (int kk = 0; kk < p.Wp / 16; ++kk)
+                    ptx::tc_mma_w(tmem + tDQ, dg_k + kstep(kk, BM), dwk + mnstep(kk), idQ, 1u);
+            }
+            if (p.bins) {
+#pragma unroll 1
+                for (int kk = 0; kk < BM / 16; ++kk)  // [Gamma | Beta]^T [Q | dZ]
+                    ptx::tc_mma_w(tmem + tW, dgb_mn + mnstep(kk), dq_mn + mnstep(kk), idW, kk > 0 ? 1u : 0u);
+            }
+            ptx::tc_commit_w(bar(S_OUT_FULL));
+        }
+        ptx::tc_commit_w(bar(S_DRAIN));
+        tc::drain_bar(bar(S_DRAIN), 0, sh.limit);
+    } else if (warp >= kRowWarp0) {
+        const int quarter = warp & 3;
+        const int il = 32 * quarter + lane;  // query row of S and dP, key row of dV and dK
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+        float *Rs = reinterpret_cast<float *>(sh.ptr + p.off_r) + il * p.SRk;
+        float *Rvs = reinterpret_cast<float *>(sh.ptr + p.off_rv) + il * p.SRv;
+        uint8_t *prow = sh.ptr + p.off_p + il * 128;
+        uint8_t *dsrow = sh.ptr + p.off_ds + il * 128;
+        uint8_t *gb = sh.ptr + p.off_gb;
+        const uint32_t sw = (uint32_t)(il & 7);
+        const int k = p.clip_k, W = p.W;
+        const int khi = p.causal ? 0 : k;
+        const bool bidir = !p.causal;
+        // this row of the bins tile starts at zero
+        if (p.bins) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                *reinterpret_cast<uint4 *>(gb + (c >> 3) * (BM * 128) + il * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        bool ok = tc::wait_bar(bar(S_A_FULL), 0, sh, p.err);
+        ok = __all_sync(0xffffffffu, ok) != 0;
+        if (ok) {
+            ptx::tc_fence_after();
+            for (int c0 = 0; c0 < p.Wp; c0 += 16) {
+                float x[16], y[16];
+                if (p.ak) ptx::tmem_ld16p(lane_base + tR + (uint32_t)c0, reinterpret_cast<uint32_t *>(x));
+                if (p.av) ptx::tmem_ld16p(lane_base + tRv + (uint32_t)c0, reinterpret_cast<uint32_t *>(y));
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    if (c0 + t < W) {
+                        if (p.ak) Rs[c0 + t] = p.c * x[t];
+                        if (p.av) Rvs[c0 + t] = y[t];
+                    }
+                }
+            }
+            const bool row_ok = il < p.n;
+            // pass 1: logits (log2 domain) over the scores, and the maximum
+            float m = -INFINITY;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float sv[32];
+                ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), sv);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int j = 32 * ch + t, dl = j - il;
+                    const bool valid = row_ok && j < nk && (!p.causal || dl <= 0);
+                    const int r = min(max(dl, -k), khi) + k;
+                    const float x = valid ? fmaf(p.c, sv[t], p.ak ? Rs[r] : 0.f) : -INFINITY;
+                    m = fmaxf(m, x);
+                    sv[t] = x;
+                }
+                __syncwarp();
+                ptx::tmem_st32f(lane_base + tS + (uint32_t)(32 * ch), sv);
+            }
+            ptx::tmem_st_wait();
+            // pass 2: row sum and D = sum_j p_ij dp_ij. Every lane runs the TMEM loads (they are
+            // warp-collective); a row without an allowed key has every logit at -inf, so with
+            // its maximum taken as 0 all its terms are exactly 0
+            const float mm = m == -INFINITY ? 0.f : m;
+            float l = 0.f, Dacc = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float x[32], dp[32];
+                ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), x);
+                ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dp);
+                ptx::tmem_ld_wait();
+                float l0 = 0.f, l1 = 0.f, d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                    const int j = 32 * ch + t;
+                    const int r0 = min(max(j - il, -k), khi) + k, r1 = min(max(j + 1 - il, -k), khi) + k;
+                    const float p0 = ptx::ex2(x[t] - mm), p1 = ptx::ex2(x[t + 1] - mm);
+                    l0 += p0;
+                    l1 += p1;
+                    d0 = fmaf(p0, dp[t] + (p.av ? Rvs[r0] : 0.f), d0);
+                    d1 = fmaf(p1, dp[t + 1] + (p.av ? Rvs[r1] : 0.f), d1);
+                }
+                l += l0 + l1;
+                Dacc += d0 + d1;
+            }
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float Dv = Dacc * inv;
+            // pass 3: P, dS (bf16 tiles) and the bins
+            float Lb = 0.f, Lg = 0.f, Rb = 0.f, Rg = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                float x[32], dp[32];
+                ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), x);
+                ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dp);
+                ptx::tmem_ld_wait();
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int t2 = 0; t2 < 16; ++t2) {
+                    float pe[2], de[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = 2 * t2 + h, j = 32 * ch + t, dl = j - il;
+                        const int r = min(max(dl, -k), khi) + k;
+                        const float pr = ptx::ex2(x[t] - mm) * inv;  // -inf logits: 0
+                        const float ds = pr * (dp[t] + (p.av ? Rvs[r] : 0.f) - Dv);
+                        pe[h] = pr;
+                        de[h] = ds;
+                        if (p.bins && pr > 0.f) {
+                            const bool isL = r == 0, isR = bidir && r == 2 * k && !isL;
+                            Lb += isL ? pr : 0.f;
+                            Lg += isL ? ds : 0.f;
+                            Rb += isR ? pr : 0.f;
+                            Rg += isR ? ds : 0.f;
+                            if (!isL && !isR) {  // an interior bin: this one key
+                                st_bf16_tile(gb, il, r, ds);
+                                st_bf16_tile(gb, il, 64 + r, pr);
+                            }
+                        }
+                    }
+                    pp[t2] = ptx::pack_bf16x2(pe[0], pe[1]);
+                    dd[t2] = ptx::pack_bf16x2(de[0], de[1]);
+                }
+                const uint32_t blk = (uint32_t)(ch >> 1) * (BN * 128);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t u = (uint32_t)((ch & 1) * 4 + w);
+                    *reinterpret_cast<uint4 *>(prow + blk + ((u ^ sw) << 4)) =
+                        make_uint4(pp[4 * w], pp[4 * w + 1], pp[4 * w + 2], pp[4 * w + 3]);
+                    *reinterpret_cast<uint4 *>(dsrow + blk + ((u ^ sw) << 4)) =
+                        make_uint4(dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
+                }
+            }
+            if (p.bins && l > 0.f) {  // the end bins
+                st_bf16_tile(gb, il, 0, Lg);
+                st_bf16_tile(gb, il, 64, Lb);
+                if (bidir && k > 0) {
+                    st_bf16_tile(gb, il, 2 * k, Rg);
+                    st_bf16_tile(gb, il, 64 + 2 * k, Rb);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(S_G_FULL));
+            ok = tc::wait_bar(bar(S_OUT_FULL), 0, sh, p.err);
+            ok = __all_sync(0xffffffffu, ok) != 0;
+        }
+        if (ok) {
+            ptx::tc_fence_after();
+            const long long row = (long long)bh * p.n + il;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float a[32], b[32], q[32];
+                ptx::tmem_ld32f(lane_base + tDV + (uint32_t)c0, a);
+                ptx::tmem_ld32f(lane_base + tDK + (uint32_t)c0, b);
+                ptx::tmem_ld32f(lane_base + tDQ + (uint32_t)c0, q);
+                ptx::tmem_ld_wait();
+                if (il < p.n) {
+                    float4 *dv = reinterpret_cast<float4 *>(p.dv + row * D + c0);
+                    float4 *dk = reinterpret_cast<float4 *>(p.dk + row * D + c0);
+                    float4 *dq = reinterpret_cast<float4 *>(p.dq + row * D + c0);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        dv[u] = make_float4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+                        dk[u] = make_float4(p.scale * b[4 * u], p.scale * b[4 * u + 1], p.scale * b[4 * u + 2],
+                                            p.scale * b[4 * u + 3]);
+                        dq[u] = make_float4(p.scale * q[4 * u], p.scale * q[4 * u + 1], p.scale * q[4 * u + 2],
+                                            p.scale * q[4 * u + 3]);
+                    }
+                }
+            }
+            // lane il < 64 (warps of quarters 0 and 1): dW^K row il in columns 0..63; lane 64 + r:
+            // dW^V row r in columns 64..127. The TMEM loads run warp-uniformly; the atomics only
+            // for table rows that exist.
+            const bool kpart = quarter < 2;
+            const int r = kpart ? il : il - 64;
+            if (p.bins && (kpart ? p.ak : p.av)) {
+                float *dst = (kpart ? p.daK : p.daV) + tho + (long long)r * D;
+                const float f = kpart ? p.scale : 1.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    float v[32];
+                    ptx::tmem_ld32f(lane_base + tW + (uint32_t)(kpart ? c0 : D + c0), v);
+                    ptx::tmem_ld_wait();
+                    if (r < W) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            red_add_v4(dst + c0 + 4 * u, f * v[4 * u], f * v[4 * u + 1], f * v[4 * u + 2],
+                                       f * v[4 * u + 3]);
+                    }
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    ptx::cta_barrier();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ==================================================================================== host
 
 inline uint32_t round_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -909,6 +1260,55 @@ cudaError_t opt_in(K kern, std::mutex &mu, bool (&opted)[64]) {
     return cudaSuccess;
 }
 
+// one-tile kernel: shared-memory layout (Q and dZ adjacent: [Q | dZ] is one operand),
+// descriptors and launch
+template <int D>
+cudaError_t launch_short(const BwdArgs &a, Params p, cudaStream_t s) {
+    const tc::DeviceInfo di = tc::device_info();
+    const bool ak = a.aK != nullptr, av = a.aV != nullptr;
+    const uint32_t tile = (uint32_t)BM * D * 2;
+    const uint32_t tab = round_up((uint32_t)p.Wp * D * 2, 1024);
+    uint32_t off = 0;
+    p.off_q = off; off += tile;
+    p.off_dz = off; off += tile;
+    p.off_k = off; off += tile;
+    p.off_v = off; off += tile;
+    p.off_wk = off; if (ak) off += tab;
+    p.off_wv = off; if (av) off += tab;
+    p.off_p = off; off += (uint32_t)BM * BN * 2;
+    p.off_ds = off; off += (uint32_t)BM * BN * 2;
+    p.off_gb = off; off += (uint32_t)BM * 128 * 2;
+    p.off_r = off; off += (uint32_t)BM * p.SRk * 4;
+    p.off_rv = off; off += (uint32_t)BM * p.SRv * 4;
+    off = round_up(off, 16);
+    p.off_bar = off; off += 8 * 32 + 16;
+    const uint32_t smem = off + 1024;
+    if (smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
+    CUtensorMap tm[6];
+    const uint64_t d = (uint64_t)D, n = (uint64_t)a.n, BH = (uint64_t)p.BH;
+    const uint64_t rs = d * 2, hs = n * d * 2;
+    if (!tc::make_map(&tm[0], a.q, d, n, BH, rs, hs, BM) || !tc::make_map(&tm[1], a.dout, d, n, BH, rs, hs, BM) ||
+        !tc::make_map(&tm[2], a.k, d, n, BH, rs, hs, BN) || !tc::make_map(&tm[3], a.v, d, n, BH, rs, hs, BN))
+        return cudaErrorInvalidValue;
+    tm[4] = tm[0];
+    tm[5] = tm[0];
+    const uint64_t Ht = p.table_heads ? (uint64_t)a.H : 1;
+    const uint64_t rows_mem = (uint64_t)(2 * a.clip_k + 1);
+    const uint64_t ths_bytes = p.table_heads ? (uint64_t)a.ths * 2 : rows_mem * d * 2;
+    if (ak && !tc::make_map(&tm[4], a.aK, d, rows_mem, Ht, rs, ths_bytes, (uint32_t)p.Wp)) return cudaErrorInvalidValue;
+    if (av && !tc::make_map(&tm[5], a.aV, d, rows_mem, Ht, rs, ths_bytes, (uint32_t)p.Wp)) return cudaErrorInvalidValue;
+    static std::mutex mu;
+    static bool opted[64] = {};
+    cudaError_t e;
+    if ((e = opt_in(bwd_short_kernel<D>, mu, opted)) != cudaSuccess) return e;
+    const int Htab = p.table_heads ? a.H : 1;
+    const size_t tab_bytes = (size_t)((long long)(Htab - 1) * a.ths + (long long)(2 * a.clip_k + 1) * a.d) * sizeof(float);
+    if (ak && (e = cudaMemsetAsync(a.daK, 0, tab_bytes, s)) != cudaSuccess) return e;
+    if (av && (e = cudaMemsetAsync(a.daV, 0, tab_bytes, s)) != cudaSuccess) return e;
+    bwd_short_kernel<D><<<(unsigned)p.BH, kThreads, smem, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], p);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     const bool ak = a.aK != nullptr, av = a.aV != nullptr;
@@ -949,6 +1349,15 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     if ((long long)p.BH * p.n_tiles > INT32_MAX) return cudaErrorNotSupported;
     if (reinterpret_cast<uintptr_t>(a.workspace) % 256 != 0) return cudaErrorNotSupported;
     ws_layout(a, W, p.SK, p.SV, &p);
+    p.daK = a.daK;
+    p.daV = a.daV;
+    p.ths = a.ths;
+    if constexpr (D == 64) {
+        if (a.n <= BM && (!(ak || av) || W <= kShortMaxW)) {
+            const cudaError_t e = launch_short<D>(a, p, s);
+            if (e != cudaErrorNotSupported) return e;
+        }
+    }
 
     // stats kernel shared memory: Q, dZ, K/V stages, table rows (TMA targets, 1024-aligned),
     // then the R and Rv rows and the barriers

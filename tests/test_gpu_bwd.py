@@ -54,6 +54,10 @@ TC_CASES = [
     ("k0", 2, 2, 150, 64, 0, False, None, True, True, False, "bf16"),
     ("value_only_causal_d128", 2, 2, 140, 128, 16, True, (1, 140), False, True, False, "bf16"),
     ("plain_tiles", 2, 2, 257, 64, 4, False, None, False, False, False, "bf16"),
+    # one query tile and one key tile per head (n <= 128, d = 64, at most 48 staged rows): the
+    # one-tile kernel, at its row limit with key padding, and a single token
+    ("one_tile_w47_padded", 3, 2, 128, 64, 23, False, (0, 128), True, True, False, "bf16"),
+    ("one_tile_n1_causal", 2, 3, 1, 64, 4, True, None, True, True, True, "bf16"),
 ]
 
 
