@@ -531,7 +531,11 @@ def launches_per_step(rp, w) -> int:
     if (w.kind == "decode" and not NO_DECODE_WORKSPACE and
             rp.relattn_decode_workspace_size(w.B, w.H, w.n, w.d) > 0):
         return 2
-    if w.kind == "bwd":  # rows, keys, tables (the two table memsets are not kernels of ours)
+    if w.kind == "bwd":  # the table memsets and the dq memset are not kernels of ours
+        rows = w.clip_k + 1 if w.causal else 2 * w.clip_k + 1
+        if (bwd_on_tensor_cores(w) and w.d == 64 and w.n <= 128 and
+                (rows <= 48 or not (w.key_term or w.value_term))):
+            return 1  # the one-tile kernel
         return 3 if (w.key_term or w.value_term) else 2
     return 1
 
