@@ -71,6 +71,7 @@ struct Params {
     float *ws_rk, *ws_rv, *ws_bb, *ws_gg, *ws_rec;  // ws_bb, ws_gg: interior bins [row][W]
     uint32_t off_q, off_dz, off_k, off_v, off_wk, off_wv, off_r, off_rv, off_ds, off_bar;
     uint32_t off_p, off_gb;      // one-tile kernel: the P tile and the gamma|beta tile
+    uint32_t off_x;              // one-tile kernel: per-row values exchanged by the two halves
     uint32_t stage_bytes;        // stats: one K (or V) stage; keys: one Q/dZ/R'/Rv' stage
     int stages;
     long long wait_limit;
@@ -889,6 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and the outputs leave TMEM by row (dq, dk, dv plain stores, the table rows by atomic adds).
 enum : int { S_LD = 0, S_A_FULL, S_G_FULL, S_OUT_FULL, S_DRAIN, kSBars };
 constexpr int kShortMaxW = 48;
+constexpr int kShortThreads = 320;  // warp 0 loads, warp 1 MMAs, warps 2-9 two threads per row
 
 __device__ __forceinline__ void st_bf16_tile(uint8_t *tile, int row, int col, float v) {
     // element (row, col) of a [128 rows][128 cols] bf16 tile in two 64-column blocks with the
@@ -899,7 +901,7 @@ __device__ __forceinline__ void st_bf16_tile(uint8_t *tile, int row, int col, fl
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kShortThreads, 1)
     bwd_short_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
@@ -916,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long tho = p.table_heads ? (long long)(bh % p.H) * p.ths : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kSBars; ++i) ptx::mbar_init(bar(i), i == S_G_FULL ? 128u : 1u);
+        for (int i = 0; i < kSBars; ++i) ptx::mbar_init(bar(i), i == S_G_FULL ? 256u : 1u);
         *sh.abort_flag = 0;
         ptx::mbar_init_fence();
     } else if (threadIdx.x == 32) {
@@ -1021,11 +1023,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit_w(bar(S_DRAIN));
         tc::drain_bar(bar(S_DRAIN), 0, sh.limit);
     } else if (warp >= kRowWarp0) {
+        // two threads per row: group g takes keys 64 g .. 64 g + 63 (chunks 2 g, 2 g + 1); the row
+        // maximum, sum, D and end bins are combined through shared memory at a named barrier
+        // of the 256 row threads (every row thread reaches each one: its waits are bounded)
+        const int g = (warp - kRowWarp0) >> 2;
         const int quarter = warp & 3;
         const int il = 32 * quarter + lane;  // query row of S and dP, key row of dV and dK
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
         float *Rs = reinterpret_cast<float *>(sh.ptr + p.off_r) + il * p.SRk;
         float *Rvs = reinterpret_cast<float *>(sh.ptr + p.off_rv) + il * p.SRv;
+        float *X = reinterpret_cast<float *>(sh.ptr + p.off_x);  // [value][group][row]
+        auto xv = [&](int v, int gg) -> float & { return X[(v * 2 + gg) * BM + il]; };
         uint8_t *prow = sh.ptr + p.off_p + il * 128;
         uint8_t *dsrow = sh.ptr + p.off_ds + il * 128;
         uint8_t *gb = sh.ptr + p.off_gb;
@@ -1033,34 +1041,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int k = p.clip_k, W = p.W;
         const int khi = p.causal ? 0 : k;
         const bool bidir = !p.causal;
-        // this row of the bins tile starts at zero
+        const bool row_ok = il < p.n;
+        // this row of the bins tile starts at zero (group g: block g)
         if (p.bins) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-                *reinterpret_cast<uint4 *>(gb + (c >> 3) * (BM * 128) + il * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(gb + g * (BM * 128) + il * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         bool ok = tc::wait_bar(bar(S_A_FULL), 0, sh, p.err);
         ok = __all_sync(0xffffffffu, ok) != 0;
-        if (ok) {
+        if (ok && (g == 0 ? p.ak : p.av)) {  // group 0 reads R, group 1 Rv
             ptx::tc_fence_after();
             for (int c0 = 0; c0 < p.Wp; c0 += 16) {
-                float x[16], y[16];
-                if (p.ak) ptx::tmem_ld16p(lane_base + tR + (uint32_t)c0, reinterpret_cast<uint32_t *>(x));
-                if (p.av) ptx::tmem_ld16p(lane_base + tRv + (uint32_t)c0, reinterpret_cast<uint32_t *>(y));
+                float x[16];
+                ptx::tmem_ld16p(lane_base + (g == 0 ? tR : tRv) + (uint32_t)c0, reinterpret_cast<uint32_t *>(x));
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    if (c0 + t < W) {
-                        if (p.ak) Rs[c0 + t] = p.c * x[t];
-                        if (p.av) Rvs[c0 + t] = y[t];
-                    }
-                }
+                for (int t = 0; t < 16; ++t)
+                    if (c0 + t < W) (g == 0 ? Rs : Rvs)[c0 + t] = g == 0 ? p.c * x[t] : x[t];
             }
-            const bool row_ok = il < p.n;
-            // pass 1: logits (log2 domain) over the scores, and the maximum
+        }
+        ok = ptx::bar_red_and(1, 256, ok);
+        // pass 1: logits (log2 domain) over the scores, and the maximum of this half
+        if (ok) {
+            ptx::tc_fence_after();
             float m = -INFINITY;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {
                 float sv[32];
                 ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), sv);
                 ptx::tmem_ld_wait();
@@ -1077,13 +1084,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_st32f(lane_base + tS + (uint32_t)(32 * ch), sv);
             }
             ptx::tmem_st_wait();
-            // pass 2: row sum and D = sum_j p_ij dp_ij. Every lane runs the TMEM loads (they are
-            // warp-collective); a row without an allowed key has every logit at -inf, so with
-            // its maximum taken as 0 all its terms are exactly 0
-            const float mm = m == -INFINITY ? 0.f : m;
+            xv(0, g) = m;
+        }
+        ok = ptx::bar_red_and(1, 256, ok);
+        // pass 2: row sum and D = sum_j p_ij dp_ij of this half. Every lane runs the TMEM loads
+        // (they are warp-collective); a row without an allowed key has every logit at -inf, so
+        // with its maximum taken as 0 all its terms are exactly 0
+        const float m = ok ? fmaxf(xv(0, 0), xv(0, 1)) : 0.f;
+        const float mm = m == -INFINITY ? 0.f : m;
+        if (ok) {
             float l = 0.f, Dacc = 0.f;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {
                 float x[32], dp[32];
                 ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), x);
                 ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dp);
@@ -1102,12 +1114,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l += l0 + l1;
                 Dacc += d0 + d1;
             }
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float Dv = Dacc * inv;
-            // pass 3: P, dS (bf16 tiles) and the bins
+            xv(1, g) = l;
+            xv(2, g) = Dacc;
+        }
+        ok = ptx::bar_red_and(1, 256, ok);
+        const float l = ok ? xv(1, 0) + xv(1, 1) : 0.f;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float Dv = ok ? (xv(2, 0) + xv(2, 1)) * inv : 0.f;
+        // pass 3: P, dS (bf16 tiles, block g) and the bins of this half's keys
+        if (ok) {
             float Lb = 0.f, Lg = 0.f, Rb = 0.f, Rg = 0.f;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {
                 float x[32], dp[32];
                 ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), x);
                 ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dp);
@@ -1149,63 +1167,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                         make_uint4(dd[4 * w], dd[4 * w + 1], dd[4 * w + 2], dd[4 * w + 3]);
                 }
             }
-            if (p.bins && l > 0.f) {  // the end bins
-                st_bf16_tile(gb, il, 0, Lg);
-                st_bf16_tile(gb, il, 64, Lb);
-                if (bidir && k > 0) {
-                    st_bf16_tile(gb, il, 2 * k, Rg);
-                    st_bf16_tile(gb, il, 64 + 2 * k, Rb);
-                }
+            xv(3, g) = Lb;
+            xv(4, g) = Lg;
+            xv(5, g) = Rb;
+            xv(6, g) = Rg;
+        }
+        ok = ptx::bar_red_and(1, 256, ok);
+        if (ok && g == 0 && p.bins && l > 0.f) {  // the end bins, both halves
+            st_bf16_tile(gb, il, 0, xv(4, 0) + xv(4, 1));
+            st_bf16_tile(gb, il, 64, xv(3, 0) + xv(3, 1));
+            if (bidir && k > 0) {
+                st_bf16_tile(gb, il, 2 * k, xv(6, 0) + xv(6, 1));
+                st_bf16_tile(gb, il, 64 + 2 * k, xv(5, 0) + xv(5, 1));
             }
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(S_G_FULL));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(S_G_FULL));
+        if (ok) {
             ok = tc::wait_bar(bar(S_OUT_FULL), 0, sh, p.err);
             ok = __all_sync(0xffffffffu, ok) != 0;
         }
-        if (ok) {
+        if (ok) {  // group g: columns 32 g .. 32 g + 31 of every output
             ptx::tc_fence_after();
             const long long row = (long long)bh * p.n + il;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float a[32], b[32], q[32];
-                ptx::tmem_ld32f(lane_base + tDV + (uint32_t)c0, a);
-                ptx::tmem_ld32f(lane_base + tDK + (uint32_t)c0, b);
-                ptx::tmem_ld32f(lane_base + tDQ + (uint32_t)c0, q);
-                ptx::tmem_ld_wait();
-                if (il < p.n) {
-                    float4 *dv = reinterpret_cast<float4 *>(p.dv + row * D + c0);
-                    float4 *dk = reinterpret_cast<float4 *>(p.dk + row * D + c0);
-                    float4 *dq = reinterpret_cast<float4 *>(p.dq + row * D + c0);
+            const int c0 = 32 * g;
+            float a[32], b[32], q[32];
+            ptx::tmem_ld32f(lane_base + tDV + (uint32_t)c0, a);
+            ptx::tmem_ld32f(lane_base + tDK + (uint32_t)c0, b);
+            ptx::tmem_ld32f(lane_base + tDQ + (uint32_t)c0, q);
+            ptx::tmem_ld_wait();
+            if (il < p.n) {
+                float4 *dv = reinterpret_cast<float4 *>(p.dv + row * D + c0);
+                float4 *dk = reinterpret_cast<float4 *>(p.dk + row * D + c0);
+                float4 *dq = reinterpret_cast<float4 *>(p.dq + row * D + c0);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        dv[u] = make_float4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-                        dk[u] = make_float4(p.scale * b[4 * u], p.scale * b[4 * u + 1], p.scale * b[4 * u + 2],
-                                            p.scale * b[4 * u + 3]);
-                        dq[u] = make_float4(p.scale * q[4 * u], p.scale * q[4 * u + 1], p.scale * q[4 * u + 2],
-                                            p.scale * q[4 * u + 3]);
-                    }
+                for (int u = 0; u < 8; ++u) {
+                    dv[u] = make_float4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+                    dk[u] = make_float4(p.scale * b[4 * u], p.scale * b[4 * u + 1], p.scale * b[4 * u + 2],
+                                        p.scale * b[4 * u + 3]);
+                    dq[u] = make_float4(p.scale * q[4 * u], p.scale * q[4 * u + 1], p.scale * q[4 * u + 2],
+                                        p.scale * q[4 * u + 3]);
                 }
             }
-            // lane il < 64 (warps of quarters 0 and 1): dW^K row il in columns 0..63; lane 64 + r:
-            // dW^V row r in columns 64..127. The TMEM loads run warp-uniformly; the atomics only
-            // for table rows that exist.
+            // lane il < 64 (quarters 0 and 1): dW^K row il in columns 0..63; lane 64 + r: dW^V row
+            // r in columns 64..127. The TMEM loads run warp-uniformly; the atomics only for table
+            // rows that exist.
             const bool kpart = quarter < 2;
             const int r = kpart ? il : il - 64;
             if (p.bins && (kpart ? p.ak : p.av)) {
-                float *dst = (kpart ? p.daK : p.daV) + tho + (long long)r * D;
+                float *dst = (kpart ? p.daK : p.daV) + tho + (long long)r * D + c0;
                 const float f = kpart ? p.scale : 1.f;
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float v[32];
-                    ptx::tmem_ld32f(lane_base + tW + (uint32_t)(kpart ? c0 : D + c0), v);
-                    ptx::tmem_ld_wait();
-                    if (r < W) {
+                float v[32];
+                ptx::tmem_ld32f(lane_base + tW + (uint32_t)((kpart ? 0 : D) + c0), v);
+                ptx::tmem_ld_wait();
+                if (r < W) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            red_add_v4(dst + c0 + 4 * u, f * v[4 * u], f * v[4 * u + 1], f * v[4 * u + 2],
-                                       f * v[4 * u + 3]);
-                    }
+                    for (int u = 0; u < 8; ++u)
+                        red_add_v4(dst + 4 * u, f * v[4 * u], f * v[4 * u + 1], f * v[4 * u + 2], f * v[4 * u + 3]);
                 }
             }
         }
@@ -1281,6 +1300,7 @@ cudaError_t launch_short(const BwdArgs &a, Params p, cudaStream_t s) {
     p.off_r = off; off += (uint32_t)BM * p.SRk * 4;
     p.off_rv = off; off += (uint32_t)BM * p.SRv * 4;
     off = round_up(off, 16);
+    p.off_x = off; off += 7 * 2 * BM * 4;
     p.off_bar = off; off += 8 * 32 + 16;
     const uint32_t smem = off + 1024;
     if (smem > (uint32_t)di.smem_optin) return cudaErrorNotSupported;
@@ -1305,7 +1325,7 @@ cudaError_t launch_short(const BwdArgs &a, Params p, cudaStream_t s) {
     const size_t tab_bytes = (size_t)((long long)(Htab - 1) * a.ths + (long long)(2 * a.clip_k + 1) * a.d) * sizeof(float);
     if (ak && (e = cudaMemsetAsync(a.daK, 0, tab_bytes, s)) != cudaSuccess) return e;
     if (av && (e = cudaMemsetAsync(a.daV, 0, tab_bytes, s)) != cudaSuccess) return e;
-    bwd_short_kernel<D><<<(unsigned)p.BH, kThreads, smem, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], p);
+    bwd_short_kernel<D><<<(unsigned)p.BH, kShortThreads, smem, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], p);
     return cudaGetLastError();
 }
 
