@@ -43,8 +43,15 @@ using tc::BN;
 using tc::kLog2e;
 using tc::Shared;
 
-constexpr int kThreads = 192;
 constexpr int kRowWarp0 = 2;
+// row groups: d = 64 runs two threads per row (each half of a tile's keys), d = 128 one (the
+// per-thread diagonal scratch of two groups would not fit beside its tiles)
+template <int D> struct Groups {
+    static constexpr int NG = D == 64 ? 2 : 1;
+    static constexpr int kRowThreads = 128 * NG;
+    static constexpr int kThreads = 64 + kRowThreads;  // warp 0 TMA, warp 1 MMA issue, row warps
+    static constexpr int CPT = 4 / NG;                  // 32-key chunks per thread and tile
+};
 constexpr int kWin = 256;       // R_win rows per key tile (the 255 offsets of a tile pair, + 1)
 constexpr int kSkew = 68;       // floats per row of the diagonal scratch
 constexpr int kMaxStages = 2;
@@ -57,15 +64,15 @@ struct Params {
     int *err;
     const __nv_bfloat16 *u, *vb;      // [H|1, d]
     __nv_bfloat16 *out;               // [B, H, n, d]
-    uint32_t off_q, off_k, off_v, off_r, off_skew, off_uk, off_vr, off_uv, off_bar;
+    uint32_t off_q, off_k, off_v, off_r, off_skew, off_uk, off_vr, off_uv, off_x, off_bar;
     uint32_t stage_kv, stage_r;       // bytes per stage: one K (or V) tile, one R_win tile
     int stages;
     long long wait_limit;
 };
 
 enum : int {
-    X_Q = 0, X_S_FULL, X_P_FULL, X_PV_DONE, X_DRAIN,
-    X_KV_FULL = 5, X_KV_EMPTY = X_KV_FULL + kMaxStages, kBars = X_KV_EMPTY + kMaxStages
+    X_Q = 0, X_S_FULL, X_S_EMPTY, X_P_FULL, X_PV_DONE, X_DRAIN,
+    X_KV_FULL = 6, X_KV_EMPTY = X_KV_FULL + kMaxStages, kBars = X_KV_EMPTY + kMaxStages
 };
 
 __device__ __forceinline__ uint64_t kstep(int kk, int rows) {
@@ -97,10 +104,14 @@ __device__ __forceinline__ float swz_dot(const uint8_t *tile, uint32_t block_byt
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Groups<D>::kThreads, 1)
     txl_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                   const __grid_constant__ Params p) {
+    // d = 64: P has its own TMEM columns, so the next tile's S and T run during this tile's
+    // softmax; d = 128: P over S (TMEM is full), the next S waits for this P V
+    constexpr bool P_OWN = D == 64;
+    constexpr int NG = Groups<D>::NG, CPT = Groups<D>::CPT, kRowThreads = Groups<D>::kRowThreads;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     Shared sh;
@@ -119,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int th = p.shared ? 0 : bh % p.H;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kBars; ++i) ptx::mbar_init(bar(i), i == X_P_FULL ? 128u : 1u);
+        for (int i = 0; i < kBars; ++i)
+            ptx::mbar_init(bar(i), (i == X_P_FULL || i == X_S_EMPTY) ? (uint32_t)kRowThreads : 1u);
         *sh.abort_flag = 0;
         ptx::mbar_init_fence();
     } else if (threadIdx.x == 32) {
@@ -133,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile uint32_t *>(sh.ptr + p.off_bar + 8 * 32), 0);
-    // TMEM columns: S (then P) at 0, T at 128, O at 384
-    constexpr uint32_t tS = 0, tT = 128, tO = 384;
+    // TMEM columns: S at 0, T at 128, O at 384; P at 448 (d = 64) or over S (d = 128)
+    constexpr uint32_t tS = 0, tT = 128, tO = 384, tP = P_OWN ? 448 : 0;
 
     auto wait_w = [&](uint32_t b, uint32_t parity) -> bool {
         const bool r = tc::wait_bar_ctrl(b, parity, sh, p.err);
@@ -180,74 +192,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idS = ptx::idesc_bf16(BM, BN, 0);
         constexpr uint32_t idT = ptx::idesc_bf16(BM, kWin, 0);
         constexpr uint32_t idPV = ptx::idesc_bf16(BM, D, 1);
-        for (int j = 0; j < J && ok; ++j) {
+        // S_j = Q K_j^T and T_j = Q R_win,j^T into their columns (free: the rows have read the
+        // previous tile's S and T, and with P over S the previous P V is done)
+        auto scores = [&](int j) -> bool {
             const int s = j % p.stages;
-            const uint32_t round = (uint32_t)(j / p.stages);
-            if (!(ok = wait_w(bar(X_KV_FULL + s), round & 1u))) break;
-            // P over S: the previous P V has read its columns (and the rows have read T)
-            if (j > 0 && !(ok = wait_w(bar(X_PV_DONE), (uint32_t)(j - 1) & 1u))) break;
+            if (!wait_w(bar(X_KV_FULL + s), (uint32_t)(j / p.stages) & 1u)) return false;
+            if (j > 0 && !wait_w(bar(X_S_EMPTY), (uint32_t)(j - 1) & 1u)) return false;
+            if (!P_OWN && j > 0 && !wait_w(bar(X_PV_DONE), (uint32_t)(j - 1) & 1u)) return false;
             ptx::tc_fence_after();
             const uint64_t dk = ptx::sdesc_sw128(sh.base + p.off_k + (uint32_t)s * p.stage_kv, 16, 1024);
             const uint64_t dr = ptx::sdesc_sw128(sh.base + p.off_r + (uint32_t)s * p.stage_r, 16, 1024);
-            const uint64_t dv = ptx::sdesc_sw128(sh.base + p.off_v + (uint32_t)s * p.stage_kv, BN * 128, 1024);
 #pragma unroll 1
-            for (int kk = 0; kk < D / 16; ++kk)  // S = Q K^T
+            for (int kk = 0; kk < D / 16; ++kk)
                 ptx::tc_mma_w(tmem + tS, dq + kstep(kk, BM), dk + kstep(kk, BN), idS, kk > 0 ? 1u : 0u);
 #pragma unroll 1
-            for (int kk = 0; kk < D / 16; ++kk)  // T = Q R_win^T
+            for (int kk = 0; kk < D / 16; ++kk)
                 ptx::tc_mma_w(tmem + tT, dq + kstep(kk, BM), dr + kstep(kk, kWin), idT, kk > 0 ? 1u : 0u);
             ptx::tc_commit_w(bar(X_S_FULL));
+            return true;
+        };
+        if (ok && J > 0) ok = scores(0);
+        for (int j = 0; j < J && ok; ++j) {
+            if (P_OWN && j + 1 < J && !(ok = scores(j + 1))) break;
+            const int s = j % p.stages;
             if (!(ok = wait_w(bar(X_P_FULL), (uint32_t)j & 1u))) break;
             ptx::tc_fence_after();
+            const uint64_t dv = ptx::sdesc_sw128(sh.base + p.off_v + (uint32_t)s * p.stage_kv, BN * 128, 1024);
 #pragma unroll 1
-            for (int kk = 0; kk < BN / 16; ++kk)  // O += P V (P bf16 pairs over S)
-                ptx::tc_mma_ts_w(tmem + tO, tmem + tS + (uint32_t)(kk * 8), dv + mnstep(kk), idPV,
+            for (int kk = 0; kk < BN / 16; ++kk)  // O += P V
+                ptx::tc_mma_ts_w(tmem + tO, tmem + tP + (uint32_t)(kk * 8), dv + mnstep(kk), idPV,
                                  (j > 0 || kk > 0) ? 1u : 0u);
             ptx::tc_commit_w(bar(X_PV_DONE));
             ptx::tc_commit_w(bar(X_KV_EMPTY + s));
+            if (!P_OWN && j + 1 < J && !(ok = scores(j + 1))) break;
         }
         ptx::tc_commit_w(bar(X_DRAIN));
         tc::drain_bar(bar(X_DRAIN), 0, sh.limit);
     } else if (warp >= kRowWarp0) {
-        // ---------------- one thread per query row (TMEM lane = row)
+        // ---------------- NG threads per query row (TMEM lane = row): group g takes chunks
+        // CPT g .. CPT g + CPT - 1 (32 keys each) of every tile; the row maximum and the row sum
+        // are combined through shared memory at a named barrier of the row threads (every row
+        // thread reaches each one: its waits are bounded)
+        const int g = (warp - kRowWarp0) >> 2;
         const int quarter = warp & 3;
         const int il = 32 * quarter + lane, ii = i0 + il;
+        const int tid = g * BM + il;  // 0 .. kRowThreads - 1
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
-        float *skew = reinterpret_cast<float *>(sh.ptr + p.off_skew) + il * kSkew;
+        float *skew = reinterpret_cast<float *>(sh.ptr + p.off_skew) + tid * kSkew;
         float *ukb = reinterpret_cast<float *>(sh.ptr + p.off_uk);   // [2][BN]
         float *vrb = reinterpret_cast<float *>(sh.ptr + p.off_vr);   // [2][kWin]
         float *uv = reinterpret_cast<float *>(sh.ptr + p.off_uv);    // u [D], then v [D]
-        if (il < D) {
-            uv[il] = __bfloat162float(p.u[(long long)th * D + il]);
-            uv[D + il] = __bfloat162float(p.vb[(long long)th * D + il]);
-        }
-        ptx::named_bar_sync(1, 128);
+        float *X = reinterpret_cast<float *>(sh.ptr + p.off_x);      // [NG][BM]: the groups' values
+        for (int e = tid; e < 2 * D; e += kRowThreads)
+            uv[e] = __bfloat162float(e < D ? p.u[(long long)th * D + e] : p.vb[(long long)th * D + e - D]);
+        ptx::named_bar_sync(1, kRowThreads);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < J && ok; ++j) {
             ok = tc::wait_bar(bar(X_S_FULL), (uint32_t)j & 1u, sh, p.err);
             ok = __all_sync(0xffffffffu, ok) != 0;
             const int s = j % p.stages, j0 = j * BN;
-            // terms (c) and (d) of this tile: u.k for its 128 keys, v.r for its 256 offsets
-            // (two buffers by tile parity; S_FULL of a tile comes after every row's P_FULL of
-            // the previous one, so no row still reads the buffer being written)
+            // terms (c) and (d) of this tile: u.k for its 128 keys, v.r for its 256 offsets; two
+            // buffers by tile parity
             float *uk = ukb + (j & 1) * BN;
             float *vr = vrb + (j & 1) * kWin;
             if (ok) {
                 ptx::tc_fence_after();
                 const uint8_t *kt = sh.ptr + p.off_k + s * p.stage_kv;
                 const uint8_t *rt = sh.ptr + p.off_r + s * p.stage_r;
-                uk[il] = swz_dot<D>(kt, BN * 128, il, uv);
-                vr[il] = swz_dot<D>(rt, kWin * 128, il, uv + D);
-                vr[il + 128] = swz_dot<D>(rt, kWin * 128, il + 128, uv + D);
+                if (g == 0) uk[il] = swz_dot<D>(kt, BN * 128, il, uv);
+                for (int o = tid; o < kWin; o += kRowThreads) vr[o] = swz_dot<D>(rt, kWin * 128, o, uv + D);
             }
-            // publishes the values; every row thread gets here (its wait above is bounded),
-            // and the AND of the outcome sends all of them on or out together
-            if (!(ok = ptx::bar_red_and(1, 128, ok))) break;
-            // pass 1: logits (log2 domain) back over S, and the row maximum
+            if (!(ok = ptx::bar_red_and(1, kRowThreads, ok))) break;
+            // pass 1: this group's logits (log2 domain), kept in registers, and their maximum
+            float x[32 * CPT];
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) {
+                const int ch = CPT * g + cc;
                 float sv[32], ta[32], tb[32];
                 const int cb = 32 * (ch - quarter + 3);  // first T column the warp's rows need
                 ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), sv);
@@ -269,22 +291,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int jl = 32 * ch + t, jj = j0 + jl;
                     const bool valid = ii < p.n && jj < nk && (!p.causal || jj <= ii);
                     const float tv = skew[t - lane + 31];  // column (j - i) + 127 of T, plus v.r
-                    const float x = valid ? p.c * (sv[t] + tv + uk[jl]) : -INFINITY;
-                    mx = fmaxf(mx, x);
-                    sv[t] = x;
+                    const float xv = valid ? p.c * (sv[t] + tv + uk[jl]) : -INFINITY;
+                    mx = fmaxf(mx, xv);
+                    x[32 * cc + t] = xv;
                 }
-                __syncwarp();
-                ptx::tmem_st32f(lane_base + tS + (uint32_t)(32 * ch), sv);
             }
-            ptx::tmem_st_wait();
-            // lazy rescale: only when the maximum grows by more than 2^8 (O holds the products of
-            // the earlier tiles; the S commit of this tile came after their P V)
+            // S and T are read: the next tile's products may overwrite them
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(X_S_EMPTY));
+            // O and (with its own columns) P hold the previous tile's product until its P V is
+            // done; the barrier below carries the outcome of this wait to every row thread
+            if (j > 0) {
+                ok = tc::wait_bar(bar(X_PV_DONE), (uint32_t)(j - 1) & 1u, sh, p.err);
+                ok = __all_sync(0xffffffffu, ok) != 0;
+                ptx::tc_fence_after();
+            }
+            X[tid] = mx;
+            if (!(ok = ptx::bar_red_and(1, kRowThreads, ok))) break;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) mx = fmaxf(mx, X[gg * BM + il]);
+            // lazy rescale: only when the maximum grows by more than 2^8
             const bool grow = mx > -INFINITY && (m == -INFINITY || mx > m + kRescaleLog2);
             const float m_new = grow ? fmaxf(m, mx) : m;
             const float al = grow ? ptx::ex2(m - m_new) : 1.f;  // m = -inf: 0 (nothing summed yet)
-            if (j > 0 && __any_sync(0xffffffffu, grow && al != 1.f)) {
+            if (j > 0 && __any_sync(0xffffffffu, grow && al != 1.f)) {  // this group's O columns
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 32 * g; c0 < D; c0 += 32 * NG) {
                     float o[32];
                     ptx::tmem_ld32f(lane_base + tO + (uint32_t)c0, o);
                     ptx::tmem_ld_wait();
@@ -297,38 +329,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l *= al;
             m = m_new;
-            // pass 2: P (bf16) over the S columns already read
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                float x[32];
-                ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), x);
-                ptx::tmem_ld_wait();
-                uint32_t pp[16];
+            // pass 2: P (bf16) for this group's keys
+            {
 #pragma unroll
-                for (int t2 = 0; t2 < 16; ++t2) {
-                    const float p0 = x[2 * t2] == -INFINITY ? 0.f : ptx::ex2(x[2 * t2] - m);
-                    const float p1 = x[2 * t2 + 1] == -INFINITY ? 0.f : ptx::ex2(x[2 * t2 + 1] - m);
-                    l += p0 + p1;
-                    pp[t2] = ptx::pack_bf16x2(p0, p1);
+                for (int cc = 0; cc < CPT; ++cc) {
+                    const int ch = CPT * g + cc;
+                    uint32_t pp[16];
+#pragma unroll
+                    for (int t2 = 0; t2 < 16; ++t2) {
+                        const float a0 = x[32 * cc + 2 * t2], a1 = x[32 * cc + 2 * t2 + 1];
+                        const float p0 = a0 == -INFINITY ? 0.f : ptx::ex2(a0 - m);
+                        const float p1 = a1 == -INFINITY ? 0.f : ptx::ex2(a1 - m);
+                        l += p0 + p1;
+                        pp[t2] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    __syncwarp();
+                    ptx::tmem_st16(lane_base + tP + (uint32_t)(16 * ch), pp);
                 }
-                __syncwarp();
-                ptx::tmem_st16(lane_base + tS + (uint32_t)(16 * ch), pp);
+                ptx::tmem_st_wait();
             }
-            ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(X_P_FULL));
         }
-        // epilogue: O / l -> bf16
+        // epilogue: the groups' row sums, then O / l -> bf16, group g writing the 32-column
+        // blocks g, g + NG, ...
+        float *XL = X + NG * BM;  // row sums apart from the maxima, which a slower thread may still read
+        XL[tid] = l;
+        ok = ptx::bar_red_and(1, kRowThreads, ok);
         if (ok && J > 0) {
             ok = tc::wait_bar(bar(X_PV_DONE), (uint32_t)(J - 1) & 1u, sh, p.err);
             ok = __all_sync(0xffffffffu, ok) != 0;
             if (ok) ptx::tc_fence_after();
         }
         if (ok) {
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float lt = 0.f;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) lt += XL[gg * BM + il];
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
             uint4 *orow = reinterpret_cast<uint4 *>(p.out + ((long long)bh * p.n + ii) * D);
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 32 * g; c0 < D; c0 += 32 * NG) {
                 float o[32];
                 if (J > 0) {
                     ptx::tmem_ld32f(lane_base + tO + (uint32_t)c0, o);
@@ -387,10 +427,11 @@ cudaError_t launch(const TxlArgs &a, cudaStream_t s) {
         p.off_k = off; off += (uint32_t)stages * p.stage_kv;
         p.off_v = off; off += (uint32_t)stages * p.stage_kv;
         p.off_r = off; off += (uint32_t)stages * p.stage_r;
-        p.off_skew = off; off += (uint32_t)BM * kSkew * 4;
+        p.off_skew = off; off += (uint32_t)Groups<D>::kRowThreads * kSkew * 4;
         p.off_uk = off; off += 2 * BN * 4;
         p.off_vr = off; off += 2 * kWin * 4;
         p.off_uv = off; off += 2 * D * 4;
+        p.off_x = off; off += 2u * Groups<D>::NG * BM * 4;
         p.off_bar = off; off += 8 * 32 + 16;
         p.stages = stages;
         return off + 1024;
@@ -422,7 +463,7 @@ cudaError_t launch(const TxlArgs &a, cudaStream_t s) {
             opted[dev] = true;
         }
     }
-    txl_tc_kernel<D><<<(unsigned)(p.BH * p.n_tiles), kThreads, smem, s>>>(tm[0], tm[1], tm[2], tm[3], p);
+    txl_tc_kernel<D><<<(unsigned)(p.BH * p.n_tiles), Groups<D>::kThreads, smem, s>>>(tm[0], tm[1], tm[2], tm[3], p);
     return cudaGetLastError();
 }
 
