@@ -288,6 +288,24 @@ RELATTN_API relattn_status_t relattn_decode_workspace_size(int B, int H, int T, 
                                                unsigned long long *bytes);
 
 /*
+ * relattn_sinusoid_table — the fixed sinusoidal encodings of every relative offset of a
+ * length-n sequence, the r of the Transformer-XL score before its projection ("Relative
+ * Position Encoding in Transformer-XL" page: r_{i-j} is a sinusoid of the distance, in the
+ * form the "Self-Attention with Relative Position Representations" page states for the
+ * original Transformer's position encodings):
+ *
+ *   out[o][2i]     = sin(p / 10000^(2i / d_model)),
+ *   out[o][2i + 1] = cos(p / 10000^(2i / d_model)),     p = o - (n - 1),  o = 0 .. 2n - 2.
+ *
+ * The angle is formed in fp64, the values rounded to `dtype` (RELATTN_BF16 or RELATTN_F32).
+ * out: caller-owned device memory of (2n - 1) * d_model elements; d_model even and >= 2.
+ * Projected by the head's W_{k,R} (a plain matrix product, [H, d, d_model] times this table)
+ * it gives the `rel` argument of relattn_txl_fwd.
+ */
+RELATTN_API relattn_status_t relattn_sinusoid_table(int n, int d_model, int dtype, void *out,
+                                        relattn_stream_t stream);
+
+/*
  * relattn_bwd — gradients of relattn_fwd (Shaw relation-aware attention) for training. The
  * pages state only the forward pass ("Self-Attention with Relative Position Representations" page, section 3.4, eq. 3 and eq. 4);
  * these are the chain rule through it:

@@ -61,3 +61,22 @@ def txl_fwd(q, k, val, rel, u, vb, causal, scale, kv_len=None):
             alpha = np.where(l > 0, p / np.where(l > 0, l, 1.0), 0.0)
             out[b, h] = alpha @ val[b, h]
     return out
+
+
+def sinusoid_table(n, d_model):
+    """The sinusoidal encodings of every relative offset of a length-n sequence, the r of the
+    Transformer-XL score before its projection W_{k,R}: row o holds offset o - (n - 1), and
+    for an offset p the components are PE(p, 2i) = sin(p / 10000^(2i / d_model)) and
+    PE(p, 2i + 1) = cos(p / 10000^(2i / d_model)) ("Self-Attention with Relative Position
+    Representations" page, the original Transformer's position encodings; "Relative Position
+    Encoding in Transformer-XL" page: r is this fixed sinusoid of the distance). fp64,
+    [2n - 1, d_model]; d_model even."""
+    if d_model % 2:
+        raise ValueError("d_model must be even")
+    pos = np.arange(-(n - 1), n, dtype=np.float64)[:, None]          # offsets
+    i2 = np.arange(0, d_model, 2, dtype=np.float64)[None, :]          # 2i
+    ang = pos / np.power(10000.0, i2 / d_model)
+    out = np.empty((2 * n - 1, d_model), dtype=np.float64)
+    out[:, 0::2] = np.sin(ang)
+    out[:, 1::2] = np.cos(ang)
+    return out

@@ -10,7 +10,8 @@ the library is not built raises ImportError.
 from __future__ import annotations
 
 _BINDING = ("relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
-            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_txl_fwd", "relattn_decode_fwd",
+            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_txl_fwd", "relattn_sinusoid_table",
+            "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",

@@ -72,13 +72,16 @@ _lib.relattn_debug_withhold_first_load.argtypes = [_I]
 _lib.relattn_debug_withhold_first_load.restype = _I
 _lib.relattn_set_short_kernel.argtypes = [_I]
 _lib.relattn_set_short_kernel.restype = _I
+_lib.relattn_sinusoid_table.argtypes = [_I, _I, _I, _P, _P]
+_lib.relattn_sinusoid_table.restype = _I
 _lib.relattn_set_bwd_tensor_cores.argtypes = [_I]
 _lib.relattn_set_bwd_tensor_cores.restype = _I
 _lib.relattn_version.argtypes = []
 _lib.relattn_version.restype = _I
 
 EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
-            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_txl_fwd", "relattn_decode_fwd",
+            "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_txl_fwd", "relattn_sinusoid_table",
+            "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
@@ -511,6 +514,17 @@ def relattn_set_short_kernel(on: bool) -> None:
     st = int(_lib.relattn_set_short_kernel(1 if on else 0))
     if st != OK:
         raise RelattnError(st, "relattn_set_short_kernel")
+
+
+def relattn_sinusoid_table(n, d_model, dtype=None, device=None, stream=None):
+    """The sinusoidal encodings of the offsets -(n-1) .. n-1: a [2n - 1, d_model] tensor
+    (bf16 by default) on `device` (default the current CUDA device)."""
+    dtype = torch.bfloat16 if dtype is None else dtype
+    out = torch.empty((2 * int(n) - 1, int(d_model)), dtype=dtype,
+                      device=device if device is not None else "cuda")
+    st = _lib.relattn_sinusoid_table(int(n), int(d_model), _dtype_code(out), _ptr(out), _stream(stream))
+    _check(st, "relattn_sinusoid_table")
+    return out
 
 
 def relattn_set_bwd_tensor_cores(on: bool) -> None:

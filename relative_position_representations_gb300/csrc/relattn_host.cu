@@ -520,6 +520,19 @@ relattn_status_t relattn_debug_withhold_first_load(int on) {
     return RELATTN_OK;
 }
 
+relattn_status_t relattn_sinusoid_table(int n, int d_model, int dtype, void *out,
+                                        relattn_stream_t stream) {
+    if (!out || n < 1 || n > (1 << 28) || d_model < 2 || d_model > (1 << 16) || (d_model & 1))
+        return RELATTN_ERR_INVALID_ARG;
+    if (dtype != RELATTN_BF16 && dtype != RELATTN_F32) return RELATTN_ERR_INVALID_ARG;
+    if (!aligned(out, dtype == RELATTN_BF16 ? 2 : 4)) return RELATTN_ERR_INVALID_ARG;
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    return from_cuda(relattn::launch_sinusoid(n, d_model, dtype == RELATTN_BF16 ? 1 : 0, out,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_set_short_kernel(int on) {
     if (on != 0 && on != 1) return RELATTN_ERR_INVALID_ARG;
     g_short_kernel.store(on);

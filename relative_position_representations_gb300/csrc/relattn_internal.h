@@ -141,6 +141,8 @@ struct TxlArgs {
 };
 // SIMT kernel; cudaErrorNotSupported when d > 128
 cudaError_t launch_txl(const TxlArgs &a, cudaStream_t s);
+// the sinusoidal encodings of the offsets -(n-1) .. n-1: [2n - 1, d_model] of bf16 or fp32
+cudaError_t launch_sinusoid(int n, int d_model, int bf16, void *out, cudaStream_t s);
 // tensor-core kernel (bf16, d = 64 or 128); txl_tc_covers says whether it takes the call
 bool txl_tc_covers(const TxlArgs &a);
 cudaError_t launch_txl_tc(const TxlArgs &a, cudaStream_t s);

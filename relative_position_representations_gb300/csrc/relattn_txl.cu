@@ -133,7 +133,37 @@ __global__ void __launch_bounds__(kWarps * 32) txl_kernel(const TxlArgs a, int r
     }
 }
 
+// The sinusoidal encodings of the relative offsets -(n-1) .. n-1: row o, components 2i and
+// 2i + 1 = sin and cos of (o - (n - 1)) / 10000^(2i / d_model). The angle is formed in fp64
+// (offsets of thousands times frequencies near 1 would lose digits in fp32), then rounded to
+// the output type.
+template <typename T>
+__global__ void sinusoid_kernel(int n, int d_model, T *out) {
+    const long long half = d_model / 2;
+    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (row, i) pair
+    if (e >= (2LL * n - 1) * half) return;
+    const long long row = e / half;
+    const int i = (int)(e - row * half);
+    const double pos = (double)(row - (n - 1));
+    const double ang = pos * exp2(-(2.0 * i / d_model) * 13.287712379549449);  // log2(10000)
+    T *o = out + row * d_model + 2 * i;
+    Vec<T>::store(o, (float)sin(ang));
+    Vec<T>::store(o + 1, (float)cos(ang));
+}
+
 }  // namespace
+
+cudaError_t launch_sinusoid(int n, int d_model, int bf16, void *out, cudaStream_t s) {
+    const long long pairs = (2LL * n - 1) * (d_model / 2);
+    if (pairs <= 0) return cudaSuccess;
+    const long long blocks = (pairs + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorNotSupported;
+    if (bf16)
+        sinusoid_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(n, d_model, static_cast<__nv_bfloat16 *>(out));
+    else
+        sinusoid_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(n, d_model, static_cast<float *>(out));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_txl(const TxlArgs &a, cudaStream_t s) {
     if (a.d > kMaxD) return cudaErrorNotSupported;

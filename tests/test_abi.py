@@ -61,6 +61,11 @@ def test_wait_limit_and_hook_arguments_checked_on_the_host(lib):
     assert lib.raw_call("relattn_set_bwd_tensor_cores", 2) == 1
     assert lib.raw_call("relattn_set_bwd_tensor_cores", 0) == 0
     assert lib.raw_call("relattn_set_bwd_tensor_cores", 1) == 0  # the default
+    # sinusoid table: a null output, an odd d_model and a bad dtype are refused on the host
+    assert lib.raw_call("relattn_sinusoid_table", 4, 8, 0, None, None) == 1
+    # (a pointer value that the host check rejects first, never dereferenced)
+    assert lib.raw_call("relattn_sinusoid_table", 4, 7, 0, 256, None) == 1
+    assert lib.raw_call("relattn_sinusoid_table", 4, 8, 7, 256, None) == 1
 
 
 @pytest.mark.parametrize("nb,md,bidir", [(32, 128, True), (32, 128, False), (16, 40, True),

@@ -79,3 +79,38 @@ def test_txl_sign_of_the_offset_matters(dtype):
     b = rp.relattn_txl_fwd(g["q"], g["k"], g["v"], g["rel"].flip(1).contiguous(), g["u"],
                            g["vb"]).cpu()
     assert float((a - b).abs().max()) > 1e-2
+
+
+@pytest.mark.parametrize("dtype,n,dm", [("f32", 1024, 64), ("bf16", 300, 768), ("f32", 1, 2)])
+def test_sinusoid_table_matches_the_oracle(dtype, n, dm):
+    """relattn_sinusoid_table against the fp64 oracle table: the angle is formed in fp64, so
+    the only error is the final rounding (fp32: half an ulp of values <= 1; bf16: 2^-9)."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    got = _rp().relattn_sinusoid_table(n, dm, dtype=tdt)
+    torch.cuda.synchronize()
+    ref = txl.sinusoid_table(n, dm)
+    err = float(np.abs(got.double().cpu().numpy() - ref).max())
+    assert err <= (1e-7 if dtype == "f32" else 4e-3), err
+
+
+def test_txl_with_projected_sinusoids_matches_the_oracle():
+    """The whole Transformer-XL position path: the library's sinusoid table, projected per head
+    by W_{k,R} (a plain matrix product), as the rel argument; the oracle takes the same
+    projection of its own fp64 table."""
+    rp = _rp()
+    B, H, n, d, dm = 2, 3, 200, 64, 96
+    g = torch.Generator().manual_seed(7)
+    q, k, v = (torch.randn((B, H, n, d), generator=g).to(torch.bfloat16) for _ in range(3))
+    wkr = (torch.randn((H, d, dm), generator=g) * dm ** -0.5)
+    u, vb = (torch.randn((H, d), generator=g).to(torch.bfloat16) for _ in range(2))
+    table = rp.relattn_sinusoid_table(n, dm, dtype=torch.float32)
+    rel = torch.einsum("hdm,om->hod", wkr.to(DEV), table).to(torch.bfloat16).contiguous()
+    got = rp.relattn_txl_fwd(q.to(DEV), k.to(DEV), v.to(DEV), rel, u.to(DEV), vb.to(DEV),
+                             causal=True, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    rel_ref = np.einsum("hdm,om->hod", wkr.double().numpy(), txl.sinusoid_table(n, dm))
+    f = lambda t: t.double().cpu().numpy()
+    ref = txl.txl_fwd(f(q), f(k), f(v), rel_ref, f(u), f(vb), True, d ** -0.5)
+    tol = 1e-2 * float(np.abs(ref).max()) + 1e-3
+    assert float(np.abs(got.float().cpu().numpy() - ref).max()) <= tol
+    assert rp.relattn_get_device_error() == 0

@@ -69,3 +69,30 @@ def test_global_content_bias_alone_is_attention_with_u_as_query():
         torch.from_numpy(uq), torch.from_numpy(k), torch.from_numpy(val), is_causal=True,
         scale=0.6).numpy()
     np.testing.assert_allclose(z, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sinusoid_table_dot_products_depend_only_on_the_offset_difference():
+    """sin(a) sin(b) + cos(a) cos(b) = cos(a - b): the dot product of the encodings of two
+    offsets is sum_i cos((p - p') w_i), a function of p - p' alone. Checked on every pair of
+    rows against the one-dimensional cosine sum, so a wrong frequency, a swapped sin/cos or a
+    shifted offset row fails."""
+    n, dm = 17, 12
+    r = txl.sinusoid_table(n, dm)
+    assert r.shape == (2 * n - 1, dm)
+    w = 1.0 / np.power(10000.0, np.arange(0, dm, 2) / dm)
+    offs = np.arange(-(n - 1), n)
+    gram = r @ r.T
+    diff = offs[:, None] - offs[None, :]
+    expect = np.cos(diff[:, :, None] * w[None, None, :]).sum(axis=2)
+    np.testing.assert_allclose(gram, expect, rtol=0, atol=1e-12)
+
+
+def test_sinusoid_table_offset_zero_and_sign():
+    """Offset 0 (row n - 1) is [0, 1, 0, 1, ...]; the sine components are odd in the offset and
+    the cosine components even, and the row of offset +1 has a positive first component."""
+    n, dm = 9, 8
+    r = txl.sinusoid_table(n, dm)
+    np.testing.assert_array_equal(r[n - 1], np.tile([0.0, 1.0], dm // 2))
+    np.testing.assert_allclose(r[n - 1 + 3, 0::2], -r[n - 1 - 3, 0::2], atol=1e-15)
+    np.testing.assert_allclose(r[n - 1 + 3, 1::2], r[n - 1 - 3, 1::2], atol=1e-15)
+    assert r[n, 0] > 0.0
