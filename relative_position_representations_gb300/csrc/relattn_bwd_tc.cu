@@ -49,6 +49,7 @@ using tc::kLog2e;
 using tc::Shared;
 
 constexpr int kThreads = 192;   // warp 0 loads, warp 1 issues MMAs, warps 2-5 one row each
+constexpr int kKeysThreads = 320;  // stats and keys kernels: warps 2-9, two threads per row / key
 constexpr int kRowWarp0 = 2;
 constexpr int kMaxW = 128;      // staged table rows (k + 1 causal, 2k + 1 otherwise)
 constexpr int kRec = 8;         // floats per row record
@@ -135,7 +136,7 @@ enum : int {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kKeysThreads, 1)
     bwd_stats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_wk, const __grid_constant__ CUtensorMap tm_wv,
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kABars; ++i)
-            ptx::mbar_init(bar(i), (i == A_R_EMPTY || i == A_S_EMPTY) ? 128u : 1u);
+            ptx::mbar_init(bar(i), (i == A_R_EMPTY || i == A_S_EMPTY) ? 256u : 1u);
         *sh.abort_flag = 0;
         ptx::mbar_init_fence();
     } else if (threadIdx.x == 32) {
@@ -256,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::tc_commit_w(bar(A_DRAIN));
         tc::drain_bar(bar(A_DRAIN), 0, sh.limit);
     } else if (warp >= kRowWarp0) {
-        // ---------------- one thread per query row (TMEM lane = row)
+        // ---------------- two threads per query row (TMEM lane = row): group g takes chunks
+        // 2 g and 2 g + 1 (32 keys each) of every key tile and runs its own online softmax over
+        // them; the halves' maxima, sums and end bins are combined once, at the end
+        const int g = (warp - kRowWarp0) >> 2;
         const int quarter = warp & 3;
         const int il = 32 * quarter + lane, i = i0 + il;
         const bool row_ok = i < p.n;
@@ -264,29 +268,31 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
         float *Rs = reinterpret_cast<float *>(sh.ptr + p.off_r) + il * p.SRk;
         float *Rvs = reinterpret_cast<float *>(sh.ptr + p.off_rv) + il * p.SRv;
+        float *X = reinterpret_cast<float *>(sh.ptr + p.off_x);  // [value][group][row]
+        auto xv = [&](int v, int gg) -> float & { return X[(v * 2 + gg) * BM + il]; };
         const int k = p.clip_k, W = p.W;
         const bool bidir = !p.causal;
         const int khi = p.causal ? 0 : k;  // largest offset with a staged row
         bool ok = tc::wait_bar(bar(A_R_FULL), 0, sh, p.err);
         ok = __all_sync(0xffffffffu, ok) != 0;
-        if (ok) {
+        if (ok) {  // group 0 reads R, group 1 Rv
             ptx::tc_fence_after();
-            for (int c0 = 0; c0 < p.Wp; c0 += 16) {
-                float x[16], y[16];
-                if (p.ak) ptx::tmem_ld16p(lane_base + (uint32_t)c0, reinterpret_cast<uint32_t *>(x));
-                if (p.av) ptx::tmem_ld16p(lane_base + 128u + (uint32_t)c0, reinterpret_cast<uint32_t *>(y));
-                ptx::tmem_ld_wait();
+            if (g == 0 ? p.ak : p.av) {
+                for (int c0 = 0; c0 < p.Wp; c0 += 16) {
+                    float x[16];
+                    ptx::tmem_ld16p(lane_base + (g == 0 ? 0u : 128u) + (uint32_t)c0, reinterpret_cast<uint32_t *>(x));
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    if (c0 + t < W) {
-                        if (p.ak) Rs[c0 + t] = x[t];
-                        if (p.av) Rvs[c0 + t] = y[t];
-                    }
+                    for (int t = 0; t < 16; ++t)
+                        if (c0 + t < W) (g == 0 ? Rs : Rvs)[c0 + t] = x[t];
                 }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(A_R_EMPTY));
         }
+        // the R and Rv rows are visible to both halves; every row thread gets here (its wait is
+        // bounded) and the AND of the outcome sends all of them on or out together
+        ok = ptx::bar_red_and(1, 256, ok);
         float m = -INFINITY, l = 0.f, Dacc = 0.f, Lb = 0.f, Ld = 0.f, Rb = 0.f, Rd = 0.f;
         for (int j = 0; j < J && ok; ++j) {
             ok = tc::wait_bar(bar(A_S_FULL), (uint32_t)j & 1u, sh, p.err);
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // pass 1: logits (log2 domain) back over the scores, and their maximum
             float mx = -INFINITY;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {
                 float s[32];
                 ptx::tmem_ld32f(lane_base + (uint32_t)(32 * ch), s);
                 ptx::tmem_ld_wait();
@@ -320,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 m = mn;
             }
             {
-                // pass 2: probabilities (unnormalised), D and the bins. Every lane runs it (the
-                // TMEM loads are warp-collective); a row with no allowed key so far has only
+                // pass 2: probabilities (unnormalised), D and the end bins. Every lane runs it
+                // (the TMEM loads are warp-collective); a row with no allowed key so far has only
                 // -inf logits, whose terms are 0
                 const float mm = m == -INFINITY ? 0.f : m;
 #pragma unroll 1
-                for (int ch = 0; ch < BN / 32; ++ch) {
+                for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {
                     float x[32], dp[32];
                     ptx::tmem_ld32f(lane_base + (uint32_t)(32 * ch), x);
                     ptx::tmem_ld32f(lane_base + 128u + (uint32_t)(32 * ch), dp);
@@ -353,15 +359,25 @@ __global__ void __launch_bounds__(kThreads, 2)
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(A_S_EMPTY));
         }
-        // per row: lse, D and the end bins; R' = c R - lse and Rv' = Rv - D in place over the
-        // shared-memory rows, then copied out by whole rows (coalesced)
-        if (ok && row_ok) {
-            const float lse = l > 0.f ? m + __log2f(l) : INFINITY;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float Dv = Dacc * inv;
+        // the two halves' running values, combined at their common maximum
+        xv(0, g) = m; xv(1, g) = l; xv(2, g) = Dacc; xv(3, g) = Lb; xv(4, g) = Ld; xv(5, g) = Rb; xv(6, g) = Rd;
+        ok = ptx::bar_red_and(1, 256, ok);
+        // per row (group 0): lse, D and the end bins; R' = c R - lse and Rv' = Rv - D in place
+        // over the shared-memory rows, then copied out by whole rows (coalesced)
+        if (ok && row_ok && g == 0) {
+            const float m0 = xv(0, 0), m1 = xv(0, 1);
+            const float mt = fmaxf(m0, m1);
+            const float a0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - mt);
+            const float a1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - mt);
+            auto comb = [&](int v) { return a0 * xv(v, 0) + a1 * xv(v, 1); };
+            const float lt = comb(1);
+            const float lse = lt > 0.f ? mt + __log2f(lt) : INFINITY;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const float Dv = comb(2) * inv;
+            const float bl = comb(3) * inv, br = comb(5) * inv;
             float4 *rec = reinterpret_cast<float4 *>(p.ws_rec + row * kRec);
-            rec[0] = make_float4(lse, Dv, Lb * inv, Ld * inv - Dv * (Lb * inv));
-            rec[1] = make_float4(Rb * inv, Rd * inv - Dv * (Rb * inv), 0.f, 0.f);
+            rec[0] = make_float4(lse, Dv, bl, comb(4) * inv - Dv * bl);
+            rec[1] = make_float4(br, comb(6) * inv - Dv * br, 0.f, 0.f);
             if (p.ak) {
                 for (int r = 0; r < W; ++r) Rs[r] = p.c * Rs[r] - lse;
             } else {
@@ -374,13 +390,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
         // every row thread gets here (its waits are bounded), so the named barrier cannot hang
-        if (ptx::bar_red_and(1, 128, ok)) {
+        if (ptx::bar_red_and(1, 256, ok)) {
             const int rows = min(BM, p.n - i0);
             const int wk = p.ak ? W : 1, wv = p.av ? W : 1;
             const float *Rs0 = reinterpret_cast<const float *>(sh.ptr + p.off_r);
             const float *Rvs0 = reinterpret_cast<const float *>(sh.ptr + p.off_rv);
             const long long row0 = (long long)bh * p.n + i0;
-            for (int rr = quarter; rr < rows; rr += 4) {
+            for (int rr = warp - kRowWarp0; rr < rows; rr += 8) {
                 float *dk = p.ws_rk + (row0 + rr) * p.SK;
                 float *dv = p.ws_rv + (row0 + rr) * p.SV;
                 for (int e = lane; e < p.SK; e += 32) dk[e] = e < wk ? Rs0[rr * p.SRk + e] : 0.f;
@@ -415,7 +431,7 @@ struct QStage {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKeysThreads, 1)
     bwd_keys_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dz,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ Params p) {
@@ -434,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kBBars; ++i)
-            ptx::mbar_init(bar(i), (i == B_P_FULL || i == B_DQ_EMPTY) ? 128u : 1u);
+            ptx::mbar_init(bar(i), (i == B_P_FULL || i == B_DQ_EMPTY) ? 256u : 1u);
         *sh.abort_flag = 0;
         ptx::mbar_init_fence();
     } else if (threadIdx.x == 32) {
@@ -526,9 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_w(bar(B_P_FULL), (uint32_t)pi & 1u))) break;
             ptx::tc_fence_after();
 #pragma unroll 1
-            for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dZ (P^T bf16 pairs in TMEM)
-                ptx::tc_mma_ts_w(tmem + tDV, tmem + tS + (uint32_t)(kk * 8), ddz_mn + mnstep(kk), idG,
-                                 (pi > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dZ (P^T bf16 pairs: 16 columns per 32-query chunk)
+                ptx::tc_mma_ts_w(tmem + tDV, tmem + tS + (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8),
+                                 ddz_mn + mnstep(kk), idG, (pi > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll 1
             for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q
                 ptx::tc_mma_w(tmem + tDK, ds_k + kstep(kk, BN), dq_mn + mnstep(kk), idG,
@@ -544,7 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit_w(bar(B_DRAIN));
         tc::drain_bar(bar(B_DRAIN), 0, sh.limit);
     } else if (warp >= kRowWarp0) {
-        // ---------------- one thread per key (TMEM lane = key) for P and dS, per query row for dQ
+        // ---------------- two threads per key (TMEM lane = key) for P and dS, group g taking the
+        // queries 64 g .. 64 g + 63 of each query tile (the elements are independent given R'
+        // and Rv', so the halves need no exchange); per query row for dQ, group g taking
+        // columns 32 g, 32 g + 64, ...
+        const int g = (warp - kRowWarp0) >> 2;
         const int quarter = warp & 3;
         const int jl = 32 * quarter + lane, j = j0 + jl;
         const bool kvalid = j < nk;
@@ -563,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float *rk = reinterpret_cast<const float *>(sh.ptr + QS::rk(p, s));
             const float *rv = reinterpret_cast<const float *>(sh.ptr + QS::rv(p, s));
 #pragma unroll 1
-            for (int ch = 0; ch < BM / 32; ++ch) {
+            for (int ch = 2 * g; ch < 2 * g + 2; ++ch) {
                 float sv[32], dpv[32];
                 ptx::tmem_ld32f(lane_base + tS + (uint32_t)(32 * ch), sv);
                 ptx::tmem_ld32f(lane_base + tDP + (uint32_t)(32 * ch), dpv);
@@ -601,8 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dd[t2] = ptx::pack_bf16x2(de[0], de[1]);
                 }
                 __syncwarp();
-                // P^T over the columns of S^T already read
-                ptx::tmem_st16(lane_base + tS + (uint32_t)(16 * ch), pp);
+                // P^T of these 32 queries over the first 16 columns of their own S^T chunk, which
+                // this thread has read (the other group's chunks may not be read yet)
+                ptx::tmem_st16(lane_base + tS + (uint32_t)(32 * ch), pp);
                 // dS^T row jl, queries 32 ch .. 32 ch + 31: 128-byte swizzled rows, two 64-query blocks
                 const uint32_t blk = (uint32_t)(ch >> 1) * (BN * 128);
 #pragma unroll
@@ -623,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qi = i0 + jl;
             float *dqr = p.dq + ((long long)bh * p.n + qi) * D;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 32 * g; c0 < D; c0 += 64) {
                 float v[32];
                 ptx::tmem_ld32f(lane_base + tDP + (uint32_t)c0, v);
                 ptx::tmem_ld_wait();
@@ -646,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
             const long long krow = (long long)bh * p.n + j;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 32 * g; c0 < D; c0 += 64) {
                 float a[32], b[32];
                 if (NQ > 0) {
                     ptx::tmem_ld32f(lane_base + tDK + (uint32_t)c0, a);
@@ -1394,6 +1415,7 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
         q.off_r = off; off += (uint32_t)BM * q.SRk * 4;
         q.off_rv = off; off += (uint32_t)BM * q.SRv * 4;
         off = round_up(off, 16);
+        q.off_x = off; off += 7 * 2 * BM * 4;
         q.off_bar = off; off += 8 * 32 + 16;
         q.stage_bytes = tile;
         q.stages = stages;
@@ -1414,7 +1436,7 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     };
     const uint32_t optin = (uint32_t)di.smem_optin;
     Params pa = p, pb = p;
-    // one key tile (n <= 128): one K/V stage, so that two CTAs share an SM
+    // two K/V stages when there is more than one key tile and they fit
     uint32_t sma = layout_a(pa, p.n_tiles > 1 ? 2 : 1);
     if (sma > optin) sma = layout_a(pa, 1);
     uint32_t smb = layout_b(pb, 2);
@@ -1465,9 +1487,9 @@ cudaError_t launch(const BwdArgs &a, cudaStream_t s) {
     // dq: the keys kernel adds dS K into it, the tables kernel the table term
     if ((e = cudaMemsetAsync(a.dq, 0, (size_t)p.BH * a.n * D * sizeof(float), s)) != cudaSuccess) return e;
     const unsigned tiles = (unsigned)(p.BH * p.n_tiles);
-    bwd_stats_kernel<D><<<tiles, kThreads, sma, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], pa);
+    bwd_stats_kernel<D><<<tiles, kKeysThreads, sma, s>>>(tm[0], tm[1], tm[2], tm[3], tm[4], tm[5], pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_keys_kernel<D><<<tiles, kThreads, smb, s>>>(tm[0], tm[1], tm[2], tm[3], pb);
+    bwd_keys_kernel<D><<<tiles, kKeysThreads, smb, s>>>(tm[0], tm[1], tm[2], tm[3], pb);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ak || av) {
         bwd_tables_kernel<D><<<tiles, kThreads, smc, s>>>(tm[0], tm[1], tm[4], pc, a.daK, a.daV, a.ths);

@@ -117,12 +117,15 @@ TXL_WORKLOADS = {
                             causal=True, table_std=0.5, scale=1.0 / 8),
 }
 
-# Gradients of the base encoder (kind "bwd"): the forward's inputs plus dout ~ N(0, 1) drawn
-# after them.
+# Gradients (kind "bwd"): the forward's inputs plus dout ~ N(0, 1) drawn after them. The base
+# encoder shape (one query tile per head) and the big decoder shape (two, causal).
 BWD_WORKLOADS = {
     "bwd_base_encoder": Workload("bwd_base_encoder", B=64, H=8, n=128, d=64, dtype="bf16",
                                  kind="bwd", clip_k=16, table_std=0.02, kv_len_range=(32, 128),
                                  scale=1.0 / 8),
+    "bwd_big_decoder": Workload("bwd_big_decoder", B=32, H=16, n=256, d=64, dtype="bf16",
+                                kind="bwd", clip_k=16, table_std=0.02, causal=True,
+                                scale=1.0 / 8),
 }
 
 # One incremental decoding step (kind "decode"): n is the cache capacity T; each sequence's
