@@ -231,12 +231,14 @@ RELATTN_API relattn_status_t relattn_txl_fwd(const void *q, const void *k, const
  *   out               [B, H, d] bf16; must not alias an input.
  *
  *   workspace         caller-owned device scratch of workspace_bytes (16-byte aligned),
- *                     or NULL. When relattn_decode_workspace_size is not 0 (a small batch:
- *                     at most 256 sequence-heads, caches longer than 512) and the workspace
- *                     is that large, each cache is split over several CTAs and combined by
- *                     a second kernel on the same stream; otherwise one CTA reads a whole
- *                     cache. The contents are scratch on entry and on return, and two
- *                     calls running at the same time must not share it.
+ *                     or NULL. When relattn_decode_workspace_size is not 0 (at most 1024
+ *                     sequences) and the workspace is that large, the cached keys of all
+ *                     sequence-heads are cut into equal ranges, one per CTA of a grid that
+ *                     fills the GPU once, whatever the mix of cache lengths; a second kernel
+ *                     on the same stream merges the ranges of each cache and adds the value
+ *                     bins. Otherwise one CTA reads a whole cache. The contents are scratch
+ *                     on entry and on return, and two calls running at the same time must
+ *                     not share it.
  *
  * bf16 only, d in {64, 128}; clip_k <= 256 (else RELATTN_ERR_UNSUPPORTED). Appending the
  * new token's key and value to the cache is the caller's job.
@@ -258,9 +260,9 @@ RELATTN_API relattn_status_t relattn_decode_fwd(const void *q, const void *k_cac
  * (a file-scope __device__ array, held by every device that loads the library until the
  * process exits), so no call allocates anything.
  *
- *   - When the split over the cache would need more than 4 MiB
- *     (relattn_decode_workspace_size > 4 MiB, e.g. 256 sequence-heads of d = 128 with
- *     T > 15872), the call runs without the split, one CTA per cache, and uses no scratch.
+ *   - When the split would need more than 4 MiB (relattn_decode_workspace_size > 4 MiB:
+ *     more than about 7000 sequence-heads at d = 128, 13000 at d = 64), the call runs
+ *     without the split, one CTA per cache, and uses no scratch.
  *   - The array is one per device and shared by every call of this entry point on that
  *     device: calls that overlap on the GPU (different streams, no ordering) race on it and
  *     give wrong results; calls on one stream are ordered. Each call writes every scratch
@@ -282,7 +284,9 @@ RELATTN_API relattn_status_t relattn_decode_fwd_noalloc(const void *q, const voi
 
 /*
  * relattn_decode_workspace_size — host only: the workspace bytes relattn_decode_fwd uses
- * to split caches of capacity T over several CTAs (0 when it runs one CTA per cache).
+ * to split the caches over the GPU: a length prefix over the sequences and one
+ * {maximum, row sum, P V[d]} record per (CTA, sequence-head) segment, (1024 + B H) records
+ * at most; 0 when it runs one CTA per cache (more than 1024 sequences, or B H T > 2^50).
  */
 RELATTN_API relattn_status_t relattn_decode_workspace_size(int B, int H, int T, int d,
                                                unsigned long long *bytes);

@@ -91,10 +91,11 @@ struct DecodeArgs {
     const int *cache_len;
     int B, H, T, d;
     void *out;
-    void *workspace;  // device scratch for the split over the cache, or null
+    void *workspace;  // device scratch for the split over all caches, or null
     unsigned long long workspace_bytes;
 };
-// bytes of workspace the split over the cache uses (0: the cache fits one CTA's piece)
+// bytes of workspace the split over all caches uses (0: more than 1024 sequences, or B * H * T
+// beyond 2^50: one CTA per cache)
 unsigned long long decode_workspace_bytes(int B, int H, int T, int d);
 // cudaErrorNotSupported when clip_k + 1 table rows exceed the kernel's bins; without a large
 // enough workspace the single-pass kernel runs

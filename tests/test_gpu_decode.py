@@ -52,7 +52,8 @@ def oracle_decode(w, x):
 
 
 def run_decode(w, x, split=False):
-    """split: pass a workspace, so caches longer than one piece go over several CTAs."""
+    """split: pass a workspace, so the cached keys of all sequence-heads are cut into equal
+    ranges, one per CTA, and merged per cache by a second kernel."""
     rp = _rp()
     g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     ws = None
@@ -78,6 +79,11 @@ CASES = [
     ("shared_tables", 2, 4, 500, 64, 16, None, True, True, True),
     ("k0", 2, 2, 200, 64, 0, None, True, True, False),
     ("k_over_len", 2, 2, 150, 64, 200, [150, 37], True, True, False),
+    # fewer cached keys than CTAs of the split (CTAs without keys between a cache's pieces)
+    ("tiny_total", 2, 2, 40, 64, 4, [3, 0], True, True, False),
+    ("one_key", 1, 1, 8, 128, 2, [1], True, True, False),
+    # many sequences of mixed lengths: ranges that start and end inside caches
+    ("many_seqs", 40, 3, 257, 64, 16, None, True, True, False),
 ]
 
 

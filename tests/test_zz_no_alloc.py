@@ -31,7 +31,7 @@ def _args(w, g):
             P(g["cache_len"]), w.B, w.H, w.n, w.d)
 
 
-@pytest.mark.parametrize("B,H,T", [(2, 4, 3000), (32, 16, 700)])  # split / one CTA per cache
+@pytest.mark.parametrize("B,H,T", [(2, 4, 3000), (32, 16, 700)])  # few / many sequence-heads
 def test_noalloc_twice_equals_workspace_call(B, H, T):
     lib = _lib()
     w = wl.Workload("noalloc", B=B, H=H, n=T, d=64, dtype="bf16", kind="decode", clip_k=16,
@@ -60,12 +60,12 @@ def test_noalloc_twice_equals_workspace_call(B, H, T):
 
 
 def test_noalloc_split_larger_than_scratch_runs_unsplit():
-    """256 sequence-heads of d = 128 over 16384 cached keys: the split would need
-    256 * 32 * 130 * 4 bytes (more than the 4 MiB array), so the call computes one CTA per
-    cache like relattn_decode_fwd without a workspace, bit for bit. Inputs are drawn on the
-    GPU (both sides are the library's own kernels; the oracle is not involved)."""
+    """8192 sequence-heads of d = 128: the split would need (1024 + 8192) records of 130
+    floats (more than the 4 MiB array), so the call computes one CTA per cache like
+    relattn_decode_fwd without a workspace, bit for bit. Inputs are drawn on the GPU (both
+    sides are the library's own kernels; the oracle is not involved)."""
     lib = _lib()
-    B, H, T, d, k = 16, 16, 16384, 128, 16
+    B, H, T, d, k = 64, 128, 384, 128, 16
     need = ctypes.c_ulonglong(0)
     assert lib.raw_call("relattn_decode_workspace_size", B, H, T, d, ctypes.byref(need)) == 0
     assert need.value > SCRATCH
