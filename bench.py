@@ -877,9 +877,10 @@ def host_cpu_model() -> str:
 def measure_e2e(rp, w, x, dev, stream, flops, args):
     """Same step through the C ABI with pinned host inputs: H2D copies, launch, D2H copy,
     every step, run as a two-slot pipeline the way an input pipeline feeds a device: the next
-    step's inputs copy in on a copy stream while this step computes on `stream`, and each
-    step's result copies out on a third stream. Per step the copies and the launch are those
-    of a serial loop; they overlap across steps, with events ordering each buffer's reuse.
+    step's inputs copy in on copy streams (one per input tensor, so the copies of one step
+    run side by side) while this step computes on `stream`, and each step's result copies out
+    on another stream. Per step the copies and the launch are those of a serial loop; they
+    overlap across steps, with events ordering each buffer's reuse.
     Decode step: the key/value caches and the tables are resident state (copied once, before
     timing); each step copies the new queries and the cache lengths."""
     import torch
@@ -895,23 +896,28 @@ def measure_e2e(rp, w, x, dev, stream, flops, args):
                       "h2d": torch.cuda.Event(), "done": torch.cuda.Event(), "d2h": torch.cuda.Event()})
     h2d = sum(v.numel() * v.element_size() for k, v in host.items()
               if v is not None and k in per_step)
-    cp_in = torch.cuda.Stream(device=dev)
+    in_keys = [k for k, v in host.items() if v is not None and k in per_step]
+    cp_in = {k: torch.cuda.Stream(device=dev) for k in in_keys}
+    for sl in slots:
+        sl["h2d"] = {k: torch.cuda.Event() for k in in_keys}
     cp_out = torch.cuda.Stream(device=dev)
+    t0_stream = torch.cuda.Stream(device=dev)  # marks the start of the timed region
     issued = [0]
 
     def step():
         sl = slots[issued[0] % 2]
         first_use = issued[0] < 2
         issued[0] += 1
-        with torch.cuda.stream(cp_in):  # inputs: once the slot's previous kernel has read them
-            if not first_use:
-                cp_in.wait_event(sl["done"])
-            for k, v in host.items():
-                if v is not None and k in per_step:
-                    sl["g"][k].copy_(v, non_blocking=True)
-            sl["h2d"].record(cp_in)
+        for k in in_keys:  # inputs: once the slot's previous kernel has read them
+            cs = cp_in[k]
+            with torch.cuda.stream(cs):
+                if not first_use:
+                    cs.wait_event(sl["done"])
+                sl["g"][k].copy_(host[k], non_blocking=True)
+                sl["h2d"][k].record(cs)
         with torch.cuda.stream(stream):  # the step, once its inputs are in and the slot's last
-            stream.wait_event(sl["h2d"])  # results are out
+            for k in in_keys:  # results are out
+                stream.wait_event(sl["h2d"][k])
             if not first_use:
                 stream.wait_event(sl["d2h"])
             res = gpu_call(rp, w, sl["g"], sl["out"], stream)
@@ -932,7 +938,9 @@ def measure_e2e(rp, w, x, dev, stream, flops, args):
     d2h = sum(t.numel() * t.element_size() for t in slots[0]["back"])
     n = max(5, min(200, args.steps))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(cp_in)
+    e0.record(t0_stream)
+    for cs in cp_in.values():
+        cs.wait_stream(t0_stream)
     for _ in range(n):
         step()
     cp_out.wait_event(slots[(issued[0] - 1) % 2]["d2h"])
@@ -946,8 +954,8 @@ def measure_e2e(rp, w, x, dev, stream, flops, args):
     return {"value": round(flops / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": round(ms, 5), "steps": n,
-            "pipeline": "two slots: H2D of the next step on a copy stream, the step on the "
-                        "compute stream, D2H of its result on a third stream"}
+            "pipeline": "two slots: H2D of the next step on copy streams (one per input "
+                        "tensor), the step on the compute stream, D2H of its result on another"}
 
 
 def run_reference(args, rank, world):
