@@ -194,6 +194,24 @@ def test_bf16_t5_variants(n, bidir, causal, kv):
     assert np.abs(got - ref).max() <= tol_for(w, ref)
 
 
+@pytest.mark.parametrize("kind,n,d,causal,scale", [
+    ("shaw", 300, 64, False, -0.125), ("shaw", 400, 128, True, -0.1), ("shaw", 300, 64, True, 0.0),
+    ("t5", 300, 64, False, -0.5), ("t5", 260, 128, True, 0.0)])
+def test_bf16_fused_kernel_negative_and_zero_scale(kind, n, d, causal, scale):
+    """The fused kernel keeps a chunk raw (its maximum taken on the unscaled scores) only for
+    a non-negative scale: a negative scale sends every chunk through the full logit, and a
+    zero scale leaves only the relative terms (T5: only the bias; Shaw: uniform weights
+    over the keys, the value bins still weighting the table rows). Sequences longer than
+    256 keys, so the long-sequence kernel runs."""
+    if kind == "t5":
+        w = wl.Workload("t5_scale", B=2, H=3, n=n, d=d, dtype="bf16", kind="t5", qkv_std=0.5,
+                        scale=scale, bidirectional=not causal, causal=causal, bias_std=2.0)
+    else:
+        w = wl.Workload("shaw_scale", B=2, H=3, n=n, d=d, dtype="bf16", clip_k=16, causal=causal,
+                        table_std=0.5, scale=scale)
+    check(w, seed=n + d)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_bf16_rising_logits_force_rescales(d):
     """Logits that keep rising along the row make the running max jump by more than 2^8
