@@ -489,7 +489,7 @@ def gpu_call(rp, w, g, out, stream):
                               kv_len=g["kv_len"], table_head_stride=wl.table_head_stride(w),
                               workspace=g["ws"], stream=stream)
     if w.kind == "decode":
-        if "ws" not in g:  # the caller's scratch for the split over the cache (made once)
+        if "ws" not in g:  # the caller's scratch for the split over the caches (made once)
             import torch
             nb = rp.relattn_decode_workspace_size(w.B, w.H, w.n, w.d)
             g["ws"] = (None if NO_DECODE_WORKSPACE else

@@ -403,7 +403,7 @@ def relattn_bwd(q, k, v, dout, aK=None, aV=None, clip_k=0, causal=False, scale=N
 
 
 def relattn_decode_workspace_size(B, H, T, d) -> int:
-    """Workspace bytes relattn_decode_fwd uses to split caches of capacity T (host only)."""
+    """Workspace bytes relattn_decode_fwd uses to split all caches over the GPU (host only)."""
     n = ctypes.c_ulonglong(0)
     _check(_lib.relattn_decode_workspace_size(int(B), int(H), int(T), int(d), ctypes.byref(n)),
            "relattn_decode_workspace_size")

@@ -2,7 +2,7 @@
 (a runtime that reserves its device budget up front, a plugin handed tensors but no
 allocator): it runs on a 4 MiB scratch array built into the library. Checked against
 relattn_decode_fwd, both through the C ABI, on two calls in a row: with a caller workspace
-of the same size when the split over the cache fits the array, and with no workspace when
+of the same size when the split over the caches fits the array, and with no workspace when
 the split would need more. The file name sorts last so that it runs after the other GPU
 tests."""
 import ctypes
