@@ -112,10 +112,13 @@ def test_tensor_core_gradients_match_oracle(case):
     _check(case, "tc")
 
 
-def test_tensor_core_gradients_full_base_encoder():
-    """The bwd_base_encoder workload at full size (B=64, H=8, n=128, d=64, k=16, both tables,
-    kv_len U{32..128}), every element of every gradient against the fp64 oracle."""
-    w = wl.BWD_WORKLOADS["bwd_base_encoder"]
+@pytest.mark.parametrize("name", ["bwd_base_encoder", "bwd_big_decoder"])
+def test_tensor_core_gradients_full_workload(name):
+    """The gradient workloads at full size, every element of every gradient against the fp64
+    oracle: bwd_base_encoder (B=64, H=8, n=128, d=64, k=16, both tables, kv_len U{32..128}:
+    the one-tile kernel) and bwd_big_decoder (B=32, H=16, n=256, d=64, k=16, causal, both
+    tables: the stats, keys and tables kernels over two query and two key tiles per head)."""
+    w = wl.BWD_WORKLOADS[name]
     x = wl.draw_bwd_inputs(w, seed=0)
     dev = {kk: (v.to(DEV) if v is not None else None) for kk, v in x.items()}
     got = _rp().relattn_bwd(dev["q"], dev["k"], dev["v"], dev["dout"], aK=dev["aK"], aV=dev["aV"],
@@ -124,7 +127,8 @@ def test_tensor_core_gradients_full_base_encoder():
     torch.cuda.synchronize()
     ref = backward.relattn_bwd(_np(x["q"]), _np(x["k"]), _np(x["v"]), _np(x["aK"]), _np(x["aV"]),
                                _np(x["dout"]), w.clip_k, w.causal, w.softmax_scale,
-                               kv_len=x["kv_len"].numpy(), table_head_stride=wl.table_head_stride(w))
+                               kv_len=None if x["kv_len"] is None else x["kv_len"].numpy(),
+                               table_head_stride=wl.table_head_stride(w))
     for nm, a, b in zip(("dq", "dk", "dv", "daK", "daV"), got, ref):
         a = a.cpu().numpy()
         tol = 1e-2 * float(np.abs(b).max()) + 1e-3
