@@ -124,7 +124,7 @@ def test_label_without_a_table_row_sets_the_status_word():
     assert float(np.abs(got - ref).max()) <= 1e-2 * float(np.abs(ref).max()) + 1e-3
 
 
-def test_large_sampled_rows():
-    w = wl.LABELED_WORKLOADS["labeled_graph"].replace(B=2)
-    rows = np.sort(np.random.default_rng(0).choice(w.B * w.H * w.n, size=300, replace=False))
-    check(w, seed=1, rows=rows)
+def test_labeled_graph_workload_all_rows():
+    """The labeled_graph workload at full size (B=16, H=8, n=512, d=64, 16 labels per sequence,
+    both tables, kv_len U{256..512}), every output row against the oracle."""
+    check(wl.LABELED_WORKLOADS["labeled_graph"], seed=1)

@@ -136,3 +136,11 @@ def test_bf16_alibi_too_long_for_shared_memory_is_unsupported():
     with pytest.raises(rp.RelattnError) as e:
         rp.relattn_alibi_fwd(q, q.clone(), q.clone(), slopes, causal=True)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("name", ["alibi_decoder", "offset_bias"])
+def test_bias_workload_all_rows(name):
+    """The scalar-bias workloads at full size (B=8, H=12, n=2048, d=64: ALiBi in a causal
+    decoder, a per-head offset table clipped at 128 in a bidirectional encoder), every output
+    row against the oracle, as bench.py times them."""
+    check(wl.BIAS_WORKLOADS[name], seed=0)
