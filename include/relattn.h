@@ -8,7 +8,8 @@
  * embeddings" page, section "T5"; ALiBi and the per-offset scalar table: the same page,
  * sections "Placement in the taxonomy" and "Two-dimensional variants". Labelled edges: the
  * section "Relation-Aware Self-Attention: The Core Modification" of the same page. Also a
- * decode step against a key/value cache and the gradients of relattn_fwd.
+ * decode step against a key/value cache, the gradients of relattn_fwd and those of the scalar
+ * offset biases.
  *
  * Conventions shared by every entry point
  *   - Tensors q, k, v, out are [B, H, n, d], contiguous, d fastest (row-major).
@@ -356,6 +357,51 @@ RELATTN_API relattn_status_t relattn_bwd(const void *q, const void *k, const voi
 /* relattn_bwd_workspace_size — host only: the workspace bytes relattn_bwd needs. */
 RELATTN_API relattn_status_t relattn_bwd_workspace_size(int B, int H, int n, int d, int clip_k,
                                             unsigned long long *bytes);
+
+/*
+ * relattn_scalar_bias_bwd — gradients of the scalar offset-bias forwards: relattn_t5bias_fwd
+ * (kind 0, "Relative position embeddings" page, section "T5"), relattn_alibi_fwd (kind 1,
+ * same page, "Placement in the taxonomy": -m_h |j - i|) and relattn_offset_bias_fwd (kind 2,
+ * a learned scalar per offset clipped at `radius`). The pages give only the forward; these
+ * are the chain rule through e_ij = scale q_i . k_j + b_h(j - i) and the softmax:
+ *
+ *   dq_i = scale sum_j de_ij k_j,   dk_j = scale sum_i de_ij q_i,   dv_j = sum_i p_ij dz_i,
+ *   de_ij = p_ij (dz_i . v_j - D_i),   D_i = sum_j p_ij dz_i . v_j,
+ *
+ * and the parameter's gradient from the per-offset sums G_h(o) = sum_(b,i) de_(i,i+o):
+ *   kind 0: bias [num_buckets, H] fp32 -> dbias [num_buckets, H], dbias[c, h] = sum of
+ *           G_h(o) over the offsets o of bucket c (num_buckets, max_distance, bidirectional as
+ *           in relattn_t5bias_fwd);
+ *   kind 1: slopes [H] fp32 -> dbias [H] = -sum_o |o| G_h(o);
+ *   kind 2: table rows of 2*radius + 1 fp32 at bias_head_stride elements between heads (0: one
+ *           shared row) -> dbias of the same layout, dbias[h, r] = sum of G_h(o) over the
+ *           offsets with clip(o, radius) + radius = r (a shared row sums over the heads);
+ *           every entry of the rows is written.
+ *
+ *   q, k, v, dout, causal, scale, kv_len, B, H, n, d, dtype   as in the forward (bf16 or
+ *                     fp32 inputs, d <= 128, n <= 4096; else RELATTN_ERR_UNSUPPORTED).
+ *   dq, dk, dv        [B, H, n, d] fp32; padded keys get zero; rows with no allowed key zero.
+ *   workspace         caller-owned device scratch of at least
+ *                     relattn_scalar_bias_bwd_workspace_size bytes (4-byte aligned): per row
+ *                     the softmax statistics, then G. Contents are scratch.
+ *
+ * fp32 arithmetic on the SIMT units (the bias term has no contraction of its own); every
+ * output is written (nothing needs clearing). Arguments that fail a check return
+ * RELATTN_ERR_INVALID_ARG before any launch.
+ */
+RELATTN_API relattn_status_t relattn_scalar_bias_bwd(const void *q, const void *k, const void *v,
+                                         const void *dout, int kind, const float *bias,
+                                         int num_buckets, int max_distance, int bidirectional,
+                                         int radius, long long bias_head_stride, int causal,
+                                         float scale, const int *kv_len, int B, int H, int n,
+                                         int d, int dtype, float *dq, float *dk, float *dv,
+                                         float *dbias, void *workspace,
+                                         unsigned long long workspace_bytes,
+                                         relattn_stream_t stream);
+
+/* relattn_scalar_bias_bwd_workspace_size — host only: the workspace bytes it needs. */
+RELATTN_API relattn_status_t relattn_scalar_bias_bwd_workspace_size(int B, int H, int n,
+                                                        unsigned long long *bytes);
 
 /*
  * relattn_labels — the integer edge label of every (i, j), computed by the same device

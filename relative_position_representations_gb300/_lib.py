@@ -56,6 +56,12 @@ _lib.relattn_bwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, _I, ctyp
 _lib.relattn_bwd.restype = _I
 _lib.relattn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.relattn_bwd_workspace_size.restype = _I
+_lib.relattn_scalar_bias_bwd.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, ctypes.c_longlong,
+                                         _I, ctypes.c_float, _P, _I, _I, _I, _I, _I, _P, _P, _P,
+                                         _P, _P, ctypes.c_ulonglong, _P]
+_lib.relattn_scalar_bias_bwd.restype = _I
+_lib.relattn_scalar_bias_bwd_workspace_size.argtypes = [_I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
+_lib.relattn_scalar_bias_bwd_workspace_size.restype = _I
 _lib.relattn_decode_workspace_size.argtypes = [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.relattn_decode_workspace_size.restype = _I
 _lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
@@ -83,7 +89,8 @@ EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_offset_bias_fwd", "relattn_labeled_fwd", "relattn_txl_fwd", "relattn_sinusoid_table",
             "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
-            "relattn_bwd_workspace_size", "relattn_labels",
+            "relattn_bwd_workspace_size", "relattn_scalar_bias_bwd",
+            "relattn_scalar_bias_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
             "relattn_debug_withhold_first_load", "relattn_set_short_kernel", "relattn_set_bwd_tensor_cores",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
@@ -400,6 +407,68 @@ def relattn_bwd(q, k, v, dout, aK=None, aV=None, clip_k=0, causal=False, scale=N
                           _stream(stream))
     _check(st, "relattn_bwd")
     return dq, dk, dv, daK, daV
+
+
+def relattn_scalar_bias_bwd_workspace_size(B, H, n) -> int:
+    """Workspace bytes relattn_scalar_bias_bwd needs (host only)."""
+    nb = ctypes.c_ulonglong(0)
+    _check(_lib.relattn_scalar_bias_bwd_workspace_size(int(B), int(H), int(n), ctypes.byref(nb)),
+           "relattn_scalar_bias_bwd_workspace_size")
+    return int(nb.value)
+
+
+_BIAS_KINDS = {"t5": 0, "alibi": 1, "table": 2}
+
+
+def relattn_scalar_bias_bwd(q, k, v, dout, kind, bias, num_buckets=32, max_distance=128,
+                            bidirectional=True, radius=0, causal=False, scale=None, kv_len=None,
+                            workspace=None, stream=None):
+    """Gradients of the scalar offset-bias forwards: returns (dq, dk, dv, dbias), fp32.
+
+    kind "t5": bias [num_buckets, H] (relattn_t5bias_fwd; scale defaults to 1.0);
+    "alibi": slopes [H] (relattn_alibi_fwd); "table": [H or 1, 2*radius+1]
+    (relattn_offset_bias_fwd; one row is shared by the heads). dbias has bias's shape.
+    workspace: a CUDA tensor of at least relattn_scalar_bias_bwd_workspace_size bytes, or
+    None to make one."""
+    if kind not in _BIAS_KINDS:
+        raise ValueError("kind must be one of %s" % sorted(_BIAS_KINDS))
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    _dev(dout, "dout", q.dtype)
+    if dout.shape != q.shape:
+        raise ValueError("dout must be [B, H, n, d] like q")
+    if bias is None:
+        raise ValueError("bias is required")
+    _dev(bias, "bias", torch.float32)
+    hs = 0
+    if kind == "t5":
+        if bias.shape != (int(num_buckets), H):
+            raise ValueError("bias must be [num_buckets, H]")
+    elif kind == "alibi":
+        if bias.shape != (H,):
+            raise ValueError("slopes must be [H]")
+    else:
+        W = 2 * int(radius) + 1
+        if bias.dim() != 2 or bias.shape[1] != W or bias.shape[0] not in (1, H):
+            raise ValueError("table must be [H or 1, 2*radius+1]")
+        hs = 0 if bias.shape[0] == 1 else W
+    _dev(kv_len, "kv_len", torch.int32)
+    if scale is None:
+        scale = 1.0 if kind == "t5" else d ** -0.5
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dv = (torch.empty(q.shape, **f32) for _ in range(3))
+    dbias = torch.empty(bias.shape, **f32)
+    need = relattn_scalar_bias_bwd_workspace_size(B, H, n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4), dtype=torch.uint8, device=q.device)
+    _dev(workspace, "workspace")
+    st = _lib.relattn_scalar_bias_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _BIAS_KINDS[kind], _ptr(bias), int(num_buckets),
+        int(max_distance), int(bool(bidirectional)), int(radius), hs, int(bool(causal)),
+        float(scale), _ptr(kv_len), B, H, n, d, dt, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "relattn_scalar_bias_bwd")
+    return dq, dk, dv, dbias
 
 
 def relattn_decode_workspace_size(B, H, T, d) -> int:

@@ -22,7 +22,7 @@ LIB = os.path.join(HERE, "librelattn.so")
 
 SOURCES = ["relattn_host.cu", "relattn_simt.cu", "relattn_tc_d64.cu", "relattn_tc_d128.cu",
            "relattn_decode.cu", "relattn_bwd.cu", "relattn_labeled.cu", "relattn_labeled_tc.cu", "relattn_txl.cu",
-           "relattn_short.cu", "relattn_bwd_tc.cu", "relattn_txl_tc.cu",
+           "relattn_short.cu", "relattn_bwd_tc.cu", "relattn_txl_tc.cu", "relattn_bias_bwd.cu",
            "t5_buckets.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I" + INCLUDE, "-I" + CSRC]

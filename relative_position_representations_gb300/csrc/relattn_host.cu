@@ -366,6 +366,66 @@ relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
                               cache_len, B, H, T, d, ws, kStaticScratchBytes, out, stream);
 }
 
+relattn_status_t relattn_scalar_bias_bwd_workspace_size(int B, int H, int n,
+                                                      unsigned long long *bytes) {
+    if (!bytes || B < 0 || H < 0 || n < 0) return RELATTN_ERR_INVALID_ARG;
+    *bytes = relattn::bias_bwd_workspace_bytes(B, H, n);
+    return RELATTN_OK;
+}
+
+relattn_status_t relattn_scalar_bias_bwd(const void *q, const void *k, const void *v,
+                                         const void *dout, int kind, const float *bias,
+                                         int num_buckets, int max_distance, int bidirectional,
+                                         int radius, long long bias_head_stride, int causal,
+                                         float scale, const int *kv_len, int B, int H, int n,
+                                         int d, int dtype, float *dq, float *dk, float *dv,
+                                         float *dbias, void *workspace,
+                                         unsigned long long workspace_bytes,
+                                         relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, dq, B, H, n, d, dtype);
+    if (st != RELATTN_OK && st != RELATTN_ERR_UNSUPPORTED) return st;
+    if (!dout || !dk || !dv || !dbias || !bias || !workspace) return RELATTN_ERR_INVALID_ARG;
+    const uintptr_t al = dtype == RELATTN_BF16 ? 2 : 4;
+    if (!aligned(dout, al) || !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dbias, 4) ||
+        !aligned(bias, 4) || !aligned(workspace, 4))
+        return RELATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    relattn::T5Buckets t5{};
+    if (kind == relattn::kBiasBuckets) {
+        if (bidirectional != 0 && bidirectional != 1) return RELATTN_ERR_INVALID_ARG;
+        if (!relattn::t5_make_buckets(num_buckets, max_distance, bidirectional, &t5))
+            return RELATTN_ERR_INVALID_ARG;
+    } else if (kind == relattn::kBiasTable) {
+        if (radius < 0 || radius > (1 << 20)) return RELATTN_ERR_INVALID_ARG;
+        if (bias_head_stride < 0 || (bias_head_stride != 0 && bias_head_stride < 2LL * radius + 1))
+            return RELATTN_ERR_INVALID_ARG;
+    } else if (kind != relattn::kBiasAlibi) {
+        return RELATTN_ERR_INVALID_ARG;
+    }
+    if (d > 128 || n > relattn::kBiasBwdMaxN) return RELATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < relattn::bias_bwd_workspace_bytes(B, H, n)) return RELATTN_ERR_INVALID_ARG;
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    relattn::BiasBwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.dout = dout;
+    a.bias = bias;
+    a.kind = kind;
+    a.num_buckets = num_buckets;
+    a.radius = radius;
+    a.head_stride = bias_head_stride;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dbias = dbias;
+    a.workspace = workspace;
+    return from_cuda(relattn::launch_bias_bwd(a, kind == relattn::kBiasBuckets ? &t5 : nullptr,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_bwd_workspace_size(int B, int H, int n, int d, int clip_k,
                                             unsigned long long *bytes) {
     if (!bytes || !shapes_ok(B, H, n, d) || clip_k < 0 || clip_k > (1 << 20))

@@ -101,6 +101,29 @@ unsigned long long decode_workspace_bytes(int B, int H, int T, int d);
 // enough workspace the single-pass kernel runs
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 
+// ---- gradients of the scalar offset biases (T5, ALiBi, per-offset table) ------------------
+constexpr int kBiasBwdMaxN = 4096;  // the bias and the de sums of every offset sit in shared memory
+struct BiasBwdArgs {
+    const void *q, *k, *v, *dout;
+    const float *bias;        // T5 [num_buckets, H], ALiBi slopes [H], table [H|1, 2R+1]
+    int kind;                 // BiasKind
+    int num_buckets;          // T5
+    int radius;               // table
+    long long head_stride;    // table: elements between heads' rows (0 = one shared row)
+    int causal;
+    float scale;
+    const int *kv_len;
+    int B, H, n, d;
+    int bf16;
+    float *dq, *dk, *dv, *dbias;
+    void *workspace;
+};
+// floats of per-row records at the start of the workspace (G, the per-offset sums, follows)
+long long bias_bwd_rec_floats(int B, int H, int n);
+unsigned long long bias_bwd_workspace_bytes(int B, int H, int n);
+// cudaErrorNotSupported for n > kBiasBwdMaxN or d > 128
+cudaError_t launch_bias_bwd(const BiasBwdArgs &a, const T5Buckets *t5, cudaStream_t s);
+
 // ---- labelled edges (SIMT, fp32 arithmetic) ----------------------------------------------
 constexpr int kMaxLabels = 256;      // uint8 labels
 constexpr int kLabelOutOfRange = 1;  // device status word value (RELATTN_ERR_INVALID_ARG)

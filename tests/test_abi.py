@@ -164,3 +164,36 @@ def test_labeled_arguments_rejected_before_any_launch(lib):
     assert lab(d=36) == 2                          # bf16: d a multiple of 8
     assert lab(d=136) == 2
     assert lab(dtype=1, d=130) == 2
+
+
+def test_scalar_bias_bwd_arguments_rejected_before_any_launch(lib):
+    BIAS = ctypes.c_void_p(0x300000)
+    WS = ctypes.c_void_p(0x400000)
+    G = [ctypes.c_void_p(0x500000 + i * 0x100000) for i in range(4)]  # dq, dk, dv, dbias
+
+    def call(kind=1, bias=BIAS, nb=32, md=128, bidir=1, radius=4, hs=0, causal=0, n=16, d=64,
+             dtype=0, dout=FAKE, ws=WS, wsb=1 << 30):
+        return lib.raw_call("relattn_scalar_bias_bwd", FAKE, FAKE, FAKE, dout, kind, bias, nb, md,
+                            bidir, radius, ctypes.c_longlong(hs), causal, ctypes.c_float(1.0), None,
+                            1, 2, n, d, dtype, G[0], G[1], G[2], G[3], ws, ctypes.c_ulonglong(wsb),
+                            None)
+
+    assert call(kind=3) == 1
+    assert call(kind=-1) == 1
+    assert call(bias=None) == 1
+    assert call(bias=ctypes.c_void_p(0x300002)) == 1      # fp32 parameters: 4-byte alignment
+    assert call(dout=None) == 1
+    assert call(ws=None) == 1
+    assert call(kind=0, nb=1) == 1                         # no valid bucket layout
+    assert call(kind=0, bidir=2) == 1
+    assert call(kind=2, radius=-1) == 1
+    assert call(kind=2, radius=4, hs=5) == 1               # head stride below 2*radius + 1
+    assert call(causal=2) == 1
+    assert call(wsb=16) == 1                               # workspace below the size query
+    assert call(n=4097) == 2                               # beyond the shared-memory offset rows
+    assert call(d=256, dtype=1) == 2
+    nb = ctypes.c_ulonglong(0)
+    assert lib.raw_call("relattn_scalar_bias_bwd_workspace_size", 2, 3, 5, ctypes.byref(nb)) == 0
+    # per-row records (3 floats for each of the 30 rows, rounded up to a multiple of 64) and
+    # the per-offset sums of every head (3 heads x 9 offsets)
+    assert nb.value == (128 + 3 * (2 * 5 - 1)) * 4
