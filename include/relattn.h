@@ -8,8 +8,8 @@
  * embeddings" page, section "T5"; ALiBi and the per-offset scalar table: the same page,
  * sections "Placement in the taxonomy" and "Two-dimensional variants". Labelled edges: the
  * section "Relation-Aware Self-Attention: The Core Modification" of the same page. Also a
- * decode step against a key/value cache, the gradients of relattn_fwd and those of the scalar
- * offset biases.
+ * decode step against a key/value cache, the gradients of relattn_fwd, of the labelled-edge
+ * forward and of the scalar offset biases.
  *
  * Conventions shared by every entry point
  *   - Tensors q, k, v, out are [B, H, n, d], contiguous, d fastest (row-major).
@@ -402,6 +402,38 @@ RELATTN_API relattn_status_t relattn_scalar_bias_bwd(const void *q, const void *
 /* relattn_scalar_bias_bwd_workspace_size — host only: the workspace bytes it needs. */
 RELATTN_API relattn_status_t relattn_scalar_bias_bwd_workspace_size(int B, int H, int n,
                                                         unsigned long long *bytes);
+
+/*
+ * relattn_labeled_bwd — gradients of relattn_labeled_fwd (the labelled-edge forward; paper
+ * summary page, section "Relation-Aware Self-Attention: The Core Modification"): relattn_bwd's
+ * chain rule with the table row of pair (i, j) read from the label matrix,
+ * r_ij = labels[b * label_batch_stride + i * n + j], in place of clip(j - i, k) + k:
+ *
+ *   dq_i = scale sum_j de_ij (k_j + aK[h][r_ij]),  dk_j = scale sum_i de_ij q_i,
+ *   dv_j = sum_i p_ij dz_i,  daK[h][r] = scale sum_{r_ij = r} de_ij q_i,
+ *   daV[h][r] = sum_{r_ij = r} p_ij dz_i,   de_ij = p_ij (dz_i . (v_j + aV[h][r_ij]) - D_i).
+ *
+ *   arguments as in relattn_labeled_fwd (num_labels 1 .. 256, labels required) and relattn_bwd
+ *   (dout of q's dtype; dq, dk, dv [B, H, n, d] fp32; daK / daV fp32 of the tables' layout,
+ *   required with their table and written whole; d <= 128).
+ *   workspace         caller-owned device scratch of at least relattn_labeled_bwd_workspace_size
+ *                     bytes (4-byte aligned); its contents are scratch.
+ * A label >= num_labels is read as the last table row and sets the device status word to
+ * RELATTN_ERR_INVALID_ARG, as in the forward. fp32 arithmetic on the SIMT units.
+ */
+RELATTN_API relattn_status_t relattn_labeled_bwd(const void *q, const void *k, const void *v,
+                                     const void *aK, const void *aV, long long table_head_stride,
+                                     int num_labels, const unsigned char *labels,
+                                     long long label_batch_stride, int causal, float scale,
+                                     const int *kv_len, int B, int H, int n, int d, int dtype,
+                                     const void *dout, float *dq, float *dk, float *dv,
+                                     float *daK, float *daV, void *workspace,
+                                     unsigned long long workspace_bytes, relattn_stream_t stream);
+
+/* relattn_labeled_bwd_workspace_size — host only: the workspace bytes it needs. */
+RELATTN_API relattn_status_t relattn_labeled_bwd_workspace_size(int B, int H, int n,
+                                                    int num_labels,
+                                                    unsigned long long *bytes);
 
 /*
  * relattn_labels — the integer edge label of every (i, j), computed by the same device

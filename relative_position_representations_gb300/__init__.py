@@ -1,6 +1,6 @@
 """relation-aware self-attention on GB300 (sm_103a): the Shaw forward, T5 / ALiBi /
 per-offset scalar biases, labelled edges, a decode step, the Shaw gradients and those
-of the scalar biases.
+of labelled edges and the scalar biases.
 
 The compute lives in librelattn.so (C ABI, include/relattn.h); this package holds its
 ctypes binding (`_lib`), the in-tree build script (`build`) and the named workloads with
@@ -15,7 +15,8 @@ _BINDING = ("relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_scalar_bias_bwd",
-            "relattn_scalar_bias_bwd_workspace_size", "relattn_labels",
+            "relattn_scalar_bias_bwd_workspace_size", "relattn_labeled_bwd",
+            "relattn_labeled_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
             "relattn_debug_withhold_first_load", "relattn_set_short_kernel",
             "relattn_set_bwd_tensor_cores",

@@ -62,6 +62,12 @@ _lib.relattn_scalar_bias_bwd.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
 _lib.relattn_scalar_bias_bwd.restype = _I
 _lib.relattn_scalar_bias_bwd_workspace_size.argtypes = [_I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.relattn_scalar_bias_bwd_workspace_size.restype = _I
+_lib.relattn_labeled_bwd.argtypes = [_P, _P, _P, _P, _P, ctypes.c_longlong, _I, _P,
+                                     ctypes.c_longlong, _I, ctypes.c_float, _P, _I, _I, _I, _I,
+                                     _I, _P, _P, _P, _P, _P, _P, _P, ctypes.c_ulonglong, _P]
+_lib.relattn_labeled_bwd.restype = _I
+_lib.relattn_labeled_bwd_workspace_size.argtypes = [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
+_lib.relattn_labeled_bwd_workspace_size.restype = _I
 _lib.relattn_decode_workspace_size.argtypes = [_I, _I, _I, _I, ctypes.POINTER(ctypes.c_ulonglong)]
 _lib.relattn_decode_workspace_size.restype = _I
 _lib.relattn_labels.argtypes = [_I, _I, _I, _I, _I, _I, _I, _P, _P]
@@ -90,7 +96,8 @@ EXPORTED = ["relattn_fwd", "relattn_t5bias_fwd", "relattn_alibi_fwd",
             "relattn_decode_fwd",
             "relattn_decode_fwd_noalloc", "relattn_decode_workspace_size", "relattn_bwd",
             "relattn_bwd_workspace_size", "relattn_scalar_bias_bwd",
-            "relattn_scalar_bias_bwd_workspace_size", "relattn_labels",
+            "relattn_scalar_bias_bwd_workspace_size", "relattn_labeled_bwd",
+            "relattn_labeled_bwd_workspace_size", "relattn_labels",
             "relattn_t5_thresholds", "relattn_set_wait_limit",
             "relattn_debug_withhold_first_load", "relattn_set_short_kernel", "relattn_set_bwd_tensor_cores",
             "relattn_get_device_error", "relattn_status_string", "relattn_version"]
@@ -469,6 +476,69 @@ def relattn_scalar_bias_bwd(q, k, v, dout, kind, bias, num_buckets=32, max_dista
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "relattn_scalar_bias_bwd")
     return dq, dk, dv, dbias
+
+
+def relattn_labeled_bwd_workspace_size(B, H, n, num_labels) -> int:
+    """Workspace bytes relattn_labeled_bwd needs (host only)."""
+    nb = ctypes.c_ulonglong(0)
+    _check(_lib.relattn_labeled_bwd_workspace_size(int(B), int(H), int(n), int(num_labels),
+                                                   ctypes.byref(nb)),
+           "relattn_labeled_bwd_workspace_size")
+    return int(nb.value)
+
+
+def relattn_labeled_bwd(q, k, v, dout, labels, aK=None, aV=None, num_labels=None, causal=False,
+                        scale=None, kv_len=None, table_head_stride=None, workspace=None,
+                        stream=None):
+    """Gradients of relattn_labeled_fwd: returns (dq, dk, dv, daK, daV), fp32 (daK / daV None
+    when the table is None). labels: uint8 [n, n] or [B, n, n]; num_labels defaults to the
+    tables' row count (required without tables). workspace: a CUDA tensor of at least
+    relattn_labeled_bwd_workspace_size bytes, or None to make one."""
+    B, H, n, d = _qkv(q, k, v)
+    dt = _dtype_code(q)
+    _dev(dout, "dout", q.dtype)
+    if dout.shape != q.shape:
+        raise ValueError("dout must be [B, H, n, d] like q")
+    ref = aK if aK is not None else aV
+    for t, nm in ((aK, "aK"), (aV, "aV")):
+        if t is not None:
+            _dev(t, nm, q.dtype)
+            if t.dim() != 3 or t.shape[2] != d or t.shape[0] not in (1, H):
+                raise ValueError("tables must be [H or 1, num_labels, d]")
+    if num_labels is None:
+        if ref is None:
+            raise ValueError("num_labels is required without tables")
+        num_labels = int(ref.shape[1])
+    if table_head_stride is None:
+        table_head_stride = 0 if (ref is None or ref.shape[0] == 1) else int(num_labels) * d
+    _dev(labels, "labels", torch.uint8)
+    if labels is None:
+        raise ValueError("labels is required")
+    if labels.shape == (n, n):
+        lbs = 0
+    elif labels.shape == (B, n, n):
+        lbs = n * n
+    else:
+        raise ValueError("labels must be [n, n] or [B, n, n]")
+    _dev(kv_len, "kv_len", torch.int32)
+    if scale is None:
+        scale = d ** -0.5
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dv = (torch.empty(q.shape, **f32) for _ in range(3))
+    daK = None if aK is None else torch.empty(aK.shape, **f32)
+    daV = None if aV is None else torch.empty(aV.shape, **f32)
+    need = relattn_labeled_bwd_workspace_size(B, H, n, num_labels)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4), dtype=torch.uint8, device=q.device)
+    _dev(workspace, "workspace")
+    st = _lib.relattn_labeled_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(aK), _ptr(aV),
+                                  int(table_head_stride), int(num_labels), _ptr(labels), int(lbs),
+                                  int(bool(causal)), float(scale), _ptr(kv_len), B, H, n, d, dt,
+                                  _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(daK), _ptr(daV),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    _check(st, "relattn_labeled_bwd")
+    return dq, dk, dv, daK, daV
 
 
 def relattn_decode_workspace_size(B, H, T, d) -> int:

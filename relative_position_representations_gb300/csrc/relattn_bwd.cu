@@ -1,4 +1,6 @@
-// Gradients of the Shaw relation-aware attention forward: dq, dk, dv, dw^K, dw^V.
+// Gradients of the Shaw relation-aware attention forward: dq, dk, dv, dw^K, dw^V (and of the
+// labelled-edge forward, where a label matrix picks the table row r of each pair in place of
+// clip(j - i, k) + k: "Relation-Aware Self-Attention: The Core Modification").
 //
 // The pages give only the forward pass ("Self-Attention with Relative Position
 // Representations" page, section 3.4: eq. 3, eq. 4 and the softmax). The gradients are the
@@ -49,6 +51,10 @@ struct Params {
     const T *q, *k, *v, *aK, *aV, *dz;
     long long ths;
     int clip_k, causal;
+    int W;                   // table rows: 2k+1, or the number of labels
+    const uint8_t *labels;   // labelled edges: row of (i, j) = labels[b * lbs + i * n + j]
+    long long lbs;
+    int *err;                // device status word (a label without a table row)
     float scale;
     const int *kv_len;
     int B, H, n, d;
@@ -60,6 +66,20 @@ __device__ __forceinline__ int keys_of(const int *kv_len, int b, int n) {
     return kv_len ? max(0, min(kv_len[b], n)) : n;
 }
 
+// table row of pair (i, j): clip(j - i, k) + k, or the pair's label (a label without a
+// table row is read as the last row and reported through the status word, as the forward
+// does); lab = the row i of the sequence's label matrix
+template <typename T>
+__device__ __forceinline__ int row_of(const Params<T> &p, const uint8_t *lab, int i, int j) {
+    if (!p.labels) return min(p.clip_k, max(-p.clip_k, j - i)) + p.clip_k;
+    const int r = lab[j];
+    if (r >= p.W) {
+        atomicCAS(p.err, 0, kLabelOutOfRange);
+        return p.W - 1;
+    }
+    return r;
+}
+
 // ---------------------------------------------------------------------------------- rows
 template <typename T>
 __global__ void __launch_bounds__(32 * kWarps) bwd_rows(const Params<T> p) {
@@ -68,11 +88,12 @@ __global__ void __launch_bounds__(32 * kWarps) bwd_rows(const Params<T> p) {
     const long long row = (long long)blockIdx.x * kWarps + warp;  // (b*H + h)*n + i
     const long long rows = (long long)p.B * p.H * p.n;
     if (row >= rows) return;
-    const int d = p.d, n = p.n, k = p.clip_k, W = 2 * k + 1;
+    const int d = p.d, n = p.n, W = p.W;
     const long long bh = row / n;
     const int i = (int)(row - bh * n), b = (int)(bh / p.H), h = (int)(bh % p.H);
     const int nk = keys_of(p.kv_len, b, n);
     const int jend = p.causal ? min(nk, i + 1) : nk;  // keys 0 .. jend-1 are allowed
+    const uint8_t *lab = p.labels ? p.labels + (long long)b * p.lbs + (long long)i * n : nullptr;
     float *R = sR[warp], *Rv = sRv[warp], *gam = sG[warp], *bet = sBe[warp];
     float qv[kMaxPer], gv[kMaxPer], acc[kMaxPer];
 #pragma unroll
@@ -118,7 +139,7 @@ __global__ void __launch_bounds__(32 * kWarps) bwd_rows(const Params<T> p) {
         }
         s = warp_sum(s);
         sv = warp_sum(sv);
-        const int r = min(k, max(-k, j - i)) + k;
+        const int r = row_of(p, lab, i, j);
         const float e = p.scale * s + R[r];
         const float dp = sv + Rv[r];
         if (e > m) {
@@ -145,7 +166,7 @@ __global__ void __launch_bounds__(32 * kWarps) bwd_rows(const Params<T> p) {
         }
         s = warp_sum(s);
         sv = warp_sum(sv);
-        const int r = min(k, max(-k, j - i)) + k;
+        const int r = row_of(p, lab, i, j);
         const float pr = __expf(p.scale * s + R[r] - m) * inv_l;
         const float de = pr * (sv + Rv[r] - D);
 #pragma unroll
@@ -192,9 +213,10 @@ __global__ void __launch_bounds__(32 * kWarps) bwd_keys(const Params<T> p) {
     const long long key = (long long)blockIdx.x * kWarps + warp;  // (b*H + h)*n + j
     const long long rows = (long long)p.B * p.H * p.n;
     if (key >= rows) return;
-    const int d = p.d, n = p.n, k = p.clip_k, W = 2 * k + 1;
+    const int d = p.d, n = p.n, W = p.W;
     const long long bh = key / n;
     const int j = (int)(key - bh * n), b = (int)(bh / p.H);
+    const uint8_t *lab0 = p.labels ? p.labels + (long long)b * p.lbs : nullptr;
     const int nk = keys_of(p.kv_len, b, n);
     float kv[kMaxPer], vv[kMaxPer], dk[kMaxPer], dv[kMaxPer];
 #pragma unroll
@@ -220,7 +242,9 @@ __global__ void __launch_bounds__(32 * kWarps) bwd_keys(const Params<T> p) {
             s = warp_sum(s);
             sv = warp_sum(sv);
             const float *rec = p.ws + (q0 + i) * rec_floats(W);
-            const int r = min(k, max(-k, j - i)) + k;
+            // (the row kernel reported an out-of-range label already)
+            const int r = p.labels ? min((int)lab0[(long long)i * n + j], W - 1)
+                                   : min(p.clip_k, max(-p.clip_k, j - i)) + p.clip_k;
             const float pr = __expf(p.scale * s + rec[3 + r] - rec[0]) * rec[1];
             const float de = pr * (sv + rec[3 + W + r] - rec[2]);
 #pragma unroll
@@ -245,7 +269,7 @@ __global__ void __launch_bounds__(32 * kWarps) bwd_keys(const Params<T> p) {
 // head's table (atomic: the batch, and with a shared table all heads, add into one row)
 template <typename T>
 __global__ void __launch_bounds__(128) bwd_tables(const Params<T> p) {
-    const int W = 2 * p.clip_k + 1, d = p.d, n = p.n;
+    const int W = p.W, d = p.d, n = p.n;
     const long long bh = blockIdx.x;
     const int r = blockIdx.y, h = (int)(bh % p.H);
     const long long tab = (long long)h * p.ths + (long long)r * d;
@@ -273,6 +297,10 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t s) {
     p.ths = a.ths;
     p.clip_k = a.clip_k;
     p.causal = a.causal;
+    p.W = a.labels ? a.num_labels : 2 * a.clip_k + 1;
+    p.labels = a.labels;
+    p.lbs = a.lbs;
+    p.err = a.err;
     p.scale = a.scale;
     p.kv_len = a.kv_len;
     p.B = a.B;
@@ -287,7 +315,7 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t s) {
     p.ws = static_cast<float *>(a.workspace);
     const long long rows = (long long)a.B * a.H * a.n;
     const unsigned blocks = (unsigned)((rows + kWarps - 1) / kWarps);
-    const int W = 2 * a.clip_k + 1;
+    const int W = p.W;
     const int Ht = a.ths == 0 ? 1 : a.H;
     cudaError_t e;
     if (p.daK) {
@@ -311,14 +339,20 @@ cudaError_t launch_t(const BwdArgs &a, cudaStream_t s) {
 
 }  // namespace bwd
 
+unsigned long long bwd_simt_workspace_bytes(int B, int H, int n, int W) {
+    return (unsigned long long)B * H * n * bwd::rec_floats(W) * sizeof(float);
+}
+
 unsigned long long bwd_workspace_bytes(int B, int H, int n, int clip_k) {
-    const unsigned long long simt = (unsigned long long)B * H * n * bwd::rec_floats(2 * clip_k + 1) * sizeof(float);
+    const unsigned long long simt = bwd_simt_workspace_bytes(B, H, n, 2 * clip_k + 1);
     const unsigned long long tc = bwd_tc_workspace_bytes(B, H, n, clip_k);
     return simt > tc ? simt : tc;
 }
 
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s) {
-    if (2 * a.clip_k + 1 > bwd::kMaxW || a.d > 32 * bwd::kMaxPer) return cudaErrorNotSupported;
+    const int W = a.labels ? a.num_labels : 2 * a.clip_k + 1;
+    if (W > bwd::kMaxW || a.d > 32 * bwd::kMaxPer) return cudaErrorNotSupported;
+    if (a.labels && !a.err) return cudaErrorInvalidValue;
     return a.bf16 ? bwd::launch_t<__nv_bfloat16>(a, s) : bwd::launch_t<float>(a, s);
 }
 

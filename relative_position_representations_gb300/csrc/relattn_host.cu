@@ -366,6 +366,67 @@ relattn_status_t relattn_decode_fwd_noalloc(const void *q, const void *k_cache,
                               cache_len, B, H, T, d, ws, kStaticScratchBytes, out, stream);
 }
 
+relattn_status_t relattn_labeled_bwd_workspace_size(int B, int H, int n, int num_labels,
+                                                  unsigned long long *bytes) {
+    if (!bytes || !shapes_ok(B, H, n, 1) || num_labels < 1 || num_labels > 256)
+        return RELATTN_ERR_INVALID_ARG;
+    *bytes = relattn::bwd_simt_workspace_bytes(B, H, n, num_labels);
+    return RELATTN_OK;
+}
+
+relattn_status_t relattn_labeled_bwd(const void *q, const void *k, const void *v, const void *aK,
+                                     const void *aV, long long table_head_stride, int num_labels,
+                                     const unsigned char *labels, long long label_batch_stride,
+                                     int causal, float scale, const int *kv_len, int B, int H,
+                                     int n, int d, int dtype, const void *dout, float *dq,
+                                     float *dk, float *dv, float *daK, float *daV,
+                                     void *workspace, unsigned long long workspace_bytes,
+                                     relattn_stream_t stream) {
+    relattn_status_t st = check_qkv(q, k, v, dq, B, H, n, d, dtype);
+    if (st != RELATTN_OK && st != RELATTN_ERR_UNSUPPORTED) return st;
+    if (!dout || !dk || !dv || !workspace) return RELATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return RELATTN_ERR_INVALID_ARG;
+    if (kv_len && !aligned(kv_len, 4)) return RELATTN_ERR_INVALID_ARG;
+    const uintptr_t al = dtype == RELATTN_BF16 ? 2 : 4;
+    if (!aligned(dout, al) || !aligned(dk, 4) || !aligned(dv, 4) || !aligned(workspace, 4))
+        return RELATTN_ERR_INVALID_ARG;
+    if (num_labels < 1 || num_labels > 256 || !labels) return RELATTN_ERR_INVALID_ARG;
+    if (label_batch_stride < 0 || (label_batch_stride != 0 && label_batch_stride < (long long)n * n))
+        return RELATTN_ERR_INVALID_ARG;
+    if ((aK && !daK) || (aV && !daV)) return RELATTN_ERR_INVALID_ARG;
+    if (aK || aV) {
+        if (table_head_stride < 0 ||
+            (table_head_stride != 0 && table_head_stride < (long long)num_labels * d))
+            return RELATTN_ERR_INVALID_ARG;
+        if ((aK && !aligned(aK, al)) || (aV && !aligned(aV, al)) || (daK && !aligned(daK, 4)) ||
+            (daV && !aligned(daV, 4)))
+            return RELATTN_ERR_INVALID_ARG;
+    }
+    if (d > 128) return RELATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < relattn::bwd_simt_workspace_bytes(B, H, n, num_labels))
+        return RELATTN_ERR_INVALID_ARG;
+    const int cc = current_cc();
+    if (cc < 0) return RELATTN_ERR_CUDA;
+    if (cc != 103) return RELATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    relattn::BwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.aK = aK; a.aV = aV; a.dout = dout;
+    a.ths = table_head_stride;
+    a.clip_k = 0;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
+    a.B = B; a.H = H; a.n = n; a.d = d;
+    a.bf16 = dtype == RELATTN_BF16 ? 1 : 0;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.daK = daK; a.daV = daV;
+    a.workspace = workspace;
+    a.labels = labels;
+    a.lbs = label_batch_stride;
+    a.num_labels = num_labels;
+    a.err = status_word_for_current_device();
+    if (!a.err) return RELATTN_ERR_CUDA;
+    return from_cuda(relattn::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 relattn_status_t relattn_scalar_bias_bwd_workspace_size(int B, int H, int n,
                                                       unsigned long long *bytes) {
     if (!bytes || B < 0 || H < 0 || n < 0) return RELATTN_ERR_INVALID_ARG;

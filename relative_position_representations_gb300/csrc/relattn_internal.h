@@ -182,12 +182,19 @@ struct BwdArgs {
     int bf16;  // 1: q, k, v, tables and dout are bf16; 0: fp32
     float *dq, *dk, *dv, *daK, *daV;
     void *workspace;  // at least bwd_workspace_bytes
-    int *err;               // tensor-core path: device status word
+    int *err;               // device status word (tensor-core waits; out-of-range labels)
     long long wait_limit;   // tensor-core path: bound of every device wait (cycles, <= 0: 2e9)
+    // labelled edges (SIMT only): the table row of pair (i, j) is labels[b * lbs + i * n + j]
+    // (num_labels rows) in place of clip(j - i, clip_k) + clip_k
+    const uint8_t *labels;
+    long long lbs;
+    int num_labels;
 };
 // the larger of the two paths' needs
 unsigned long long bwd_workspace_bytes(int B, int H, int n, int clip_k);
-// SIMT kernels; cudaErrorNotSupported when 2k+1 > 257 or d > 128
+// the SIMT kernels' need for W table rows (2k+1, or the number of labels)
+unsigned long long bwd_simt_workspace_bytes(int B, int H, int n, int W);
+// SIMT kernels; cudaErrorNotSupported when the table rows exceed 257 or d > 128
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t s);
 // tensor-core kernels (bf16, d = 64 or 128, at most 128 staged table rows, workspace aligned
 // to 256 bytes); bwd_tc_covers says whether they take the call

@@ -197,3 +197,34 @@ def test_scalar_bias_bwd_arguments_rejected_before_any_launch(lib):
     # per-row records (3 floats for each of the 30 rows, rounded up to a multiple of 64) and
     # the per-offset sums of every head (3 heads x 9 offsets)
     assert nb.value == (128 + 3 * (2 * 5 - 1)) * 4
+
+
+def test_labeled_bwd_arguments_rejected_before_any_launch(lib):
+    TAB = ctypes.c_void_p(0x300000)
+    LAB = ctypes.c_void_p(0x380000)
+    WS = ctypes.c_void_p(0x400000)
+    G = [ctypes.c_void_p(0x500000 + i * 0x100000) for i in range(5)]  # dq, dk, dv, daK, daV
+
+    def call(aK=TAB, aV=None, ths=0, L=8, labels=LAB, lbs=0, causal=0, n=16, d=64, dtype=0,
+             daK=G[3], daV=G[4], ws=WS, wsb=1 << 30):
+        return lib.raw_call("relattn_labeled_bwd", FAKE, FAKE, FAKE, aK, aV, ctypes.c_longlong(ths),
+                            L, labels, ctypes.c_longlong(lbs), causal, ctypes.c_float(1.0), None,
+                            1, 2, n, d, dtype, FAKE, G[0], G[1], G[2], daK, daV, ws,
+                            ctypes.c_ulonglong(wsb), None)
+
+    assert call(L=0) == 1
+    assert call(L=257) == 1
+    assert call(labels=None) == 1
+    assert call(lbs=100) == 1                          # below n * n
+    assert call(ths=8 * 64 - 1) == 1                   # below num_labels * d
+    assert call(daK=None) == 1                         # a table without its gradient
+    assert call(aV=TAB, daV=None) == 1
+    assert call(causal=2) == 1
+    assert call(ws=None) == 1
+    assert call(wsb=16) == 1
+    assert call(d=256, dtype=1) == 2
+    nb = ctypes.c_ulonglong(0)
+    assert lib.raw_call("relattn_labeled_bwd_workspace_size", 2, 3, 5, 8, ctypes.byref(nb)) == 0
+    # per query row: m, 1/l, D and four values per label (R, Rv and the two bins)
+    assert nb.value == 2 * 3 * 5 * (3 + 4 * 8) * 4
+    assert lib.raw_call("relattn_labeled_bwd_workspace_size", 2, 3, 5, 0, ctypes.byref(nb)) == 1
