@@ -379,7 +379,8 @@ RELATTN_API relattn_status_t relattn_bwd_workspace_size(int B, int H, int n, int
  *           every entry of the rows is written.
  *
  *   q, k, v, dout, causal, scale, kv_len, B, H, n, d, dtype   as in the forward (bf16 or
- *                     fp32 inputs, d <= 128, n <= 4096; else RELATTN_ERR_UNSUPPORTED).
+ *                     fp32 inputs, d <= 128, n <= 4096, B * H <= 65535; else
+ *                     RELATTN_ERR_UNSUPPORTED).
  *   dq, dk, dv        [B, H, n, d] fp32; padded keys get zero; rows with no allowed key zero.
  *   workspace         caller-owned device scratch of at least
  *                     relattn_scalar_bias_bwd_workspace_size bytes (4-byte aligned): per row

@@ -465,6 +465,7 @@ relattn_status_t relattn_scalar_bias_bwd(const void *q, const void *k, const voi
         return RELATTN_ERR_INVALID_ARG;
     }
     if (d > 128 || n > relattn::kBiasBwdMaxN) return RELATTN_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535) return RELATTN_ERR_UNSUPPORTED;  // sequence-heads on grid y
     if (workspace_bytes < relattn::bias_bwd_workspace_bytes(B, H, n)) return RELATTN_ERR_INVALID_ARG;
     const int cc = current_cc();
     if (cc < 0) return RELATTN_ERR_CUDA;

@@ -191,6 +191,9 @@ def test_scalar_bias_bwd_arguments_rejected_before_any_launch(lib):
     assert call(causal=2) == 1
     assert call(wsb=16) == 1                               # workspace below the size query
     assert call(n=4097) == 2                               # beyond the shared-memory offset rows
+    assert lib.raw_call("relattn_scalar_bias_bwd", FAKE, FAKE, FAKE, FAKE, 1, BIAS, 32, 128, 1, 4,
+                        ctypes.c_longlong(0), 0, ctypes.c_float(1.0), None, 256, 257, 16, 64, 0,
+                        G[0], G[1], G[2], G[3], WS, ctypes.c_ulonglong(1 << 40), None) == 2
     assert call(d=256, dtype=1) == 2
     nb = ctypes.c_ulonglong(0)
     assert lib.raw_call("relattn_scalar_bias_bwd_workspace_size", 2, 3, 5, ctypes.byref(nb)) == 0
